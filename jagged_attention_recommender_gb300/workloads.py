@@ -1,0 +1,218 @@
+"""Seeded synthetic jagged GDPA workloads.
+
+This module only draws inputs: sequence lengths, bf16 value tensors laid out
+``[tokens, H, D]`` and int32 offset prefix sums.  It holds none of the
+attention arithmetic, so the CUDA path and the CPU oracle can both be fed from
+it without sharing any of the method.
+
+The five workloads follow the shape classes the GEM training write-up lists
+for its attention variants (techfeed summary of "GEM Training", section
+"why LLM infrastructure does not carry over": jagged user histories of
+hundreds to tens of thousands of tokens; self-attention, long-query/short-KV
+cross attention, short-query/long-KV pooled attention), plus the 64-token
+block-aligned window of the "BlockAttention" section.  Exact sizes and
+distributions are the benchmark configurations of this project:
+
+==============  ====================================================================
+name            recipe
+==============  ====================================================================
+tiny            B=4, H=2, D=64, L ~ U{1..128}; softmax; scale 1/sqrt(D)
+self_long       B=256, H=4, D=128, L = clip(round(lognormal(6.9, 0.8)), 100, 4096)
+cross_gelu      B=512, H=4, D=128, Lq ~ U{256..4096}, Lkv ~ U{8..64}; Q, K rows
+                L2-normalised per (token, head) then x4; GELU; scale 1.0
+pma             B=256, H=8, D=64, 32 seed queries shared by every sample
+                (materialised per sample), Lkv = clip(round(lognormal(7.6, 1.0)),
+                100, 16384); softmax; scale 1/sqrt(D)
+block_window    B=64, H=4, D=128, L = 64 * U{8..512}; window of 4 blocks of 64
+                (own block causal + 3 previous); softmax; scale 1/sqrt(D)
+==============  ====================================================================
+
+Draw order (fixed): lengths first, then one 63-bit sub-seed per value tensor
+(Q, K, V), all from ``numpy.random.default_rng(seed)``.  Values are drawn in
+fixed chunks of tokens, each chunk from ``default_rng([sub_seed, chunk])``, so
+the result does not depend on how many threads draw it.  Values are float32
+N(0, 1), rounded to bf16 with round-to-nearest-even and kept as raw uint16
+bit patterns.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ACT_SOFTMAX = 0
+ACT_GELU_TANH = 1
+
+CHUNK_TOKENS = 16384
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    seed: int
+    B: int
+    H: int
+    D: int
+    act: int
+    window_blocks: int
+    scale: float
+    kind: str  # "self", "cross", "pma", "window"
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 0, 4, 2, 64, ACT_SOFTMAX, 0, 1.0 / math.sqrt(64), "self"),
+    "self_long": Workload("self_long", 1, 256, 4, 128, ACT_SOFTMAX, 0, 1.0 / math.sqrt(128), "self"),
+    "cross_gelu": Workload("cross_gelu", 2, 512, 4, 128, ACT_GELU_TANH, 0, 1.0, "cross"),
+    "pma": Workload("pma", 3, 256, 8, 64, ACT_SOFTMAX, 0, 1.0 / math.sqrt(64), "pma"),
+    "block_window": Workload("block_window", 4, 64, 4, 128, ACT_SOFTMAX, 4, 1.0 / math.sqrt(128), "window"),
+}
+
+PMA_SEEDS = 32
+BLOCK = 64
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (round to nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
+    return ((u + bias) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def draw_lengths(w: Workload, rng: np.random.Generator, B: int | None = None):
+    """Per-sequence (Lq, Lkv) for ``B`` sequences (default: the workload's B)."""
+    B = w.B if B is None else B
+    if w.name == "tiny":
+        L = rng.integers(1, 128, size=B, endpoint=True)
+        return L, L
+    if w.name == "self_long":
+        L = np.clip(np.round(rng.lognormal(6.9, 0.8, size=B)), 100, 4096).astype(np.int64)
+        return L, L
+    if w.name == "cross_gelu":
+        Lq = rng.integers(256, 4096, size=B, endpoint=True)
+        Lkv = rng.integers(8, 64, size=B, endpoint=True)
+        return Lq, Lkv
+    if w.name == "pma":
+        Lkv = np.clip(np.round(rng.lognormal(7.6, 1.0, size=B)), 100, 16384).astype(np.int64)
+        return np.full(B, PMA_SEEDS, dtype=np.int64), Lkv
+    if w.name == "block_window":
+        L = BLOCK * rng.integers(8, 512, size=B, endpoint=True)
+        return L, L
+    raise KeyError(w.name)
+
+
+def offsets_of(lengths) -> np.ndarray:
+    c = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    if c.size and c[-1] >= 2**31:
+        raise ValueError("total token count does not fit int32 offsets")
+    off = np.zeros(len(lengths) + 1, dtype=np.int32)
+    off[1:] = c
+    return off
+
+
+def _normal_chunked(sub_seed: int, tokens: int, H: int, D: int, threads: int) -> np.ndarray:
+    out = np.empty((tokens, H, D), dtype=np.float32)
+    n_chunks = (tokens + CHUNK_TOKENS - 1) // CHUNK_TOKENS
+
+    def fill(c):
+        lo = c * CHUNK_TOKENS
+        hi = min(tokens, lo + CHUNK_TOKENS)
+        g = np.random.default_rng([sub_seed, c])
+        out[lo:hi] = g.standard_normal((hi - lo, H, D), dtype=np.float32)
+
+    if threads > 1 and n_chunks > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(fill, range(n_chunks)))
+    else:
+        for c in range(n_chunks):
+            fill(c)
+    return out
+
+
+def _qk_norm_x4(x: np.ndarray) -> np.ndarray:
+    """Input recipe of the cross workload: each (token, head) row scaled to L2 norm 4."""
+    n = np.sqrt(np.einsum("thd,thd->th", x, x, dtype=np.float32))
+    return x * (np.float32(4.0) / np.maximum(n, np.float32(1e-30)))[..., None]
+
+
+@dataclasses.dataclass
+class JaggedBatch:
+    workload: Workload
+    q: np.ndarray          # uint16 bf16 bits [Tq, H, D]
+    k: np.ndarray          # uint16 bf16 bits [Tkv, H, D]
+    v: np.ndarray          # uint16 bf16 bits [Tkv, H, D]
+    q_offsets: np.ndarray  # int32 [B+1]
+    kv_offsets: np.ndarray  # int32 [B+1]
+
+    @property
+    def B(self) -> int:
+        return len(self.q_offsets) - 1
+
+    @property
+    def H(self) -> int:
+        return self.workload.H
+
+    @property
+    def D(self) -> int:
+        return self.workload.D
+
+    def lengths(self):
+        return np.diff(self.q_offsets).astype(np.int64), np.diff(self.kv_offsets).astype(np.int64)
+
+    def subset(self, seqs) -> "JaggedBatch":
+        """The batch made of sequences ``seqs`` (in that order), copied contiguous."""
+        seqs = [int(s) for s in seqs]
+        qo, ko = self.q_offsets, self.kv_offsets
+        q = np.concatenate([self.q[qo[s]:qo[s + 1]] for s in seqs]) if seqs else self.q[:0]
+        k = np.concatenate([self.k[ko[s]:ko[s + 1]] for s in seqs]) if seqs else self.k[:0]
+        v = np.concatenate([self.v[ko[s]:ko[s + 1]] for s in seqs]) if seqs else self.v[:0]
+        return JaggedBatch(self.workload, np.ascontiguousarray(q), np.ascontiguousarray(k),
+                           np.ascontiguousarray(v),
+                           offsets_of([qo[s + 1] - qo[s] for s in seqs]),
+                           offsets_of([ko[s + 1] - ko[s] for s in seqs]))
+
+
+def make_batch(name: str, B: int | None = None, seed: int | None = None,
+               lengths=None, threads: int | None = None) -> JaggedBatch:
+    """Draw the seeded batch of workload ``name``.
+
+    ``B`` and ``seed`` override the workload's batch size and seed (smaller
+    cases with the same distributions); ``lengths`` = (Lq, Lkv) arrays override
+    the length draw entirely (edge-case tests).
+    """
+    w = WORKLOADS[name]
+    seed = w.seed if seed is None else seed
+    threads = threads or min(16, os.cpu_count() or 1)
+    rng = np.random.default_rng(seed)
+    if lengths is None:
+        Lq, Lkv = draw_lengths(w, rng, B)
+    else:
+        Lq, Lkv = (np.asarray(x, dtype=np.int64) for x in lengths)
+    subs = [int(s) for s in rng.integers(0, 2**63 - 1, size=3)]
+    H, D = w.H, w.D
+    Tq, Tkv = int(Lq.sum()), int(Lkv.sum())
+    if w.kind == "pma":
+        seeds = _normal_chunked(subs[0], PMA_SEEDS, H, D, 1)
+        qf = np.empty((Tq, H, D), dtype=np.float32)
+        qo = offsets_of(Lq)
+        for b in range(len(Lq)):
+            n = int(Lq[b])
+            qf[qo[b]:qo[b] + n] = seeds[:n]
+    else:
+        qf = _normal_chunked(subs[0], Tq, H, D, threads)
+    kf = _normal_chunked(subs[1], Tkv, H, D, threads)
+    if w.kind == "cross":
+        qf = _qk_norm_x4(qf)
+        kf = _qk_norm_x4(kf)
+    q = f32_to_bf16_bits(qf)
+    del qf
+    k = f32_to_bf16_bits(kf)
+    del kf
+    v = f32_to_bf16_bits(_normal_chunked(subs[2], Tkv, H, D, threads))
+    return JaggedBatch(w, q, k, v, offsets_of(Lq), offsets_of(Lkv))

@@ -1,0 +1,85 @@
+"""fp64 CPU oracle for the jagged GDPA forward pass -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it.  The arithmetic lives in ``gdpa_oracle.c`` (plain C,
+built with gcc by :func:`build`); this module only marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdpa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc (plain C, -O2, pthreads)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared", "-pthread",
+                           "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        lib.oracle_gdpa_fwd.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int]
+        lib.oracle_gdpa_fwd.restype = ctypes.c_int
+        lib.oracle_gelu_tanh.argtypes = [ctypes.c_double]
+        lib.oracle_gelu_tanh.restype = ctypes.c_double
+        lib.oracle_num_cpus.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def gdpa_fwd(q, k, v, q_offsets, kv_offsets, H: int, D: int, act: int, window_blocks: int,
+             scale: float, nthreads: int = 0) -> np.ndarray:
+    """Oracle output, fp64 ``[Tq, H, D]``.
+
+    ``q``, ``k``, ``v`` are uint16 bf16 bit patterns ``[tokens, H, D]``;
+    offsets are int32 prefix sums ``[B+1]``.
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    qo = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ko = np.ascontiguousarray(kv_offsets, dtype=np.int32)
+    B = len(qo) - 1
+    out = np.zeros((int(qo[-1]), H, D), dtype=np.float64)
+    rc = lib.oracle_gdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(qo), _ptr(ko), B, H, D, act,
+                             window_blocks, float(scale), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gdpa_fwd returned %d" % rc)
+    return out
+
+
+def gdpa_fwd_batch(batch, nthreads: int = 0) -> np.ndarray:
+    w = batch.workload
+    return gdpa_fwd(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, w.H, w.D, w.act,
+                    w.window_blocks, w.scale, nthreads)
+
+
+def gelu_tanh(x: float) -> float:
+    return _load().oracle_gelu_tanh(float(x))
+
+
+def num_cpus() -> int:
+    return _load().oracle_num_cpus()

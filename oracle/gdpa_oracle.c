@@ -1,0 +1,196 @@
+/*
+ * gdpa_oracle.c -- plain fp64 CPU oracle for the jagged GDPA forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code with the CUDA library.
+ *
+ * What it computes (one (sequence b, head h) at a time, every query row i):
+ *
+ *   s_ij = scale * <q_i, k_j>            over the bf16 inputs widened to fp64
+ *
+ *   softmax:  o_i = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),
+ *             m_i = max_j s_ij,  o_i = 0 when the key set is empty
+ *   GELU:     o_i = (1 / Lkv_b) * sum_j gelu(s_ij) v_j,
+ *             gelu(x) = x/2 * (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
+ *             o_i = 0 when Lkv_b = 0
+ *
+ * with j over the key set K(i):
+ *   full attention:  every key j < Lkv_b of the same sequence;
+ *   block window W:  blocks of 64 tokens counted from the sequence start,
+ *                    beta(t) = floor(t / 64); keys of the W-1 previous blocks
+ *                    and keys j <= i of the query's own block.
+ *
+ * Sources: jagged, unpadded sequences and the three shape classes (self,
+ * long-query/short-KV cross, short-query/long-KV pooled) -- techfeed summary
+ * of "GEM Training", section on why LLM infrastructure does not carry over,
+ * and its JFA section; attention with the softmax replaced by another
+ * activation (GELU, evaluated through tanh) -- same page, GDPA section, and
+ * the remio.ai commentary, section on model/system co-design; 64-token
+ * block-aligned windows, window a whole number of blocks -- techfeed summary,
+ * BlockAttention section, and the aigeeknews translation, co-design section.
+ * The output normalisation 1/Lkv of the GELU form and the window-of-blocks
+ * semantics (own block causal plus the previous W-1 blocks, one softmax over
+ * the union) are this project's readings of those passages.
+ *
+ * The oracle follows that definition literally: it loops over sequences,
+ * heads, queries and keys, in fp64, with libm's exp and tanh.  There is no
+ * tiling, no online (running-max) rescaling and no reordering.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_ACT_SOFTMAX 0
+#define ORACLE_ACT_GELU_TANH 1
+#define ORACLE_BLOCK 64
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an IEEE float). */
+static double bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+double oracle_gelu_tanh(double x) {
+  const double c = sqrt(2.0 / M_PI);
+  return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+/* Is key j in the key set of query i (both counted from the sequence start)? */
+static int key_in_set(int64_t i, int64_t j, int window_blocks) {
+  if (window_blocks <= 0) return 1;
+  int64_t bi = i / ORACLE_BLOCK, bj = j / ORACLE_BLOCK;
+  if (bj == bi) return j <= i;                        /* own block, causal */
+  return bj < bi && bj >= bi - (window_blocks - 1);   /* W-1 previous blocks */
+}
+
+typedef struct {
+  const uint16_t *q, *k, *v;
+  const int32_t *q_off, *kv_off;
+  int B, H, D, act, window_blocks;
+  double scale;
+  double* out;
+  int64_t next_task; /* shared counter over (b, h) tasks */
+} job_t;
+
+static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, double* qrow, double* s) {
+  const int H = J->H, D = J->D;
+  const int64_t q0 = J->q_off[b], Lq = J->q_off[b + 1] - q0;
+  const int64_t k0 = J->kv_off[b], Lkv = J->kv_off[b + 1] - k0;
+  for (int64_t j = 0; j < Lkv; ++j)
+    for (int d = 0; d < D; ++d) {
+      kbuf[j * D + d] = bf16_to_double(J->k[((k0 + j) * H + h) * D + d]);
+      vbuf[j * D + d] = bf16_to_double(J->v[((k0 + j) * H + h) * D + d]);
+    }
+  for (int64_t i = 0; i < Lq; ++i) {
+    double* o = J->out + ((q0 + i) * H + h) * (int64_t)D;
+    for (int d = 0; d < D; ++d) {
+      qrow[d] = bf16_to_double(J->q[((q0 + i) * H + h) * D + d]);
+      o[d] = 0.0;
+    }
+    /* scores over the key set */
+    int any = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Lkv; ++j) {
+      if (!key_in_set(i, j, J->window_blocks)) continue;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qrow[d] * kbuf[j * D + d];
+      s[j] = J->scale * dot;
+      if (s[j] > m) m = s[j];
+      any = 1;
+    }
+    if (!any) continue; /* empty key set: output stays 0 */
+    if (J->act == ORACLE_ACT_SOFTMAX) {
+      double den = 0.0;
+      for (int64_t j = 0; j < Lkv; ++j) {
+        if (!key_in_set(i, j, J->window_blocks)) continue;
+        double w = exp(s[j] - m);
+        den += w;
+        for (int d = 0; d < D; ++d) o[d] += w * vbuf[j * D + d];
+      }
+      for (int d = 0; d < D; ++d) o[d] /= den;
+    } else {
+      for (int64_t j = 0; j < Lkv; ++j) {
+        if (!key_in_set(i, j, J->window_blocks)) continue;
+        double g = oracle_gelu_tanh(s[j]);
+        for (int d = 0; d < D; ++d) o[d] += g * vbuf[j * D + d];
+      }
+      for (int d = 0; d < D; ++d) o[d] /= (double)Lkv;
+    }
+  }
+}
+
+static void* worker(void* arg) {
+  job_t* J = (job_t*)arg;
+  int64_t max_kv = 0;
+  for (int b = 0; b < J->B; ++b) {
+    int64_t L = J->kv_off[b + 1] - J->kv_off[b];
+    if (L > max_kv) max_kv = L;
+  }
+  double* kbuf = (double*)malloc(sizeof(double) * (size_t)(max_kv * J->D + 1));
+  double* vbuf = (double*)malloc(sizeof(double) * (size_t)(max_kv * J->D + 1));
+  double* qrow = (double*)malloc(sizeof(double) * (size_t)J->D);
+  double* s = (double*)malloc(sizeof(double) * (size_t)(max_kv + 1));
+  if (!kbuf || !vbuf || !qrow || !s) {
+    free(kbuf); free(vbuf); free(qrow); free(s);
+    return (void*)1;
+  }
+  const int64_t ntask = (int64_t)J->B * J->H;
+  for (;;) {
+    int64_t t = __atomic_fetch_add(&J->next_task, 1, __ATOMIC_RELAXED);
+    if (t >= ntask) break;
+    run_task(J, (int)(t / J->H), (int)(t % J->H), kbuf, vbuf, qrow, s);
+  }
+  free(kbuf); free(vbuf); free(qrow); free(s);
+  return NULL;
+}
+
+int oracle_num_cpus(void) {
+  long n = sysconf(_SC_NPROCESSORS_ONLN);
+  return n > 0 ? (int)n : 1;
+}
+
+/*
+ * q: bf16 bits [Tq, H, D]; k, v: bf16 bits [Tkv, H, D]; q_off, kv_off: int32
+ * [B+1] prefix sums starting at 0; out: fp64 [Tq, H, D] (fully written).
+ * window_blocks > 0 needs q_off == kv_off.  nthreads <= 0 uses every online
+ * CPU.  Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
+                    const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
+                    double* out, int nthreads) {
+  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH)) return 1;
+  if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
+  for (int b = 0; b < B; ++b) {
+    if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;
+    if (window_blocks > 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
+  }
+  if (B == 0 || q_off[B] == 0) return 0;
+  if (!q || !out || (kv_off[B] > 0 && (!k || !v))) return 1;
+  job_t J = {q, k, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0};
+  if (nthreads <= 0) nthreads = oracle_num_cpus();
+  if (nthreads > B * H) nthreads = B * H;
+  if (nthreads < 1) nthreads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return 2;
+  int started = 0, failed = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, worker, &J) != 0) break;
+    ++started;
+  }
+  if (started == 0) { /* no thread could start: run on this one */
+    failed = worker(&J) != NULL;
+  }
+  for (int t = 0; t < started; ++t) {
+    void* r = NULL;
+    pthread_join(th[t], &r);
+    if (r) failed = 1;
+  }
+  free(th);
+  return failed ? 2 : 0;
+}
