@@ -1,0 +1,383 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the jagged GDPA forward pass on GB300.
+
+One step = the whole forward path over one batch of the workload: host tile
+planning from the batch's offsets, work-list upload, and the persistent
+tcgen05 kernel (``gdpa_fwd_async`` through the C ABI).  Inputs are resident
+in HBM before the timed region; the workload's inputs (Q, K, V ~1 GB for the
+default workload) are larger than the 126 MB L2, so no L2 flush is done
+between steps.
+
+Prints one JSON line (rank 0).  ``value`` is useful TFLOPS: 4*D*H per
+unmasked (query, key) pair, summed over all ranks, over the max-over-ranks
+time.  ``--impl reference`` times the fp64 CPU oracle instead (the slow
+baseline arm) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from jagged_attention_recommender_gb300.metrics import algorithmic_bytes, useful_flops  # noqa: E402
+from jagged_attention_recommender_gb300.workloads import WORKLOADS, make_batch  # noqa: E402
+
+METRIC = "jagged GDPA fwd useful TFLOPS (unpadded) & % of GB300 roofline, 1 GPU"
+DEFAULT_WORKLOAD = "self_long"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+RECIPES = {
+    "tiny": "B=4 H=2 D=64, L~U{1..128}, softmax, scale=1/sqrt(D)",
+    "self_long": "B=256 H=4 D=128, L=clip(round(lognormal(6.9,0.8)),100,4096), softmax non-causal, scale=1/sqrt(D)",
+    "cross_gelu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, GELU-tanh (ALU), scale=1, /Lkv",
+    "pma": "B=256 H=8 D=64, 32 shared seed queries per sample, Lkv=clip(round(lognormal(7.6,1.0)),100,16384), softmax",
+    "block_window": "B=64 H=4 D=128, L=64*U{8..512}, 64-token blocks, window 4 blocks (own causal + 3 previous), softmax",
+}
+BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "jagged_attention_recommender_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel build."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(workload)
+        if e and e.get("kernel_hash") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(batch, target_s: float, seed: int = 2024):
+    """A seeded subset of whole sequences sized for ~target_s of oracle CPU time."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(batch.B)
+    # calibrate the oracle's rate on a first small slice
+    probe = [int(order[0])]
+    sub = batch.subset(probe)
+    t0 = time.perf_counter()
+    oracle.gdpa_fwd_batch(sub)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rate = useful_flops(sub) / dt  # single-sequence rate: at most H threads busy
+    cores = oracle.num_cpus()
+    rate_all = rate * max(1.0, min(cores, 4 * batch.H) / batch.H)
+    want = rate_all * target_s
+    seqs, acc = [], 0.0
+    for s in order:
+        f = useful_flops(batch.subset([int(s)]))
+        seqs.append(int(s))
+        acc += f
+        if acc >= want:
+            break
+    return batch.subset(seqs), seqs
+
+
+def time_oracle(sample, reps=1):
+    import oracle
+
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.gdpa_fwd_batch(sample)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    batch = make_batch(args.workload)
+    total_steps = args.steps + args.warmup
+    per_step = max(0.5, min(10.0, 150.0 / max(1, total_steps)))
+    sample, seqs = oracle_sample(batch, per_step)
+    flops = useful_flops(sample)
+    for _ in range(args.warmup):
+        time_oracle(sample)
+    times = time_oracle(sample, args.steps)
+    t = sum(times)
+    value = flops * args.steps / t / 1e12
+    cores = oracle.num_cpus()
+    desc = "%d of %d sequences (seeded), all %d heads, %.3g useful GFLOP per step" % (
+        len(seqs), batch.B, w.H, flops / 1e9)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
+                   "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from jagged_attention_recommender_gb300 import build as gbuild
+    from jagged_attention_recommender_gb300 import gdpa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    gbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = WORKLOADS[args.workload]
+    batch = make_batch(args.workload, seed=w.seed + 1000 * rank)
+    flops = useful_flops(batch)
+    nbytes = algorithmic_bytes(batch)
+    H, D, B = w.H, w.D, batch.B
+    Tq = int(batch.q_offsets[-1])
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v = dev(batch.q), dev(batch.k), dev(batch.v)
+    qo = torch.from_numpy(batch.q_offsets).cuda()
+    ko = torch.from_numpy(batch.kv_offsets).cuda()
+    out = torch.empty((Tq, H, D), dtype=torch.bfloat16, device="cuda")
+    h_qo, h_ko = batch.q_offsets, batch.kv_offsets
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdpa.gdpa_fwd_async(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, out, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = gdpa.gdpa_device_status()
+    if st != gdpa.GDPA_OK:
+        raise SystemExit("device status after warm-up: " + gdpa.gdpa_status_string(st))
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    st = gdpa.gdpa_device_status()
+    if st != gdpa.GDPA_OK:
+        raise SystemExit("device status after timing: " + gdpa.gdpa_status_string(st))
+    elapsed_ms = e0.elapsed_time(e1)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if dist:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    total_flops = flops * world
+    value = total_flops * K / (elapsed_ms / 1e3) / 1e12
+
+    # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step)
+    hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
+    hk = torch.from_numpy(batch.k.view(np.int16)).pin_memory()
+    hv = torch.from_numpy(batch.v.view(np.int16)).pin_memory()
+    ho = torch.empty((Tq, H, D), dtype=torch.int16).pin_memory()
+    h2d = int(hq.numel() + hk.numel() + hv.numel()) * 2 + 2 * 4 * (B + 1)
+    d2h = int(ho.numel()) * 2
+    gdpa.gdpa_fwd_host(hq, hk, hv, h_qo, h_ko, B, H, D, w.act, w.window_blocks, w.scale, ho, stream)
+    e2e_t = []
+    for _ in range(max(1, args.e2e_steps)):
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        gdpa.gdpa_fwd_host(hq, hk, hv, h_qo, h_ko, B, H, D, w.act, w.window_blocks, w.scale, ho, stream)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_t)
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = total_flops / e2e_s / 1e12
+
+    peaks, peak_src = load_peaks()
+    bound = BOUND[args.workload]
+    if bound == "tensor":
+        achieved = flops / (launch_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = nbytes / (launch_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    traffic = traffic_per_launch(args.workload)
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic, "peak_source": peak_src + (" (burst)" if bound == "tensor" else ""),
+                "launch_ms": launch_ms, "useful_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+                "kernel_hash": kernel_hash()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        sample, seqs = oracle_sample(batch, args.cpu_seconds)
+        t = time_oracle(sample)[0]
+        cpu = {"value": useful_flops(sample) / t / 1e12, "unit": "TFLOPS", "cores": oracle.num_cpus(),
+               "kind": "oracle", "sample": "%d of %d sequences (seeded), all %d heads, %.3g useful GFLOP, %.1f s" % (
+                   len(seqs), B, H, useful_flops(sample) / 1e9, t)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
+                       "global_batch": B * world, "tokens_q": Tq, "tokens_kv": int(batch.kv_offsets[-1]),
+                       "l2": "inputs %.2f GB > 126 MB L2; no flush" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
+                       "parallelism": "dp%d (independent batches, no collective)" % world,
+                       "entry": "gdpa_fwd_async (host plan + upload + kernel per step)"},
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_s * 1e3, "entry": "gdpa_fwd_host"},
+            "gpu_launches": K,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * gdpa.h -- C ABI of libgdpa: forward pass of jagged Generalized Dot-Product
+ * Attention (GDPA) on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (techfeed summary of "GEM Training", sections "JFA" and
+ * "GDPA"; remio.ai commentary, section on model/system co-design): attention
+ * over a batch of variable-length, unpadded sequences, where the activation
+ * applied to the scores is either a softmax or a GELU (tanh form), and where
+ * the self-attention variant may be restricted to 64-token block-aligned
+ * windows (techfeed summary, section "BlockAttention"; aigeeknews translation,
+ * co-design section).  For sequence b, head h and query row i < Lq_b:
+ *
+ *   s_ij = scale * <q_i, k_j>                                  j in K(i)
+ *   softmax : o_i = sum_j exp(s_ij - max s) v_j / sum_j exp(s_ij - max s)
+ *   GELU    : o_i = (1/Lkv_b) * sum_j gelu_tanh(s_ij) v_j
+ *
+ *   K(i) = all keys j < Lkv_b of sequence b            (window_blocks == 0)
+ *        = keys j <= i with floor(i/64) - floor(j/64) <= window_blocks - 1
+ *                                                      (window_blocks  > 0)
+ *
+ * An empty key set gives o_i = 0.  The GELU is evaluated on the ALU only: the
+ * tanh is rewritten as a logistic function whose exponential is a range-reduced
+ * 6th-order Taylor polynomial (GDPA section: "ALU-only activation", valid
+ * because QK-norm bounds the scores).  It is within 1e-3 of the exact tanh-GELU
+ * for |s| <= 17 and saturates correctly beyond.
+ *
+ * Data layout (all pointers are device pointers unless named h_*):
+ *   q    bf16 [Tq,  H, D]   row-major, contiguous, Tq  = q_offsets[B]
+ *   k, v bf16 [Tkv, H, D]   row-major, contiguous, Tkv = kv_offsets[B]
+ *   out  bf16 [Tq,  H, D]   every row is written (zeros for empty key sets)
+ *   q_offsets, kv_offsets  int32 [B+1], offsets[0] = 0, non-decreasing
+ * q, k, v and out must be 16-byte aligned.  D must be 64 or 128.  Tq and Tkv
+ * must be below 2^31.  window_blocks > 0 requires q_offsets == kv_offsets and
+ * act == GDPA_ACT_SOFTMAX.
+ *
+ * Ownership: the caller owns every buffer it passes; the library never frees
+ * them and keeps no reference after the call returns (the GPU may still be
+ * reading them until the stream reaches the end of the launched work).  The
+ * library owns its plans and an internal per-device work-list buffer.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  All GPU work is enqueued on it.
+ *
+ * Errors: every entry point returns a gdpa_status_t and never throws or
+ * aborts.  Kernel-side failures (a bounded wait that ran out) are recorded in
+ * a device status word; gdpa_device_status() reads and clears it.
+ */
+#ifndef GDPA_H_
+#define GDPA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDPA_ACT_SOFTMAX = 0,   /* online softmax */
+  GDPA_ACT_GELU_TANH = 1  /* (1/Lkv) * sum gelu_tanh(s) v, ALU-only polynomial */
+} gdpa_act_t;
+
+typedef enum {
+  GDPA_OK = 0,
+  GDPA_ERR_INVALID_ARG = 1,    /* bad pointer, size, offsets or combination */
+  GDPA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  GDPA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  GDPA_ERR_DEVICE_TIMEOUT = 4, /* a kernel wait ran out of time (device status word) */
+  GDPA_ERR_NO_MEMORY = 5       /* host or device allocation failed, or capacity too small */
+} gdpa_status_t;
+
+/* One unit of GPU work: query rows [q0, q0+128) of sequence `seq`, head
+ * `head`, against keys from `kv0` (sequence-local) to the end of its key
+ * range.  Produced by the host tile planner (GDPA section: valid tiles are
+ * precomputed on the CPU, empty ones skipped, and spread over the SMs). */
+typedef struct {
+  int32_t seq;
+  int32_t head;
+  int32_t q0;
+  int32_t kv0;
+} gdpa_work_item_t;
+
+typedef struct gdpa_plan gdpa_plan_t;
+
+/*
+ * gdpa_fwd -- the whole forward pass in one call.
+ * q_offsets / kv_offsets are DEVICE pointers: the call copies them to the host
+ * (this synchronises `stream` once), plans the work list, uploads it to a
+ * library-owned device buffer and launches the kernel on `stream`.  `scale`
+ * multiplies every score.  Returns GDPA_OK once the kernel is enqueued.
+ */
+gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                       const int32_t* kv_offsets, int B, int H, int D, int act, int window_blocks,
+                       float scale, void* out, void* stream);
+
+/*
+ * gdpa_fwd_async -- the whole forward pass, fully asynchronous: the caller
+ * passes the offsets twice, as HOST arrays (h_*, read during the call to plan
+ * the work list; the caller may reuse them once the call returns) and as
+ * DEVICE arrays (read by the kernel, same values).  Planning runs on the
+ * calling thread while earlier work on `stream` is still executing; the work
+ * list goes up through a library-owned pinned buffer.  No synchronisation.
+ */
+gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                             const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
+                             int B, int H, int D, int act, int window_blocks, float scale, void* out,
+                             void* stream);
+
+/*
+ * gdpa_plan_create -- build a reusable plan from HOST offsets (the same
+ * arrays the caller will later pass on the device).  Allocates the plan and
+ * its device work list; *plan is NULL on failure.  Planning is host work:
+ * tile enumeration plus longest-processing-time-first balancing over the SMs
+ * of the current device.
+ */
+gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
+                               int D, int act, int window_blocks, gdpa_plan_t** plan);
+
+/*
+ * gdpa_fwd_planned -- launch the forward pass with a plan; fully asynchronous
+ * on `stream`.  The device offsets must hold the values the plan was built
+ * from (not checked on the device).
+ */
+gdpa_status_t gdpa_fwd_planned(const gdpa_plan_t* plan, const void* q, const void* k, const void* v,
+                               const int32_t* q_offsets, const int32_t* kv_offsets, float scale,
+                               void* out, void* stream);
+
+/* Frees the plan (synchronises the device if its buffers may be in use). */
+void gdpa_plan_destroy(gdpa_plan_t* plan);
+
+/* Number of work items / CTAs of a plan (for reporting); -1 on NULL. */
+int64_t gdpa_plan_num_items(const gdpa_plan_t* plan);
+int gdpa_plan_num_ctas(const gdpa_plan_t* plan);
+
+/*
+ * gdpa_fwd_host -- end-to-end call with HOST buffers: copies q, k, v and the
+ * offsets to library-owned device buffers on `stream`, runs the forward pass
+ * and copies `h_out` back, then synchronises `stream`.  Host buffers should be
+ * pinned (page-locked) for full copy bandwidth.
+ */
+gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const void* h_v, const int32_t* h_q_offsets,
+                            const int32_t* h_kv_offsets, int B, int H, int D, int act, int window_blocks,
+                            float scale, void* h_out, void* stream);
+
+/*
+ * gdpa_plan_enumerate -- the host planner alone, no GPU needed.  Fills
+ * `items` (capacity `capacity`) grouped by CTA and `cta_begin` [num_ctas+1]
+ * (items of CTA c are items[cta_begin[c] .. cta_begin[c+1])); `cost` (may be
+ * NULL) receives each item's estimated cost.  *n_items always receives the
+ * required count; GDPA_ERR_NO_MEMORY if it exceeds `capacity`.
+ */
+gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
+                                  int D, int act, int window_blocks, int num_ctas,
+                                  gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
+                                  int64_t* cost, int64_t* n_items);
+
+/*
+ * gdpa_act_eval -- evaluates the kernel's device activation elementwise:
+ * y[i] = gelu(x[i]) with the ALU-only polynomial (act = GDPA_ACT_GELU_TANH),
+ * or y[i] = 2^x[i] with the exponential the softmax path uses
+ * (act = GDPA_ACT_SOFTMAX).  x, y: device fp32 [n].  For accuracy tests.
+ */
+gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
+
+/*
+ * gdpa_device_status -- synchronises `stream`, then reads and clears the
+ * device status word of the current device.  Returns GDPA_OK or
+ * GDPA_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait; its output is
+ * undefined) or GDPA_ERR_CUDA.
+ */
+gdpa_status_t gdpa_device_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* gdpa_status_string(int status);
+
+/* Library version, e.g. "gdpa 0.1 sm_103a". */
+const char* gdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDPA_H_ */

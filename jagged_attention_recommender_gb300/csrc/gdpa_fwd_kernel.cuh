@@ -1,0 +1,498 @@
+// gdpa_fwd_kernel.cuh -- persistent, warp-specialised jagged GDPA forward
+// kernel for sm_103a (tcgen05 tensor cores, tensor memory, TMA).
+//
+// One CTA per SM walks its own list of work items (a 128-row query tile of
+// one (sequence, head) against its key range; built on the host, see
+// gdpa_plan.cpp).  Roles inside the CTA (192 threads):
+//
+//   warp 0      TMA producer: stages the Q tile (2 stages) and K, V tiles
+//               (NKV stages) into 128-byte-swizzled shared memory;
+//   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory
+//               (two S buffers), then O += P V with P read straight from
+//               tensor memory (two O buffers, one per in-flight item);
+//   warps 2..5  activation + epilogue, one query row per thread: reads S
+//               from TMEM, masks the ragged edge / window, applies the
+//               online softmax (running max with lazy rescaling of O) or the
+//               ALU-only GELU, writes P (bf16) back over S, and at the end of
+//               the item normalises O (1/l, or 1/Lkv for GELU) and stores it.
+//
+// The MMA issuer runs one K/V tile ahead: it issues S(g+1) = Q K(g+1)^T
+// before O += P(g) V(g), so the tensor core works on the next tile while the
+// activation warps process the current one, and this look-ahead crosses item
+// boundaries (the "outer loop" pipelining that matters when a key range is a
+// single tile: GDPA section of the techfeed summary of "GEM Training").
+//
+// Synchronisation is by mbarriers only; every wait is bounded in time and a
+// timeout is reported in the device status word instead of hanging.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "gelu_alu.cuh"
+#include "sm103_ptx.cuh"
+
+namespace gdpa {
+
+struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
+  CUtensorMap tm_q;  // 2-D view [T, H*D] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const int4* items;         // work items grouped by CTA: {seq, head, q0, kv0}
+  const int32_t* cta_begin;  // [gridDim.x + 1]
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  __nv_bfloat16* out;
+  int* status;               // device status word (bit set on a wait timeout)
+  unsigned long long timeout_ns;
+  int H;
+  int window_blocks;
+  float score_scale;         // softmax: scale * log2(e); GELU: scale
+};
+
+enum : int { kActSoftmax = 0, kActGelu = 1 };
+
+enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4 };
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int KCH = D / 64;               // 64-element (128-byte) column chunks
+  static constexpr int CHUNK_BYTES = 128 * 128;    // one chunk: 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;
+  static constexpr int NQ = 2;
+  static constexpr int NKV = (D == 64) ? 4 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NKV * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NKV * TILE_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 192;
+  static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Shared-memory barrier block.
+template <int NKV>
+struct Bars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[NKV], v_full[NKV], kv_empty[NKV];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done;
+  uint64_t o_empty[2];
+  uint64_t mma_drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct ItemView {
+  int h, q0, kv0, kv_end, n_kv, q_rows, q_tok, kv_tok, Lkv;
+};
+
+template <bool WIN>
+__device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
+  const int4 it = __ldg(p.items + idx);
+  ItemView v;
+  const int b = it.x;
+  v.h = it.y;
+  v.q0 = it.z;
+  v.kv0 = it.w;
+  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
+  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
+  v.q_tok = qs + v.q0;
+  v.kv_tok = ks;
+  v.Lkv = ke - ks;
+  v.q_rows = min(128, qe - qs - v.q0);
+  v.kv_end = WIN ? min(v.Lkv, v.q0 + 128) : v.Lkv;
+  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
+  return v;
+}
+
+__device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {
+  *abort = 1;
+  atomicOr(p.status, bit);
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D, bool WIN>
+__device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, int ibeg, int iend) {
+  using C = FwdCfg<D>;
+  volatile int* abort = &B.abort;
+  int qi = 0;
+  uint32_t g = 0;
+  bool ok = true;
+  int q_armed[2] = {-1, -1};            // last parity armed per Q stage (for draining)
+  int kv_armed[C::NKV];
+#pragma unroll
+  for (int s = 0; s < C::NKV; ++s) kv_armed[s] = -1;
+  ptx::prefetch_tensormap(&p.tm_q);
+  ptx::prefetch_tensormap(&p.tm_k);
+  ptx::prefetch_tensormap(&p.tm_v);
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const ItemView t = decode_item<WIN>(p, idx);
+    if (t.n_kv == 0) continue;
+    const int qs = qi & 1;
+    ok = ptx::mbar_wait(&B.q_empty[qs], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
+    if (!ok) break;
+    ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
+    q_armed[qs] = (qi >> 1) & 1;
+    uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
+#pragma unroll
+    for (int c = 0; c < C::KCH; ++c)
+      ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+    for (int j = 0; j < t.n_kv; ++j, ++g) {
+      const int s = g % C::NKV;
+      const uint32_t ph = (g / C::NKV) & 1;
+      ok = ptx::mbar_wait(&B.kv_empty[s], ph ^ 1, p.timeout_ns, abort);
+      if (!ok) break;
+      const int y = t.kv_tok + t.kv0 + 128 * j;
+      uint8_t* sk = sm + C::OFF_K + s * C::TILE_BYTES;
+      uint8_t* sv = sm + C::OFF_V + s * C::TILE_BYTES;
+      ptx::mbar_arrive_expect_tx(&B.k_full[s], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        ptx::tma_load_2d(sk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[s], t.h * D + 64 * c, y);
+      ptx::mbar_arrive_expect_tx(&B.v_full[s], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        ptx::tma_load_2d(sv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[s], t.h * D + 64 * c, y);
+      kv_armed[s] = (int)ph;
+    }
+    ++qi;
+  }
+  if (!ok) report_failure(p, abort, kStatusProducer);
+  // Let every bulk copy this thread started land before the CTA can exit.
+  const int never = 0;
+  const unsigned long long drain_ns = 100000000ull;
+  for (int s = 0; s < 2; ++s)
+    if (q_armed[s] >= 0) ptx::mbar_wait(&B.q_full[s], (uint32_t)q_armed[s], drain_ns, &never);
+#pragma unroll
+  for (int s = 0; s < C::NKV; ++s) {
+    if (kv_armed[s] >= 0) {
+      ptx::mbar_wait(&B.k_full[s], (uint32_t)kv_armed[s], drain_ns, &never);
+      ptx::mbar_wait(&B.v_full[s], (uint32_t)kv_armed[s], drain_ns, &never);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+struct PendingPV {
+  uint32_t g;
+  int s, sb, ob, qi, first, n16;
+};
+
+template <int D>
+__device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem,
+                                         const PendingPV& P) {
+  using C = FwdCfg<D>;
+  volatile int* abort = &B.abort;
+  if (!ptx::mbar_wait(&B.p_full[P.sb], (P.g >> 1) & 1, p.timeout_ns, abort)) return false;
+  if (P.first && !ptx::mbar_wait(&B.o_empty[P.ob], ((P.qi >> 1) & 1) ^ 1, p.timeout_ns, abort)) return false;
+  if (!ptx::mbar_wait(&B.v_full[P.s], (P.g / C::NKV) & 1, p.timeout_ns, abort)) return false;
+  ptx::tc_fence_after();
+  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + P.s * C::TILE_BYTES);
+  const uint32_t o_col = P.ob ? C::TM_O1 : C::TM_O0;
+  const uint32_t p_col = P.sb ? C::TM_S1 : C::TM_S0;
+  constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
+  for (int kk = 0; kk < P.n16; ++kk) {
+    // B = V tile, MN-major: 16 keys = two 8-row groups (SBO = 1024 B apart);
+    // the two 64-column halves of D sit one chunk apart (LBO).
+    const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::CHUNK_BYTES, 1024);
+    ptx::mma_ts(tmem + o_col, tmem + p_col + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
+  }
+  ptx::mma_commit(&B.kv_empty[P.s]);
+  ptx::mma_commit(&B.o_done);
+  return true;
+}
+
+template <int D, bool WIN>
+__device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem, int ibeg,
+                        int iend) {
+  using C = FwdCfg<D>;
+  volatile int* abort = &B.abort;
+  int qi = 0;
+  uint32_t g = 0;
+  bool ok = true;
+  bool have_prev = false;
+  PendingPV prev = {0, 0, 0, 0, 0, 0, 0};
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const ItemView t = decode_item<WIN>(p, idx);
+    if (t.n_kv == 0) continue;
+    const int qs = qi & 1;
+    ok = ptx::mbar_wait(&B.q_full[qs], (qi >> 1) & 1, p.timeout_ns, abort);
+    if (!ok) break;
+    const uint32_t q_base = ptx::smem_u32(sm + C::OFF_Q + qs * C::TILE_BYTES);
+    for (int j = 0; j < t.n_kv; ++j, ++g) {
+      const int s = g % C::NKV;
+      ok = ptx::mbar_wait(&B.k_full[s], (g / C::NKV) & 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int ncols = min(128, t.kv_end - t.kv0 - 128 * j);
+      const int n16 = (ncols + 15) >> 4;
+      const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + s * C::TILE_BYTES);
+      const int sb = g & 1;
+      const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
+        const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+        ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base + off, 16, 1024), ptx::sdesc_sw128(k_base + off, 16, 1024),
+                    idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(&B.s_full[sb]);
+      if (j == t.n_kv - 1) ptx::mma_commit(&B.q_empty[qs]);
+      if (have_prev) {
+        ok = issue_pv<D>(p, sm, B, tmem, prev);
+        if (!ok) break;
+      }
+      prev = PendingPV{g, s, sb, qi & 1, qi, j == 0 ? 1 : 0, n16};
+      have_prev = true;
+    }
+    ++qi;
+  }
+  if (ok && have_prev) ok = issue_pv<D>(p, sm, B, tmem, prev);
+  if (!ok) report_failure(p, abort, kStatusMma);
+  // Every MMA this thread issued is complete once this commit lands.
+  ptx::mma_commit(&B.mma_drain);
+  const int never = 0;
+  ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
+}
+
+// ------------------------------------------------------------------ activation + epilogue
+
+template <int D, int ACT, bool WIN>
+__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem, int ibeg, int iend,
+                               int warp, int lane) {
+  using C = FwdCfg<D>;
+  volatile int* abort = &B.abort;
+  const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const float sl = p.score_scale;
+  const int H = p.H;
+  int qi = 0;
+  uint32_t g = 0;
+  bool ok = true;
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const ItemView t = decode_item<WIN>(p, idx);
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + row) * H + t.h) * D;
+    if (t.n_kv == 0) {  // no keys: the output rows are zero
+      if (row < t.q_rows) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    const int ob = qi & 1;
+    const uint32_t o_col = ob ? C::TM_O1 : C::TM_O0;
+    float m_run = -INFINITY, l_run = 0.0f;
+    const int i_seq = t.q0 + row;  // query index inside its sequence
+    int win_lo = 0;
+    if (WIN) {
+      const int blk = i_seq / 64 - (p.window_blocks - 1);
+      win_lo = blk > 0 ? blk * 64 : 0;
+    }
+    for (int j = 0; j < t.n_kv; ++j, ++g) {
+      const int sb = g & 1;
+      ok = ptx::mbar_wait(&B.s_full[sb], (g >> 1) & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t s_addr = tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0);
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      ptx::tmem_wait_ld();
+      // valid key columns of this row: [c_lo, c_hi]
+      const int kv_t0 = t.kv0 + 128 * j;
+      int c_lo = 0, c_hi = min(128, t.kv_end - kv_t0) - 1;
+      if (WIN) {
+        c_lo = max(0, win_lo - kv_t0);
+        c_hi = min(c_hi, i_seq - kv_t0);
+      }
+      const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 127);
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (ACT == kActSoftmax) {
+        // Scores become log2-domain values x = s * scale * log2(e); masked
+        // columns become -inf.  With scale > 0 the scaling is folded into the
+        // exponent's FMA; otherwise it is applied first.
+        const bool fold = sl > 0.0f;
+        if (!fold) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * sl);
+        }
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < c_lo || c > c_hi) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], __uint_as_float(sr[c + u]));
+        }
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        if (fold) mx *= sl;
+        const float m_new = fmaxf(m_run, mx);
+        if (j == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
+          alpha = ptx::ex2_approx(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+          rescale = true;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+        const float mul = fold ? sl : 1.0f;
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float e = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + u]), mul, -m_use));
+            s4[u] += e;
+            sr[c + u] = __float_as_uint(e);
+          }
+        }
+        l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sr[c] = ptx::pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+      } else {  // GELU
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float a = gelu_tanh_alu(__uint_as_float(sr[2 * c]) * sl);
+          float b = gelu_tanh_alu(__uint_as_float(sr[2 * c + 1]) * sl);
+          if (!full) {
+            a = (2 * c >= c_lo && 2 * c <= c_hi) ? a : 0.0f;
+            b = (2 * c + 1 >= c_lo && 2 * c + 1 <= c_hi) ? b : 0.0f;
+          }
+          sr[c] = ptx::pack_bf16x2(a, b);
+        }
+      }
+      // P (bf16 pairs) overwrites the first 64 columns of this S buffer.
+      ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      ptx::tmem_wait_st();
+      if (g >= 1) {  // O += P(g-1) V(g-1) has landed
+        ok = ptx::mbar_wait(&B.o_done, (g - 1) & 1, p.timeout_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
+        ptx::tc_fence_after();
+        const uint32_t o_addr = tmem + lane_off + o_col;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(o_addr + 32 * c, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          ptx::tmem_st32(o_addr + 32 * c, r);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.p_full[sb]);
+    }
+    if (!ok) break;
+    // epilogue: wait for the item's last O += P V, normalise, store
+    ok = ptx::mbar_wait(&B.o_done, (g - 1) & 1, p.timeout_ns, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    float inv;
+    if (ACT == kActSoftmax)
+      inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    else
+      inv = 1.0f / static_cast<float>(t.Lkv);
+    const uint32_t o_addr = tmem + lane_off + o_col;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld32(o_addr + 32 * c, r);
+      ptx::tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+      if (row < t.q_rows) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&B.o_empty[ob]);
+    ++qi;
+  }
+  if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D, int ACT, bool WIN>
+__global__ void __launch_bounds__(192, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+  Bars<C::NKV>& B = *reinterpret_cast<Bars<C::NKV>*>(sm + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ibeg = p.cta_begin[blockIdx.x];
+  const int iend = p.cta_begin[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&B.q_full[i], 1);
+      ptx::mbar_init(&B.q_empty[i], 1);
+      ptx::mbar_init(&B.s_full[i], 1);
+      ptx::mbar_init(&B.p_full[i], 128);
+      ptx::mbar_init(&B.o_empty[i], 128);
+    }
+    for (int i = 0; i < C::NKV; ++i) {
+      ptx::mbar_init(&B.k_full[i], 1);
+      ptx::mbar_init(&B.v_full[i], 1);
+      ptx::mbar_init(&B.kv_empty[i], 1);
+    }
+    ptx::mbar_init(&B.o_done, 1);
+    ptx::mbar_init(&B.mma_drain, 1);
+    B.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&B.tmem_slot, C::TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = B.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<D, WIN>(p, sm, B, ibeg, iend);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+  } else {
+    run_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp, lane);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace gdpa

@@ -1,0 +1,54 @@
+// gdpa_internal.h -- declarations shared by the host side of libgdpa
+// (planner, API layer, kernel launchers).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/gdpa.h"
+
+namespace gdpa {
+
+constexpr int kBlockM = 128;      // query rows per work item (one tcgen05 M=128 tile)
+constexpr int kBlockN = 128;      // keys per K/V tile
+constexpr int kWindowBlock = 64;  // block size of the block-aligned window
+
+inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blocks) {
+  if (B < 0 || H <= 0 || window_blocks < 0) return GDPA_ERR_INVALID_ARG;
+  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH) return GDPA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GDPA_ERR_UNSUPPORTED;
+  if (window_blocks > 0 && act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if ((int64_t)H * D > (1 << 20)) return GDPA_ERR_UNSUPPORTED;
+  return GDPA_OK;
+}
+
+gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks,
+                               int64_t* Tq, int64_t* Tkv);
+
+gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
+                         int num_ctas, std::vector<gdpa_work_item_t>& items, std::vector<int32_t>& cta_begin,
+                         std::vector<int64_t>* cost);
+
+// Everything one launch of the forward kernel needs besides the tensor maps.
+struct LaunchArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const int32_t* q_off;   // device
+  const int32_t* kv_off;  // device
+  const gdpa_work_item_t* items;  // device, grouped by CTA
+  const int32_t* cta_begin;       // device [num_ctas + 1]
+  int num_ctas;
+  int64_t Tq, Tkv;
+  int H, D, act, window_blocks;
+  float scale;
+  void* stream;
+};
+
+// Defined in gdpa_kernels.cu.
+gdpa_status_t launch_forward(const LaunchArgs& a);
+gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
+gdpa_status_t read_and_clear_device_status(void* stream);
+
+}  // namespace gdpa

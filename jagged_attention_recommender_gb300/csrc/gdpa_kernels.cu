@@ -1,0 +1,169 @@
+// gdpa_kernels.cu -- kernel instantiations and launchers: TMA tensor-map
+// encoding, the device status word, the activation evaluation kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "gdpa_fwd_kernel.cuh"
+#include "gdpa_internal.h"
+
+namespace gdpa {
+
+// Device status word: bits set by kernels whose bounded waits ran out.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D view of a [rows, H, D] bf16 tensor as [rows, H*D]; boxes of 128 rows x
+// 64 columns (128 bytes, the swizzle width).  Rows past the end read as zero.
+gdpa_status_t encode_rows(CUtensorMap* m, const void* base, int64_t rows, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return GDPA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+int* status_ptr(int device) {
+  static std::mutex mu;
+  static int* ptrs[kMaxDevices] = {};
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[device] = static_cast<int*>(p);
+  }
+  return ptrs[device];
+}
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long ns = [] {
+    const char* e = std::getenv("GDPA_WAIT_TIMEOUT_MS");
+    long long ms = e ? std::atoll(e) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<unsigned long long>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+template <int D, int ACT, bool WIN>
+gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
+  using C = FwdCfg<D>;
+  static std::mutex mu;
+  static bool attr_done[kMaxDevices] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_done[device]) {
+      if (cudaFuncSetAttribute(gdpa_fwd_kernel<D, ACT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+      attr_done[device] = true;
+    }
+  }
+  gdpa_fwd_kernel<D, ACT, WIN><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+__global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = act == kActGelu ? gelu_tanh_alu(x[i]) : ptx::ex2_approx(x[i]);
+}
+
+}  // namespace
+
+gdpa_status_t launch_forward(const LaunchArgs& a) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (device < 0 || device >= kMaxDevices) return GDPA_ERR_UNSUPPORTED;
+  if (a.num_ctas <= 0 || a.Tq <= 0) return GDPA_OK;
+  int* status = status_ptr(device);
+  if (!status) return GDPA_ERR_CUDA;
+  FwdParams prm;
+  gdpa_status_t st = encode_rows(&prm.tm_q, a.q, a.Tq, a.H, a.D);
+  if (st != GDPA_OK) return st;
+  // With no keys at all no K/V tile is ever loaded; any valid address will do.
+  const void* kb = a.Tkv > 0 ? a.k : a.q;
+  const void* vb = a.Tkv > 0 ? a.v : a.q;
+  const int64_t kv_rows = a.Tkv > 0 ? a.Tkv : a.Tq;
+  if ((st = encode_rows(&prm.tm_k, kb, kv_rows, a.H, a.D)) != GDPA_OK) return st;
+  if ((st = encode_rows(&prm.tm_v, vb, kv_rows, a.H, a.D)) != GDPA_OK) return st;
+  prm.items = reinterpret_cast<const int4*>(a.items);
+  prm.cta_begin = a.cta_begin;
+  prm.q_off = a.q_off;
+  prm.kv_off = a.kv_off;
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.status = status;
+  prm.timeout_ns = wait_timeout_ns();
+  prm.H = a.H;
+  prm.window_blocks = a.window_blocks;
+  prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
+  cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+  const bool win = a.window_blocks > 0;
+  if (a.D == 128) {
+    if (a.act == GDPA_ACT_GELU_TANH) return launch_t<128, kActGelu, false>(prm, a.num_ctas, s, device);
+    return win ? launch_t<128, kActSoftmax, true>(prm, a.num_ctas, s, device)
+               : launch_t<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
+  }
+  if (a.D == 64) {
+    if (a.act == GDPA_ACT_GELU_TANH) return launch_t<64, kActGelu, false>(prm, a.num_ctas, s, device);
+    return win ? launch_t<64, kActSoftmax, true>(prm, a.num_ctas, s, device)
+               : launch_t<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
+  }
+  return GDPA_ERR_UNSUPPORTED;
+}
+
+gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream) {
+  if (n <= 0) return GDPA_OK;
+  const int threads = 256;
+  const int64_t want = (n + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+  act_eval_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(act, x, y, n);
+  return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+gdpa_status_t read_and_clear_device_status(void* stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return GDPA_ERR_CUDA;
+  int* status = status_ptr(device);
+  if (!status) return GDPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDPA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return GDPA_ERR_CUDA;
+    return GDPA_ERR_DEVICE_TIMEOUT;
+  }
+  return GDPA_OK;
+}
+
+}  // namespace gdpa

@@ -1,0 +1,167 @@
+// gdpa_plan.cpp -- host-side jagged tile planner.
+//
+// GDPA section of the techfeed summary of "GEM Training" (jagged tile
+// scheduling): the valid tiles are worked out on the CPU ahead of the launch,
+// empty tiles are never emitted, and the tiles are spread over the SMs so
+// that one long sequence cannot leave most SMs idle.  The pages balance with
+// a zigzag SM assignment; this planner uses longest-processing-time-first
+// (LPT) list scheduling over a min-heap of per-CTA loads, which bounds the
+// finish time by 4/3 of optimal and subsumes the zigzag order.
+//
+// Work unit: one 128-row query tile of one (sequence, head), against its key
+// range [kv0, kv_end):
+//   full attention : kv0 = 0, kv_end = Lkv
+//   block window W : kv0 = 64 * max(0, q0/64 - (W-1)), kv_end = min(L, q0 + 128)
+// Items whose key range is empty (Lkv = 0) are still emitted (cheap) because
+// their output rows must be zero-filled.
+#include "gdpa_internal.h"
+
+#include <algorithm>
+#include <climits>
+#include <cstring>
+#include <vector>
+
+namespace gdpa {
+
+gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks,
+                               int64_t* Tq, int64_t* Tkv) {
+  if (B < 0) return GDPA_ERR_INVALID_ARG;
+  if (B == 0) {
+    *Tq = 0;
+    *Tkv = 0;
+    return GDPA_OK;
+  }
+  if (!q_off || !kv_off) return GDPA_ERR_INVALID_ARG;
+  if (q_off[0] != 0 || kv_off[0] != 0) return GDPA_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return GDPA_ERR_INVALID_ARG;
+    if (window_blocks > 0 && (q_off[b + 1] != kv_off[b + 1])) return GDPA_ERR_INVALID_ARG;
+  }
+  *Tq = q_off[B];
+  *Tkv = kv_off[B];
+  return GDPA_OK;
+}
+
+// Estimated cost of one item, in units of "key columns of a 128-row tile".
+// A tile of n key columns costs its MMA + activation work (~n, padded to the
+// 16-column MMA granule) plus a fixed part for the query-tile load and the
+// epilogue store.
+static int64_t item_cost(int64_t kv_len) {
+  if (kv_len <= 0) return 8;
+  return ((kv_len + 15) / 16) * 16 + 96;
+}
+
+gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
+                         int num_ctas, std::vector<gdpa_work_item_t>& items_out,
+                         std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
+  if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
+  std::vector<gdpa_work_item_t> items;
+  std::vector<int64_t> cost;
+  int64_t n = 0;
+  for (int b = 0; b < B; ++b) n += (int64_t)((q_off[b + 1] - q_off[b] + kBlockM - 1) / kBlockM) * H;
+  items.reserve((size_t)n);
+  cost.reserve((size_t)n);
+  for (int b = 0; b < B; ++b) {
+    const int64_t Lq = q_off[b + 1] - q_off[b];
+    const int64_t Lkv = kv_off[b + 1] - kv_off[b];
+    for (int64_t q0 = 0; q0 < Lq; q0 += kBlockM) {
+      int64_t kv0 = 0, kv_end = Lkv;
+      if (window_blocks > 0) {
+        int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
+        kv0 = blk > 0 ? blk * kWindowBlock : 0;
+        kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
+      }
+      if (kv_end < kv0) kv_end = kv0;
+      const int64_t c = item_cost(kv_end - kv0);
+      for (int h = 0; h < H; ++h) {
+        items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});
+        cost.push_back(c);
+      }
+    }
+  }
+  // LPT: order by decreasing cost, then give each item to the CTA with the
+  // least load so far.  Costs are multiples of 16 (or the small constant of
+  // an empty item), so a stable bucket sort on cost/16 gives the order in
+  // O(n); ties keep sequence/head/tile order, so the tiles of one (sequence,
+  // head) land on different CTAs at about the same time and share its K/V
+  // through L2.  The least-loaded CTA comes from a tournament tree (min over
+  // a complete binary tree of per-CTA loads), O(log #CTAs) per item.
+  const size_t n_items = items.size();
+  int64_t max_bucket = 0;
+  for (size_t i = 0; i < n_items; ++i) max_bucket = std::max<int64_t>(max_bucket, cost[i] >> 4);
+  std::vector<uint32_t> order(n_items);
+  if (max_bucket <= (int64_t)4 * (int64_t)n_items + 1024) {
+    std::vector<uint32_t> start((size_t)max_bucket + 2, 0);
+    for (size_t i = 0; i < n_items; ++i) start[(size_t)(max_bucket - (cost[i] >> 4)) + 1]++;
+    for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
+    for (size_t i = 0; i < n_items; ++i) order[start[(size_t)(max_bucket - (cost[i] >> 4))]++] = (uint32_t)i;
+  } else {
+    for (size_t i = 0; i < n_items; ++i) order[i] = (uint32_t)i;
+    std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) { return cost[a] > cost[b]; });
+  }
+  int leaves = 1;
+  while (leaves < num_ctas) leaves <<= 1;
+  std::vector<int64_t> load(leaves, INT64_MAX);
+  for (int c = 0; c < num_ctas; ++c) load[c] = 0;
+  std::vector<int32_t> tree(2 * (size_t)leaves);  // tree[k] = CTA with the least load below node k
+  for (int c = 0; c < leaves; ++c) tree[leaves + c] = c;
+  for (int k = leaves - 1; k >= 1; --k) {
+    const int32_t a = tree[2 * k], b = tree[2 * k + 1];
+    tree[k] = load[b] < load[a] ? b : a;
+  }
+  std::vector<int32_t> owner(n_items);
+  std::vector<int64_t> count(num_ctas, 0);
+  for (size_t k = 0; k < n_items; ++k) {
+    const uint32_t idx = order[k];
+    const int32_t c = tree[1];
+    owner[idx] = c;
+    count[c]++;
+    load[c] += cost[idx];
+    for (size_t node = ((size_t)leaves + c) >> 1; node >= 1; node >>= 1) {
+      const int32_t a = tree[2 * node], b = tree[2 * node + 1];
+      tree[node] = load[b] < load[a] ? b : a;
+    }
+  }
+  cta_begin.assign((size_t)num_ctas + 1, 0);
+  for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + (int32_t)count[c];
+  std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
+  items_out.resize(items.size());
+  if (cost_out) cost_out->resize(items.size());
+  for (size_t k = 0; k < n_items; ++k) {  // within a CTA: decreasing cost (LPT order)
+    const uint32_t idx = order[k];
+    int32_t pos = fill[owner[idx]]++;
+    items_out[pos] = items[idx];
+    if (cost_out) (*cost_out)[pos] = cost[idx];
+  }
+  return GDPA_OK;
+}
+
+}  // namespace gdpa
+
+extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B,
+                                             int H, int D, int act, int window_blocks, int num_ctas,
+                                             gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
+                                             int64_t* cost, int64_t* n_items) {
+  if (n_items) *n_items = 0;
+  gdpa_status_t st = gdpa::validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  if (num_ctas <= 0 || !n_items || (capacity > 0 && !items) || !cta_begin) return GDPA_ERR_INVALID_ARG;
+  int64_t Tq = 0, Tkv = 0;
+  st = gdpa::validate_offsets(h_q_offsets, h_kv_offsets, B, window_blocks, &Tq, &Tkv);
+  if (st != GDPA_OK) return st;
+  std::vector<gdpa_work_item_t> v;
+  std::vector<int32_t> cb;
+  std::vector<int64_t> c;
+  try {
+    st = gdpa::plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, num_ctas, v, cb, &c);
+  } catch (...) {
+    return GDPA_ERR_NO_MEMORY;
+  }
+  if (st != GDPA_OK) return st;
+  *n_items = (int64_t)v.size();
+  if ((int64_t)v.size() > capacity) return GDPA_ERR_NO_MEMORY;
+  if (!v.empty()) std::memcpy(items, v.data(), v.size() * sizeof(gdpa_work_item_t));
+  std::memcpy(cta_begin, cb.data(), cb.size() * sizeof(int32_t));
+  if (cost && !c.empty()) std::memcpy(cost, c.data(), c.size() * sizeof(int64_t));
+  return GDPA_OK;
+}

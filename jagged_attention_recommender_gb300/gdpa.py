@@ -1,0 +1,206 @@
+"""Python binding of libgdpa (the C ABI in include/gdpa.h).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library.  Functions keep the C names.  Device tensors may be torch tensors or
+raw integer addresses; host arrays are numpy arrays.  A non-OK status raises
+:class:`GdpaError`.  If ``libgdpa.so`` has not been built the import of the
+library fails loudly -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdpa.so")
+
+GDPA_ACT_SOFTMAX = 0
+GDPA_ACT_GELU_TANH = 1
+
+GDPA_OK = 0
+GDPA_ERR_INVALID_ARG = 1
+GDPA_ERR_UNSUPPORTED = 2
+GDPA_ERR_CUDA = 3
+GDPA_ERR_DEVICE_TIMEOUT = 4
+GDPA_ERR_NO_MEMORY = 5
+
+# Every symbol include/gdpa.h declares.
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+           "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
+           "gdpa_status_string", "gdpa_version")
+
+
+class GdpaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s" % (where, gdpa_status_string(code)))
+
+
+class WorkItem(ctypes.Structure):
+    _fields_ = [("seq", ctypes.c_int32), ("head", ctypes.c_int32), ("q0", ctypes.c_int32), ("kv0", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgdpa.so (raises if it was never built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libgdpa.so is not built (%s); run jagged_attention_recommender_gb300.build" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.gdpa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
+    L.gdpa_fwd_async.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
+    L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
+    L.gdpa_fwd_planned.argtypes = [P, P, P, P, P, P, F, P, P]
+    L.gdpa_plan_destroy.argtypes = [P]
+    L.gdpa_plan_destroy.restype = None
+    L.gdpa_plan_num_items.argtypes = [P]
+    L.gdpa_plan_num_items.restype = I64
+    L.gdpa_plan_num_ctas.argtypes = [P]
+    L.gdpa_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
+    L.gdpa_plan_enumerate.argtypes = [P, P, I, I, I, I, I, I, P, I64, P, P, ctypes.POINTER(I64)]
+    L.gdpa_act_eval.argtypes = [I, P, P, I64, P]
+    L.gdpa_device_status.argtypes = [P]
+    L.gdpa_status_string.argtypes = [I]
+    L.gdpa_status_string.restype = ctypes.c_char_p
+    L.gdpa_version.argtypes = []
+    L.gdpa_version.restype = ctypes.c_char_p
+    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
+                 "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status"):
+        getattr(L, name).restype = I
+    _lib = L
+    return L
+
+
+def _addr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check(code: int, where: str):
+    if code != GDPA_OK:
+        raise GdpaError(code, where)
+
+
+def gdpa_status_string(code: int) -> str:
+    return lib().gdpa_status_string(int(code)).decode()
+
+
+def gdpa_version() -> str:
+    return lib().gdpa_version().decode()
+
+
+def gdpa_fwd(q, k, v, q_offsets, kv_offsets, B, H, D, act, window_blocks, scale, out, stream=None):
+    _check(lib().gdpa_fwd(_addr(q), _addr(k), _addr(v), _addr(q_offsets), _addr(kv_offsets), int(B), int(H),
+                          int(D), int(act), int(window_blocks), float(scale), _addr(out), _stream(stream)),
+           "gdpa_fwd")
+
+
+def gdpa_fwd_async(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, window_blocks, scale,
+                   out, stream=None):
+    """Host offsets (numpy int32) plan the work; device offsets feed the kernel.  No sync."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    _check(lib().gdpa_fwd_async(_addr(q), _addr(k), _addr(v), qo.ctypes.data, ko.ctypes.data, _addr(q_offsets),
+                                _addr(kv_offsets), int(B), int(H), int(D), int(act), int(window_blocks),
+                                float(scale), _addr(out), _stream(stream)), "gdpa_fwd_async")
+
+
+class Plan:
+    """Owns a gdpa_plan_t; freed by gdpa_plan_destroy (or when collected)."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    @property
+    def num_items(self) -> int:
+        return lib().gdpa_plan_num_items(self.handle)
+
+    @property
+    def num_ctas(self) -> int:
+        return lib().gdpa_plan_num_ctas(self.handle)
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            try:
+                lib().gdpa_plan_destroy(self.handle)
+            except Exception:
+                pass
+            self.handle = None
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def gdpa_plan_create(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks) -> Plan:
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    h = ctypes.c_void_p()
+    _check(lib().gdpa_plan_create(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
+                                  int(window_blocks), ctypes.byref(h)), "gdpa_plan_create")
+    return Plan(h.value)
+
+
+def gdpa_fwd_planned(plan: Plan, q, k, v, q_offsets, kv_offsets, scale, out, stream=None):
+    _check(lib().gdpa_fwd_planned(plan.handle, _addr(q), _addr(k), _addr(v), _addr(q_offsets), _addr(kv_offsets),
+                                  float(scale), _addr(out), _stream(stream)), "gdpa_fwd_planned")
+
+
+def gdpa_plan_destroy(plan: Plan):
+    if plan.handle:
+        lib().gdpa_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+def gdpa_fwd_host(h_q, h_k, h_v, h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, scale, h_out,
+                  stream=None):
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    _check(lib().gdpa_fwd_host(_addr(h_q), _addr(h_k), _addr(h_v), qo.ctypes.data, ko.ctypes.data, int(B),
+                               int(H), int(D), int(act), int(window_blocks), float(scale), _addr(h_out),
+                               _stream(stream)), "gdpa_fwd_host")
+
+
+def gdpa_plan_enumerate(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, num_ctas):
+    """Host planner only: returns (items [n, 4] int32, cta_begin [num_ctas+1], cost [n])."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    n = ctypes.c_int64(0)
+    cta = np.zeros(num_ctas + 1, dtype=np.int32)
+    code = lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
+                                     int(window_blocks), int(num_ctas), None, 0, cta.ctypes.data, None,
+                                     ctypes.byref(n))
+    if code not in (GDPA_OK, GDPA_ERR_NO_MEMORY):
+        raise GdpaError(code, "gdpa_plan_enumerate")
+    items = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    cost = np.zeros(max(n.value, 1), dtype=np.int64)
+    _check(lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
+                                     int(window_blocks), int(num_ctas), items.ctypes.data, n.value,
+                                     cta.ctypes.data, cost.ctypes.data, ctypes.byref(n)), "gdpa_plan_enumerate")
+    return items[:n.value], cta, cost[:n.value]
+
+
+def gdpa_act_eval(act, x, y, stream=None):
+    _check(lib().gdpa_act_eval(int(act), _addr(x), _addr(y), int(x.numel()), _stream(stream)), "gdpa_act_eval")
+
+
+def gdpa_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status code."""
+    return lib().gdpa_device_status(_stream(stream))

@@ -1,0 +1,130 @@
+"""Host-side tests of libgdpa (no GPU): the C ABI loads and exports every
+declared symbol, argument validation, and the jagged tile planner
+(coverage, key ranges, load balance)."""
+from __future__ import annotations
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+from jagged_attention_recommender_gb300 import build as gbuild
+from jagged_attention_recommender_gb300 import gdpa
+from jagged_attention_recommender_gb300.workloads import WORKLOADS, draw_lengths, offsets_of
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gbuild.build()
+    yield
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdpa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdpa_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_functions()
+    assert set(names) == set(gdpa.EXPORTS)
+    L = gdpa.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert gdpa.gdpa_version().startswith("gdpa")
+    assert gdpa.gdpa_status_string(0) == "GDPA_OK"
+    assert gdpa.gdpa_status_string(4) == "GDPA_ERR_DEVICE_TIMEOUT"
+    assert gdpa.gdpa_status_string(99) == "GDPA_ERR_UNKNOWN"
+
+
+def test_shape_validation_needs_no_gpu():
+    # rejected before any CUDA call
+    with pytest.raises(gdpa.GdpaError) as e:
+        gdpa.gdpa_fwd(0, 0, 0, 0, 0, 1, 1, 96, 0, 0, 1.0, 0, stream=0)
+    assert e.value.code == gdpa.GDPA_ERR_UNSUPPORTED
+    with pytest.raises(gdpa.GdpaError) as e:
+        gdpa.gdpa_fwd(0, 0, 0, 0, 0, 1, 0, 64, 0, 0, 1.0, 0, stream=0)
+    assert e.value.code == gdpa.GDPA_ERR_INVALID_ARG
+    with pytest.raises(gdpa.GdpaError) as e:  # GELU with a window is not implemented
+        gdpa.gdpa_fwd(0, 0, 0, 0, 0, 1, 1, 64, 1, 2, 1.0, 0, stream=0)
+    assert e.value.code == gdpa.GDPA_ERR_UNSUPPORTED
+    with pytest.raises(gdpa.GdpaError) as e:
+        gdpa.gdpa_fwd(0, 0, 0, 0, 0, 1, 1, 64, 7, 0, 1.0, 0, stream=0)
+    assert e.value.code == gdpa.GDPA_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    gdpa.gdpa_fwd(0, 0, 0, 0, 0, 0, 1, 64, 0, 0, 1.0, 0, stream=0)
+
+
+def test_enumerate_rejects_bad_offsets():
+    for qo, ko, wb in [([0, 5, 3], [0, 1, 2], 0),   # decreasing
+                       ([1, 5], [0, 5], 0),         # not starting at 0
+                       ([0, 5], [0, 4], 2)]:        # window needs equal offsets
+        with pytest.raises(gdpa.GdpaError) as e:
+            gdpa.gdpa_plan_enumerate(qo, ko, len(qo) - 1, 2, 64, 0, wb, 8)
+        assert e.value.code == gdpa.GDPA_ERR_INVALID_ARG
+
+
+def check_plan(Lq, Lkv, H, wb, num_ctas):
+    qo, ko = offsets_of(Lq), offsets_of(Lkv)
+    B = len(Lq)
+    items, cta, cost = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas)
+    n = len(items)
+    # CSR over CTAs
+    assert cta[0] == 0 and cta[-1] == n and np.all(np.diff(cta) >= 0)
+    # every (sequence, head, query row) is covered exactly once
+    cover = {}
+    for (b, h, q0, kv0) in items:
+        assert 0 <= b < B and 0 <= h < H and q0 % 128 == 0 and 0 <= q0 < Lq[b]
+        key = (int(b), int(h), int(q0))
+        assert key not in cover
+        cover[key] = int(kv0)
+    expect = {(b, h, q0) for b in range(B) for h in range(H) for q0 in range(0, int(Lq[b]), 128)}
+    assert set(cover) == expect
+    # key ranges: full attention starts at 0; a window tile starts at the first
+    # key any of its rows may see
+    for (b, h, q0), kv0 in cover.items():
+        if wb == 0:
+            assert kv0 == 0
+        else:
+            assert kv0 == max(0, (q0 // 64 - (wb - 1)) * 64)
+    # greedy list scheduling bound: max load <= mean load + largest item
+    loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(num_ctas)])
+    if n:
+        assert loads.max() <= cost.sum() / num_ctas + cost.max()
+        # LPT order inside each CTA: non-increasing cost
+        for c in range(num_ctas):
+            seg = cost[cta[c]:cta[c + 1]]
+            assert np.all(np.diff(seg) <= 0)
+    return items, cta, cost, loads
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_coverage_random(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 40))
+    Lq = rng.integers(0, 700, size=B)
+    Lkv = rng.integers(0, 700, size=B)
+    check_plan(Lq, Lkv, int(rng.integers(1, 5)), 0, int(rng.integers(1, 20)))
+
+
+@pytest.mark.parametrize("wb", [1, 2, 4, 9])
+def test_plan_coverage_window(wb):
+    rng = np.random.default_rng(wb)
+    L = rng.integers(0, 900, size=13)
+    check_plan(L, L, 2, wb, 7)
+
+
+def test_plan_empty_sequences():
+    items, cta, cost, _ = check_plan(np.array([0, 0, 5]), np.array([3, 0, 0]), 2, 0, 4)
+    assert len(items) == 2 and set(items[:, 0]) == {2}
+
+
+def test_plan_balances_the_long_jagged_workload():
+    w = WORKLOADS["self_long"]
+    Lq, Lkv = draw_lengths(w, np.random.default_rng(w.seed))
+    _, _, cost, loads = check_plan(Lq, Lkv, w.H, 0, 152)
+    # skew (max / mean CTA load) stays close to 1
+    assert loads.max() / loads.mean() < 1.05
