@@ -79,14 +79,25 @@ def run_gpu(batch, entry="fwd", guard_rows=0):
     return res
 
 
-def assert_parity(got, ref, what=""):
+def assert_parity(got, ref, what="", bf16_scaled=False):
+    """The workload bar: max |d| <= 1e-2 and rel-L2 <= 5e-3.
+
+    With ``bf16_scaled`` (edge cases whose outputs are large, e.g. one key with
+    a GELU score near 16) the absolute bar grows by one bf16 ulp of the value,
+    2^-8 |o|: rounding the exact result to bf16 alone errs by up to 2^-9 |o|,
+    which exceeds 1e-2 once |o| > 5.
+    """
     assert got.shape == ref.shape
     assert np.isfinite(got).all(), "non-finite output " + what
-    err = np.abs(got - ref).max() if got.size else 0.0
+    if not got.size:
+        return 0.0, 0.0
+    d = np.abs(got - ref)
+    bar = MAX_ABS + (np.abs(ref) * 2.0 ** -8 if bf16_scaled else 0.0)
+    worst = np.unravel_index(np.argmax(d - bar), d.shape)
     rl2 = rel_l2(got, ref)
-    assert err <= MAX_ABS, "%s max abs err %.3e" % (what, err)
+    assert np.all(d <= bar), "%s max abs err %.3e at %s (|ref| %.3g)" % (what, d[worst], worst, abs(ref[worst]))
     assert rl2 <= REL_L2, "%s rel L2 err %.3e" % (what, rl2)
-    return err, rl2
+    return float(d.max()), rl2
 
 
 # ------------------------------------------------------------------ activation functions
@@ -160,7 +171,7 @@ def test_edge_lengths_cross_gelu(D):
     Lq = np.array([1, 129, 300, 0, 64, 77, 128])
     Lkv = np.array([0, 1, 8, 5, 64, 65, 300])  # empty KV, one key, several K/V tiles
     b = small_batch(rng, Lq, Lkv, 2, D, act=ACT_GELU_TANH, qk_norm=True, scale=1.0)
-    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "cross gelu D=%d" % D)
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "cross gelu D=%d" % D, bf16_scaled=True)
 
 
 @pytest.mark.parametrize("D", [64, 128])
