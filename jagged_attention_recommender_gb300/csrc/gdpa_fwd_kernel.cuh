@@ -5,8 +5,9 @@
 // one (sequence, head) against its key range; built on the host, see
 // gdpa_plan.cpp).  Roles inside the CTA (192 threads):
 //
-//   warp 0      TMA producer: stages the Q tile (2 stages) and K, V tiles
-//               (NKV stages) into 128-byte-swizzled shared memory;
+//   warp 0      TMA producer: stages the Q tile (2 stages), K tiles (NK
+//               stages) and V tiles (NV stages) into 128-byte-swizzled
+//               shared memory; K is released after Q K^T, V after P V;
 //   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory
 //               (two S buffers), then O += P V with P read straight from
 //               tensor memory (two O buffers, one per in-flight item);
@@ -63,11 +64,12 @@ struct FwdCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;    // one chunk: 128 rows x 128 bytes
   static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;
   static constexpr int NQ = 2;
-  static constexpr int NKV = (D == 64) ? 4 : 2;
+  static constexpr int NK = (D == 64) ? 4 : 3;   // K stages
+  static constexpr int NV = (D == 64) ? 4 : 2;   // V stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NKV * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NKV * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
@@ -78,10 +80,10 @@ struct FwdCfg {
 };
 
 // Shared-memory barrier block.
-template <int NKV>
+template <int NK, int NV>
 struct Bars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[NKV], v_full[NKV], kv_empty[NKV];
+  uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
   uint64_t o_empty[2];
@@ -121,16 +123,18 @@ __device__ __forceinline__ void report_failure(const FwdParams& p, volatile int*
 // ------------------------------------------------------------------ producer
 
 template <int D, bool WIN>
-__device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, int ibeg, int iend) {
+__device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, int ibeg, int iend) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
   int q_armed[2] = {-1, -1};            // last parity armed per Q stage (for draining)
-  int kv_armed[C::NKV];
+  int k_armed[C::NK], v_armed[C::NV];
 #pragma unroll
-  for (int s = 0; s < C::NKV; ++s) kv_armed[s] = -1;
+  for (int s = 0; s < C::NK; ++s) k_armed[s] = -1;
+#pragma unroll
+  for (int s = 0; s < C::NV; ++s) v_armed[s] = -1;
   ptx::prefetch_tensormap(&p.tm_q);
   ptx::prefetch_tensormap(&p.tm_k);
   ptx::prefetch_tensormap(&p.tm_v);
@@ -147,22 +151,27 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
     for (int c = 0; c < C::KCH; ++c)
       ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
-      const int s = g % C::NKV;
-      const uint32_t ph = (g / C::NKV) & 1;
-      ok = ptx::mbar_wait(&B.kv_empty[s], ph ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
+      const int sk_i = g % C::NK, sv_i = g % C::NV;
+      const uint32_t phk = (g / C::NK) & 1, phv = (g / C::NV) & 1;
       const int y = t.kv_tok + t.kv0 + 128 * j;
-      uint8_t* sk = sm + C::OFF_K + s * C::TILE_BYTES;
-      uint8_t* sv = sm + C::OFF_V + s * C::TILE_BYTES;
-      ptx::mbar_arrive_expect_tx(&B.k_full[s], C::TILE_BYTES);
+      uint8_t* sk = sm + C::OFF_K + sk_i * C::TILE_BYTES;
+      uint8_t* sv = sm + C::OFF_V + sv_i * C::TILE_BYTES;
+      // K is released once its Q K^T is done, V once its P V is done, so the
+      // next K tile streams in while the current P V still runs.
+      ok = ptx::mbar_wait(&B.k_empty[sk_i], phk ^ 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::mbar_arrive_expect_tx(&B.k_full[sk_i], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[s], t.h * D + 64 * c, y);
-      ptx::mbar_arrive_expect_tx(&B.v_full[s], C::TILE_BYTES);
+        ptx::tma_load_2d(sk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[sk_i], t.h * D + 64 * c, y);
+      k_armed[sk_i] = (int)phk;
+      ok = ptx::mbar_wait(&B.v_empty[sv_i], phv ^ 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::mbar_arrive_expect_tx(&B.v_full[sv_i], C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[s], t.h * D + 64 * c, y);
-      kv_armed[s] = (int)ph;
+        ptx::tma_load_2d(sv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[sv_i], t.h * D + 64 * c, y);
+      v_armed[sv_i] = (int)phv;
     }
     ++qi;
   }
@@ -173,31 +182,31 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
   for (int s = 0; s < 2; ++s)
     if (q_armed[s] >= 0) ptx::mbar_wait(&B.q_full[s], (uint32_t)q_armed[s], drain_ns, &never);
 #pragma unroll
-  for (int s = 0; s < C::NKV; ++s) {
-    if (kv_armed[s] >= 0) {
-      ptx::mbar_wait(&B.k_full[s], (uint32_t)kv_armed[s], drain_ns, &never);
-      ptx::mbar_wait(&B.v_full[s], (uint32_t)kv_armed[s], drain_ns, &never);
-    }
-  }
+  for (int s = 0; s < C::NK; ++s)
+    if (k_armed[s] >= 0) ptx::mbar_wait(&B.k_full[s], (uint32_t)k_armed[s], drain_ns, &never);
+#pragma unroll
+  for (int s = 0; s < C::NV; ++s)
+    if (v_armed[s] >= 0) ptx::mbar_wait(&B.v_full[s], (uint32_t)v_armed[s], drain_ns, &never);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
 struct PendingPV {
   uint32_t g;
-  int s, sb, ob, qi, first, n16;
+  int sb, ob, qi, first, n16;
 };
 
 template <int D>
-__device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem,
+__device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem,
                                          const PendingPV& P) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   if (!ptx::mbar_wait(&B.p_full[P.sb], (P.g >> 1) & 1, p.timeout_ns, abort)) return false;
   if (P.first && !ptx::mbar_wait(&B.o_empty[P.ob], ((P.qi >> 1) & 1) ^ 1, p.timeout_ns, abort)) return false;
-  if (!ptx::mbar_wait(&B.v_full[P.s], (P.g / C::NKV) & 1, p.timeout_ns, abort)) return false;
+  const int sv = P.g % C::NV;
+  if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
-  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + P.s * C::TILE_BYTES);
+  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::TILE_BYTES);
   const uint32_t o_col = P.ob ? C::TM_O1 : C::TM_O0;
   const uint32_t p_col = P.sb ? C::TM_S1 : C::TM_S0;
   constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
@@ -207,13 +216,13 @@ __device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<F
     const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::CHUNK_BYTES, 1024);
     ptx::mma_ts(tmem + o_col, tmem + p_col + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
   }
-  ptx::mma_commit(&B.kv_empty[P.s]);
+  ptx::mma_commit(&B.v_empty[sv]);
   ptx::mma_commit(&B.o_done);
   return true;
 }
 
 template <int D, bool WIN>
-__device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem, int ibeg,
+__device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem, int ibeg,
                         int iend) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
@@ -221,7 +230,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B
   uint32_t g = 0;
   bool ok = true;
   bool have_prev = false;
-  PendingPV prev = {0, 0, 0, 0, 0, 0, 0};
+  PendingPV prev = {0, 0, 0, 0, 0, 0};
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<WIN>(p, idx);
     if (t.n_kv == 0) continue;
@@ -230,8 +239,8 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B
     if (!ok) break;
     const uint32_t q_base = ptx::smem_u32(sm + C::OFF_Q + qs * C::TILE_BYTES);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
-      const int s = g % C::NKV;
-      ok = ptx::mbar_wait(&B.k_full[s], (g / C::NKV) & 1, p.timeout_ns, abort);
+      const int s = g % C::NK;
+      ok = ptx::mbar_wait(&B.k_full[s], (g / C::NK) & 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::tc_fence_after();
       const int ncols = min(128, t.kv_end - t.kv0 - 128 * j);
@@ -248,12 +257,13 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B
                     idesc, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(&B.s_full[sb]);
+      ptx::mma_commit(&B.k_empty[s]);
       if (j == t.n_kv - 1) ptx::mma_commit(&B.q_empty[qs]);
       if (have_prev) {
         ok = issue_pv<D>(p, sm, B, tmem, prev);
         if (!ok) break;
       }
-      prev = PendingPV{g, s, sb, qi & 1, qi, j == 0 ? 1 : 0, n16};
+      prev = PendingPV{g, sb, qi & 1, qi, j == 0 ? 1 : 0, n16};
       have_prev = true;
     }
     ++qi;
@@ -269,7 +279,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NKV>& B
 // ------------------------------------------------------------------ activation + epilogue
 
 template <int D, int ACT, bool WIN>
-__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NKV>& B, uint32_t tmem, int ibeg, int iend,
+__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem, int ibeg, int iend,
                                int warp, int lane) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_fwd_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
-  Bars<C::NKV>& B = *reinterpret_cast<Bars<C::NKV>*>(sm + C::OFF_BAR);
+  Bars<C::NK, C::NV>& B = *reinterpret_cast<Bars<C::NK, C::NV>*>(sm + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ibeg = p.cta_begin[blockIdx.x];
@@ -462,10 +472,13 @@ __global__ void __launch_bounds__(192, 1) gdpa_fwd_kernel(const __grid_constant_
       ptx::mbar_init(&B.p_full[i], 128);
       ptx::mbar_init(&B.o_empty[i], 128);
     }
-    for (int i = 0; i < C::NKV; ++i) {
+    for (int i = 0; i < C::NK; ++i) {
       ptx::mbar_init(&B.k_full[i], 1);
+      ptx::mbar_init(&B.k_empty[i], 1);
+    }
+    for (int i = 0; i < C::NV; ++i) {
       ptx::mbar_init(&B.v_full[i], 1);
-      ptx::mbar_init(&B.kv_empty[i], 1);
+      ptx::mbar_init(&B.v_empty[i], 1);
     }
     ptx::mbar_init(&B.o_done, 1);
     ptx::mbar_init(&B.mma_drain, 1);

@@ -83,16 +83,18 @@ def assert_parity(got, ref, what="", bf16_scaled=False):
     """The workload bar: max |d| <= 1e-2 and rel-L2 <= 5e-3.
 
     With ``bf16_scaled`` (edge cases whose outputs are large, e.g. one key with
-    a GELU score near 16) the absolute bar grows by one bf16 ulp of the value,
-    2^-8 |o|: rounding the exact result to bf16 alone errs by up to 2^-9 |o|,
-    which exceeds 1e-2 once |o| > 5.
+    a GELU score near 16, |o| ~ 10-30) the absolute bar grows by 2^-7 |o|:
+    P is rounded to bf16 before P.V (relative error up to 2^-9) and the output
+    is rounded to bf16 (up to half an ulp, which is up to 2^-8 |o|), so the
+    exact result can legitimately move by about 1.5 * 2^-8 |o|, more than 1e-2
+    once |o| > 2.6.
     """
     assert got.shape == ref.shape
     assert np.isfinite(got).all(), "non-finite output " + what
     if not got.size:
         return 0.0, 0.0
     d = np.abs(got - ref)
-    bar = MAX_ABS + (np.abs(ref) * 2.0 ** -8 if bf16_scaled else 0.0)
+    bar = MAX_ABS + (np.abs(ref) * 2.0 ** -7 if bf16_scaled else 0.0)
     worst = np.unravel_index(np.argmax(d - bar), d.shape)
     rl2 = rel_l2(got, ref)
     assert np.all(d <= bar), "%s max abs err %.3e at %s (|ref| %.3g)" % (what, d[worst], worst, abs(ref[worst]))
