@@ -68,9 +68,10 @@ typedef enum {
   GDPA_ERR_NO_MEMORY = 5       /* host or device allocation failed, or capacity too small */
 } gdpa_status_t;
 
-/* One unit of GPU work: query rows [q0, q0+128) of sequence `seq`, head
- * `head`, against keys from `kv0` (sequence-local) to the end of its key
- * range.  Produced by the host tile planner (GDPA section: valid tiles are
+/* One unit of GPU work: query rows [q0, q0+R) of sequence `seq`, head
+ * `head` (R = 128, or 256 for full attention over sequences averaging more
+ * than 128 queries), against keys from `kv0` (sequence-local) to the end of
+ * its key range.  Produced by the host tile planner (GDPA section: valid tiles are
  * precomputed on the CPU, empty ones skipped, and spread over the SMs). */
 typedef struct {
   int32_t seq;
@@ -145,13 +146,14 @@ gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const void* h_v, c
  * gdpa_plan_enumerate -- the host planner alone, no GPU needed.  Fills
  * `items` (capacity `capacity`) grouped by CTA and `cta_begin` [num_ctas+1]
  * (items of CTA c are items[cta_begin[c] .. cta_begin[c+1])); `cost` (may be
- * NULL) receives each item's estimated cost.  *n_items always receives the
- * required count; GDPA_ERR_NO_MEMORY if it exceeds `capacity`.
+ * NULL) receives each item's estimated cost; `rows_per_item` (may be NULL)
+ * receives R.  *n_items always receives the required count;
+ * GDPA_ERR_NO_MEMORY if it exceeds `capacity`.
  */
 gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
                                   int D, int act, int window_blocks, int num_ctas,
                                   gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
-                                  int64_t* cost, int64_t* n_items);
+                                  int64_t* cost, int64_t* n_items, int32_t* rows_per_item);
 
 /*
  * gdpa_act_eval -- evaluates the kernel's device activation elementwise:
@@ -168,6 +170,16 @@ gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* 
  * undefined) or GDPA_ERR_CUDA.
  */
 gdpa_status_t gdpa_device_status(void* stream);
+
+/*
+ * gdpa_wait_selftest -- launches one thread that waits, with the same
+ * bounded mbarrier wait every role of the forward kernel uses, on a barrier
+ * nothing ever arrives on.  After `timeout_ms` (1..10000) the wait gives up
+ * and sets the device status word; gdpa_device_status() then returns
+ * GDPA_ERR_DEVICE_TIMEOUT and the context stays usable.  For tests of the
+ * failure path: no fault, trap or hang is involved.
+ */
+gdpa_status_t gdpa_wait_selftest(int timeout_ms, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* gdpa_status_string(int status);

@@ -2,6 +2,8 @@
 // validation, planning, library-owned buffers, launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -12,6 +14,7 @@
 struct gdpa_plan {
   int B, H, D, act, window_blocks;
   int num_ctas;
+  int rows_per_item;
   int device;
   int64_t n_items, Tq, Tkv;
   void* d_buf;  // work items followed by cta_begin
@@ -23,6 +26,8 @@ namespace gdpa {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxChunks = 8;                        // gdpa_fwd_host pipeline depth
+constexpr double kChunkBytes = 64.0 * (1 << 20);     // target bytes in + out per chunk
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -71,10 +76,27 @@ struct DeviceCtx {
   std::mutex mu;
   Buf h_stage{nullptr, 0, true};  // pinned: offsets in, work list out
   Buf d_work;                     // device work list + cta_begin
-  Buf d_io;                       // gdpa_fwd_host: q, k, v, out, offsets
+  Buf d_io;                       // gdpa_fwd_host: q, k, v, out, offsets, work lists
+  Buf h_io{nullptr, 0, true};     // gdpa_fwd_host: pinned offsets + work lists
   cudaEvent_t stage_free = nullptr;  // host staging buffer may be overwritten
   cudaEvent_t work_free = nullptr;   // device buffers no longer read by an earlier launch
   bool events_ok = false;
+  // gdpa_fwd_host pipeline: copy-in and copy-out streams, per-chunk events
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[kMaxChunks] = {}, ev_done[kMaxChunks] = {};
+  bool host_path_ok = false;
+  gdpa_status_t init_host_path() {
+    if (host_path_ok) return GDPA_OK;
+    if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
+    for (int i = 0; i < kMaxChunks; ++i)
+      if (cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+    host_path_ok = true;
+    return GDPA_OK;
+  }
   gdpa_status_t init() {
     if (events_ok) return GDPA_OK;
     if (cudaEventCreateWithFlags(&stage_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
@@ -96,11 +118,14 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Plans on the host and uploads the work list through the pinned staging
 // buffer into c.d_work (both guarded by events against earlier calls).
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
-                              int window_blocks, int sms, cudaStream_t stream, int* num_ctas) {
+                              int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
+                              int64_t* n_items) {
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
-  int64_t n = 0;
-  for (int b = 0; b < B; ++b) n += (int64_t)((h_q_off[b + 1] - h_q_off[b] + kBlockM - 1) / kBlockM) * H;
+  const int rpi = choose_rows_per_item(h_q_off, B, window_blocks);
+  const int64_t n = count_plan_items(h_q_off, B, H, rpi);
+  *rows_per_item = rpi;
+  *n_items = n;
   if (n == 0) {
     *num_ctas = 0;
     return GDPA_OK;
@@ -108,7 +133,7 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   const int ctas = (int)(n < sms ? n : sms);
   gdpa_status_t st;
   try {
-    st = plan_items(h_q_off, h_kv_off, B, H, window_blocks, ctas, items, cta_begin, nullptr);
+    st = plan_items(h_q_off, h_kv_off, B, H, window_blocks, rpi, ctas, items, cta_begin, nullptr);
   } catch (const std::bad_alloc&) {
     return GDPA_ERR_NO_MEMORY;
   }
@@ -133,9 +158,10 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
 
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
                               const int32_t* d_q_off, const int32_t* d_kv_off, int64_t Tq, int64_t Tkv, int H, int D,
-                              int act, int window_blocks, float scale, int num_ctas, int64_t n_items,
-                              cudaStream_t stream) {
+                              int act, int window_blocks, float scale, int num_ctas, int rows_per_item,
+                              int64_t n_items, cudaStream_t stream) {
   LaunchArgs a;
+  a.rows_per_item = rows_per_item;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -159,11 +185,6 @@ gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const 
   return cudaEventRecord(c.work_free, stream) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
-int64_t count_items(const int32_t* h_q_off, int B, int H) {
-  int64_t n = 0;
-  for (int b = 0; b < B; ++b) n += (int64_t)((h_q_off[b + 1] - h_q_off[b] + kBlockM - 1) / kBlockM) * H;
-  return n;
-}
 
 gdpa_status_t check_tensors(const void* q, const void* k, const void* v, const void* out, int64_t Tq, int64_t Tkv) {
   if (Tq > 0 && (!q || !out || !aligned16(q) || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
@@ -205,10 +226,11 @@ extern "C" gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, c
   if ((st = validate_offsets(hq, hk, B, window_blocks, &Tq, &Tkv)) != GDPA_OK) return st;
   if ((st = check_tensors(q, k, v, out, Tq, Tkv)) != GDPA_OK) return st;
   if (Tq == 0) return GDPA_OK;
-  int num_ctas = 0;
-  if ((st = plan_and_upload(c, hq, hk, B, H, window_blocks, sms, s, &num_ctas)) != GDPA_OK) return st;
+  int num_ctas = 0, rpi = 0;
+  int64_t n_items = 0;
+  if ((st = plan_and_upload(c, hq, hk, B, H, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK) return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                         count_items(hq, B, H), s);
+                         rpi, n_items, s);
 }
 
 extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
@@ -229,11 +251,13 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
   std::lock_guard<std::mutex> lock(c.mu);
   if ((st = c.init()) != GDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int num_ctas = 0;
-  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, window_blocks, sms, s, &num_ctas)) != GDPA_OK)
+  int num_ctas = 0, rpi = 0;
+  int64_t n_items = 0;
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) !=
+      GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                         count_items(h_q_offsets, B, H), s);
+                         rpi, n_items, s);
 }
 
 extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
@@ -260,14 +284,16 @@ extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int3
   P->d_buf = nullptr;
   P->d_items = nullptr;
   P->d_cta_begin = nullptr;
-  const int64_t n = B > 0 ? count_items(h_q_offsets, B, H) : 0;
+  P->rows_per_item = choose_rows_per_item(h_q_offsets, B, window_blocks);
+  const int64_t n = B > 0 ? count_plan_items(h_q_offsets, B, H, P->rows_per_item) : 0;
   P->n_items = n;
   P->num_ctas = (int)(n < sms ? n : sms);
   if (n > 0) {
     std::vector<gdpa_work_item_t> items;
     std::vector<int32_t> cta_begin;
     try {
-      st = plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, P->num_ctas, items, cta_begin, nullptr);
+      st = plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, P->rows_per_item, P->num_ctas, items, cta_begin,
+                      nullptr);
     } catch (const std::bad_alloc&) {
       st = GDPA_ERR_NO_MEMORY;
     }
@@ -318,6 +344,7 @@ extern "C" gdpa_status_t gdpa_fwd_planned(const gdpa_plan_t* plan, const void* q
   a.items = plan->d_items;
   a.cta_begin = plan->d_cta_begin;
   a.num_ctas = plan->num_ctas;
+  a.rows_per_item = plan->rows_per_item;
   a.Tq = plan->Tq;
   a.Tkv = plan->Tkv;
   a.H = plan->H;
@@ -338,6 +365,11 @@ extern "C" void gdpa_plan_destroy(gdpa_plan_t* plan) {
 extern "C" int64_t gdpa_plan_num_items(const gdpa_plan_t* plan) { return plan ? plan->n_items : -1; }
 extern "C" int gdpa_plan_num_ctas(const gdpa_plan_t* plan) { return plan ? plan->num_ctas : -1; }
 
+// End-to-end call with host buffers.  The batch is cut into up to 8 chunks of
+// whole sequences (~64 MB of input + output each); chunk i's inputs stream in
+// on a copy stream while chunk i-1 computes on `stream` and chunk i-2's
+// output streams back on a second copy stream.  Planning of each chunk runs
+// on the host while the copies are in flight.
 extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const void* h_v, const int32_t* h_q_offsets,
                                        const int32_t* h_kv_offsets, int B, int H, int D, int act, int window_blocks,
                                        float scale, void* h_out, void* stream) {
@@ -353,40 +385,142 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
   if ((st = num_sms(&device, &sms)) != GDPA_OK) return st;
   DeviceCtx& c = ctx(device);
   std::lock_guard<std::mutex> lock(c.mu);
-  if ((st = c.init()) != GDPA_OK) return st;
+  if ((st = c.init()) != GDPA_OK || (st = c.init_host_path()) != GDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row = (size_t)H * D * 2;
+  const int32_t* qo = h_q_offsets;
+  const int32_t* ko = h_kv_offsets;
+
+  // chunk boundaries (sequence indices), balanced by bytes moved
+  const double total = (double)(2 * Tq + 2 * Tkv) * (double)row;
+  int C = (int)std::min<double>(kMaxChunks, std::max(1.0, std::floor(total / kChunkBytes)));
+  if (C > B) C = B;
+  int cut[kMaxChunks + 1];
+  cut[0] = 0;
+  cut[C] = B;
+  {
+    int b = 0;
+    double acc = 0.0;
+    for (int i = 1; i < C; ++i) {
+      const double goal = total * i / C;
+      while (b < B - (C - i) && (acc < goal || b < cut[i - 1] + 1)) {
+        acc += (double)(2 * (qo[b + 1] - qo[b]) + 2 * (ko[b + 1] - ko[b])) * (double)row;
+        ++b;
+      }
+      cut[i] = b;
+    }
+  }
+  // per-chunk sizes of the rebased offsets and work lists
+  int64_t n_items[kMaxChunks];
+  int ctas[kMaxChunks], rpi[kMaxChunks];
+  size_t off_at[kMaxChunks], work_at[kMaxChunks], item_bytes[kMaxChunks];
+  size_t meta = 0;
+  for (int i = 0; i < C; ++i) {
+    const int nb = cut[i + 1] - cut[i];
+    // rows per item depend only on the lengths, which rebasing keeps
+    std::vector<int32_t> tmp(nb + 1);
+    for (int b = 0; b <= nb; ++b) tmp[b] = qo[cut[i] + b] - qo[cut[i]];
+    rpi[i] = choose_rows_per_item(tmp.data(), nb, window_blocks);
+    const int64_t n = count_plan_items(tmp.data(), nb, H, rpi[i]);
+    n_items[i] = n;
+    ctas[i] = (int)(n < sms ? n : sms);
+    off_at[i] = meta;
+    meta += align_up(2 * ((size_t)nb + 1) * sizeof(int32_t), 256);
+    work_at[i] = meta;
+    item_bytes[i] = align_up((size_t)n * sizeof(gdpa_work_item_t), 16);
+    meta += align_up(item_bytes[i] + ((size_t)ctas[i] + 1) * sizeof(int32_t), 256);
+  }
   const size_t bq = align_up((size_t)Tq * row, 256), bkv = align_up((size_t)Tkv * row, 256);
-  const size_t boff = align_up(((size_t)B + 1) * sizeof(int32_t), 256);
-  const size_t total = 2 * bq + 2 * bkv + 2 * boff;
-  if (c.d_io.cap < total) {
+  const size_t need = 2 * bq + 2 * bkv + meta;
+  if (c.d_io.cap < need) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;
-    if ((st = c.d_io.ensure(total)) != GDPA_OK) return st;
+    if ((st = c.d_io.ensure(need)) != GDPA_OK) return st;
   }
+  if ((st = c.h_io.ensure(meta)) != GDPA_OK) return st;
   char* base = static_cast<char*>(c.d_io.p);
-  void* dq = base;
-  void* dout = base + bq;
-  void* dk = base + 2 * bq;
-  void* dv = base + 2 * bq + bkv;
-  int32_t* dqo = reinterpret_cast<int32_t*>(base + 2 * bq + 2 * bkv);
-  int32_t* dko = reinterpret_cast<int32_t*>(base + 2 * bq + 2 * bkv + boff);
-  if (cudaStreamWaitEvent(s, c.work_free, 0) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (cudaMemcpyAsync(dq, h_q, (size_t)Tq * row, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (Tkv > 0) {
-    if (cudaMemcpyAsync(dk, h_k, (size_t)Tkv * row, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
-    if (cudaMemcpyAsync(dv, h_v, (size_t)Tkv * row, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  char* dq = base;
+  char* dout = base + bq;
+  char* dk = base + 2 * bq;
+  char* dv = base + 2 * bq + bkv;
+  char* dmeta = base + 2 * bq + 2 * bkv;
+  char* hmeta = static_cast<char*>(c.h_io.p);
+
+  // copies in, chunk by chunk, behind whatever `stream` already holds
+  if (cudaEventRecord(c.ev_start, s) != cudaSuccess || cudaStreamWaitEvent(c.s_in, c.ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(c.s_out, c.ev_start, 0) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  for (int i = 0; i < C; ++i) {
+    const size_t q0 = (size_t)qo[cut[i]] * row, q1 = (size_t)qo[cut[i + 1]] * row;
+    const size_t k0 = (size_t)ko[cut[i]] * row, k1 = (size_t)ko[cut[i + 1]] * row;
+    if (q1 > q0 &&
+        cudaMemcpyAsync(dq + q0, static_cast<const char*>(h_q) + q0, q1 - q0, cudaMemcpyHostToDevice, c.s_in) !=
+            cudaSuccess)
+      return GDPA_ERR_CUDA;
+    if (k1 > k0) {
+      if (cudaMemcpyAsync(dk + k0, static_cast<const char*>(h_k) + k0, k1 - k0, cudaMemcpyHostToDevice, c.s_in) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(dv + k0, static_cast<const char*>(h_v) + k0, k1 - k0, cudaMemcpyHostToDevice, c.s_in) !=
+              cudaSuccess)
+        return GDPA_ERR_CUDA;
+    }
+    if (cudaEventRecord(c.ev_in[i], c.s_in) != cudaSuccess) return GDPA_ERR_CUDA;
   }
-  const size_t ob = ((size_t)B + 1) * sizeof(int32_t);
-  if (cudaMemcpyAsync(dqo, h_q_offsets, ob, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (cudaMemcpyAsync(dko, h_kv_offsets, ob, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  int num_ctas = 0;
-  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, window_blocks, sms, s, &num_ctas)) != GDPA_OK)
-    return st;
-  if ((st = launch_with_ctx(c, dq, dk, dv, dout, dqo, dko, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                            count_items(h_q_offsets, B, H), s)) != GDPA_OK)
-    return st;
-  if (cudaMemcpyAsync(h_out, dout, (size_t)Tq * row, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return GDPA_ERR_CUDA;
+  // plan each chunk on the host while its inputs travel; launch; copy out
+  std::vector<gdpa_work_item_t> items;
+  std::vector<int32_t> cta_begin;
+  for (int i = 0; i < C; ++i) {
+    const int b0 = cut[i], nb = cut[i + 1] - cut[i];
+    int32_t* hqo = reinterpret_cast<int32_t*>(hmeta + off_at[i]);
+    int32_t* hko = hqo + nb + 1;
+    for (int b = 0; b <= nb; ++b) {
+      hqo[b] = qo[b0 + b] - qo[b0];
+      hko[b] = ko[b0 + b] - ko[b0];
+    }
+    const int64_t Tq_i = hqo[nb], Tkv_i = hko[nb];
+    if (n_items[i] > 0) {
+      try {
+        st = plan_items(hqo, hko, nb, H, window_blocks, rpi[i], ctas[i], items, cta_begin, nullptr);
+      } catch (const std::bad_alloc&) {
+        st = GDPA_ERR_NO_MEMORY;
+      }
+      if (st != GDPA_OK) return st;
+      std::memcpy(hmeta + work_at[i], items.data(), items.size() * sizeof(gdpa_work_item_t));
+      std::memcpy(hmeta + work_at[i] + item_bytes[i], cta_begin.data(), cta_begin.size() * sizeof(int32_t));
+    }
+    const size_t meta_end = i + 1 < C ? off_at[i + 1] : meta;
+    if (cudaMemcpyAsync(dmeta + off_at[i], hmeta + off_at[i], meta_end - off_at[i], cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaStreamWaitEvent(s, c.ev_in[i], 0) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    if (n_items[i] > 0) {
+      LaunchArgs a;
+      a.q = dq + (size_t)qo[b0] * row;
+      a.k = dk + (size_t)ko[b0] * row;
+      a.v = dv + (size_t)ko[b0] * row;
+      a.out = dout + (size_t)qo[b0] * row;
+      a.q_off = reinterpret_cast<const int32_t*>(dmeta + off_at[i]);
+      a.kv_off = a.q_off + nb + 1;
+      a.items = reinterpret_cast<const gdpa_work_item_t*>(dmeta + work_at[i]);
+      a.cta_begin = reinterpret_cast<const int32_t*>(dmeta + work_at[i] + item_bytes[i]);
+      a.num_ctas = ctas[i];
+      a.rows_per_item = rpi[i];
+      a.Tq = Tq_i;
+      a.Tkv = Tkv_i;
+      a.H = H;
+      a.D = D;
+      a.act = act;
+      a.window_blocks = window_blocks;
+      a.scale = scale;
+      a.stream = s;
+      if ((st = launch_forward(a)) != GDPA_OK) return st;
+    }
+    if (cudaEventRecord(c.ev_done[i], s) != cudaSuccess || cudaStreamWaitEvent(c.s_out, c.ev_done[i], 0) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+    if (Tq_i > 0 && cudaMemcpyAsync(static_cast<char*>(h_out) + (size_t)qo[b0] * row, dout + (size_t)qo[b0] * row,
+                                    (size_t)Tq_i * row, cudaMemcpyDeviceToHost, c.s_out) != cudaSuccess)
+      return GDPA_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(c.s_out) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return GDPA_ERR_CUDA;
   return GDPA_OK;
 }
 
@@ -397,6 +531,11 @@ extern "C" gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_
 }
 
 extern "C" gdpa_status_t gdpa_device_status(void* stream) { return read_and_clear_device_status(stream); }
+
+extern "C" gdpa_status_t gdpa_wait_selftest(int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return GDPA_ERR_INVALID_ARG;
+  return launch_wait_selftest(timeout_ms, stream);
+}
 
 extern "C" const char* gdpa_status_string(int status) {
   switch (status) {

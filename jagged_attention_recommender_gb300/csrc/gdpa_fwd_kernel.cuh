@@ -311,6 +311,9 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       const int blk = i_seq / 64 - (p.window_blocks - 1);
       win_lo = blk > 0 ? blk * 64 : 0;
     }
+    // A warp whose 32 rows all lie past the end of the query tile keeps the
+    // barrier protocol but skips the math (e.g. 3 of 4 warps for 32 queries).
+    const bool rows_live = __any_sync(0xffffffffu, row < t.q_rows);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
       const int sb = g & 1;
       ok = ptx::mbar_wait(&B.s_full[sb], (g >> 1) & 1, p.timeout_ns, abort);
@@ -318,82 +321,101 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t s_addr = tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0);
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      ptx::tmem_wait_ld();
-      // valid key columns of this row: [c_lo, c_hi]
-      const int kv_t0 = t.kv0 + 128 * j;
-      int c_lo = 0, c_hi = min(128, t.kv_end - kv_t0) - 1;
-      if (WIN) {
-        c_lo = max(0, win_lo - kv_t0);
-        c_hi = min(c_hi, i_seq - kv_t0);
-      }
-      const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 127);
       float alpha = 1.0f;
       bool rescale = false;
-      if (ACT == kActSoftmax) {
-        // Scores become log2-domain values x = s * scale * log2(e); masked
-        // columns become -inf.  With scale > 0 the scaling is folded into the
-        // exponent's FMA; otherwise it is applied first.
-        const bool fold = sl > 0.0f;
-        if (!fold) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * sl);
+      if (rows_live) {
+        // valid key columns of this row: [c_lo, c_hi]; only the 32-column
+        // chunks below the warp's largest c_hi are read and processed.
+        const int kv_t0 = t.kv0 + 128 * j;
+        int c_lo = 0, c_hi = min(128, t.kv_end - kv_t0) - 1;
+        if (WIN) {
+          c_lo = max(0, win_lo - kv_t0);
+          c_hi = min(c_hi, i_seq - kv_t0);
         }
-        if (!full) {
+        const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 127);
+        const int nch = (static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(max(c_hi, 0)))) >> 5) + 1;
+        uint32_t sr[128];
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < c_lo || c > c_hi) sr[c] = __float_as_uint(-INFINITY);
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int c = 0; c < 4; ++c)
+          if (c < nch) ptx::tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        ptx::tmem_wait_ld();
+        if (ACT == kActSoftmax) {
+          // Scores become log2-domain values x = s * scale * log2(e); masked
+          // columns become -inf.  With scale > 0 the scaling is folded into
+          // the exponent's FMA; otherwise it is applied first.
+          const bool fold = sl > 0.0f;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], __uint_as_float(sr[c + u]));
-        }
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        if (fold) mx *= sl;
-        const float m_new = fmaxf(m_run, mx);
-        if (j == 0) {
-          m_run = m_new;
-        } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
-          alpha = ptx::ex2_approx(m_run - m_new);
-          l_run *= alpha;
-          m_run = m_new;
-          rescale = true;
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-        const float mul = fold ? sl : 1.0f;
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int u = 0; u < 32; ++u) {
+              const int c = 32 * ch + u;
+              float x = __uint_as_float(sr[c]);
+              if (!fold) x *= sl;
+              if (!full && (c < c_lo || c > c_hi)) x = -INFINITY;
+              sr[c] = __float_as_uint(x);
+              m4[u & 3] = fmaxf(m4[u & 3], x);
+            }
+          }
+          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          if (fold) mx *= sl;
+          const float m_new = fmaxf(m_run, mx);
+          if (j == 0) {
+            m_run = m_new;
+          } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
+            alpha = ptx::ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            rescale = true;
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+          const float mul = fold ? sl : 1.0f;
+          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float e = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + u]), mul, -m_use));
-            s4[u] += e;
-            sr[c + u] = __float_as_uint(e);
+            for (int u = 0; u < 32; ++u) {
+              const int c = 32 * ch + u;
+              const float e = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), mul, -m_use));
+              s4[u & 3] += e;
+              sr[c] = __float_as_uint(e);
+            }
+          }
+          l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c = 16 * ch + u;
+              sr[c] = ptx::pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+            }
+          }
+        } else {  // GELU
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c = 16 * ch + u;
+              float a = gelu_tanh_alu(__uint_as_float(sr[2 * c]) * sl);
+              float b = gelu_tanh_alu(__uint_as_float(sr[2 * c + 1]) * sl);
+              if (!full) {
+                a = (2 * c >= c_lo && 2 * c <= c_hi) ? a : 0.0f;
+                b = (2 * c + 1 >= c_lo && 2 * c + 1 <= c_hi) ? b : 0.0f;
+              }
+              sr[c] = ptx::pack_bf16x2(a, b);
+            }
           }
         }
-        l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) sr[c] = ptx::pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
-      } else {  // GELU
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float a = gelu_tanh_alu(__uint_as_float(sr[2 * c]) * sl);
-          float b = gelu_tanh_alu(__uint_as_float(sr[2 * c + 1]) * sl);
-          if (!full) {
-            a = (2 * c >= c_lo && 2 * c <= c_hi) ? a : 0.0f;
-            b = (2 * c + 1 >= c_lo && 2 * c + 1 <= c_hi) ? b : 0.0f;
-          }
-          sr[c] = ptx::pack_bf16x2(a, b);
-        }
+        // P (bf16 pairs) overwrites the first 16 * nch columns of this S
+        // buffer; P V reads no column beyond them.
+        ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        if (nch > 2) ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        ptx::tmem_wait_st();
       }
-      // P (bf16 pairs) overwrites the first 64 columns of this S buffer.
-      ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_wait_st();
       if (g >= 1) {  // O += P(g-1) V(g-1) has landed
         ok = ptx::mbar_wait(&B.o_done, (g - 1) & 1, p.timeout_ns, abort);
         ok = __all_sync(0xffffffffu, ok);
@@ -430,6 +452,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
     const uint32_t o_addr = tmem + lane_off + o_col;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
+      if (!rows_live) break;
       uint32_t r[32];
       ptx::tmem_ld32(o_addr + 32 * c, r);
       ptx::tmem_wait_ld();

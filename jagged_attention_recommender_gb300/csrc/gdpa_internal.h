@@ -25,9 +25,17 @@ inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blo
 gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks,
                                int64_t* Tq, int64_t* Tkv);
 
+// Query rows per work item: 256 (two 128-row tiles sharing every K/V tile)
+// for full attention when the batch's sequences average more than 128
+// queries, else 128.
+int choose_rows_per_item(const int32_t* q_off, int B, int window_blocks);
+
+// Number of work items plan_items will emit.
+int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item);
+
 gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
-                         int num_ctas, std::vector<gdpa_work_item_t>& items, std::vector<int32_t>& cta_begin,
-                         std::vector<int64_t>* cost);
+                         int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items,
+                         std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost);
 
 // Everything one launch of the forward kernel needs besides the tensor maps.
 struct LaunchArgs {
@@ -40,6 +48,7 @@ struct LaunchArgs {
   const gdpa_work_item_t* items;  // device, grouped by CTA
   const int32_t* cta_begin;       // device [num_ctas + 1]
   int num_ctas;
+  int rows_per_item;      // 128: one query tile per item; 256: two
   int64_t Tq, Tkv;
   int H, D, act, window_blocks;
   float scale;
@@ -50,5 +59,6 @@ struct LaunchArgs {
 gdpa_status_t launch_forward(const LaunchArgs& a);
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
 gdpa_status_t read_and_clear_device_status(void* stream);
+gdpa_status_t launch_wait_selftest(int timeout_ms, void* stream);
 
 }  // namespace gdpa

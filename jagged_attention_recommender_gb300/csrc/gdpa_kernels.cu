@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "gdpa_fwd_kernel.cuh"
+#include "gdpa_fwd_pair.cuh"
 #include "gdpa_internal.h"
 
 namespace gdpa {
@@ -74,22 +75,37 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
+template <typename Kernel>
+gdpa_status_t launch_k(Kernel kernel, int threads, int smem, const FwdParams& prm, int grid, cudaStream_t stream,
+                       int device, bool* attr_done, std::mutex* mu) {
+  {
+    std::lock_guard<std::mutex> lock(*mu);
+    if (!attr_done[device]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+      attr_done[device] = true;
+    }
+  }
+  kernel<<<grid, threads, smem, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+// One query tile per work item (any key range, block window included).
 template <int D, int ACT, bool WIN>
 gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
   using C = FwdCfg<D>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!attr_done[device]) {
-      if (cudaFuncSetAttribute(gdpa_fwd_kernel<D, ACT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM_BYTES) != cudaSuccess)
-        return GDPA_ERR_CUDA;
-      attr_done[device] = true;
-    }
-  }
-  gdpa_fwd_kernel<D, ACT, WIN><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+  return launch_k(gdpa_fwd_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, prm, grid, stream, device, attr_done, &mu);
+}
+
+// Two query tiles per work item (full attention).
+template <int D, int ACT>
+gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
+  using C = PairCfg<D>;
+  static std::mutex mu;
+  static bool attr_done[kMaxDevices] = {};
+  return launch_k(gdpa_fwd_pair_kernel<D, ACT>, C::THREADS, C::SMEM_BYTES, prm, grid, stream, device, attr_done, &mu);
 }
 
 __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
@@ -97,7 +113,30 @@ __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __r
     y[i] = act == kActGelu ? gelu_tanh_alu(x[i]) : ptx::ex2_approx(x[i]);
 }
 
+// One thread waits, with the forward kernel's bounded wait, on an mbarrier
+// that nothing ever arrives on; when the limit runs out it records the
+// timeout in the status word exactly as the forward kernel's roles do.
+__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  ptx::mbar_init(&bar, 1);
+  abort_flag = 0;
+  ptx::fence_mbar_init();
+  if (!ptx::mbar_wait(&bar, 0, limit_ns, &abort_flag)) atomicOr(status, kStatusActivation);
+}
+
 }  // namespace
+
+gdpa_status_t launch_wait_selftest(int timeout_ms, void* stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return GDPA_ERR_CUDA;
+  int* status = status_ptr(device);
+  if (!status) return GDPA_ERR_CUDA;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, static_cast<unsigned long long>(timeout_ms) * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
 
 gdpa_status_t launch_forward(const LaunchArgs& a) {
   int device = 0;
@@ -127,6 +166,17 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks > 0;
+  if (a.rows_per_item == 256) {
+    if (win) return GDPA_ERR_INVALID_ARG;
+    if (a.D == 128)
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<128, kActGelu>(prm, a.num_ctas, s, device)
+                                         : launch_pair<128, kActSoftmax>(prm, a.num_ctas, s, device);
+    if (a.D == 64)
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<64, kActGelu>(prm, a.num_ctas, s, device)
+                                         : launch_pair<64, kActSoftmax>(prm, a.num_ctas, s, device);
+    return GDPA_ERR_UNSUPPORTED;
+  }
+  if (a.rows_per_item != 128) return GDPA_ERR_INVALID_ARG;
   if (a.D == 128) {
     if (a.act == GDPA_ACT_GELU_TANH) return launch_t<128, kActGelu, false>(prm, a.num_ctas, s, device);
     return win ? launch_t<128, kActSoftmax, true>(prm, a.num_ctas, s, device)

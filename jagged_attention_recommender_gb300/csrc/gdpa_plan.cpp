@@ -8,8 +8,9 @@
 // (LPT) list scheduling over a min-heap of per-CTA loads, which bounds the
 // finish time by 4/3 of optimal and subsumes the zigzag order.
 //
-// Work unit: one 128-row query tile of one (sequence, head), against its key
-// range [kv0, kv_end):
+// Work unit: 128 query rows (or 256, two tiles sharing every K/V tile, for
+// full attention over sequences that average more than 128 queries) of one
+// (sequence, head), against its key range [kv0, kv_end):
 //   full attention : kv0 = 0, kv_end = Lkv
 //   block window W : kv0 = 64 * max(0, q0/64 - (W-1)), kv_end = min(L, q0 + 128)
 // Items whose key range is empty (Lkv = 0) are still emitted (cheap) because
@@ -51,20 +52,33 @@ static int64_t item_cost(int64_t kv_len) {
   return ((kv_len + 15) / 16) * 16 + 96;
 }
 
+int choose_rows_per_item(const int32_t* q_off, int B, int window_blocks) {
+  if (window_blocks > 0 || B <= 0) return kBlockM;
+  int64_t busy = 0;
+  for (int b = 0; b < B; ++b) busy += q_off[b + 1] > q_off[b] ? 1 : 0;
+  return (busy > 0 && q_off[B] > (int64_t)kBlockM * busy) ? 2 * kBlockM : kBlockM;
+}
+
+int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item) {
+  int64_t n = 0;
+  for (int b = 0; b < B; ++b) n += (int64_t)((q_off[b + 1] - q_off[b] + rows_per_item - 1) / rows_per_item) * H;
+  return n;
+}
+
 gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
-                         int num_ctas, std::vector<gdpa_work_item_t>& items_out,
+                         int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items_out,
                          std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
   if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
+  if (rows_per_item != kBlockM && !(rows_per_item == 2 * kBlockM && window_blocks == 0)) return GDPA_ERR_INVALID_ARG;
   std::vector<gdpa_work_item_t> items;
   std::vector<int64_t> cost;
-  int64_t n = 0;
-  for (int b = 0; b < B; ++b) n += (int64_t)((q_off[b + 1] - q_off[b] + kBlockM - 1) / kBlockM) * H;
+  const int64_t n = count_plan_items(q_off, B, H, rows_per_item);
   items.reserve((size_t)n);
   cost.reserve((size_t)n);
   for (int b = 0; b < B; ++b) {
     const int64_t Lq = q_off[b + 1] - q_off[b];
     const int64_t Lkv = kv_off[b + 1] - kv_off[b];
-    for (int64_t q0 = 0; q0 < Lq; q0 += kBlockM) {
+    for (int64_t q0 = 0; q0 < Lq; q0 += rows_per_item) {
       int64_t kv0 = 0, kv_end = Lkv;
       if (window_blocks > 0) {
         int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
@@ -72,7 +86,8 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
         kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
       }
       if (kv_end < kv0) kv_end = kv0;
-      const int64_t c = item_cost(kv_end - kv0);
+      const int64_t tiles = std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM;  // 1 or 2
+      const int64_t c = tiles * item_cost(kv_end - kv0);
       for (int h = 0; h < H; ++h) {
         items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});
         cost.push_back(c);
@@ -141,7 +156,7 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
 extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B,
                                              int H, int D, int act, int window_blocks, int num_ctas,
                                              gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
-                                             int64_t* cost, int64_t* n_items) {
+                                             int64_t* cost, int64_t* n_items, int32_t* rows_per_item) {
   if (n_items) *n_items = 0;
   gdpa_status_t st = gdpa::validate_shape(B, H, D, act, window_blocks);
   if (st != GDPA_OK) return st;
@@ -152,8 +167,10 @@ extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const i
   std::vector<gdpa_work_item_t> v;
   std::vector<int32_t> cb;
   std::vector<int64_t> c;
+  const int rpi = gdpa::choose_rows_per_item(h_q_offsets, B, window_blocks);
+  if (rows_per_item) *rows_per_item = rpi;
   try {
-    st = gdpa::plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, num_ctas, v, cb, &c);
+    st = gdpa::plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, rpi, num_ctas, v, cb, &c);
   } catch (...) {
     return GDPA_ERR_NO_MEMORY;
   }

@@ -29,7 +29,7 @@ GDPA_ERR_NO_MEMORY = 5
 # Every symbol include/gdpa.h declares.
 EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
-           "gdpa_status_string", "gdpa_version")
+           "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
 
 class GdpaError(RuntimeError):
@@ -64,15 +64,17 @@ def lib() -> ctypes.CDLL:
     L.gdpa_plan_num_items.restype = I64
     L.gdpa_plan_num_ctas.argtypes = [P]
     L.gdpa_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
-    L.gdpa_plan_enumerate.argtypes = [P, P, I, I, I, I, I, I, P, I64, P, P, ctypes.POINTER(I64)]
+    L.gdpa_plan_enumerate.argtypes = [P, P, I, I, I, I, I, I, P, I64, P, P, ctypes.POINTER(I64),
+                                      ctypes.POINTER(ctypes.c_int32)]
     L.gdpa_act_eval.argtypes = [I, P, P, I64, P]
     L.gdpa_device_status.argtypes = [P]
+    L.gdpa_wait_selftest.argtypes = [I, P]
     L.gdpa_status_string.argtypes = [I]
     L.gdpa_status_string.restype = ctypes.c_char_p
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
     for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
-                 "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status"):
+                 "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
     return L
@@ -179,21 +181,26 @@ def gdpa_fwd_host(h_q, h_k, h_v, h_q_offsets, h_kv_offsets, B, H, D, act, window
                                _stream(stream)), "gdpa_fwd_host")
 
 
-def gdpa_plan_enumerate(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, num_ctas):
-    """Host planner only: returns (items [n, 4] int32, cta_begin [num_ctas+1], cost [n])."""
+def gdpa_plan_enumerate(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, num_ctas, with_rows=False):
+    """Host planner only: returns (items [n, 4] int32, cta_begin [num_ctas+1], cost [n])
+    (and the query rows per item when ``with_rows``)."""
     qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
     n = ctypes.c_int64(0)
+    rows = ctypes.c_int32(0)
     cta = np.zeros(num_ctas + 1, dtype=np.int32)
     code = lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
                                      int(window_blocks), int(num_ctas), None, 0, cta.ctypes.data, None,
-                                     ctypes.byref(n))
+                                     ctypes.byref(n), ctypes.byref(rows))
     if code not in (GDPA_OK, GDPA_ERR_NO_MEMORY):
         raise GdpaError(code, "gdpa_plan_enumerate")
     items = np.zeros((max(n.value, 1), 4), dtype=np.int32)
     cost = np.zeros(max(n.value, 1), dtype=np.int64)
     _check(lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
                                      int(window_blocks), int(num_ctas), items.ctypes.data, n.value,
-                                     cta.ctypes.data, cost.ctypes.data, ctypes.byref(n)), "gdpa_plan_enumerate")
+                                     cta.ctypes.data, cost.ctypes.data, ctypes.byref(n), ctypes.byref(rows)),
+           "gdpa_plan_enumerate")
+    if with_rows:
+        return items[:n.value], cta, cost[:n.value], rows.value
     return items[:n.value], cta, cost[:n.value]
 
 
@@ -204,3 +211,7 @@ def gdpa_act_eval(act, x, y, stream=None):
 def gdpa_device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status code."""
     return lib().gdpa_device_status(_stream(stream))
+
+
+def gdpa_wait_selftest(timeout_ms: int, stream=None):
+    _check(lib().gdpa_wait_selftest(int(timeout_ms), _stream(stream)), "gdpa_wait_selftest")

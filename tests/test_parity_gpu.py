@@ -8,6 +8,8 @@ are compared on a seeded sample of whole sequences (every row, every head).
 """
 from __future__ import annotations
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -217,6 +219,17 @@ def test_all_entry_points_agree_and_are_deterministic():
     assert np.array_equal(a, b) and np.array_equal(a, c) and np.array_equal(a, d) and np.array_equal(a, e)
 
 
+def test_host_entry_pipelines_chunks_exactly():
+    # ~300 MB in + out: the host entry point splits it into several chunks of
+    # whole sequences; every item computes exactly as in the one-shot launch.
+    batch = make_batch("self_long", B=64, seed=78)
+    a = run_gpu(batch, "fwd")
+    c = run_gpu(batch, "host")
+    assert np.array_equal(a, c)
+    sub = batch.subset(sample_sequences(batch, 3, 5))
+    assert_parity(run_gpu(sub, "host"), oracle.gdpa_fwd_batch(sub), "host chunks")
+
+
 def test_empty_batch_is_noop():
     rng = np.random.default_rng(6000)
     b = small_batch(rng, [0, 0], [3, 0], 2, 64)
@@ -247,3 +260,19 @@ def test_full_workload_sampled_parity(name):
     got_sub = np.concatenate([got[qo[s]:qo[s + 1]] for s in seqs])
     assert_parity(got_sub, ref, name)
     assert np.isfinite(got).all()
+
+
+# ------------------------------------------------------------------ failure path
+
+def test_bounded_wait_times_out_and_context_survives():
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_OK
+    t0 = time.perf_counter()
+    gdpa.gdpa_wait_selftest(200)
+    st = gdpa.gdpa_device_status()
+    dt = time.perf_counter() - t0
+    assert st == gdpa.GDPA_ERR_DEVICE_TIMEOUT
+    assert 0.15 < dt < 5.0
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_OK  # the word was cleared
+    # the context is still usable: a normal forward pass still matches the oracle
+    batch = make_batch("tiny", seed=91)
+    assert_parity(run_gpu(batch), oracle.gdpa_fwd_batch(batch), "after timeout")

@@ -70,18 +70,21 @@ def test_enumerate_rejects_bad_offsets():
 def check_plan(Lq, Lkv, H, wb, num_ctas):
     qo, ko = offsets_of(Lq), offsets_of(Lkv)
     B = len(Lq)
-    items, cta, cost = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas)
+    items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas, with_rows=True)
     n = len(items)
+    busy = Lq[Lq > 0]
+    expect_R = 256 if (wb == 0 and busy.size and busy.sum() > 128 * busy.size) else 128
+    assert R == expect_R
     # CSR over CTAs
     assert cta[0] == 0 and cta[-1] == n and np.all(np.diff(cta) >= 0)
     # every (sequence, head, query row) is covered exactly once
     cover = {}
     for (b, h, q0, kv0) in items:
-        assert 0 <= b < B and 0 <= h < H and q0 % 128 == 0 and 0 <= q0 < Lq[b]
+        assert 0 <= b < B and 0 <= h < H and q0 % R == 0 and 0 <= q0 < Lq[b]
         key = (int(b), int(h), int(q0))
         assert key not in cover
         cover[key] = int(kv0)
-    expect = {(b, h, q0) for b in range(B) for h in range(H) for q0 in range(0, int(Lq[b]), 128)}
+    expect = {(b, h, q0) for b in range(B) for h in range(H) for q0 in range(0, int(Lq[b]), R)}
     assert set(cover) == expect
     # key ranges: full attention starts at 0; a window tile starts at the first
     # key any of its rows may see
@@ -118,7 +121,7 @@ def test_plan_coverage_window(wb):
 
 
 def test_plan_empty_sequences():
-    items, cta, cost, _ = check_plan(np.array([0, 0, 5]), np.array([3, 0, 0]), 2, 0, 4)
+    items, cta, cost, _ = check_plan(np.array([0, 0, 5]), np.array([3, 0, 0]), 2, 0, 4)  # average 5 rows: R = 128
     assert len(items) == 2 and set(items[:, 0]) == {2}
 
 
