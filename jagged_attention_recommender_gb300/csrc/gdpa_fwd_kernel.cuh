@@ -3,11 +3,11 @@
 //
 // One CTA per SM walks its own list of work items (a 128-row query tile of
 // one (sequence, head) against its key range; built on the host, see
-// gdpa_plan.cpp).  Roles inside the CTA (192 threads):
+// gdpa_plan.cpp).  Roles inside the CTA (224 threads):
 //
-//   warp 0      TMA producer: stages the Q tile (2 stages), K tiles (NK
-//               stages) and V tiles (NV stages) into 128-byte-swizzled
-//               shared memory; K is released after Q K^T, V after P V;
+//   warp 0      TMA producer for the Q tile (2 stages) and K tiles (NK
+//               stages); warp 6 TMA producer for V tiles (NV stages); all
+//               128-byte swizzled; K is released after Q K^T, V after P V;
 //   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory
 //               (two S buffers), then O += P V with P read straight from
 //               tensor memory (two O buffers, one per in-flight item);
@@ -74,7 +74,7 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 224;  // 7 warps
   static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -122,56 +122,68 @@ __device__ __forceinline__ void report_failure(const FwdParams& p, volatile int*
 
 // ------------------------------------------------------------------ producer
 
-template <int D, bool WIN>
+// Two producer threads, each in order on its own resource: one stages Q and
+// K tiles, the other V tiles.  A K load therefore never waits behind a V
+// slot (freed only when an earlier P V completes), which would otherwise
+// chain one load latency into every pair of tiles.
+template <int D, bool WIN, bool LOAD_V>
 __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, int ibeg, int iend) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
-  int q_armed[2] = {-1, -1};            // last parity armed per Q stage (for draining)
+  int q_armed[2] = {-1, -1};  // last parity armed per stage (for draining)
   int k_armed[C::NK], v_armed[C::NV];
 #pragma unroll
   for (int s = 0; s < C::NK; ++s) k_armed[s] = -1;
 #pragma unroll
   for (int s = 0; s < C::NV; ++s) v_armed[s] = -1;
-  ptx::prefetch_tensormap(&p.tm_q);
-  ptx::prefetch_tensormap(&p.tm_k);
-  ptx::prefetch_tensormap(&p.tm_v);
+  if (LOAD_V) {
+    ptx::prefetch_tensormap(&p.tm_v);
+  } else {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+  }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<WIN>(p, idx);
     if (t.n_kv == 0) continue;
-    const int qs = qi & 1;
-    ok = ptx::mbar_wait(&B.q_empty[qs], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
-    if (!ok) break;
-    ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
-    q_armed[qs] = (qi >> 1) & 1;
-    uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
+    if (!LOAD_V) {
+      const int qs = qi & 1;
+      ok = ptx::mbar_wait(&B.q_empty[qs], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
+      q_armed[qs] = (qi >> 1) & 1;
+      uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
 #pragma unroll
-    for (int c = 0; c < C::KCH; ++c)
-      ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+      for (int c = 0; c < C::KCH; ++c)
+        ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+    }
     for (int j = 0; j < t.n_kv; ++j, ++g) {
-      const int sk_i = g % C::NK, sv_i = g % C::NV;
-      const uint32_t phk = (g / C::NK) & 1, phv = (g / C::NV) & 1;
       const int y = t.kv_tok + t.kv0 + 128 * j;
-      uint8_t* sk = sm + C::OFF_K + sk_i * C::TILE_BYTES;
-      uint8_t* sv = sm + C::OFF_V + sv_i * C::TILE_BYTES;
-      // K is released once its Q K^T is done, V once its P V is done, so the
-      // next K tile streams in while the current P V still runs.
-      ok = ptx::mbar_wait(&B.k_empty[sk_i], phk ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.k_full[sk_i], C::TILE_BYTES);
+      if (!LOAD_V) {  // K is released once its Q K^T is done
+        const int si = g % C::NK;
+        const uint32_t ph = (g / C::NK) & 1;
+        ok = ptx::mbar_wait(&B.k_empty[si], ph ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        uint8_t* dst = sm + C::OFF_K + si * C::TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.k_full[si], C::TILE_BYTES);
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[sk_i], t.h * D + 64 * c, y);
-      k_armed[sk_i] = (int)phk;
-      ok = ptx::mbar_wait(&B.v_empty[sv_i], phv ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.v_full[sv_i], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dst + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[si], t.h * D + 64 * c, y);
+        k_armed[si] = (int)ph;
+      } else {  // V is released once its P V is done
+        const int si = g % C::NV;
+        const uint32_t ph = (g / C::NV) & 1;
+        ok = ptx::mbar_wait(&B.v_empty[si], ph ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        uint8_t* dst = sm + C::OFF_V + si * C::TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.v_full[si], C::TILE_BYTES);
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[sv_i], t.h * D + 64 * c, y);
-      v_armed[sv_i] = (int)phv;
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dst + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[si], t.h * D + 64 * c, y);
+        v_armed[si] = (int)ph;
+      }
     }
     ++qi;
   }
@@ -325,7 +337,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       bool rescale = false;
       if (rows_live) {
         // valid key columns of this row: [c_lo, c_hi]; only the 32-column
-        // chunks below the warp's largest c_hi are read and processed.
+        // chunks that hold keys of the tile are read and processed.
         const int kv_t0 = t.kv0 + 128 * j;
         int c_lo = 0, c_hi = min(128, t.kv_end - kv_t0) - 1;
         if (WIN) {
@@ -333,7 +345,8 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
           c_hi = min(c_hi, i_seq - kv_t0);
         }
         const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 127);
-        const int nch = (static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(max(c_hi, 0)))) >> 5) + 1;
+        // chunks up to the tile's key extent: P V reads P over all of them
+        const int nch = (min(128, t.kv_end - kv_t0) + 31) >> 5;
         uint32_t sr[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -476,7 +489,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 // ------------------------------------------------------------------ kernel
 
 template <int D, int ACT, bool WIN>
-__global__ void __launch_bounds__(192, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(224, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -518,7 +531,9 @@ __global__ void __launch_bounds__(192, 1) gdpa_fwd_kernel(const __grid_constant_
   const uint32_t tmem = B.tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<D, WIN>(p, sm, B, ibeg, iend);
+    if (lane == 0) run_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+  } else if (warp == 6) {
+    if (lane == 0) run_producer<D, WIN, true>(p, sm, B, ibeg, iend);
   } else if (warp == 1) {
     if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
   } else {

@@ -12,8 +12,9 @@
 //   warpgroup A works on S_A(g) while the tensor core runs the B half, and
 //   the other way round.
 //
-// Threads (320): warp 0 TMA producer, warp 1 MMA issuer + TMEM owner,
-// warps 2-5 tile A activation/epilogue, warps 6-9 tile B.  TMEM (512
+// Threads (352): warp 0 TMA producer for Q and K, warp 10 TMA producer for
+// V, warp 1 MMA issuer + TMEM owner, warps 2-5 tile A activation/epilogue,
+// warps 6-9 tile B.  TMEM (512
 // columns): S_A 0, S_B 128, O_A 256, O_B 384.  An activation thread holds
 // one query row; it reads S from TMEM twice (row max, then exponentials) in
 // 32-column chunks, so only ~64 scores are live in registers at a time.
@@ -41,7 +42,7 @@ struct PairCfg {
   __host__ __device__ static constexpr uint32_t tm_s(int x) { return x ? 128u : 0u; }    // S_A, S_B
   __host__ __device__ static constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }  // O_A, O_B
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;  // 11 warps
   static_assert(384 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -83,7 +84,9 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
 
 // ------------------------------------------------------------------ producer
 
-template <int D>
+// Two producer threads: one stages Q and K, the other V, so that a K load
+// never waits behind a V slot.
+template <int D, bool LOAD_V>
 __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, int ibeg, int iend) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
@@ -95,46 +98,56 @@ __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, i
     for (int s = 0; s < C::NQS; ++s) q_armed[t][s] = -1;
   for (int s = 0; s < C::NK; ++s) k_armed[s] = -1;
   for (int s = 0; s < C::NV; ++s) v_armed[s] = -1;
-  ptx::prefetch_tensormap(&p.tm_q);
-  ptx::prefetch_tensormap(&p.tm_k);
-  ptx::prefetch_tensormap(&p.tm_v);
+  if (LOAD_V) {
+    ptx::prefetch_tensormap(&p.tm_v);
+  } else {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+  }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const PairItem t = decode_pair(p, idx);
     if (t.n_kv == 0) continue;
-    for (int x = 0; x < 2 && ok; ++x) {
-      if (t.rows[x] == 0) continue;
-      const int s = qn[x] % C::NQS;
-      const uint32_t ph = (qn[x] / C::NQS) & 1;
-      ok = ptx::mbar_wait(&B.q_empty[x][s], ph ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.q_full[x][s], C::TILE_BYTES);
-      q_armed[x][s] = (int)ph;
-      uint8_t* sq = sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::TILE_BYTES;
+    if (!LOAD_V) {
+      for (int x = 0; x < 2 && ok; ++x) {
+        if (t.rows[x] == 0) continue;
+        const int s = qn[x] % C::NQS;
+        const uint32_t ph = (qn[x] / C::NQS) & 1;
+        ok = ptx::mbar_wait(&B.q_empty[x][s], ph ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.q_full[x][s], C::TILE_BYTES);
+        q_armed[x][s] = (int)ph;
+        uint8_t* sq = sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::TILE_BYTES;
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[x][s], t.h * D + 64 * c, t.q_tok + 128 * x);
-      ++qn[x];
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[x][s], t.h * D + 64 * c, t.q_tok + 128 * x);
+        ++qn[x];
+      }
     }
     for (int j = 0; j < t.n_kv && ok; ++j, ++g) {
-      const int sk = g % C::NK, sv = g % C::NV;
-      const uint32_t phk = (g / C::NK) & 1, phv = (g / C::NV) & 1;
       const int y = t.kv_tok + 128 * j;
-      ok = ptx::mbar_wait(&B.k_empty[sk], phk ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.k_full[sk], C::TILE_BYTES);
-      uint8_t* dk = sm + C::OFF_K + sk * C::TILE_BYTES;
+      if (!LOAD_V) {
+        const int sk = g % C::NK;
+        const uint32_t phk = (g / C::NK) & 1;
+        ok = ptx::mbar_wait(&B.k_empty[sk], phk ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.k_full[sk], C::TILE_BYTES);
+        uint8_t* dk = sm + C::OFF_K + sk * C::TILE_BYTES;
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(dk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[sk], t.h * D + 64 * c, y);
-      k_armed[sk] = (int)phk;
-      ok = ptx::mbar_wait(&B.v_empty[sv], phv ^ 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.v_full[sv], C::TILE_BYTES);
-      uint8_t* dv = sm + C::OFF_V + sv * C::TILE_BYTES;
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dk + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[sk], t.h * D + 64 * c, y);
+        k_armed[sk] = (int)phk;
+      } else {
+        const int sv = g % C::NV;
+        const uint32_t phv = (g / C::NV) & 1;
+        ok = ptx::mbar_wait(&B.v_empty[sv], phv ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.v_full[sv], C::TILE_BYTES);
+        uint8_t* dv = sm + C::OFF_V + sv * C::TILE_BYTES;
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(dv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[sv], t.h * D + 64 * c, y);
-      v_armed[sv] = (int)phv;
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dv + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[sv], t.h * D + 64 * c, y);
+        v_armed[sv] = (int)phv;
+      }
     }
   }
   if (!ok) report_failure(p, abort, kStatusProducer);
@@ -203,6 +216,12 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
     }
     if (!ok) break;
     for (int j = 0; j < t.n_kv; ++j, ++g) {
+      // O_A += P_A(prev) V(prev) needs no K: issue it before waiting for K(g).
+      if (pend[0]) {
+        ok = pair_issue_pv<D>(p, sm, B, tmem, 0, pv[0]);
+        if (!ok) break;
+        pend[0] = false;
+      }
       const int sk = g % C::NK;
       ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
       if (!ok) break;
@@ -298,9 +317,11 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
         const bool full = ncols == 128;
         const int nch = (ncols + 31) >> 5;
         if (ACT == kActSoftmax) {
+          // Scores in log2 units: x = s * scale * log2(e).  With scale > 0
+          // the scaling is folded into the exponent's FMA.
           const bool fold = sl > 0.0f;
           // pass 1: row max over the valid columns
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
           for (int cp = 0; cp < 2; ++cp) {
             if (2 * cp >= nch) break;
@@ -311,17 +332,24 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (2 * cp + h >= nch) break;
+              if (full && fold) {
 #pragma unroll
-              for (int u = 0; u < 32; ++u) {
-                const int c = 64 * cp + 32 * h + u;
-                float v = __uint_as_float(r[h][u]);
-                if (!fold) v *= sl;
-                if (!full && c >= ncols) v = -INFINITY;
-                m4[u & 3] = fmaxf(m4[u & 3], v);
+                for (int u = 0; u < 32; u += 4) {
+                  m2[0] = ptx::max3(m2[0], __uint_as_float(r[h][u]), __uint_as_float(r[h][u + 1]));
+                  m2[1] = ptx::max3(m2[1], __uint_as_float(r[h][u + 2]), __uint_as_float(r[h][u + 3]));
+                }
+              } else {  // ragged tile, or scale <= 0 (scale first, then take the max)
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                  const int c = 64 * cp + 32 * h + u;
+                  float v = __uint_as_float(r[h][u]);
+                  if (!fold) v *= sl;
+                  m2[u & 1] = fmaxf(m2[u & 1], c < ncols ? v : -INFINITY);
+                }
               }
             }
           }
-          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          float mx = fmaxf(m2[0], m2[1]);
           if (fold) mx *= sl;
           const float m_new = fmaxf(m_run, mx);
           if (j == 0) {
@@ -333,9 +361,10 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             rescale = true;
           }
           const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-          const float mul = fold ? sl : 1.0f;
+          const uint64_t mul2 = ptx::f2_pack(sl, sl);   // scale * log2(e), both lanes
+          const uint64_t neg2 = ptx::f2_pack(-m_use, -m_use);
           // pass 2: exponentials, row sum, P (bf16 pairs) over the scores
-          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
           for (int cp = 0; cp < 2; ++cp) {
             if (2 * cp >= nch) break;
@@ -347,20 +376,39 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             for (int h = 0; h < 2; ++h) {
               if (2 * cp + h >= nch) break;
               uint32_t pk[16];
+              if (full) {
 #pragma unroll
-              for (int u = 0; u < 16; ++u) {
-                const int c = 64 * cp + 32 * h + 2 * u;
-                float a = fmaf(__uint_as_float(r[h][2 * u]), mul, -m_use);
-                float b = fmaf(__uint_as_float(r[h][2 * u + 1]), mul, -m_use);
-                a = (full || c < ncols) ? ptx::ex2_approx(a) : 0.0f;
-                b = (full || c + 1 < ncols) ? ptx::ex2_approx(b) : 0.0f;
-                s4[u & 3] += a + b;
-                pk[u] = ptx::pack_bf16x2(a, b);
+                for (int u = 0; u < 16; ++u) {
+                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
+                                                  mul2, neg2);
+                  float a, b;
+                  ptx::f2_unpack(x2, a, b);
+                  a = ptx::ex2_approx(a);
+                  b = ptx::ex2_approx(b);
+                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                  pk[u] = ptx::pack_bf16x2(a, b);
+                }
+              } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const int c = 64 * cp + 32 * h + 2 * u;
+                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
+                                                  mul2, neg2);
+                  float a, b;
+                  ptx::f2_unpack(x2, a, b);
+                  a = c < ncols ? ptx::ex2_approx(a) : 0.0f;
+                  b = c + 1 < ncols ? ptx::ex2_approx(b) : 0.0f;
+                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                  pk[u] = ptx::pack_bf16x2(a, b);
+                }
               }
               ptx::tmem_st16(s_addr + 32 * cp + 16 * h, pk);
             }
           }
-          l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+          float sa, sb;
+          ptx::f2_unpack(acc01, sa, sb);
+          l_run += sa + sb;
         } else {  // GELU, one pass
 #pragma unroll
           for (int cp = 0; cp < 2; ++cp) {
@@ -445,7 +493,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
 // ------------------------------------------------------------------ kernel
 
 template <int D, int ACT>
-__global__ void __launch_bounds__(320, 1) gdpa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(352, 1) gdpa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
   using C = PairCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -487,7 +535,9 @@ __global__ void __launch_bounds__(320, 1) gdpa_fwd_pair_kernel(const __grid_cons
   ptx::tc_fence_after();
   const uint32_t tmem = B.tmem_slot;
   if (warp == 0) {
-    if (lane == 0) pair_producer<D>(p, sm, B, ibeg, iend);
+    if (lane == 0) pair_producer<D, false>(p, sm, B, ibeg, iend);
+  } else if (warp == 10) {
+    if (lane == 0) pair_producer<D, true>(p, sm, B, ibeg, iend);
   } else if (warp == 1) {
     if (lane == 0) pair_mma<D>(p, sm, B, tmem, ibeg, iend);
   } else {
