@@ -107,6 +107,32 @@ gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void* v, const 
                              void* stream);
 
 /*
+ * gdpa_fwd_noalloc -- gdpa_fwd for callers that must not allocate memory.
+ * The pages describe no such entry point; it exists for users of this
+ * library.  Some callers cannot allocate where they run attention: a serving
+ * process that splits all device memory into a fixed arena at start-up and
+ * forbids allocation on its request path, or a framework hook that must not
+ * go around its own caching allocator.  This call allocates nothing -- no
+ * cudaMalloc, cudaFree, cudaMallocHost or other allocating routine -- on the
+ * device or the host: the work list lives in a file-scope device array of
+ * 4 MiB (every GPU that loads the library holds it until the process exits)
+ * and is planned in fixed host arrays.
+ * Arguments, layout and results are those of gdpa_fwd (device offsets, one
+ * synchronisation of `stream` to read them).  Limits: B <= 65536 sequences
+ * and at most 261632 work items (query tiles x heads, about 33M query rows
+ * x heads); larger requests return GDPA_ERR_NO_MEMORY before any GPU work.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the array and the host arrays: calls are serialised on the
+ * host, but two calls whose kernels overlap on the GPU (different streams)
+ * race on the work list -- order them on one stream or synchronise between
+ * them.  Each call rewrites the whole part of the array its launch reads.
+ */
+gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                               const int32_t* kv_offsets, int B, int H, int D, int act, int window_blocks,
+                               float scale, void* out, void* stream);
+
+/*
  * gdpa_plan_create -- build a reusable plan from HOST offsets (the same
  * arrays the caller will later pass on the device).  Allocates the plan and
  * its device work list; *plan is NULL on failure.  Planning is host work:

@@ -1,7 +1,7 @@
 """Builds ``libgdpa.so`` in-tree with nvcc for sm_103a.
 
-Three translation units are compiled in parallel (the kernels, the API layer,
-the host planner) and linked into one shared library next to this file.  The
+Four translation units are compiled in parallel (the kernels, the API layer,
+the host planner, the allocation-free entry point) and linked into one shared library next to this file.  The
 CUDA runtime is linked statically, so the library needs only the driver at
 run time.  Nothing here needs a GPU: nvcc cross-compiles for sm_103a.
 """
@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libgdpa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdpa_kernels.cu", "gdpa_api.cu", "gdpa_plan.cpp"]
+SOURCES = ["gdpa_kernels.cu", "gdpa_api.cu", "gdpa_plan.cpp", "gdpa_noalloc.cu"]
 
 
 def _nvcc() -> str:

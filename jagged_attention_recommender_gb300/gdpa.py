@@ -27,7 +27,7 @@ GDPA_ERR_DEVICE_TIMEOUT = 4
 GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
-EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
            "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
     P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     L.gdpa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
     L.gdpa_fwd_async.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P]
+    L.gdpa_fwd_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
     L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
     L.gdpa_fwd_planned.argtypes = [P, P, P, P, P, P, F, P, P]
     L.gdpa_plan_destroy.argtypes = [P]
@@ -73,7 +74,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_status_string.restype = ctypes.c_char_p
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
-    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
+    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
                  "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
@@ -116,6 +117,13 @@ def gdpa_fwd(q, k, v, q_offsets, kv_offsets, B, H, D, act, window_blocks, scale,
     _check(lib().gdpa_fwd(_addr(q), _addr(k), _addr(v), _addr(q_offsets), _addr(kv_offsets), int(B), int(H),
                           int(D), int(act), int(window_blocks), float(scale), _addr(out), _stream(stream)),
            "gdpa_fwd")
+
+
+def gdpa_fwd_noalloc(q, k, v, q_offsets, kv_offsets, B, H, D, act, window_blocks, scale, out, stream=None):
+    """gdpa_fwd without any allocation (fixed 4 MiB device work-list array; see include/gdpa.h)."""
+    _check(lib().gdpa_fwd_noalloc(_addr(q), _addr(k), _addr(v), _addr(q_offsets), _addr(kv_offsets), int(B), int(H),
+                                  int(D), int(act), int(window_blocks), float(scale), _addr(out), _stream(stream)),
+           "gdpa_fwd_noalloc")
 
 
 def gdpa_fwd_async(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, window_blocks, scale,
