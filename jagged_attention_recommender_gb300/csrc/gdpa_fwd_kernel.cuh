@@ -357,21 +357,30 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
           // columns become -inf.  With scale > 0 the scaling is folded into
           // the exponent's FMA; otherwise it is applied first.
           const bool fold = sl > 0.0f;
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             if (ch >= nch) continue;
+            if (full && fold) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const int c = 32 * ch + u;
-              float x = __uint_as_float(sr[c]);
-              if (!fold) x *= sl;
-              if (!full && (c < c_lo || c > c_hi)) x = -INFINITY;
-              sr[c] = __float_as_uint(x);
-              m4[u & 3] = fmaxf(m4[u & 3], x);
+              for (int u = 0; u < 32; u += 4) {
+                const int c = 32 * ch + u;
+                m2[0] = ptx::max3(m2[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                m2[1] = ptx::max3(m2[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const int c = 32 * ch + u;
+                float x = __uint_as_float(sr[c]);
+                if (!fold) x *= sl;
+                if (!full && (c < c_lo || c > c_hi)) x = -INFINITY;
+                sr[c] = __float_as_uint(x);
+                m2[u & 1] = fmaxf(m2[u & 1], x);
+              }
             }
           }
-          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          float mx = fmaxf(m2[0], m2[1]);
           if (fold) mx *= sl;
           const float m_new = fmaxf(m_run, mx);
           if (j == 0) {
@@ -383,29 +392,31 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
             rescale = true;
           }
           const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-          const float mul = fold ? sl : 1.0f;
-          float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (ch >= nch) continue;
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const int c = 32 * ch + u;
-              const float e = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), mul, -m_use));
-              s4[u & 3] += e;
-              sr[c] = __float_as_uint(e);
-            }
-          }
-          l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          // masked entries hold -inf and give exactly 0; with scale > 0 the
+          // entries are still unscaled and take the scale in the packed FMA
+          const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
+          const uint64_t neg2 = ptx::f2_splat(-m_use);
+          uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             if (ch >= nch) continue;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-              const int c = 16 * ch + u;
-              sr[c] = ptx::pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+              const int c = 32 * ch + 2 * u;
+              const uint64_t x2 =
+                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
+              float a, b;
+              ptx::f2_unpack(x2, a, b);
+              a = ptx::ex2_approx(a);
+              b = ptx::ex2_approx(b);
+              acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);
             }
           }
+          const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+          float sa, sb;
+          ptx::f2_unpack(acc01, sa, sb);
+          l_run += sa + sb;
         } else {  // GELU
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -413,8 +424,8 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               const int c = 16 * ch + u;
-              float a = gelu_tanh_alu(__uint_as_float(sr[2 * c]) * sl);
-              float b = gelu_tanh_alu(__uint_as_float(sr[2 * c + 1]) * sl);
+              float a, b;
+              gelu_tanh_alu2(__uint_as_float(sr[2 * c]) * sl, __uint_as_float(sr[2 * c + 1]) * sl, a, b);
               if (!full) {
                 a = (2 * c >= c_lo && 2 * c <= c_hi) ? a : 0.0f;
                 b = (2 * c + 1 >= c_lo && 2 * c + 1 <= c_hi) ? b : 0.0f;

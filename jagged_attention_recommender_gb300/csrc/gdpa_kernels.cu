@@ -108,9 +108,21 @@ gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, i
   return launch_k(gdpa_fwd_pair_kernel<D, ACT>, C::THREADS, C::SMEM_BYTES, prm, grid, stream, device, attr_done, &mu);
 }
 
+// Evaluates the activation exactly as the kernels do: GELU two arguments at
+// a time with the packed evaluation, exp2 on the special-function unit.
 __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = act == kActGelu ? gelu_tanh_alu(x[i]) : ptx::ex2_approx(x[i]);
+  for (int64_t i = 2 * (blockIdx.x * (int64_t)blockDim.x + threadIdx.x); i < n;
+       i += 2 * (int64_t)gridDim.x * blockDim.x) {
+    if (act == kActGelu) {
+      float a, b;
+      gelu_tanh_alu2(x[i], i + 1 < n ? x[i + 1] : 0.0f, a, b);
+      y[i] = a;
+      if (i + 1 < n) y[i + 1] = b;
+    } else {
+      y[i] = ptx::ex2_approx(x[i]);
+      if (i + 1 < n) y[i + 1] = ptx::ex2_approx(x[i + 1]);
+    }
+  }
 }
 
 // One thread waits, with the forward kernel's bounded wait, on an mbarrier

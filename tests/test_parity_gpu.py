@@ -202,6 +202,27 @@ def test_window_d64():
     assert_parity(run_gpu(b), oracle.gdpa_fwd_batch(b), "window D=64")
 
 
+@pytest.mark.parametrize("jump", [16.0, 64.0, 96.0])
+def test_softmax_score_jumps_between_key_tiles(jump):
+    # Keys of the first 128-key tile score 0, later keys score `jump` (scale 1):
+    # the running max rises by jump*log2(e) between tiles.  16 takes the
+    # deferred rescale, 64 and 96 overrun the single pass and redo the tile.
+    # Enough queries per sequence to take the two-tile items.
+    from tests.helpers import bits
+    rng = np.random.default_rng(5100)
+    L, H, D = 300, 1, 64
+    b = small_batch(rng, [L, L], [L, L], H, D, scale=1.0)
+    q = np.ones((2 * L, H, D), np.float32)
+    k = np.zeros((2 * L, H, D), np.float32)
+    for s0 in (0, L):
+        k[s0 + 128:s0 + L] = jump / D
+    from tests.helpers import with_values
+    b = with_values(b, q=bits(q), k=bits(k))
+    got = run_gpu(b)
+    ref = oracle.gdpa_fwd_batch(b)
+    assert_parity(got, ref, "jump %g" % jump)
+
+
 def test_zero_and_negative_scale():
     rng = np.random.default_rng(5000)
     for scale in (0.0, -0.09):
