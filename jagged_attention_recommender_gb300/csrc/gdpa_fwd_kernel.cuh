@@ -50,6 +50,7 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   int H;
   int window_blocks;
   float score_scale;         // softmax: scale * log2(e); GELU: scale
+  int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
 };
 
 enum : int { kActSoftmax = 0, kActGelu = 1 };
@@ -113,6 +114,23 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   v.kv_end = WIN ? min(v.Lkv, v.q0 + 128) : v.Lkv;
   v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
   return v;
+}
+
+// 32 bf16 values (16 packed words) to global memory: two 32-byte stores when
+// `v8` (the address is 32-byte aligned), else four 16-byte stores.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16], bool v8) {
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
+                 "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                 : "memory");
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16), "r"(pk[8]), "r"(pk[9]),
+                 "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+                 : "memory");
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
 }
 
 __device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {
@@ -484,11 +502,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-      if (row < t.q_rows) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-      }
+      if (row < t.q_rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&B.o_empty[ob]);

@@ -304,9 +304,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     }
     if (rows == 0) continue;  // this side has no tile in the item
     const bool rows_live = __any_sync(0xffffffffu, row < rows);
-    // m_run: the max that O and l are currently scaled by; m_pend: the max the
-    // next tile should use (raised when a tile's own max ran far above m_run).
-    float m_run = -INFINITY, l_run = 0.0f, m_pend = -INFINITY;
+    float m_run = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < t.n_kv; ++j, ++gx) {
       ok = ptx::mbar_wait(&B.s_full[x], gx & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
@@ -319,98 +317,98 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
         const bool full = ncols == 128;
         const int nch = (ncols + 31) >> 5;
         if (ACT == kActSoftmax) {
-          // Scores in log2 units: x = s * scale * log2(e).
-          // Full tiles after the first one with scale > 0 take a single pass
-          // against the running max, finding the tile's own max on the way.
-          // O and l stay exact whatever that max is (this tile's P is just
-          // larger); if it ran more than 2^8 above m_run the next tile switches
-          // to it (O and l are rescaled before that tile's P V), and beyond
-          // 2^64 the tile is redone with its row max found first.
+          // Scores in log2 units: x = s * scale * log2(e).  With scale > 0
+          // the scaling is folded into the exponent's FMA.
           const bool fold = sl > 0.0f;
-          bool need_max = !(fold && full && j > 0);
-          for (int attempt = 0; attempt < 2; ++attempt) {
-            if (need_max) {  // pass 1: row max over the valid columns
-              float m2[2] = {-INFINITY, -INFINITY};
-#pragma unroll 1
-              for (int c = 0; c < nch; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld32(s_addr + 32 * c, r);
-                ptx::tmem_wait_ld();
+          // pass 1: row max over the valid columns
+          float m2[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+          for (int cp = 0; cp < 2; ++cp) {
+            if (2 * cp >= nch) break;
+            uint32_t r[2][32];
+            ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
+            if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (2 * cp + h >= nch) break;
+              if (full && fold) {
+#pragma unroll
+                for (int u = 0; u < 32; u += 4) {
+                  m2[0] = ptx::max3(m2[0], __uint_as_float(r[h][u]), __uint_as_float(r[h][u + 1]));
+                  m2[1] = ptx::max3(m2[1], __uint_as_float(r[h][u + 2]), __uint_as_float(r[h][u + 3]));
+                }
+              } else {  // ragged tile, or scale <= 0 (scale first, then take the max)
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                  float v = __uint_as_float(r[u]) * sl;
-                  m2[u & 1] = fmaxf(m2[u & 1], (full || 32 * c + u < ncols) ? v : -INFINITY);
+                  const int c = 64 * cp + 32 * h + u;
+                  float v = __uint_as_float(r[h][u]);
+                  if (!fold) v *= sl;
+                  m2[u & 1] = fmaxf(m2[u & 1], c < ncols ? v : -INFINITY);
                 }
               }
-              const float m_new = fmaxf(m_run, fmaxf(m2[0], m2[1]));
-              if (m_run == -INFINITY) {
-                m_run = m_new;  // nothing accumulated yet: no rescale
-              } else if (m_new > m_run + 8.0f) {
-                const float a = ptx::ex2_approx(m_run - m_new);
-                alpha *= a;
-                l_run *= a;
-                m_run = m_new;
-                rescale = true;
-              }
-              m_pend = m_run;
-            } else if (m_pend != m_run) {  // the switch the previous tile asked for
-              const float a = ptx::ex2_approx(m_run - m_pend);
-              alpha *= a;
-              l_run *= a;
-              m_run = m_pend;
-              rescale = true;
             }
-            // pass 2: exponentials and row sum; P (bf16 pairs) is kept in
-            // registers and written over the scores only once the tile is
-            // accepted, so a redo still finds S intact.
-            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-            const uint64_t mul2 = ptx::f2_splat(sl);
-            const uint64_t neg2 = ptx::f2_splat(-m_use);
-            float tm2[2] = {-INFINITY, -INFINITY};
-            uint64_t acc[2] = {0, 0};
-            uint32_t pk[64];
+          }
+          float mx = fmaxf(m2[0], m2[1]);
+          if (fold) mx *= sl;
+          const float m_new = fmaxf(m_run, mx);
+          if (j == 0) {
+            m_run = m_new;
+          } else if (m_new > m_run + 8.0f) {
+            alpha = ptx::ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            rescale = true;
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+          const uint64_t mul2 = ptx::f2_pack(sl, sl);   // scale * log2(e), both lanes
+          const uint64_t neg2 = ptx::f2_pack(-m_use, -m_use);
+          // pass 2: exponentials, row sum, P (bf16 pairs) over the scores
+          uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
-            for (int cp = 0; cp < 2; ++cp) {
-              if (2 * cp >= nch) break;
-              uint32_t r[2][32];
-              ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
-              if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
-              ptx::tmem_wait_ld();
+          for (int cp = 0; cp < 2; ++cp) {
+            if (2 * cp >= nch) break;
+            uint32_t r[2][32];
+            ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
+            if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
+            ptx::tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                if (2 * cp + h >= nch) break;
+            for (int h = 0; h < 2; ++h) {
+              if (2 * cp + h >= nch) break;
+              uint32_t pk[16];
+              if (full) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
+                                                  mul2, neg2);
+                  float a, b;
+                  ptx::f2_unpack(x2, a, b);
+                  a = ptx::ex2_approx(a);
+                  b = ptx::ex2_approx(b);
+                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                  pk[u] = ptx::pack_bf16x2(a, b);
+                }
+              } else {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                   const int c = 64 * cp + 32 * h + 2 * u;
-                  const float s0 = __uint_as_float(r[h][2 * u]), s1 = __uint_as_float(r[h][2 * u + 1]);
-                  if (!need_max) tm2[u & 1] = ptx::max3(tm2[u & 1], s0, s1);
+                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
+                                                  mul2, neg2);
                   float a, b;
-                  ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s0, s1), mul2, neg2), a, b);
-                  a = ptx::ex2_approx(a);
-                  b = ptx::ex2_approx(b);
-                  if (!full) {
-                    a = c < ncols ? a : 0.0f;
-                    b = c + 1 < ncols ? b : 0.0f;
-                  }
-                  acc[u & 1] = ptx::f2_add(acc[u & 1], ptx::f2_pack(a, b));
-                  pk[32 * cp + 16 * h + u] = ptx::pack_bf16x2(a, b);
+                  ptx::f2_unpack(x2, a, b);
+                  a = c < ncols ? ptx::ex2_approx(a) : 0.0f;
+                  b = c + 1 < ncols ? ptx::ex2_approx(b) : 0.0f;
+                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                  pk[u] = ptx::pack_bf16x2(a, b);
                 }
               }
+              ptx::tmem_st16(s_addr + 32 * cp + 16 * h, pk);
             }
-            const float tmx = fmaxf(tm2[0], tm2[1]) * sl;
-            if (!need_max && __any_sync(0xffffffffu, tmx > m_run + 64.0f)) {
-              need_max = true;  // redo this tile with its row max found first
-              continue;
-            }
-            float sa, sb;
-            ptx::f2_unpack(ptx::f2_add(acc[0], acc[1]), sa, sb);
-            l_run += sa + sb;
-            if (!need_max && tmx > m_run + 8.0f) m_pend = tmx;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              if (q4 < nch) ptx::tmem_st16(s_addr + 16 * q4, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
-            break;
           }
+          const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+          float sa, sb;
+          ptx::f2_unpack(acc01, sa, sb);
+          l_run += sa + sb;
         } else {  // GELU, one pass
 #pragma unroll
           for (int cp = 0; cp < 2; ++cp) {
@@ -479,11 +477,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        if (row < rows) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        if (row < rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
       }
     }
     ptx::tc_fence_before();

@@ -176,6 +176,7 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.H = a.H;
   prm.window_blocks = a.window_blocks;
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
+  prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks > 0;
   if (a.rows_per_item == 256) {
