@@ -83,13 +83,14 @@ struct DeviceCtx {
   bool events_ok = false;
   // gdpa_fwd_host pipeline: copy-in and copy-out streams, per-chunk events
   cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[kMaxChunks] = {}, ev_done[kMaxChunks] = {};
+  cudaEvent_t ev_start = nullptr, ev_meta = nullptr, ev_in[kMaxChunks] = {}, ev_done[kMaxChunks] = {};
   bool host_path_ok = false;
   gdpa_status_t init_host_path() {
     if (host_path_ok) return GDPA_OK;
     if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess) return GDPA_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess) return GDPA_ERR_CUDA;
     if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&ev_meta, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
     for (int i = 0; i < kMaxChunks; ++i)
       if (cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) != cudaSuccess)
@@ -445,11 +446,16 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
   char* dmeta = base + 2 * bq + 2 * bkv;
   char* hmeta = static_cast<char*>(c.h_io.p);
 
-  // copies in, chunk by chunk, behind whatever `stream` already holds
+  // All copies in run in order on one copy stream: chunk 0's inputs, then
+  // every chunk's offsets and work list in one piece, then the other chunks'
+  // inputs; chunk i computes as soon as its inputs are in and copies out on a
+  // second copy stream, so the host link carries inputs and outputs at once.
+  // (A work list uploaded later on the compute stream would queue behind all
+  // the input copies on the same copy engine and hold every kernel back.)
   if (cudaEventRecord(c.ev_start, s) != cudaSuccess || cudaStreamWaitEvent(c.s_in, c.ev_start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(c.s_out, c.ev_start, 0) != cudaSuccess)
     return GDPA_ERR_CUDA;
-  for (int i = 0; i < C; ++i) {
+  auto copy_in = [&](int i) -> gdpa_status_t {
     const size_t q0 = (size_t)qo[cut[i]] * row, q1 = (size_t)qo[cut[i + 1]] * row;
     const size_t k0 = (size_t)ko[cut[i]] * row, k1 = (size_t)ko[cut[i + 1]] * row;
     if (q1 > q0 &&
@@ -463,9 +469,10 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
               cudaSuccess)
         return GDPA_ERR_CUDA;
     }
-    if (cudaEventRecord(c.ev_in[i], c.s_in) != cudaSuccess) return GDPA_ERR_CUDA;
-  }
-  // plan each chunk on the host while its inputs travel; launch; copy out
+    return cudaEventRecord(c.ev_in[i], c.s_in) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+  };
+  if ((st = copy_in(0)) != GDPA_OK) return st;
+  // plan every chunk on the host while chunk 0 travels
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
   for (int i = 0; i < C; ++i) {
@@ -476,7 +483,6 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
       hqo[b] = qo[b0 + b] - qo[b0];
       hko[b] = ko[b0 + b] - ko[b0];
     }
-    const int64_t Tq_i = hqo[nb], Tkv_i = hko[nb];
     if (n_items[i] > 0) {
       try {
         st = plan_items(hqo, hko, nb, H, window_blocks, rpi[i], ctas[i], items, cta_begin, nullptr);
@@ -487,11 +493,17 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
       std::memcpy(hmeta + work_at[i], items.data(), items.size() * sizeof(gdpa_work_item_t));
       std::memcpy(hmeta + work_at[i] + item_bytes[i], cta_begin.data(), cta_begin.size() * sizeof(int32_t));
     }
-    const size_t meta_end = i + 1 < C ? off_at[i + 1] : meta;
-    if (cudaMemcpyAsync(dmeta + off_at[i], hmeta + off_at[i], meta_end - off_at[i], cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaStreamWaitEvent(s, c.ev_in[i], 0) != cudaSuccess)
-      return GDPA_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(dmeta, hmeta, meta, cudaMemcpyHostToDevice, c.s_in) != cudaSuccess ||
+      cudaEventRecord(c.ev_meta, c.s_in) != cudaSuccess || cudaStreamWaitEvent(s, c.ev_meta, 0) != cudaSuccess)
+    return GDPA_ERR_CUDA;
+  for (int i = 1; i < C; ++i)
+    if ((st = copy_in(i)) != GDPA_OK) return st;
+  for (int i = 0; i < C; ++i) {
+    const int b0 = cut[i], nb = cut[i + 1] - cut[i];
+    const int32_t* hqo = reinterpret_cast<const int32_t*>(hmeta + off_at[i]);
+    const int64_t Tq_i = hqo[nb], Tkv_i = hqo[2 * nb + 1];
+    if (cudaStreamWaitEvent(s, c.ev_in[i], 0) != cudaSuccess) return GDPA_ERR_CUDA;
     if (n_items[i] > 0) {
       LaunchArgs a;
       a.q = dq + (size_t)qo[b0] * row;
