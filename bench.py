@@ -79,21 +79,37 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+# Source files each forward kernel is compiled from (the shared headers plus
+# its own); the hash keys the committed ncu traffic figure to the kernel.
+KERNEL_SOURCES = {
+    "gdpa_fwd_pair_kernel": ["gdpa_fwd_common.cuh", "sm103_ptx.cuh", "gelu_alu.cuh", "gdpa_fwd_pair.cuh"],
+    "gdpa_fwd_kernel": ["gdpa_fwd_common.cuh", "sm103_ptx.cuh", "gelu_alu.cuh", "gdpa_fwd_kernel.cuh"],
+}
+
+
+def kernel_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "jagged_attention_recommender_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "jagged_attention_recommender_gb300", "csrc", f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel build."""
+def kernel_for(batch, gdpa_mod, num_ctas: int) -> str:
+    """The kernel the planner picks for this batch (256-row items: the pair kernel)."""
+    w = batch.workload
+    _, _, _, rows = gdpa_mod.gdpa_plan_enumerate(batch.q_offsets, batch.kv_offsets, batch.B, w.H, w.D, w.act,
+                                                 w.window_blocks, num_ctas, with_rows=True)
+    return "gdpa_fwd_pair_kernel" if rows == 256 else "gdpa_fwd_kernel"
+
+
+def traffic_per_launch(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel's current source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t.get(workload)
-        if e and e.get("kernel_hash") == kernel_hash():
+        if e and e.get("kernel") == kernel and e.get("kernel_hash") == kernel_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -332,11 +348,12 @@ def run_ours(args, rank, world, local):
         achieved = nbytes / (launch_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
-    traffic = traffic_per_launch(args.workload)
+    kernel = kernel_for(batch, gdpa, torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
+    traffic = traffic_per_launch(args.workload, kernel)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": traffic, "peak_source": peak_src + (" (burst)" if bound == "tensor" else ""),
                 "launch_ms": launch_ms, "useful_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
-                "kernel_hash": kernel_hash()}
+                "kernel": kernel, "kernel_hash": kernel_hash(kernel)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

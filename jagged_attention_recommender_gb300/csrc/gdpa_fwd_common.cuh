@@ -1,0 +1,57 @@
+// gdpa_fwd_common.cuh -- what both forward kernels share: the launch
+// parameter block, the activation and status codes, and the row store.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "gelu_alu.cuh"
+#include "sm103_ptx.cuh"
+
+namespace gdpa {
+
+struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
+  CUtensorMap tm_q;  // 2-D view [T, H*D] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const int4* items;         // work items grouped by CTA: {seq, head, q0, kv0}
+  const int32_t* cta_begin;  // [gridDim.x + 1]
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  __nv_bfloat16* out;
+  int* status;               // device status word (bit set on a wait timeout)
+  unsigned long long timeout_ns;
+  int H;
+  int window_blocks;
+  float score_scale;         // softmax: scale * log2(e); GELU: scale
+  int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
+};
+
+enum : int { kActSoftmax = 0, kActGelu = 1 };
+
+enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatusEpilogue = 8 };
+
+// 32 bf16 values (16 packed words) to global memory: two 32-byte stores when
+// `v8` (the address is 32-byte aligned), else four 16-byte stores.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16], bool v8) {
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
+                 "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                 : "memory");
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16), "r"(pk[8]), "r"(pk[9]),
+                 "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+                 : "memory");
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+}
+
+__device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {
+  *abort = 1;
+  atomicOr(p.status, bit);
+}
+
+}  // namespace gdpa

@@ -3,19 +3,24 @@
 //
 // One CTA per SM walks its own list of work items (a 128-row query tile of
 // one (sequence, head) against its key range; built on the host, see
-// gdpa_plan.cpp).  Roles inside the CTA (224 threads):
+// gdpa_plan.cpp).  Roles inside the CTA (384 threads, three warpgroups):
 //
-//   warp 0      TMA producer for the Q tile (2 stages) and K tiles (NK
-//               stages); warp 6 TMA producer for V tiles (NV stages); all
+//   warpgroup 0 (registers handed back to the pool):
+//     warp 0    TMA producer for the Q tile (2 stages) and K tiles (NK
+//               stages); warp 2 TMA producer for V tiles (NV stages); all
 //               128-byte swizzled; K is released after Q K^T, V after P V;
-//   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory
+//     warp 1    MMA issuer (one thread): S = Q K^T into tensor memory
 //               (two S buffers), then O += P V with P read straight from
 //               tensor memory (two O buffers, one per in-flight item);
-//   warps 2..5  activation + epilogue, one query row per thread: reads S
-//               from TMEM, masks the ragged edge / window, applies the
-//               online softmax (running max with lazy rescaling of O) or the
-//               ALU-only GELU, writes P (bf16) back over S, and at the end of
-//               the item normalises O (1/l, or 1/Lkv for GELU) and stores it.
+//   warpgroup 1 (240 registers a thread): activation, one query row per
+//               thread: reads its whole row of S from TMEM at once, masks the
+//               ragged edge / window, applies the online softmax (running max
+//               with lazy rescaling of O) or the ALU-only GELU, and writes P
+//               (bf16) back over S; at the end of an item it hands the row
+//               sum to the epilogue through shared memory;
+//   warpgroup 2 epilogue: waits for the item's last O += P V, normalises O
+//               (1/l, or 1/Lkv for GELU), stores it, and frees the O buffer,
+//               while the activation warps already work on the next item.
 //
 // The MMA issuer runs one K/V tile ahead: it issues S(g+1) = Q K(g+1)^T
 // before O += P(g) V(g), so the tensor core works on the next tile while the
@@ -23,39 +28,18 @@
 // boundaries (the "outer loop" pipelining that matters when a key range is a
 // single tile: GDPA section of the techfeed summary of "GEM Training").
 //
+// Masks are applied per 32-column chunk and the chunk's class (all keys
+// valid, none valid, some valid) is agreed on by the warp: only the chunk
+// that holds a row's ragged end or its causal diagonal pays for a per-element
+// test, and chunks with no valid key are skipped (their P is zero).
+//
 // Synchronisation is by mbarriers only; every wait is bounded in time and a
 // timeout is reported in the device status word instead of hanging.
 #pragma once
 
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cstdint>
-
-#include "gelu_alu.cuh"
-#include "sm103_ptx.cuh"
+#include "gdpa_fwd_common.cuh"
 
 namespace gdpa {
-
-struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
-  CUtensorMap tm_q;  // 2-D view [T, H*D] bf16, box 64 x 128, 128-byte swizzle
-  CUtensorMap tm_k;
-  CUtensorMap tm_v;
-  const int4* items;         // work items grouped by CTA: {seq, head, q0, kv0}
-  const int32_t* cta_begin;  // [gridDim.x + 1]
-  const int32_t* q_off;
-  const int32_t* kv_off;
-  __nv_bfloat16* out;
-  int* status;               // device status word (bit set on a wait timeout)
-  unsigned long long timeout_ns;
-  int H;
-  int window_blocks;
-  float score_scale;         // softmax: scale * log2(e); GELU: scale
-  int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
-};
-
-enum : int { kActSoftmax = 0, kActGelu = 1 };
-
-enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4 };
 
 template <int D>
 struct FwdCfg {
@@ -70,12 +54,20 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
+  static constexpr int OFF_L = OFF_V + NV * TILE_BYTES;  // row sums, 2 x 128 floats
+  static constexpr int OFF_BAR = OFF_L + 2 * 128 * 4;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 224;  // 7 warps
+  static constexpr int THREADS = 384;  // 3 warpgroups
+  // Registers per thread after reallocation: control warpgroup, activation
+  // warpgroup; the epilogue keeps the launch count.  Each SM sub-partition
+  // holds one warp of each warpgroup, so the launch count R must satisfy
+  // REGS_CTRL + REGS_ACT + R <= 3 R.
+  static constexpr int REGS_CTRL = 56;
+  static constexpr int REGS_ACT = 248;
+  static constexpr int MIN_LAUNCH_REGS = (REGS_CTRL + REGS_ACT + 1) / 2;
   static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -86,8 +78,10 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done;
-  uint64_t o_empty[2];
+  uint64_t o_done;              // after every O += P V (activation)
+  uint64_t o_full[2];           // after an item's last O += P V into O[b] (epilogue)
+  uint64_t o_empty[2];          // the epilogue has drained O[b] (MMA)
+  uint64_t l_full[2], l_empty[2];  // row sums of the item using O[b] (activation <-> epilogue)
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort;
@@ -114,28 +108,6 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   v.kv_end = WIN ? min(v.Lkv, v.q0 + 128) : v.Lkv;
   v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
   return v;
-}
-
-// 32 bf16 values (16 packed words) to global memory: two 32-byte stores when
-// `v8` (the address is 32-byte aligned), else four 16-byte stores.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16], bool v8) {
-  if (v8) {
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
-                 "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
-                 : "memory");
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16), "r"(pk[8]), "r"(pk[9]),
-                 "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
-                 : "memory");
-  } else {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-  }
-}
-
-__device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {
-  *abort = 1;
-  atomicOr(p.status, bit);
 }
 
 // ------------------------------------------------------------------ producer
@@ -223,7 +195,7 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
 
 struct PendingPV {
   uint32_t g;
-  int sb, ob, qi, first, n16;
+  int sb, ob, qi, first, last, n16;
 };
 
 template <int D>
@@ -248,6 +220,7 @@ __device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<F
   }
   ptx::mma_commit(&B.v_empty[sv]);
   ptx::mma_commit(&B.o_done);
+  if (P.last) ptx::mma_commit(&B.o_full[P.ob]);
   return true;
 }
 
@@ -260,7 +233,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
   uint32_t g = 0;
   bool ok = true;
   bool have_prev = false;
-  PendingPV prev = {0, 0, 0, 0, 0, 0};
+  PendingPV prev = {0, 0, 0, 0, 0, 0, 0};
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<WIN>(p, idx);
     if (t.n_kv == 0) continue;
@@ -293,7 +266,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
         ok = issue_pv<D>(p, sm, B, tmem, prev);
         if (!ok) break;
       }
-      prev = PendingPV{g, sb, qi & 1, qi, j == 0 ? 1 : 0, n16};
+      prev = PendingPV{g, sb, qi & 1, qi, j == 0 ? 1 : 0, j == t.n_kv - 1 ? 1 : 0, n16};
       have_prev = true;
     }
     ++qi;
@@ -306,34 +279,28 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
   ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
 }
 
-// ------------------------------------------------------------------ activation + epilogue
+// ------------------------------------------------------------------ activation
+
+// Per-element validity of score column c (tile-relative) for this row.
+__device__ __forceinline__ bool col_ok(int c, int c_lo, int c_hi) { return c >= c_lo && c <= c_hi; }
 
 template <int D, int ACT, bool WIN>
-__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem, int ibeg, int iend,
-                               int warp, int lane) {
+__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, float* l_buf, uint32_t tmem,
+                               int ibeg, int iend, int warp, int lane) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float sl = p.score_scale;
-  const int H = p.H;
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<WIN>(p, idx);
-    __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + row) * H + t.h) * D;
-    if (t.n_kv == 0) {  // no keys: the output rows are zero
-      if (row < t.q_rows) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      continue;
-    }
+    if (t.n_kv == 0) continue;  // the epilogue writes the zero rows
     const int ob = qi & 1;
-    const uint32_t o_col = ob ? C::TM_O1 : C::TM_O0;
+    const uint32_t o_addr = tmem + lane_off + (ob ? C::TM_O1 : C::TM_O0);
     float m_run = -INFINITY, l_run = 0.0f;
     const int i_seq = t.q0 + row;  // query index inside its sequence
     int win_lo = 0;
@@ -354,21 +321,30 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       float alpha = 1.0f;
       bool rescale = false;
       if (rows_live) {
-        // valid key columns of this row: [c_lo, c_hi]; only the 32-column
-        // chunks that hold keys of the tile are read and processed.
+        // valid key columns of this row: [c_lo, c_hi] (tile-relative)
         const int kv_t0 = t.kv0 + 128 * j;
-        int c_lo = 0, c_hi = min(128, t.kv_end - kv_t0) - 1;
+        const int ncols = min(128, t.kv_end - kv_t0);  // the tile's key extent
+        int c_lo = 0, c_hi = ncols - 1;
         if (WIN) {
           c_lo = max(0, win_lo - kv_t0);
           c_hi = min(c_hi, i_seq - kv_t0);
         }
-        const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 127);
-        // chunks up to the tile's key extent: P V reads P over all of them
-        const int nch = (min(128, t.kv_end - kv_t0) + 31) >> 5;
+        const int nch = (ncols + 31) >> 5;  // chunks P V reads
+        // chunk classes agreed on by the warp: bit ch of `fullm` = every key
+        // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
+        // has a valid key in it
+        uint32_t fullm = 0, livem = 0;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int lo = 32 * ch, hi = 32 * ch + 31;
+          if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
+          if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
+        }
+        // The whole row of scores in registers, one TMEM round trip.
         uint32_t sr[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (c < nch) ptx::tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        for (int ch = 0; ch < 4; ++ch)
+          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
         ptx::tmem_wait_ld();
         if (ACT == kActSoftmax) {
           // Scores become log2-domain values x = s * scale * log2(e); masked
@@ -378,21 +354,21 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
           float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
-            if (ch >= nch) continue;
-            if (full && fold) {
+            if (!((livem >> ch) & 1u)) continue;
+            if (((fullm >> ch) & 1u) && fold) {
 #pragma unroll
               for (int u = 0; u < 32; u += 4) {
                 const int c = 32 * ch + u;
                 m2[0] = ptx::max3(m2[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
                 m2[1] = ptx::max3(m2[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
               }
-            } else {
+            } else {  // ragged end / diagonal chunk, or scale <= 0
 #pragma unroll
               for (int u = 0; u < 32; ++u) {
                 const int c = 32 * ch + u;
                 float x = __uint_as_float(sr[c]);
                 if (!fold) x *= sl;
-                if (!full && (c < c_lo || c > c_hi)) x = -INFINITY;
+                if (!col_ok(c, c_lo, c_hi)) x = -INFINITY;
                 sr[c] = __float_as_uint(x);
                 m2[u & 1] = fmaxf(m2[u & 1], x);
               }
@@ -418,6 +394,11 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
+#pragma unroll
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               const int c = 32 * ch + 2 * u;
@@ -428,27 +409,33 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
               a = ptx::ex2_approx(a);
               b = ptx::ex2_approx(b);
               acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
-              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);
+              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);  // P overwrites scores already consumed
             }
           }
           const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
-          float sa, sb;
-          ptx::f2_unpack(acc01, sa, sb);
-          l_run += sa + sb;
+          float sa, sb2;
+          ptx::f2_unpack(acc01, sa, sb2);
+          l_run += sa + sb2;
         } else {  // GELU
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
+            const bool full = (fullm >> ch) & 1u;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-              const int c = 16 * ch + u;
+              const int c = 32 * ch + 2 * u;
               float a, b;
-              gelu_tanh_alu2(__uint_as_float(sr[2 * c]) * sl, __uint_as_float(sr[2 * c + 1]) * sl, a, b);
+              gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, a, b);
               if (!full) {
-                a = (2 * c >= c_lo && 2 * c <= c_hi) ? a : 0.0f;
-                b = (2 * c + 1 >= c_lo && 2 * c + 1 <= c_hi) ? b : 0.0f;
+                a = col_ok(c, c_lo, c_hi) ? a : 0.0f;
+                b = col_ok(c + 1, c_lo, c_hi) ? b : 0.0f;
               }
-              sr[c] = ptx::pack_bf16x2(a, b);
+              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);
             }
           }
         }
@@ -465,7 +452,6 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       }
       if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
         ptx::tc_fence_after();
-        const uint32_t o_addr = tmem + lane_off + o_col;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -481,45 +467,91 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       ptx::mbar_arrive(&B.p_full[sb]);
     }
     if (!ok) break;
-    // epilogue: wait for the item's last O += P V, normalise, store
-    ok = ptx::mbar_wait(&B.o_done, (g - 1) & 1, p.timeout_ns, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    ptx::tc_fence_after();
-    float inv;
-    if (ACT == kActSoftmax)
-      inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    else
-      inv = 1.0f / static_cast<float>(t.Lkv);
-    const uint32_t o_addr = tmem + lane_off + o_col;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      if (!rows_live) break;
-      uint32_t r[32];
-      ptx::tmem_ld32(o_addr + 32 * c, r);
-      ptx::tmem_wait_ld();
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-      if (row < t.q_rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
+    if (ACT == kActSoftmax) {  // hand the row sum to the epilogue
+      ok = ptx::mbar_wait(&B.l_empty[ob], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      l_buf[ob * 128 + row] = l_run;
+      ptx::mbar_arrive(&B.l_full[ob]);
     }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&B.o_empty[ob]);
     ++qi;
   }
   if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
 }
 
+// ------------------------------------------------------------------ epilogue
+
+template <int D, int ACT, bool WIN>
+__device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, const float* l_buf,
+                             uint32_t tmem, int ibeg, int iend, int warp, int lane) {
+  using C = FwdCfg<D>;
+  volatile int* abort = &B.abort;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const int H = p.H;
+  const bool v8 = p.out_align32 != 0;
+  int qi = 0;
+  bool ok = true;
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const ItemView t = decode_item<WIN>(p, idx);
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + row) * H + t.h) * D;
+    if (t.n_kv == 0) {  // no keys: the output rows are zero
+      if (row < t.q_rows) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    const int ob = qi & 1;
+    const uint32_t ph = (qi >> 1) & 1;
+    float inv;
+    if (ACT == kActSoftmax) {
+      ok = ptx::mbar_wait(&B.l_full[ob], ph, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const float l = l_buf[ob * 128 + row];
+      ptx::mbar_arrive(&B.l_empty[ob]);
+      inv = l > 0.0f ? 1.0f / l : 0.0f;
+    } else {
+      inv = 1.0f / static_cast<float>(t.Lkv);
+    }
+    ok = ptx::mbar_wait(&B.o_full[ob], ph, p.timeout_ns, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    if (__any_sync(0xffffffffu, row < t.q_rows)) {
+      const uint32_t o_addr = tmem + lane_off + (ob ? C::TM_O1 : C::TM_O0);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld32(o_addr + 32 * c, r);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        if (row < t.q_rows) store_row32(orow + 32 * c, pk, v8);
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&B.o_empty[ob]);
+    ++qi;
+  }
+  if (!ok && lane == 0) report_failure(p, abort, kStatusEpilogue);
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int D, int ACT, bool WIN>
-__global__ void __launch_bounds__(224, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
   Bars<C::NK, C::NV>& B = *reinterpret_cast<Bars<C::NK, C::NV>*>(sm + C::OFF_BAR);
+  float* l_buf = reinterpret_cast<float*>(sm + C::OFF_L);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ibeg = p.cta_begin[blockIdx.x];
@@ -531,7 +563,10 @@ __global__ void __launch_bounds__(224, 1) gdpa_fwd_kernel(const __grid_constant_
       ptx::mbar_init(&B.q_empty[i], 1);
       ptx::mbar_init(&B.s_full[i], 1);
       ptx::mbar_init(&B.p_full[i], 128);
+      ptx::mbar_init(&B.o_full[i], 1);
       ptx::mbar_init(&B.o_empty[i], 128);
+      ptx::mbar_init(&B.l_full[i], 128);
+      ptx::mbar_init(&B.l_empty[i], 128);
     }
     for (int i = 0; i < C::NK; ++i) {
       ptx::mbar_init(&B.k_full[i], 1);
@@ -555,14 +590,20 @@ __global__ void __launch_bounds__(224, 1) gdpa_fwd_kernel(const __grid_constant_
   ptx::tc_fence_after();
   const uint32_t tmem = B.tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) run_producer<D, WIN, false>(p, sm, B, ibeg, iend);
-  } else if (warp == 6) {
-    if (lane == 0) run_producer<D, WIN, true>(p, sm, B, ibeg, iend);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
-  } else {
-    run_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp, lane);
+  if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
+    ptx::regs_dec<C::REGS_CTRL>();
+    if (warp == 0) {
+      if (lane == 0) run_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+    } else if (warp == 2) {
+      if (lane == 0) run_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+    } else if (warp == 1) {
+      if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+    }
+  } else if (warp < 8) {  // warpgroup 1: activation, a whole row of scores in registers
+    ptx::regs_inc<C::REGS_ACT>();
+    run_activation<D, ACT, WIN>(p, B, l_buf, tmem, ibeg, iend, warp, lane);
+  } else {  // warpgroup 2: epilogue, at the launch register count
+    run_epilogue<D, ACT, WIN>(p, B, l_buf, tmem, ibeg, iend, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();

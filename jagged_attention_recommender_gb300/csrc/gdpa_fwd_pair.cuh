@@ -20,7 +20,7 @@
 // 32-column chunks, so only ~64 scores are live in registers at a time.
 #pragma once
 
-#include "gdpa_fwd_kernel.cuh"
+#include "gdpa_fwd_common.cuh"
 
 namespace gdpa {
 

@@ -75,12 +75,18 @@ unsigned long long wait_timeout_ns() {
   return ns;
 }
 
+// `min_regs`: a kernel that moves registers between its warpgroups needs at
+// least this many registers a thread at launch, or its register increase
+// would wait forever; such a build is refused instead of launched.
 template <typename Kernel>
-gdpa_status_t launch_k(Kernel kernel, int threads, int smem, const FwdParams& prm, int grid, cudaStream_t stream,
-                       int device, bool* attr_done, std::mutex* mu) {
+gdpa_status_t launch_k(Kernel kernel, int threads, int smem, int min_regs, const FwdParams& prm, int grid,
+                       cudaStream_t stream, int device, bool* attr_done, std::mutex* mu) {
   {
     std::lock_guard<std::mutex> lock(*mu);
     if (!attr_done[device]) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return GDPA_ERR_CUDA;
+      if (fa.numRegs < min_regs || fa.maxThreadsPerBlock < threads) return GDPA_ERR_UNSUPPORTED;
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDPA_ERR_CUDA;
       attr_done[device] = true;
@@ -96,7 +102,8 @@ gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int 
   using C = FwdCfg<D>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  return launch_k(gdpa_fwd_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, prm, grid, stream, device, attr_done, &mu);
+  return launch_k(gdpa_fwd_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
+                  device, attr_done, &mu);
 }
 
 // Two query tiles per work item (full attention).
@@ -105,7 +112,8 @@ gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, i
   using C = PairCfg<D>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  return launch_k(gdpa_fwd_pair_kernel<D, ACT>, C::THREADS, C::SMEM_BYTES, prm, grid, stream, device, attr_done, &mu);
+  return launch_k(gdpa_fwd_pair_kernel<D, ACT>, C::THREADS, C::SMEM_BYTES, 0, prm, grid, stream, device, attr_done,
+                  &mu);
 }
 
 // Evaluates the activation exactly as the kernels do: GELU two arguments at

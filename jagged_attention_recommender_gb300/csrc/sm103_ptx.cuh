@@ -193,6 +193,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ register reallocation
+
+// Moves registers between the warpgroups of a CTA: every warp of a
+// warpgroup executes the same call.  `dec` returns registers to the CTA's
+// pool; `inc` waits until the pool holds enough.  The launch must have
+// allocated at least the sum of the per-warp counts the roles end up with
+// (the host checks this against the kernel's register count).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ misc
 
 // 2^x on the special-function unit (ex2.approx, flush-to-zero).
