@@ -119,11 +119,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Plans on the host and uploads the work list through the pinned staging
 // buffer into c.d_work (both guarded by events against earlier calls).
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
-                              int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
+                              int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
                               int64_t* n_items) {
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
-  const int rpi = choose_rows_per_item(h_q_off, B, window_blocks);
+  const int rpi = choose_rows_per_item(h_q_off, B, D, window_blocks);
   const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *rows_per_item = rpi;
   *n_items = n;
@@ -229,7 +229,7 @@ extern "C" gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, c
   if (Tq == 0) return GDPA_OK;
   int num_ctas = 0, rpi = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, hq, hk, B, H, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK) return st;
+  if ((st = plan_and_upload(c, hq, hk, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK) return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
                          rpi, n_items, s);
 }
@@ -254,7 +254,7 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int num_ctas = 0, rpi = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) !=
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) !=
       GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
@@ -285,7 +285,7 @@ extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int3
   P->d_buf = nullptr;
   P->d_items = nullptr;
   P->d_cta_begin = nullptr;
-  P->rows_per_item = choose_rows_per_item(h_q_offsets, B, window_blocks);
+  P->rows_per_item = choose_rows_per_item(h_q_offsets, B, D, window_blocks);
   const int64_t n = B > 0 ? count_plan_items(h_q_offsets, B, H, P->rows_per_item) : 0;
   P->n_items = n;
   P->num_ctas = (int)(n < sms ? n : sms);
@@ -421,7 +421,7 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
     // rows per item depend only on the lengths, which rebasing keeps
     std::vector<int32_t> tmp(nb + 1);
     for (int b = 0; b <= nb; ++b) tmp[b] = qo[cut[i] + b] - qo[cut[i]];
-    rpi[i] = choose_rows_per_item(tmp.data(), nb, window_blocks);
+    rpi[i] = choose_rows_per_item(tmp.data(), nb, D, window_blocks);
     const int64_t n = count_plan_items(tmp.data(), nb, H, rpi[i]);
     n_items[i] = n;
     ctas[i] = (int)(n < sms ? n : sms);

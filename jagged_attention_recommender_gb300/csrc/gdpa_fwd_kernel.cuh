@@ -41,7 +41,7 @@
 
 namespace gdpa {
 
-template <int D>
+template <int D, bool KS = false>
 struct FwdCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -55,7 +55,14 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_L = OFF_V + NV * TILE_BYTES;  // row sums, 2 x 128 floats
-  static constexpr int OFF_BAR = OFF_L + 2 * 128 * 4;
+  // Key split only: row maxima (2 x 128 floats) and the exchange buffer in
+  // which the four warps' partial output rows meet (4 x 32 rows of 64
+  // floats, rows padded to 68 floats so that 16-byte accesses by a warp are
+  // free of bank conflicts).
+  static constexpr int OFF_M = OFF_L + 2 * 128 * 4;
+  static constexpr int X_STRIDE = 68;
+  static constexpr int OFF_X = OFF_M + (KS ? 2 * 128 * 4 : 0);
+  static constexpr int OFF_BAR = OFF_X + (KS ? 4 * 32 * X_STRIDE * 4 : 0);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
@@ -70,6 +77,7 @@ struct FwdCfg {
   static constexpr int MIN_LAUNCH_REGS = (REGS_CTRL + REGS_ACT + 1) / 2;
   static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!KS || D == 64, "key split is built for D = 64");
 };
 
 // Shared-memory barrier block.
@@ -82,6 +90,7 @@ struct Bars {
   uint64_t o_full[2];           // after an item's last O += P V into O[b] (epilogue)
   uint64_t o_empty[2];          // the epilogue has drained O[b] (MMA)
   uint64_t l_full[2], l_empty[2];  // row sums of the item using O[b] (activation <-> epilogue)
+  uint64_t x_full, x_empty;     // key split: partial rows written / read (epilogue warps)
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort;
@@ -116,7 +125,7 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
 // K tiles, the other V tiles.  A K load therefore never waits behind a V
 // slot (freed only when an earlier P V completes), which would otherwise
 // chain one load latency into every pair of tiles.
-template <int D, bool WIN, bool LOAD_V>
+template <int D, bool WIN, bool LOAD_V, bool KS>
 __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, int ibeg, int iend) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
@@ -145,9 +154,17 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
       ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
       q_armed[qs] = (qi >> 1) & 1;
       uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
+      if (KS) {  // the (at most) 32 queries in each lane quarter: the Q map's box is 32 rows
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+        for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            ptx::tma_load_2d(sq + c * C::CHUNK_BYTES + r * 32 * 128, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(sq + c * C::CHUNK_BYTES, &p.tm_q, &B.q_full[qs], t.h * D + 64 * c, t.q_tok);
+      }
     }
     for (int j = 0; j < t.n_kv; ++j, ++g) {
       const int y = t.kv_tok + t.kv0 + 128 * j;
@@ -284,9 +301,9 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
 // Per-element validity of score column c (tile-relative) for this row.
 __device__ __forceinline__ bool col_ok(int c, int c_lo, int c_hi) { return c >= c_lo && c <= c_hi; }
 
-template <int D, int ACT, bool WIN>
-__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, float* l_buf, uint32_t tmem,
-                               int ibeg, int iend, int warp, int lane) {
+template <int D, int ACT, bool WIN, bool KS>
+__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, float* l_buf, float* m_buf,
+                               uint32_t tmem, int ibeg, int iend, int warp, int lane) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -310,7 +327,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
     }
     // A warp whose 32 rows all lie past the end of the query tile keeps the
     // barrier protocol but skips the math (e.g. 3 of 4 warps for 32 queries).
-    const bool rows_live = __any_sync(0xffffffffu, row < t.q_rows);
+    const bool rows_live = __any_sync(0xffffffffu, (KS ? lane : row) < t.q_rows);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
       const int sb = g & 1;
       ok = ptx::mbar_wait(&B.s_full[sb], (g >> 1) & 1, p.timeout_ns, abort);
@@ -320,130 +337,226 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       const uint32_t s_addr = tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0);
       float alpha = 1.0f;
       bool rescale = false;
-      if (rows_live) {
-        // valid key columns of this row: [c_lo, c_hi] (tile-relative)
-        const int kv_t0 = t.kv0 + 128 * j;
-        const int ncols = min(128, t.kv_end - kv_t0);  // the tile's key extent
-        int c_lo = 0, c_hi = ncols - 1;
-        if (WIN) {
-          c_lo = max(0, win_lo - kv_t0);
-          c_hi = min(c_hi, i_seq - kv_t0);
-        }
-        const int nch = (ncols + 31) >> 5;  // chunks P V reads
-        // chunk classes agreed on by the warp: bit ch of `fullm` = every key
-        // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
-        // has a valid key in it
-        uint32_t fullm = 0, livem = 0;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int lo = 32 * ch, hi = 32 * ch + 31;
-          if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
-          if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
-        }
-        // The whole row of scores in registers, one TMEM round trip.
-        uint32_t sr[128];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
-        ptx::tmem_wait_ld();
-        if (ACT == kActSoftmax) {
-          // Scores become log2-domain values x = s * scale * log2(e); masked
-          // columns become -inf.  With scale > 0 the scaling is folded into
-          // the exponent's FMA; otherwise it is applied first.
-          const bool fold = sl > 0.0f;
-          float m2[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (!((livem >> ch) & 1u)) continue;
-            if (((fullm >> ch) & 1u) && fold) {
-#pragma unroll
-              for (int u = 0; u < 32; u += 4) {
-                const int c = 32 * ch + u;
-                m2[0] = ptx::max3(m2[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                m2[1] = ptx::max3(m2[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+      if constexpr (KS) {
+        if (rows_live) {
+          // Key split: every warp holds the same queries and owns the 32-key
+          // block [32 q, 32 q + 32) of the tile (its diagonal block of S).
+          const int ncols = min(128, t.kv_end - 128 * j);
+          const int nch = (ncols + 31) >> 5;
+          const int cb = 32 * quarter;
+          const bool live = cb < ncols, full = cb + 32 <= ncols;  // warp-uniform
+          uint32_t sr[32];
+          uint32_t pk[16];
+          if (live) {
+            ptx::tmem_ld32(s_addr + cb, sr);
+            ptx::tmem_wait_ld();
+          }
+          if (ACT == kActSoftmax) {
+            const bool fold = sl > 0.0f;
+            float mx = -INFINITY;
+            if (live) {
+              float m2[2] = {-INFINITY, -INFINITY};
+              if (full && fold) {
+  #pragma unroll
+                for (int u = 0; u < 32; u += 4) {
+                  m2[0] = ptx::max3(m2[0], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]));
+                  m2[1] = ptx::max3(m2[1], __uint_as_float(sr[u + 2]), __uint_as_float(sr[u + 3]));
+                }
+              } else {
+  #pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                  float x = __uint_as_float(sr[u]);
+                  if (!fold) x *= sl;
+                  if (cb + u >= ncols) x = -INFINITY;
+                  sr[u] = __float_as_uint(x);
+                  m2[u & 1] = fmaxf(m2[u & 1], x);
+                }
               }
-            } else {  // ragged end / diagonal chunk, or scale <= 0
-#pragma unroll
-              for (int u = 0; u < 32; ++u) {
-                const int c = 32 * ch + u;
-                float x = __uint_as_float(sr[c]);
-                if (!fold) x *= sl;
-                if (!col_ok(c, c_lo, c_hi)) x = -INFINITY;
-                sr[c] = __float_as_uint(x);
-                m2[u & 1] = fmaxf(m2[u & 1], x);
+              mx = fmaxf(m2[0], m2[1]);
+              if (fold) mx *= sl;
+            }
+            const float m_new = fmaxf(m_run, mx);
+            if (j == 0) {
+              m_run = m_new;
+            } else if (m_new > m_run + 8.0f) {
+              alpha = ptx::ex2_approx(m_run - m_new);
+              l_run *= alpha;
+              m_run = m_new;
+              rescale = true;
+            }
+            if (live) {
+              const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+              const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
+              const uint64_t neg2 = ptx::f2_splat(-m_use);
+              uint64_t acc[4] = {0, 0, 0, 0};
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const uint64_t x2 =
+                    ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), mul2, neg2);
+                float a, b;
+                ptx::f2_unpack(x2, a, b);
+                a = ptx::ex2_approx(a);
+                b = ptx::ex2_approx(b);
+                acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                pk[u] = ptx::pack_bf16x2(a, b);
               }
+              const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+              float sa, sb2;
+              ptx::f2_unpack(acc01, sa, sb2);
+              l_run += sa + sb2;
             }
-          }
-          float mx = fmaxf(m2[0], m2[1]);
-          if (fold) mx *= sl;
-          const float m_new = fmaxf(m_run, mx);
-          if (j == 0) {
-            m_run = m_new;
-          } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
-            alpha = ptx::ex2_approx(m_run - m_new);
-            l_run *= alpha;
-            m_run = m_new;
-            rescale = true;
-          }
-          const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-          // masked entries hold -inf and give exactly 0; with scale > 0 the
-          // entries are still unscaled and take the scale in the packed FMA
-          const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
-          const uint64_t neg2 = ptx::f2_splat(-m_use);
-          uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (ch >= nch) continue;
-            if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
-#pragma unroll
-              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
-              continue;
-            }
-#pragma unroll
+          } else if (live) {  // GELU
+  #pragma unroll
             for (int u = 0; u < 16; ++u) {
-              const int c = 32 * ch + 2 * u;
-              const uint64_t x2 =
-                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
               float a, b;
-              ptx::f2_unpack(x2, a, b);
-              a = ptx::ex2_approx(a);
-              b = ptx::ex2_approx(b);
-              acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
-              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);  // P overwrites scores already consumed
-            }
-          }
-          const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
-          float sa, sb2;
-          ptx::f2_unpack(acc01, sa, sb2);
-          l_run += sa + sb2;
-        } else {  // GELU
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (ch >= nch) continue;
-            if (!((livem >> ch) & 1u)) {
-#pragma unroll
-              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
-              continue;
-            }
-            const bool full = (fullm >> ch) & 1u;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int c = 32 * ch + 2 * u;
-              float a, b;
-              gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, a, b);
+              gelu_tanh_alu2(__uint_as_float(sr[2 * u]) * sl, __uint_as_float(sr[2 * u + 1]) * sl, a, b);
               if (!full) {
-                a = col_ok(c, c_lo, c_hi) ? a : 0.0f;
-                b = col_ok(c + 1, c_lo, c_hi) ? b : 0.0f;
+                a = cb + 2 * u < ncols ? a : 0.0f;
+                b = cb + 2 * u + 1 < ncols ? b : 0.0f;
               }
-              sr[16 * ch + u] = ptx::pack_bf16x2(a, b);
+              pk[u] = ptx::pack_bf16x2(a, b);
             }
           }
+          // P: this warp's block, zeros in the other blocks P V reads
+          uint32_t zero[16];
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) zero[u] = 0u;
+  #pragma unroll
+          for (int jb = 0; jb < 4; ++jb) {
+            if (jb >= nch) break;
+            if (jb == quarter && live)
+              ptx::tmem_st16(s_addr + 16 * jb, pk);
+            else
+              ptx::tmem_st16(s_addr + 16 * jb, zero);
+          }
+          ptx::tmem_wait_st();
         }
-        // P (bf16 pairs) overwrites the first 16 * nch columns of this S
-        // buffer; P V reads no column beyond them.
-        ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        if (nch > 2) ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        ptx::tmem_wait_st();
+      } else {
+        if (rows_live) {
+          // valid key columns of this row: [c_lo, c_hi] (tile-relative)
+          const int kv_t0 = t.kv0 + 128 * j;
+          const int ncols = min(128, t.kv_end - kv_t0);  // the tile's key extent
+          int c_lo = 0, c_hi = ncols - 1;
+          if (WIN) {
+            c_lo = max(0, win_lo - kv_t0);
+            c_hi = min(c_hi, i_seq - kv_t0);
+          }
+          const int nch = (ncols + 31) >> 5;  // chunks P V reads
+          // chunk classes agreed on by the warp: bit ch of `fullm` = every key
+          // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
+          // has a valid key in it
+          uint32_t fullm = 0, livem = 0;
+  #pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int lo = 32 * ch, hi = 32 * ch + 31;
+            if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
+            if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
+          }
+          // The whole row of scores in registers, one TMEM round trip.
+          uint32_t sr[128];
+  #pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
+          ptx::tmem_wait_ld();
+          if (ACT == kActSoftmax) {
+            // Scores become log2-domain values x = s * scale * log2(e); masked
+            // columns become -inf.  With scale > 0 the scaling is folded into
+            // the exponent's FMA; otherwise it is applied first.
+            const bool fold = sl > 0.0f;
+            float m2[2] = {-INFINITY, -INFINITY};
+  #pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              if (!((livem >> ch) & 1u)) continue;
+              if (((fullm >> ch) & 1u) && fold) {
+  #pragma unroll
+                for (int u = 0; u < 32; u += 4) {
+                  const int c = 32 * ch + u;
+                  m2[0] = ptx::max3(m2[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                  m2[1] = ptx::max3(m2[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                }
+              } else {  // ragged end / diagonal chunk, or scale <= 0
+  #pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                  const int c = 32 * ch + u;
+                  float x = __uint_as_float(sr[c]);
+                  if (!fold) x *= sl;
+                  if (!col_ok(c, c_lo, c_hi)) x = -INFINITY;
+                  sr[c] = __float_as_uint(x);
+                  m2[u & 1] = fmaxf(m2[u & 1], x);
+                }
+              }
+            }
+            float mx = fmaxf(m2[0], m2[1]);
+            if (fold) mx *= sl;
+            const float m_new = fmaxf(m_run, mx);
+            if (j == 0) {
+              m_run = m_new;
+            } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
+              alpha = ptx::ex2_approx(m_run - m_new);
+              l_run *= alpha;
+              m_run = m_new;
+              rescale = true;
+            }
+            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+            // masked entries hold -inf and give exactly 0; with scale > 0 the
+            // entries are still unscaled and take the scale in the packed FMA
+            const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
+            const uint64_t neg2 = ptx::f2_splat(-m_use);
+            uint64_t acc[4] = {0, 0, 0, 0};
+  #pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              if (ch >= nch) continue;
+              if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
+  #pragma unroll
+                for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+                continue;
+              }
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const int c = 32 * ch + 2 * u;
+                const uint64_t x2 =
+                    ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
+                float a, b;
+                ptx::f2_unpack(x2, a, b);
+                a = ptx::ex2_approx(a);
+                b = ptx::ex2_approx(b);
+                acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
+                sr[16 * ch + u] = ptx::pack_bf16x2(a, b);  // P overwrites scores already consumed
+              }
+            }
+            const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+            float sa, sb2;
+            ptx::f2_unpack(acc01, sa, sb2);
+            l_run += sa + sb2;
+          } else {  // GELU
+  #pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              if (ch >= nch) continue;
+              if (!((livem >> ch) & 1u)) {
+  #pragma unroll
+                for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+                continue;
+              }
+              const bool full = (fullm >> ch) & 1u;
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const int c = 32 * ch + 2 * u;
+                float a, b;
+                gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, a, b);
+                if (!full) {
+                  a = col_ok(c, c_lo, c_hi) ? a : 0.0f;
+                  b = col_ok(c + 1, c_lo, c_hi) ? b : 0.0f;
+                }
+                sr[16 * ch + u] = ptx::pack_bf16x2(a, b);
+              }
+            }
+          }
+          // P (bf16 pairs) overwrites the first 16 * nch columns of this S
+          // buffer; P V reads no column beyond them.
+          ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          if (nch > 2) ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          ptx::tmem_wait_st();
+        }
       }
       if (g >= 1) {  // O += P(g-1) V(g-1) has landed
         ok = ptx::mbar_wait(&B.o_done, (g - 1) & 1, p.timeout_ns, abort);
@@ -472,6 +585,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       l_buf[ob * 128 + row] = l_run;
+      if (KS) m_buf[ob * 128 + row] = m_run;
       ptx::mbar_arrive(&B.l_full[ob]);
     }
     ++qi;
@@ -481,9 +595,104 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 
 // ------------------------------------------------------------------ epilogue
 
-template <int D, int ACT, bool WIN>
+// Key split: the four warps hold partial results of the same queries over
+// disjoint key blocks (row max m_k, row sum l_k, unnormalised O_k).  Thread
+// (k, i) weighs its partial row by 2^(m_k - M) / sum_j 2^(m_j - M) l_j (the
+// softmax merge; 1/Lkv for GELU), writes it to the exchange buffer, and after
+// all four have written sums the four rows over its 16-column share of the
+// output row of query i.
+template <int D, int ACT>
+__device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B,
+                                                   const float* l_buf, const float* m_buf, float* x_buf, uint32_t tmem,
+                                                   const ItemView& t, int ob, uint32_t ph, uint32_t& xr, int quarter,
+                                                   int lane, bool v8) {
+  using C = FwdCfg<D, true>;
+  volatile int* abort = &B.abort;
+  float w;
+  if (ACT == kActSoftmax) {
+    bool ok = ptx::mbar_wait(&B.l_full[ob], ph, p.timeout_ns, abort);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    float mk[4], lk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mk[k] = m_buf[ob * 128 + 32 * k + lane];
+      lk[k] = l_buf[ob * 128 + 32 * k + lane];
+    }
+    ptx::mbar_arrive(&B.l_empty[ob]);
+    const float M = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
+    float den = 0.0f, own = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float e = mk[k] == -INFINITY ? 0.0f : ptx::ex2_approx(mk[k] - M);
+      den += e * lk[k];
+      if (k == quarter) own = e;
+    }
+    w = den > 0.0f ? own / den : 0.0f;
+  } else {
+    w = 1.0f / static_cast<float>(t.Lkv);
+  }
+  bool ok = ptx::mbar_wait(&B.o_full[ob], ph, p.timeout_ns, abort);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  ok = ptx::mbar_wait(&B.x_empty, (xr & 1) ^ 1, p.timeout_ns, abort);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  ptx::tc_fence_after();
+  const uint32_t o_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (ob ? C::TM_O1 : C::TM_O0);
+  float* xrow = x_buf + (quarter * 32 + lane) * C::X_STRIDE;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(o_addr + 32 * c, r);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(xrow + 32 * c + i) =
+          make_float4(__uint_as_float(r[i]) * w, __uint_as_float(r[i + 1]) * w, __uint_as_float(r[i + 2]) * w,
+                      __uint_as_float(r[i + 3]) * w);
+  }
+  ptx::tc_fence_before();
+  ptx::mbar_arrive(&B.o_empty[ob]);  // O[ob] has been read
+  ptx::mbar_arrive(&B.x_full);
+  ok = ptx::mbar_wait(&B.x_full, xr & 1, p.timeout_ns, abort);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float* src = x_buf + (k * 32 + lane) * C::X_STRIDE + 16 * quarter;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src + i);
+      acc[i] += v.x;
+      acc[i + 1] += v.y;
+      acc[i + 2] += v.z;
+      acc[i + 3] += v.w;
+    }
+  }
+  ptx::mbar_arrive(&B.x_empty);
+  ++xr;
+  if (lane < t.q_rows) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    __nv_bfloat16* dst = p.out + (static_cast<size_t>(t.q_tok + lane) * p.H + t.h) * D + 16 * quarter;
+    if (v8) {
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(pk[0]), "r"(pk[1]),
+                   "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                   : "memory");
+    } else {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  }
+  return true;
+}
+
+template <int D, int ACT, bool WIN, bool KS>
 __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, const float* l_buf,
-                             uint32_t tmem, int ibeg, int iend, int warp, int lane) {
+                             const float* m_buf, float* x_buf, uint32_t tmem, int ibeg, int iend, int warp,
+                             int lane) {
   using C = FwdCfg<D>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
@@ -492,12 +701,14 @@ __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::
   const int H = p.H;
   const bool v8 = p.out_align32 != 0;
   int qi = 0;
+  uint32_t xr = 0;  // key split: exchange rounds
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<WIN>(p, idx);
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: the output rows are zero
-      if (row < t.q_rows) {
+      if (KS ? (quarter == 0 && lane < t.q_rows) : row < t.q_rows) {
+        if (KS) orow = p.out + (static_cast<size_t>(t.q_tok + lane) * H + t.h) * D;
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -506,6 +717,11 @@ __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::
     }
     const int ob = qi & 1;
     const uint32_t ph = (qi >> 1) & 1;
+    if constexpr (KS) {
+      ok = epilogue_key_split<D, ACT>(p, B, l_buf, m_buf, x_buf, tmem, t, ob, ph, xr, quarter, lane, v8);
+      ++qi;
+      continue;
+    }
     float inv;
     if (ACT == kActSoftmax) {
       ok = ptx::mbar_wait(&B.l_full[ob], ph, p.timeout_ns, abort);
@@ -544,14 +760,16 @@ __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int ACT, bool WIN>
+template <int D, int ACT, bool WIN, bool KS>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, KS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
   Bars<C::NK, C::NV>& B = *reinterpret_cast<Bars<C::NK, C::NV>*>(sm + C::OFF_BAR);
   float* l_buf = reinterpret_cast<float*>(sm + C::OFF_L);
+  float* m_buf = reinterpret_cast<float*>(sm + C::OFF_M);  // key split only
+  float* x_buf = reinterpret_cast<float*>(sm + C::OFF_X);  // key split only
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ibeg = p.cta_begin[blockIdx.x];
@@ -577,6 +795,8 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
       ptx::mbar_init(&B.v_empty[i], 1);
     }
     ptx::mbar_init(&B.o_done, 1);
+    ptx::mbar_init(&B.x_full, 128);
+    ptx::mbar_init(&B.x_empty, 128);
     ptx::mbar_init(&B.mma_drain, 1);
     B.abort = 0;
     ptx::fence_mbar_init();
@@ -593,17 +813,17 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
     ptx::regs_dec<C::REGS_CTRL>();
     if (warp == 0) {
-      if (lane == 0) run_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+      if (lane == 0) run_producer<D, WIN, false, KS>(p, sm, B, ibeg, iend);
     } else if (warp == 2) {
-      if (lane == 0) run_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+      if (lane == 0) run_producer<D, WIN, true, KS>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
       if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
     }
   } else if (warp < 8) {  // warpgroup 1: activation, a whole row of scores in registers
     ptx::regs_inc<C::REGS_ACT>();
-    run_activation<D, ACT, WIN>(p, B, l_buf, tmem, ibeg, iend, warp, lane);
+    run_activation<D, ACT, WIN, KS>(p, B, l_buf, m_buf, tmem, ibeg, iend, warp, lane);
   } else {  // warpgroup 2: epilogue, at the launch register count
-    run_epilogue<D, ACT, WIN>(p, B, l_buf, tmem, ibeg, iend, warp, lane);
+    run_epilogue<D, ACT, WIN, KS>(p, B, l_buf, m_buf, x_buf, tmem, ibeg, iend, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -12,6 +12,7 @@ namespace gdpa {
 constexpr int kBlockM = 128;      // query rows per work item (one tcgen05 M=128 tile)
 constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kWindowBlock = 64;  // block size of the block-aligned window
+constexpr int kKeySplitRows = 32; // query rows of a key-split item
 
 inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blocks) {
   if (B < 0 || H <= 0 || window_blocks < 0) return GDPA_ERR_INVALID_ARG;
@@ -25,10 +26,12 @@ inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blo
 gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks,
                                int64_t* Tq, int64_t* Tkv);
 
-// Query rows per work item: 256 (two 128-row tiles sharing every K/V tile)
-// for full attention when the batch's sequences average more than 128
-// queries, else 128.
-int choose_rows_per_item(const int32_t* q_off, int B, int window_blocks);
+// Query rows per work item: 32 (key-split items: every sequence has at most
+// 32 queries, D = 64, full attention; the four activation warps share the
+// queries and split each K/V tile), 256 (two 128-row tiles sharing every
+// K/V tile) for full attention when the batch's sequences average more than
+// 128 queries, else 128.
+int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks);
 
 // Number of work items plan_items will emit.
 int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item);
@@ -48,7 +51,7 @@ struct LaunchArgs {
   const gdpa_work_item_t* items;  // device, grouped by CTA
   const int32_t* cta_begin;       // device [num_ctas + 1]
   int num_ctas;
-  int rows_per_item;      // 128: one query tile per item; 256: two
+  int rows_per_item;      // 128: one query tile per item; 256: two; 32: key split
   int64_t Tq, Tkv;
   int H, D, act, window_blocks;
   float scale;

@@ -37,14 +37,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D view of a [rows, H, D] bf16 tensor as [rows, H*D]; boxes of 128 rows x
-// 64 columns (128 bytes, the swizzle width).  Rows past the end read as zero.
-gdpa_status_t encode_rows(CUtensorMap* m, const void* base, int64_t rows, int H, int D) {
+// 2-D view of a [rows, H, D] bf16 tensor as [rows, H*D]; boxes of
+// `box_rows` rows x 64 columns (128 bytes, the swizzle width).  Rows past the
+// end read as zero.
+gdpa_status_t encode_rows(CUtensorMap* m, const void* base, int64_t rows, int H, int D, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return GDPA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -96,13 +97,14 @@ gdpa_status_t launch_k(Kernel kernel, int threads, int smem, int min_regs, const
   return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
-// One query tile per work item (any key range, block window included).
-template <int D, int ACT, bool WIN>
+// One query tile per work item (any key range, block window included); KS:
+// at most 32 queries per item, the key range split over the four warps.
+template <int D, int ACT, bool WIN, bool KS = false>
 gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, KS>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  return launch_k(gdpa_fwd_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
+  return launch_k(gdpa_fwd_kernel<D, ACT, WIN, KS>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
                   device, attr_done, &mu);
 }
 
@@ -166,7 +168,8 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   int* status = status_ptr(device);
   if (!status) return GDPA_ERR_CUDA;
   FwdParams prm;
-  gdpa_status_t st = encode_rows(&prm.tm_q, a.q, a.Tq, a.H, a.D);
+  const bool key_split = a.rows_per_item == kKeySplitRows;
+  gdpa_status_t st = encode_rows(&prm.tm_q, a.q, a.Tq, a.H, a.D, key_split ? kKeySplitRows : kBlockM);
   if (st != GDPA_OK) return st;
   // With no keys at all no K/V tile is ever loaded; any valid address will do.
   const void* kb = a.Tkv > 0 ? a.k : a.q;
@@ -196,6 +199,11 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
       return a.act == GDPA_ACT_GELU_TANH ? launch_pair<64, kActGelu>(prm, a.num_ctas, s, device)
                                          : launch_pair<64, kActSoftmax>(prm, a.num_ctas, s, device);
     return GDPA_ERR_UNSUPPORTED;
+  }
+  if (key_split) {
+    if (win || a.D != 64) return GDPA_ERR_INVALID_ARG;
+    return a.act == GDPA_ACT_GELU_TANH ? launch_t<64, kActGelu, false, true>(prm, a.num_ctas, s, device)
+                                       : launch_t<64, kActSoftmax, false, true>(prm, a.num_ctas, s, device);
   }
   if (a.rows_per_item != 128) return GDPA_ERR_INVALID_ARG;
   if (a.D == 128) {

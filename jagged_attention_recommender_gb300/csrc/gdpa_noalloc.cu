@@ -66,7 +66,7 @@ gdpa_status_t na_plan(const int32_t* qo, const int32_t* ko, int B, int H, int wi
         kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
       }
       if (kv_end < kv0) kv_end = kv0;
-      const int64_t tiles = std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM;
+      const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM);
       const int64_t c = tiles * na_item_cost(kv_end - kv0);
       for (int h = 0; h < H; ++h) {
         if (n >= kNaMaxItems) return GDPA_ERR_NO_MEMORY;
@@ -155,7 +155,7 @@ extern "C" gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const vo
     return GDPA_ERR_INVALID_ARG;
   if (Tq >= (int64_t)1 << 31 || Tkv >= (int64_t)1 << 31) return GDPA_ERR_UNSUPPORTED;
   if (Tq == 0) return GDPA_OK;
-  const int rpi = choose_rows_per_item(hq, B, window_blocks);
+  const int rpi = choose_rows_per_item(hq, B, D, window_blocks);
   const int64_t n_est = count_plan_items(hq, B, H, rpi);
   if (n_est > kNaMaxItems) return GDPA_ERR_NO_MEMORY;
   const int num_ctas = (int)std::min<int64_t>(std::min<int64_t>(n_est, sms), kNaMaxCtas);

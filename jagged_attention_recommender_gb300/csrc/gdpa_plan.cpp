@@ -52,10 +52,15 @@ static int64_t item_cost(int64_t kv_len) {
   return ((kv_len + 15) / 16) * 16 + 96;
 }
 
-int choose_rows_per_item(const int32_t* q_off, int B, int window_blocks) {
+int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks) {
   if (window_blocks > 0 || B <= 0) return kBlockM;
-  int64_t busy = 0;
-  for (int b = 0; b < B; ++b) busy += q_off[b + 1] > q_off[b] ? 1 : 0;
+  int64_t busy = 0, max_lq = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t lq = q_off[b + 1] - q_off[b];
+    busy += lq > 0 ? 1 : 0;
+    max_lq = std::max<int64_t>(max_lq, lq);
+  }
+  if (busy > 0 && D == 64 && max_lq <= kKeySplitRows) return kKeySplitRows;
   return (busy > 0 && q_off[B] > (int64_t)kBlockM * busy) ? 2 * kBlockM : kBlockM;
 }
 
@@ -69,7 +74,8 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
                          int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items_out,
                          std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
   if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
-  if (rows_per_item != kBlockM && !(rows_per_item == 2 * kBlockM && window_blocks == 0)) return GDPA_ERR_INVALID_ARG;
+  if (rows_per_item != kBlockM && !((rows_per_item == 2 * kBlockM || rows_per_item == kKeySplitRows) && window_blocks == 0))
+    return GDPA_ERR_INVALID_ARG;
   std::vector<gdpa_work_item_t> items;
   std::vector<int64_t> cost;
   const int64_t n = count_plan_items(q_off, B, H, rows_per_item);
@@ -86,7 +92,8 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
         kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
       }
       if (kv_end < kv0) kv_end = kv0;
-      const int64_t tiles = std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM;  // 1 or 2
+      // query tiles the item's K/V feeds: 1 or 2 (a key-split item is one tile)
+      const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM);
       const int64_t c = tiles * item_cost(kv_end - kv0);
       for (int h = 0; h < H; ++h) {
         items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});
@@ -167,7 +174,7 @@ extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const i
   std::vector<gdpa_work_item_t> v;
   std::vector<int32_t> cb;
   std::vector<int64_t> c;
-  const int rpi = gdpa::choose_rows_per_item(h_q_offsets, B, window_blocks);
+  const int rpi = gdpa::choose_rows_per_item(h_q_offsets, B, D, window_blocks);
   if (rows_per_item) *rows_per_item = rpi;
   try {
     st = gdpa::plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, rpi, num_ctas, v, cb, &c);

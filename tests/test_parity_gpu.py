@@ -187,6 +187,47 @@ def test_cross_softmax_long_kv(D):
     assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "pma-like D=%d" % D)
 
 
+# Key-split items (D = 64, every sequence at most 32 queries): the four
+# activation warps share the queries and split each K/V tile into 32-key
+# blocks; key counts around the block and tile edges, and query counts below
+# and at 32.
+KS_LQ = [1, 7, 31, 32, 32, 5, 32, 32, 17, 32, 32, 32, 2, 32]
+KS_LKV = [1, 31, 32, 33, 95, 96, 97, 127, 128, 129, 255, 256, 0, 1000]
+
+
+@pytest.mark.parametrize("H", [1, 3, 8])
+def test_key_split_edges_softmax(H):
+    rng = np.random.default_rng(3100 + H)
+    b = small_batch(rng, np.array(KS_LQ), np.array(KS_LKV), H, 64)
+    items, _, _, rows = gdpa.gdpa_plan_enumerate(b.q_offsets, b.kv_offsets, b.B, H, 64, 0, 0, 8, with_rows=True)
+    assert rows == 32
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "key split H=%d" % H)
+
+
+def test_key_split_edges_gelu():
+    rng = np.random.default_rng(3200)
+    b = small_batch(rng, np.array(KS_LQ), np.array(KS_LKV), 2, 64, act=ACT_GELU_TANH, qk_norm=True, scale=1.0)
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "key split gelu", bf16_scaled=True)
+
+
+def test_key_split_merges_blocks_with_far_apart_maxima():
+    # Each 32-key block of a tile has its own running max; blocks whose keys
+    # score 0, 20 and 60 (scale 1) must merge by 2^(m_k - M) exactly, and
+    # later tiles raise the max again (lazy rescale inside one warp).
+    from tests.helpers import bits, with_values
+    rng = np.random.default_rng(3300)
+    Lkv, H, D = 520, 2, 64
+    b = small_batch(rng, [32, 9], [Lkv, Lkv], H, D, scale=1.0)
+    q = np.ones((41, H, D), np.float32)
+    k = rng.standard_normal((2 * Lkv, H, D)).astype(np.float32) * 0.01
+    for s0 in (0, Lkv):
+        k[s0 + 32:s0 + 64] += 20.0 / D
+        k[s0 + 100:s0 + 128] += 60.0 / D
+        k[s0 + 300:s0 + 310] += 90.0 / D
+    b = with_values(b, q=bits(q), k=bits(k))
+    assert_parity(run_gpu(b), oracle.gdpa_fwd_batch(b), "key split maxima")
+
+
 @pytest.mark.parametrize("wb", [1, 2, 4, 7])
 def test_window_variants(wb):
     rng = np.random.default_rng(4000 + wb)

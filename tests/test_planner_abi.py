@@ -125,6 +125,23 @@ def test_plan_empty_sequences():
     assert len(items) == 2 and set(items[:, 0]) == {2}
 
 
+def test_short_query_batches_take_key_split_items():
+    # D = 64, full attention, every sequence at most 32 queries: one 32-row
+    # item per (sequence, head); otherwise the 128/256-row rule applies
+    qo, ko = offsets_of(np.array([32, 0, 5, 32])), offsets_of(np.array([900, 40, 0, 3000]))
+    items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, 4, 3, 64, 0, 0, 5, with_rows=True)
+    assert R == 32
+    assert sorted(map(tuple, items[:, :3].tolist())) == sorted((b, h, 0) for b in (0, 2, 3) for h in range(3))
+    assert np.all(items[:, 3] == 0) and cta[-1] == len(items)
+    # cost grows with the key range
+    by_seq = {int(b): c for (b, _, _, _), c in zip(items, cost)}
+    assert by_seq[3] > by_seq[0] > by_seq[2]
+    for D, wb, lq in ((128, 0, 32), (64, 2, 32), (64, 0, 33)):
+        q2 = offsets_of(np.array([lq, lq]))
+        _, _, _, R2 = gdpa.gdpa_plan_enumerate(q2, q2, 2, 1, D, 0, wb, 4, with_rows=True)
+        assert R2 == 128
+
+
 def test_plan_balances_the_long_jagged_workload():
     w = WORKLOADS["self_long"]
     Lq, Lkv = draw_lengths(w, np.random.default_rng(w.seed))
