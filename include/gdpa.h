@@ -185,7 +185,8 @@ gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_k
  * gdpa_act_eval -- evaluates the kernel's device activation elementwise:
  * y[i] = gelu(x[i]) with the ALU-only polynomial (act = GDPA_ACT_GELU_TANH),
  * or y[i] = 2^x[i] with the exponential the softmax path uses
- * (act = GDPA_ACT_SOFTMAX).  x, y: device fp32 [n].  For accuracy tests.
+ * (act = GDPA_ACT_SOFTMAX).  x, y: device fp32 [n].  For accuracy tests;
+ * GDPA_ERR_INVALID_ARG for any other act.
  */
 gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
 

@@ -124,8 +124,8 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
   const int rpi = choose_rows_per_item(h_q_off, B, D, window_blocks);
-  const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *rows_per_item = rpi;
+  const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *n_items = n;
   if (n == 0) {
     *num_ctas = 0;
@@ -227,9 +227,11 @@ extern "C" gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, c
   if ((st = validate_offsets(hq, hk, B, window_blocks, &Tq, &Tkv)) != GDPA_OK) return st;
   if ((st = check_tensors(q, k, v, out, Tq, Tkv)) != GDPA_OK) return st;
   if (Tq == 0) return GDPA_OK;
-  int num_ctas = 0, rpi = 0;
+  int num_ctas = 0;
+  int rpi = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, hq, hk, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK) return st;
+  if ((st = plan_and_upload(c, hq, hk, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK)
+    return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
                          rpi, n_items, s);
 }
@@ -252,10 +254,11 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
   std::lock_guard<std::mutex> lock(c.mu);
   if ((st = c.init()) != GDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int num_ctas = 0, rpi = 0;
+  int num_ctas = 0;
+  int rpi = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) !=
-      GDPA_OK)
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi,
+                            &n_items)) != GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
                          rpi, n_items, s);
@@ -293,7 +296,8 @@ extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int3
     std::vector<gdpa_work_item_t> items;
     std::vector<int32_t> cta_begin;
     try {
-      st = plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, P->rows_per_item, P->num_ctas, items, cta_begin,
+      st = plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, P->rows_per_item, P->num_ctas, items,
+                      cta_begin,
                       nullptr);
     } catch (const std::bad_alloc&) {
       st = GDPA_ERR_NO_MEMORY;
@@ -413,7 +417,8 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
   }
   // per-chunk sizes of the rebased offsets and work lists
   int64_t n_items[kMaxChunks];
-  int ctas[kMaxChunks], rpi[kMaxChunks];
+  int ctas[kMaxChunks];
+  int rpi[kMaxChunks];
   size_t off_at[kMaxChunks], work_at[kMaxChunks], item_bytes[kMaxChunks];
   size_t meta = 0;
   for (int i = 0; i < C; ++i) {

@@ -41,20 +41,30 @@
 
 namespace gdpa {
 
-template <int D, bool KS = false>
+// Item kinds, one kernel instantiation each:
+//   full      128 query rows against the whole key range in 128-key tiles;
+//   window    128 query rows against their block window;
+//   key split at most 32 queries, each warp owns a 32-key block of every tile.
+enum : int { kModeFull = 0, kModeWindow = 1, kModeKeySplit = 2 };
+
+template <int D, int MODE = kModeFull>
 struct FwdCfg {
+  static constexpr bool WIN = MODE == kModeWindow;
+  static constexpr bool KS = MODE == kModeKeySplit;
   static constexpr int BM = 128;
-  static constexpr int BN = 128;
+  static constexpr int BN = 128;                   // keys per K/V tile
   static constexpr int KCH = D / 64;               // 64-element (128-byte) column chunks
-  static constexpr int CHUNK_BYTES = 128 * 128;    // one chunk: 128 rows x 128 bytes
+  static constexpr int CHUNK_BYTES = 128 * 128;    // Q chunk: 128 rows x 128 bytes
   static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;
-  static constexpr int NQ = 2;
-  static constexpr int NK = (D == 64) ? 4 : 3;   // K stages
-  static constexpr int NV = (D == 64) ? 4 : 2;   // V stages
+  static constexpr int KV_CHUNK_BYTES = BN * 128;  // K/V chunk: BN rows x 128 bytes
+  static constexpr int KV_TILE_BYTES = KCH * KV_CHUNK_BYTES;
+  static constexpr int NQ = 2;                                // Q stages
+  static constexpr int NK = (D == 64) ? 4 : 3;                // K stages
+  static constexpr int NV = (D == 64) ? 4 : 2;                // V stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
-  static constexpr int OFF_L = OFF_V + NV * TILE_BYTES;  // row sums, 2 x 128 floats
+  static constexpr int OFF_V = OFF_K + NK * KV_TILE_BYTES;
+  static constexpr int OFF_L = OFF_V + NV * KV_TILE_BYTES;  // row sums, 2 x 128 floats
   // Key split only: row maxima (2 x 128 floats) and the exchange buffer in
   // which the four warps' partial output rows meet (4 x 32 rows of 64
   // floats, rows padded to 68 floats so that 16-byte accesses by a warp are
@@ -81,9 +91,9 @@ struct FwdCfg {
 };
 
 // Shared-memory barrier block.
-template <int NK, int NV>
+template <int NQ, int NK, int NV>
 struct Bars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[NQ], q_empty[NQ];
   uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;              // after every O += P V (activation)
@@ -96,12 +106,17 @@ struct Bars {
   int abort;
 };
 
+template <int D, int MODE>
+using FwdBars = Bars<FwdCfg<D, MODE>::NQ, FwdCfg<D, MODE>::NK, FwdCfg<D, MODE>::NV>;
+
 struct ItemView {
   int h, q0, kv0, kv_end, n_kv, q_rows, q_tok, kv_tok, Lkv;
 };
 
-template <bool WIN>
+template <int MODE>
 __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
+  constexpr bool WIN = MODE == kModeWindow;
+  constexpr int BN = 128;
   const int4 it = __ldg(p.items + idx);
   ItemView v;
   const int b = it.x;
@@ -115,7 +130,7 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   v.Lkv = ke - ks;
   v.q_rows = min(128, qe - qs - v.q0);
   v.kv_end = WIN ? min(v.Lkv, v.q0 + 128) : v.Lkv;
-  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
+  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;
   return v;
 }
 
@@ -125,14 +140,17 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
 // K tiles, the other V tiles.  A K load therefore never waits behind a V
 // slot (freed only when an earlier P V completes), which would otherwise
 // chain one load latency into every pair of tiles.
-template <int D, bool WIN, bool LOAD_V, bool KS>
-__device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, int ibeg, int iend) {
-  using C = FwdCfg<D>;
+template <int D, int MODE, bool LOAD_V>
+__device__ void run_producer(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, int ibeg, int iend) {
+  using C = FwdCfg<D, MODE>;
+  constexpr bool KS = C::KS;
   volatile int* abort = &B.abort;
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
-  int q_armed[2] = {-1, -1};  // last parity armed per stage (for draining)
+  int q_armed[C::NQ];  // last parity armed per stage (for draining)
+#pragma unroll
+  for (int s = 0; s < C::NQ; ++s) q_armed[s] = -1;
   int k_armed[C::NK], v_armed[C::NV];
 #pragma unroll
   for (int s = 0; s < C::NK; ++s) k_armed[s] = -1;
@@ -145,14 +163,15 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const ItemView t = decode_item<WIN>(p, idx);
+    const ItemView t = decode_item<MODE>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
-      const int qs = qi & 1;
-      ok = ptx::mbar_wait(&B.q_empty[qs], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
+      const int qs = qi % C::NQ;
+      const uint32_t qph = (qi / C::NQ) & 1;
+      ok = ptx::mbar_wait(&B.q_empty[qs], qph ^ 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
-      q_armed[qs] = (qi >> 1) & 1;
+      q_armed[qs] = (int)qph;
       uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
       if (KS) {  // the (at most) 32 queries in each lane quarter: the Q map's box is 32 rows
 #pragma unroll
@@ -167,28 +186,28 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
       }
     }
     for (int j = 0; j < t.n_kv; ++j, ++g) {
-      const int y = t.kv_tok + t.kv0 + 128 * j;
+      const int y = t.kv_tok + t.kv0 + C::BN * j;
       if (!LOAD_V) {  // K is released once its Q K^T is done
         const int si = g % C::NK;
         const uint32_t ph = (g / C::NK) & 1;
         ok = ptx::mbar_wait(&B.k_empty[si], ph ^ 1, p.timeout_ns, abort);
         if (!ok) break;
-        uint8_t* dst = sm + C::OFF_K + si * C::TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(&B.k_full[si], C::TILE_BYTES);
+        uint8_t* dst = sm + C::OFF_K + si * C::KV_TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.k_full[si], C::KV_TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          ptx::tma_load_2d(dst + c * C::CHUNK_BYTES, &p.tm_k, &B.k_full[si], t.h * D + 64 * c, y);
+          ptx::tma_load_2d(dst + c * C::KV_CHUNK_BYTES, &p.tm_k, &B.k_full[si], t.h * D + 64 * c, y);
         k_armed[si] = (int)ph;
       } else {  // V is released once its P V is done
         const int si = g % C::NV;
         const uint32_t ph = (g / C::NV) & 1;
         ok = ptx::mbar_wait(&B.v_empty[si], ph ^ 1, p.timeout_ns, abort);
         if (!ok) break;
-        uint8_t* dst = sm + C::OFF_V + si * C::TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(&B.v_full[si], C::TILE_BYTES);
+        uint8_t* dst = sm + C::OFF_V + si * C::KV_TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.v_full[si], C::KV_TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          ptx::tma_load_2d(dst + c * C::CHUNK_BYTES, &p.tm_v, &B.v_full[si], t.h * D + 64 * c, y);
+          ptx::tma_load_2d(dst + c * C::KV_CHUNK_BYTES, &p.tm_v, &B.v_full[si], t.h * D + 64 * c, y);
         v_armed[si] = (int)ph;
       }
     }
@@ -198,7 +217,7 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK
   // Let every bulk copy this thread started land before the CTA can exit.
   const int never = 0;
   const unsigned long long drain_ns = 100000000ull;
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < C::NQ; ++s)
     if (q_armed[s] >= 0) ptx::mbar_wait(&B.q_full[s], (uint32_t)q_armed[s], drain_ns, &never);
 #pragma unroll
   for (int s = 0; s < C::NK; ++s)
@@ -215,24 +234,24 @@ struct PendingPV {
   int sb, ob, qi, first, last, n16;
 };
 
-template <int D>
-__device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem,
+template <int D, int MODE>
+__device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, uint32_t tmem,
                                          const PendingPV& P) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, MODE>;
   volatile int* abort = &B.abort;
   if (!ptx::mbar_wait(&B.p_full[P.sb], (P.g >> 1) & 1, p.timeout_ns, abort)) return false;
   if (P.first && !ptx::mbar_wait(&B.o_empty[P.ob], ((P.qi >> 1) & 1) ^ 1, p.timeout_ns, abort)) return false;
   const int sv = P.g % C::NV;
   if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
-  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::TILE_BYTES);
+  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::KV_TILE_BYTES);
   const uint32_t o_col = P.ob ? C::TM_O1 : C::TM_O0;
   const uint32_t p_col = P.sb ? C::TM_S1 : C::TM_S0;
   constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
   for (int kk = 0; kk < P.n16; ++kk) {
     // B = V tile, MN-major: 16 keys = two 8-row groups (SBO = 1024 B apart);
     // the two 64-column halves of D sit one chunk apart (LBO).
-    const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::CHUNK_BYTES, 1024);
+    const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK_BYTES, 1024);
     ptx::mma_ts(tmem + o_col, tmem + p_col + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
   }
   ptx::mma_commit(&B.v_empty[sv]);
@@ -241,10 +260,9 @@ __device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, Bars<F
   return true;
 }
 
-template <int D, bool WIN>
-__device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, uint32_t tmem, int ibeg,
-                        int iend) {
-  using C = FwdCfg<D>;
+template <int D, int MODE>
+__device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, uint32_t tmem, int ibeg, int iend) {
+  using C = FwdCfg<D, MODE>;
   volatile int* abort = &B.abort;
   int qi = 0;
   uint32_t g = 0;
@@ -252,10 +270,10 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
   bool have_prev = false;
   PendingPV prev = {0, 0, 0, 0, 0, 0, 0};
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const ItemView t = decode_item<WIN>(p, idx);
+    const ItemView t = decode_item<MODE>(p, idx);
     if (t.n_kv == 0) continue;
-    const int qs = qi & 1;
-    ok = ptx::mbar_wait(&B.q_full[qs], (qi >> 1) & 1, p.timeout_ns, abort);
+    const int qs = qi % C::NQ;
+    ok = ptx::mbar_wait(&B.q_full[qs], (qi / C::NQ) & 1, p.timeout_ns, abort);
     if (!ok) break;
     const uint32_t q_base = ptx::smem_u32(sm + C::OFF_Q + qs * C::TILE_BYTES);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
@@ -263,24 +281,25 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
       ok = ptx::mbar_wait(&B.k_full[s], (g / C::NK) & 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int ncols = min(128, t.kv_end - t.kv0 - 128 * j);
+      const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
       const int n16 = (ncols + 15) >> 4;
       const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
-      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + s * C::TILE_BYTES);
+      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + s * C::KV_TILE_BYTES);
       const int sb = g & 1;
       const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
-        const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-        ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base + off, 16, 1024), ptx::sdesc_sw128(k_base + off, 16, 1024),
+        const uint32_t qoff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+        const uint32_t koff = (kk >> 2) * C::KV_CHUNK_BYTES + (kk & 3) * 32;
+        ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024), ptx::sdesc_sw128(k_base + koff, 16, 1024),
                     idesc, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(&B.s_full[sb]);
       ptx::mma_commit(&B.k_empty[s]);
       if (j == t.n_kv - 1) ptx::mma_commit(&B.q_empty[qs]);
       if (have_prev) {
-        ok = issue_pv<D>(p, sm, B, tmem, prev);
+        ok = issue_pv<D, MODE>(p, sm, B, tmem, prev);
         if (!ok) break;
       }
       prev = PendingPV{g, sb, qi & 1, qi, j == 0 ? 1 : 0, j == t.n_kv - 1 ? 1 : 0, n16};
@@ -288,7 +307,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
     }
     ++qi;
   }
-  if (ok && have_prev) ok = issue_pv<D>(p, sm, B, tmem, prev);
+  if (ok && have_prev) ok = issue_pv<D, MODE>(p, sm, B, tmem, prev);
   if (!ok) report_failure(p, abort, kStatusMma);
   // Every MMA this thread issued is complete once this commit lands.
   ptx::mma_commit(&B.mma_drain);
@@ -301,10 +320,12 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, Bars<FwdCfg<D>::NK, Fwd
 // Per-element validity of score column c (tile-relative) for this row.
 __device__ __forceinline__ bool col_ok(int c, int c_lo, int c_hi) { return c >= c_lo && c <= c_hi; }
 
-template <int D, int ACT, bool WIN, bool KS>
-__device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, float* l_buf, float* m_buf,
-                               uint32_t tmem, int ibeg, int iend, int warp, int lane) {
-  using C = FwdCfg<D>;
+template <int D, int ACT, int MODE>
+__device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l_buf, float* m_buf, uint32_t tmem,
+                               int ibeg, int iend, int warp, int lane) {
+  using C = FwdCfg<D, MODE>;
+  constexpr bool WIN = C::WIN, KS = C::KS;
+  constexpr int NCH = C::BN / 32;  // 32-column chunks of a score tile
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int row = quarter * 32 + lane;
@@ -314,7 +335,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
   uint32_t g = 0;
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const ItemView t = decode_item<WIN>(p, idx);
+    const ItemView t = decode_item<MODE>(p, idx);
     if (t.n_kv == 0) continue;  // the epilogue writes the zero rows
     const int ob = qi & 1;
     const uint32_t o_addr = tmem + lane_off + (ob ? C::TM_O1 : C::TM_O0);
@@ -357,13 +378,13 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
             if (live) {
               float m2[2] = {-INFINITY, -INFINITY};
               if (full && fold) {
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 32; u += 4) {
                   m2[0] = ptx::max3(m2[0], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]));
                   m2[1] = ptx::max3(m2[1], __uint_as_float(sr[u + 2]), __uint_as_float(sr[u + 3]));
                 }
               } else {
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 32; ++u) {
                   float x = __uint_as_float(sr[u]);
                   if (!fold) x *= sl;
@@ -389,7 +410,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
               const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
               const uint64_t neg2 = ptx::f2_splat(-m_use);
               uint64_t acc[4] = {0, 0, 0, 0};
-  #pragma unroll
+#pragma unroll
               for (int u = 0; u < 16; ++u) {
                 const uint64_t x2 =
                     ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), mul2, neg2);
@@ -406,7 +427,7 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
               l_run += sa + sb2;
             }
           } else if (live) {  // GELU
-  #pragma unroll
+#pragma unroll
             for (int u = 0; u < 16; ++u) {
               float a, b;
               gelu_tanh_alu2(__uint_as_float(sr[2 * u]) * sl, __uint_as_float(sr[2 * u + 1]) * sl, a, b);
@@ -419,9 +440,9 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
           }
           // P: this warp's block, zeros in the other blocks P V reads
           uint32_t zero[16];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 16; ++u) zero[u] = 0u;
-  #pragma unroll
+#pragma unroll
           for (int jb = 0; jb < 4; ++jb) {
             if (jb >= nch) break;
             if (jb == quarter && live)
@@ -434,8 +455,8 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
       } else {
         if (rows_live) {
           // valid key columns of this row: [c_lo, c_hi] (tile-relative)
-          const int kv_t0 = t.kv0 + 128 * j;
-          const int ncols = min(128, t.kv_end - kv_t0);  // the tile's key extent
+          const int kv_t0 = t.kv0 + C::BN * j;
+          const int ncols = min(C::BN, t.kv_end - kv_t0);  // the tile's key extent
           int c_lo = 0, c_hi = ncols - 1;
           if (WIN) {
             c_lo = max(0, win_lo - kv_t0);
@@ -446,16 +467,16 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
           // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
           // has a valid key in it
           uint32_t fullm = 0, livem = 0;
-  #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
             const int lo = 32 * ch, hi = 32 * ch + 31;
             if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
             if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
           }
           // The whole row of scores in registers, one TMEM round trip.
-          uint32_t sr[128];
-  #pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
+          uint32_t sr[C::BN];
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch)
             if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
           ptx::tmem_wait_ld();
           if (ACT == kActSoftmax) {
@@ -464,18 +485,18 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
             // the exponent's FMA; otherwise it is applied first.
             const bool fold = sl > 0.0f;
             float m2[2] = {-INFINITY, -INFINITY};
-  #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
               if (!((livem >> ch) & 1u)) continue;
               if (((fullm >> ch) & 1u) && fold) {
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 32; u += 4) {
                   const int c = 32 * ch + u;
                   m2[0] = ptx::max3(m2[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
                   m2[1] = ptx::max3(m2[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
                 }
               } else {  // ragged end / diagonal chunk, or scale <= 0
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 32; ++u) {
                   const int c = 32 * ch + u;
                   float x = __uint_as_float(sr[c]);
@@ -503,11 +524,11 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
             const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
             const uint64_t neg2 = ptx::f2_splat(-m_use);
             uint64_t acc[4] = {0, 0, 0, 0};
-  #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
               if (ch >= nch) continue;
               if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
                 continue;
               }
@@ -529,16 +550,16 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
             ptx::f2_unpack(acc01, sa, sb2);
             l_run += sa + sb2;
           } else {  // GELU
-  #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
               if (ch >= nch) continue;
               if (!((livem >> ch) & 1u)) {
-  #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
                 continue;
               }
               const bool full = (fullm >> ch) & 1u;
-  #pragma unroll
+#pragma unroll
               for (int u = 0; u < 16; ++u) {
                 const int c = 32 * ch + 2 * u;
                 float a, b;
@@ -602,11 +623,11 @@ __device__ void run_activation(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>
 // all four have written sums the four rows over its 16-column share of the
 // output row of query i.
 template <int D, int ACT>
-__device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B,
+__device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, FwdBars<D, kModeKeySplit>& B,
                                                    const float* l_buf, const float* m_buf, float* x_buf, uint32_t tmem,
                                                    const ItemView& t, int ob, uint32_t ph, uint32_t& xr, int quarter,
                                                    int lane, bool v8) {
-  using C = FwdCfg<D, true>;
+  using C = FwdCfg<D, kModeKeySplit>;
   volatile int* abort = &B.abort;
   float w;
   if (ACT == kActSoftmax) {
@@ -689,11 +710,11 @@ __device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, Bars<FwdC
   return true;
 }
 
-template <int D, int ACT, bool WIN, bool KS>
-__device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::NV>& B, const float* l_buf,
-                             const float* m_buf, float* x_buf, uint32_t tmem, int ibeg, int iend, int warp,
-                             int lane) {
-  using C = FwdCfg<D>;
+template <int D, int ACT, int MODE>
+__device__ void run_epilogue(const FwdParams& p, FwdBars<D, MODE>& B, const float* l_buf, const float* m_buf,
+                             float* x_buf, uint32_t tmem, int ibeg, int iend, int warp, int lane) {
+  using C = FwdCfg<D, MODE>;
+  constexpr bool KS = C::KS;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
@@ -704,7 +725,7 @@ __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::
   uint32_t xr = 0;  // key split: exchange rounds
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const ItemView t = decode_item<WIN>(p, idx);
+    const ItemView t = decode_item<MODE>(p, idx);
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: the output rows are zero
       if (KS ? (quarter == 0 && lane < t.q_rows) : row < t.q_rows) {
@@ -760,13 +781,13 @@ __device__ void run_epilogue(const FwdParams& p, Bars<FwdCfg<D>::NK, FwdCfg<D>::
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int ACT, bool WIN, bool KS>
+template <int D, int ACT, int MODE>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D, KS>;
+  using C = FwdCfg<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
-  Bars<C::NK, C::NV>& B = *reinterpret_cast<Bars<C::NK, C::NV>*>(sm + C::OFF_BAR);
+  FwdBars<D, MODE>& B = *reinterpret_cast<FwdBars<D, MODE>*>(sm + C::OFF_BAR);
   float* l_buf = reinterpret_cast<float*>(sm + C::OFF_L);
   float* m_buf = reinterpret_cast<float*>(sm + C::OFF_M);  // key split only
   float* x_buf = reinterpret_cast<float*>(sm + C::OFF_X);  // key split only
@@ -776,9 +797,11 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   const int iend = p.cta_begin[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NQ; ++i) {
       ptx::mbar_init(&B.q_full[i], 1);
       ptx::mbar_init(&B.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&B.s_full[i], 1);
       ptx::mbar_init(&B.p_full[i], 128);
       ptx::mbar_init(&B.o_full[i], 1);
@@ -813,17 +836,17 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
     ptx::regs_dec<C::REGS_CTRL>();
     if (warp == 0) {
-      if (lane == 0) run_producer<D, WIN, false, KS>(p, sm, B, ibeg, iend);
+      if (lane == 0) run_producer<D, MODE, false>(p, sm, B, ibeg, iend);
     } else if (warp == 2) {
-      if (lane == 0) run_producer<D, WIN, true, KS>(p, sm, B, ibeg, iend);
+      if (lane == 0) run_producer<D, MODE, true>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
-      if (lane == 0) run_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+      if (lane == 0) run_mma<D, MODE>(p, sm, B, tmem, ibeg, iend);
     }
   } else if (warp < 8) {  // warpgroup 1: activation, a whole row of scores in registers
     ptx::regs_inc<C::REGS_ACT>();
-    run_activation<D, ACT, WIN, KS>(p, B, l_buf, m_buf, tmem, ibeg, iend, warp, lane);
+    run_activation<D, ACT, MODE>(p, B, l_buf, m_buf, tmem, ibeg, iend, warp, lane);
   } else {  // warpgroup 2: epilogue, at the launch register count
-    run_epilogue<D, ACT, WIN, KS>(p, B, l_buf, m_buf, x_buf, tmem, ibeg, iend, warp, lane);
+    run_epilogue<D, ACT, MODE>(p, B, l_buf, m_buf, x_buf, tmem, ibeg, iend, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -1,8 +1,10 @@
 // gdpa_fwd_pair.cuh -- jagged GDPA forward, two query tiles per work item.
 //
-// Full (non-window) attention.  A work item is 256 query rows of one
-// (sequence, head) -- tile A = rows [q0, q0+128), tile B = [q0+128, q0+256),
-// B may be empty -- against the sequence's whole key range.  Every K/V tile
+// A work item is 256 query rows of one (sequence, head) -- tile A = rows
+// [q0, q0+128), tile B = [q0+128, q0+256), B may be empty -- against the
+// sequence's whole key range (full attention) or against the keys of the
+// two tiles' block windows, each tile taking only the K/V tiles its rows
+// may see (window).  Every K/V tile
 // staged in shared memory feeds both tiles' MMAs, which halves the K/V
 // traffic per FLOP against one tile per item, and the two activation
 // warpgroups (one per tile) take turns with the tensor core:
@@ -12,12 +14,12 @@
 //   warpgroup A works on S_A(g) while the tensor core runs the B half, and
 //   the other way round.
 //
-// Threads (352): warp 0 TMA producer for Q and K, warp 10 TMA producer for
-// V, warp 1 MMA issuer + TMEM owner, warps 2-5 tile A activation/epilogue,
-// warps 6-9 tile B.  TMEM (512
-// columns): S_A 0, S_B 128, O_A 256, O_B 384.  An activation thread holds
-// one query row; it reads S from TMEM twice (row max, then exponentials) in
-// 32-column chunks, so only ~64 scores are live in registers at a time.
+// Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
+// and K (warp 0), the MMA issuer + TMEM owner (warp 1) and the TMA producer
+// for V (warp 2), and hands its registers to warpgroups 1 and 2, the
+// activation/epilogue of tiles A and B (216 registers a thread, so a whole
+// row of 128 scores stays in registers: S is read from TMEM once).  TMEM
+// (512 columns): S_A 0, S_B 128, O_A 256, O_B 384.
 #pragma once
 
 #include "gdpa_fwd_common.cuh"
@@ -42,7 +44,14 @@ struct PairCfg {
   __host__ __device__ static constexpr uint32_t tm_s(int x) { return x ? 128u : 0u; }    // S_A, S_B
   __host__ __device__ static constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }  // O_A, O_B
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 352;  // 11 warps
+  static constexpr int THREADS = 384;  // 3 warpgroups
+  // Registers per thread after reallocation: the control warpgroup hands
+  // registers to the two activation warpgroups.  Each SM sub-partition holds
+  // one warp of each, so the launch count R must satisfy
+  // REGS_CTRL + 2 REGS_ACT <= 3 R.
+  static constexpr int REGS_CTRL = 72;
+  static constexpr int REGS_ACT = 216;
+  static constexpr int MIN_LAUNCH_REGS = (REGS_CTRL + 2 * REGS_ACT + 2) / 3;
   static_assert(384 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -59,26 +68,44 @@ struct PairBars {
 };
 
 struct PairItem {
-  int h, q0, kv_end, n_kv, q_tok, kv_tok, Lkv;
+  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
   int rows[2];  // valid rows of tile A and tile B (B may be 0)
+  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each tile attends to
 };
 
+// Full attention: both tiles attend to every K/V tile of the item.  Block
+// window: the item's keys run from the first key tile A's rows may see to
+// the last query of tile B; tile A takes the K/V tiles up to its own last
+// query, tile B those from the first tile that holds a key its rows may see.
+template <bool WIN>
 __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
   const int4 it = __ldg(p.items + idx);
   PairItem v;
   const int b = it.x;
   v.h = it.y;
   v.q0 = it.z;
+  v.kv0 = WIN ? it.w : 0;
   const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
   const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
   v.q_tok = qs + v.q0;
   v.kv_tok = ks;
   v.Lkv = ke - ks;
-  v.kv_end = v.Lkv;
   const int left = qe - qs - v.q0;
   v.rows[0] = min(128, left);
   v.rows[1] = max(0, min(128, left - 128));
-  v.n_kv = (v.Lkv + 127) / 128;
+  v.kv_end = WIN ? min(v.Lkv, v.q0 + v.rows[0] + v.rows[1]) : v.Lkv;
+  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
+  v.t0[0] = 0;
+  v.t1[0] = v.n_kv;
+  v.t0[1] = 0;
+  v.t1[1] = v.rows[1] > 0 ? v.n_kv : 0;
+  if (WIN) {
+    const int end_a = min(v.Lkv, v.q0 + 128);
+    v.t1[0] = end_a > v.kv0 ? (end_a - v.kv0 + 127) / 128 : 0;
+    const int blk = (v.q0 + 128) / 64 - (p.window_blocks - 1);
+    const int lo_b = blk > 0 ? blk * 64 : 0;
+    v.t0[1] = (lo_b - v.kv0) / 128;
+  }
   return v;
 }
 
@@ -86,7 +113,7 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
 
 // Two producer threads: one stages Q and K, the other V, so that a K load
 // never waits behind a V slot.
-template <int D, bool LOAD_V>
+template <int D, bool WIN, bool LOAD_V>
 __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, int ibeg, int iend) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
@@ -105,7 +132,7 @@ __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, i
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair(p, idx);
+    const PairItem t = decode_pair<WIN>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {
@@ -124,7 +151,7 @@ __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, i
       }
     }
     for (int j = 0; j < t.n_kv && ok; ++j, ++g) {
-      const int y = t.kv_tok + 128 * j;
+      const int y = t.kv_tok + t.kv0 + 128 * j;
       if (!LOAD_V) {
         const int sk = g % C::NK;
         const uint32_t phk = (g / C::NK) & 1;
@@ -191,7 +218,7 @@ __device__ __forceinline__ bool pair_issue_pv(const FwdParams& p, uint8_t* sm, P
   return true;
 }
 
-template <int D>
+template <int D, bool WIN>
 __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32_t tmem, int ibeg, int iend) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
@@ -204,7 +231,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   bool pend_v = false;
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair(p, idx);
+    const PairItem t = decode_pair<WIN>(p, idx);
     if (t.n_kv == 0) continue;
     const bool has[2] = {t.rows[0] > 0, t.rows[1] > 0};
     uint32_t q_base[2] = {0, 0};
@@ -226,18 +253,22 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
       ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int ncols = min(128, t.kv_end - 128 * j);
+      const int ncols = min(128, t.kv_end - t.kv0 - 128 * j);
       const int n16 = (ncols + 15) >> 4;
       const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
       const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + sk * C::TILE_BYTES);
+      bool act[2];
       for (int x = 0; x < 2; ++x) {
-        // O_x += P_x(prev) V(prev) must precede S_x = Q_x K^T: P_x lives in S_x's columns.
+        // O_x += P_x(prev) V(prev) must precede S_x = Q_x K^T: P_x lives in
+        // S_x's columns.  A pending P V is issued here even when this tile
+        // has no S_x, so that every P V of the previous tile is issued now.
         if (pend[x]) {
           ok = pair_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
           if (!ok) break;
           pend[x] = false;
         }
-        if (!has[x]) continue;
+        act[x] = has[x] && j >= t.t0[x] && j < t.t1[x];
+        if (!act[x]) continue;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
@@ -254,8 +285,8 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
           if (has[x]) ptx::mma_commit(&B.q_empty[x][qn[x] % C::NQS]);
       }
       for (int x = 0; x < 2; ++x) {
-        if (!has[x]) continue;
-        pv[x] = PairPV{gx[x], g, qn[x], j == 0 ? 1 : 0, n16};
+        if (!act[x]) continue;
+        pv[x] = PairPV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
         pend[x] = true;
         ++gx[x];
       }
@@ -276,7 +307,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
 
 // ------------------------------------------------------------------ activation + epilogue
 
-template <int D, int ACT>
+template <int D, int ACT, bool WIN>
 __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tmem, int ibeg, int iend, int x,
                                 int warp, int lane) {
   using C = PairCfg<D>;
@@ -291,8 +322,8 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
   uint32_t gx = 0;
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair(p, idx);
-    const int rows = t.rows[x];
+    const PairItem t = decode_pair<WIN>(p, idx);
+    const int rows = x ? t.rows[1] : t.rows[0];
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: zero output rows
       if (row < rows) {
@@ -305,7 +336,16 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     if (rows == 0) continue;  // this side has no tile in the item
     const bool rows_live = __any_sync(0xffffffffu, row < rows);
     float m_run = -INFINITY, l_run = 0.0f;
-    for (int j = 0; j < t.n_kv; ++j, ++gx) {
+    const int i_seq = t.q0 + 128 * x + row;  // query index inside its sequence
+    int win_lo = 0;
+    if (WIN) {
+      const int blk = i_seq / 64 - (p.window_blocks - 1);
+      win_lo = blk > 0 ? blk * 64 : 0;
+    }
+    const int j0 = x ? t.t0[1] : t.t0[0], j1 = x ? t.t1[1] : t.t1[0];  // this side's K/V tiles
+    const int kv0 = t.kv0, kv_end = t.kv_end;
+    const float inv_lkv = 1.0f / static_cast<float>(max(t.Lkv, 1));
+    for (int j = j0; j < j1; ++j, ++gx) {
       ok = ptx::mbar_wait(&B.s_full[x], gx & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -313,46 +353,82 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
       float alpha = 1.0f;
       bool rescale = false;
       if (rows_live) {
-        const int ncols = min(128, t.kv_end - 128 * j);  // same for every row
-        const bool full = ncols == 128;
-        const int nch = (ncols + 31) >> 5;
+        // valid key columns of this row: [c_lo, c_hi] (tile-relative)
+        const int kv_t0 = kv0 + 128 * j;
+        const int ncols = min(128, kv_end - kv_t0);  // the tile's key extent
+        int c_lo = 0, c_hi = ncols - 1;
+        if (WIN) {
+          c_lo = max(0, win_lo - kv_t0);
+          c_hi = min(c_hi, i_seq - kv_t0);
+        }
+        const int nch = (ncols + 31) >> 5;  // chunks P V reads
+        // chunk classes agreed on by the warp: bit ch of `fullm` = every key
+        // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
+        // has a valid key in it.  Full attention masks only the ragged end
+        // of the last tile, the same for every row.
+        uint32_t fullm, livem;
+        if (WIN) {
+          fullm = 0;
+          livem = 0;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int lo = 32 * ch, hi = 32 * ch + 31;
+            if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
+            if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
+          }
+        } else {
+          livem = (1u << nch) - 1u;
+          fullm = (1u << (ncols >> 5)) - 1u;
+        }
+        // The whole row of scores in registers, one TMEM round trip.
+        uint32_t sr[128];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
+        ptx::tmem_wait_ld();
         if (ACT == kActSoftmax) {
-          // Scores in log2 units: x = s * scale * log2(e).  With scale > 0
-          // the scaling is folded into the exponent's FMA.
+          // Scores in log2 units: x = s * scale * log2(e); masked columns
+          // become -inf.  With scale > 0 the scaling is folded into the
+          // exponent's FMA; otherwise it is applied first.
           const bool fold = sl > 0.0f;
-          // pass 1: row max over the valid columns
-          float m2[2] = {-INFINITY, -INFINITY};
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (!WIN && fullm == 0xFu && fold) {
 #pragma unroll
-          for (int cp = 0; cp < 2; ++cp) {
-            if (2 * cp >= nch) break;
-            uint32_t r[2][32];
-            ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
-            if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
-            ptx::tmem_wait_ld();
+            for (int c = 0; c < 128; c += 8) {
+              m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+              m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
+          } else
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (2 * cp + h >= nch) break;
-              if (full && fold) {
+          for (int ch = 0; ch < 4; ++ch) {
+            if (!((livem >> ch) & 1u)) continue;
+            if (((fullm >> ch) & 1u) && fold) {
 #pragma unroll
-                for (int u = 0; u < 32; u += 4) {
-                  m2[0] = ptx::max3(m2[0], __uint_as_float(r[h][u]), __uint_as_float(r[h][u + 1]));
-                  m2[1] = ptx::max3(m2[1], __uint_as_float(r[h][u + 2]), __uint_as_float(r[h][u + 3]));
-                }
-              } else {  // ragged tile, or scale <= 0 (scale first, then take the max)
+              for (int u = 0; u < 32; u += 8) {
+                const int c = 32 * ch + u;
+                m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+              }
+            } else {  // ragged end / window edge / diagonal chunk, or scale <= 0
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                  const int c = 64 * cp + 32 * h + u;
-                  float v = __uint_as_float(r[h][u]);
-                  if (!fold) v *= sl;
-                  m2[u & 1] = fmaxf(m2[u & 1], c < ncols ? v : -INFINITY);
-                }
+              for (int u = 0; u < 32; ++u) {
+                const int c = 32 * ch + u;
+                float v = __uint_as_float(sr[c]);
+                if (!fold) v *= sl;
+                if (c < c_lo || c > c_hi) v = -INFINITY;
+                sr[c] = __float_as_uint(v);
+                m4[u & 3] = fmaxf(m4[u & 3], v);
               }
             }
           }
-          float mx = fmaxf(m2[0], m2[1]);
+          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           if (fold) mx *= sl;
           const float m_new = fmaxf(m_run, mx);
-          if (j == 0) {
+          if (j == j0) {
             m_run = m_new;
           } else if (m_new > m_run + 8.0f) {
             alpha = ptx::ex2_approx(m_run - m_new);
@@ -361,85 +437,69 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             rescale = true;
           }
           const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-          const uint64_t mul2 = ptx::f2_pack(sl, sl);   // scale * log2(e), both lanes
-          const uint64_t neg2 = ptx::f2_pack(-m_use, -m_use);
-          // pass 2: exponentials, row sum, P (bf16 pairs) over the scores
+          // masked entries hold -inf and give exactly 0; with scale > 0 the
+          // entries are still unscaled and take the scale in the packed FMA
+          const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
+          const uint64_t neg2 = ptx::f2_splat(-m_use);
           uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
-          for (int cp = 0; cp < 2; ++cp) {
-            if (2 * cp >= nch) break;
-            uint32_t r[2][32];
-            ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
-            if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
-            ptx::tmem_wait_ld();
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (2 * cp + h >= nch) break;
-              uint32_t pk[16];
-              if (full) {
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
-                                                  mul2, neg2);
-                  float a, b;
-                  ptx::f2_unpack(x2, a, b);
-                  a = ptx::ex2_approx(a);
-                  b = ptx::ex2_approx(b);
-                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
-                  pk[u] = ptx::pack_bf16x2(a, b);
-                }
-              } else {
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                  const int c = 64 * cp + 32 * h + 2 * u;
-                  const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[h][2 * u]), __uint_as_float(r[h][2 * u + 1])),
-                                                  mul2, neg2);
-                  float a, b;
-                  ptx::f2_unpack(x2, a, b);
-                  a = c < ncols ? ptx::ex2_approx(a) : 0.0f;
-                  b = c + 1 < ncols ? ptx::ex2_approx(b) : 0.0f;
-                  acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(a, b));
-                  pk[u] = ptx::pack_bf16x2(a, b);
-                }
-              }
-              ptx::tmem_st16(s_addr + 32 * cp + 16 * h, pk);
+            for (int u = 0; u < 16; ++u) {
+              const int c = 32 * ch + 2 * u;
+              const uint64_t x2 =
+                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
+              float e0, e1;
+              ptx::f2_unpack(x2, e0, e1);
+              e0 = ptx::ex2_approx(e0);
+              e1 = ptx::ex2_approx(e1);
+              acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(e0, e1));
+              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);  // P overwrites scores already consumed
             }
           }
           const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
           float sa, sb;
           ptx::f2_unpack(acc01, sa, sb);
           l_run += sa + sb;
-        } else {  // GELU, one pass
+        } else {  // GELU
 #pragma unroll
-          for (int cp = 0; cp < 2; ++cp) {
-            if (2 * cp >= nch) break;
-            uint32_t r[2][32];
-            ptx::tmem_ld32(s_addr + 64 * cp, r[0]);
-            if (2 * cp + 1 < nch) ptx::tmem_ld32(s_addr + 64 * cp + 32, r[1]);
-            ptx::tmem_wait_ld();
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (2 * cp + h >= nch) break;
-              uint32_t pk[16];
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
+            const bool full = (fullm >> ch) & 1u;
 #pragma unroll
-              for (int u = 0; u < 16; ++u) {
-                const int c = 64 * cp + 32 * h + 2 * u;
-                float a, b;
-                gelu_tanh_alu2(__uint_as_float(r[h][2 * u]) * sl, __uint_as_float(r[h][2 * u + 1]) * sl, a, b);
-                if (!full) {
-                  a = c < ncols ? a : 0.0f;
-                  b = c + 1 < ncols ? b : 0.0f;
-                }
-                pk[u] = ptx::pack_bf16x2(a, b);
+            for (int u = 0; u < 16; ++u) {
+              const int c = 32 * ch + 2 * u;
+              float e0, e1;
+              gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, e0, e1);
+              if (!full) {
+                e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
+                e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;
               }
-              ptx::tmem_st16(s_addr + 32 * cp + 16 * h, pk);
+              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);
             }
           }
         }
+        // P (bf16 pairs) over the first 16 * nch columns of S_x; P V reads
+        // no column beyond them.
+        ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        if (nch > 2) ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         ptx::tmem_wait_st();
       }
       // O_x += P_x(g-1) V(g-1) was issued before S_x(g) and has landed; the
-      // wait is immediate and keeps this thread's view of the phase exact.
+      // wait keeps this side's view of the barrier phase exact (and spaces
+      // the two sides' activations apart, which measured faster than
+      // letting them overlap).
       if (gx >= 1) {
         ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);
         ok = __all_sync(0xffffffffu, ok);
@@ -462,11 +522,11 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
       ptx::mbar_arrive(&B.p_full[x]);
     }
     if (!ok) break;
-    ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);
+    ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);  // the item's last P V
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     ptx::tc_fence_after();
-    const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : 1.0f / static_cast<float>(t.Lkv);
+    const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : inv_lkv;
     if (rows_live) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -488,8 +548,8 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, int ACT>
-__global__ void __launch_bounds__(352, 1) gdpa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+template <int D, int ACT, bool WIN>
+__global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
   using C = PairCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -530,14 +590,18 @@ __global__ void __launch_bounds__(352, 1) gdpa_fwd_pair_kernel(const __grid_cons
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = B.tmem_slot;
-  if (warp == 0) {
-    if (lane == 0) pair_producer<D, false>(p, sm, B, ibeg, iend);
-  } else if (warp == 10) {
-    if (lane == 0) pair_producer<D, true>(p, sm, B, ibeg, iend);
-  } else if (warp == 1) {
-    if (lane == 0) pair_mma<D>(p, sm, B, tmem, ibeg, iend);
-  } else {
-    pair_activation<D, ACT>(p, B, tmem, ibeg, iend, warp < 6 ? 0 : 1, warp, lane);
+  if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
+    ptx::regs_dec<C::REGS_CTRL>();
+    if (warp == 0) {
+      if (lane == 0) pair_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+    } else if (warp == 2) {
+      if (lane == 0) pair_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+    } else if (warp == 1) {
+      if (lane == 0) pair_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+    }
+  } else {  // warpgroups 1 and 2: tiles A and B, a whole row of scores in registers
+    ptx::regs_inc<C::REGS_ACT>();
+    pair_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp < 8 ? 0 : 1, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -26,12 +26,22 @@ inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blo
 gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks,
                                int64_t* Tq, int64_t* Tkv);
 
-// Query rows per work item: 32 (key-split items: every sequence has at most
-// 32 queries, D = 64, full attention; the four activation warps share the
-// queries and split each K/V tile), 256 (two 128-row tiles sharing every
-// K/V tile) for full attention when the batch's sequences average more than
-// 128 queries, else 128.
+// Query rows per work item, chosen per batch:
+//   window                                   256 (two 128-row tiles whose
+//                                            windows overlap)
+//   D = 64, every sequence <= 32 queries     32 (key split: the four
+//                                            activation warps share the
+//                                            queries and split each tile)
+//   sequences average > 128 queries          256 (two 128-row tiles sharing
+//                                            every K/V tile)
+//   otherwise                                128
 int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks);
+
+// First key of the block window of a query tile starting at q0.
+int64_t window_start(int64_t q0, int window_blocks);
+
+// Planner cost of an item (units of key columns of a 128-row tile).
+int64_t plan_item_cost(int64_t q0, int64_t Lq, int64_t Lkv, int window_blocks, int rows_per_item);
 
 // Number of work items plan_items will emit.
 int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item);

@@ -97,25 +97,39 @@ gdpa_status_t launch_k(Kernel kernel, int threads, int smem, int min_regs, const
   return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
-// One query tile per work item (any key range, block window included); KS:
-// at most 32 queries per item, the key range split over the four warps.
-template <int D, int ACT, bool WIN, bool KS = false>
+// One query tile per work item; MODE: full attention, block window or key
+// split (at most 32 queries, the key range split over the four warps).
+template <int D, int ACT, int MODE>
 gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
-  using C = FwdCfg<D, KS>;
+  using C = FwdCfg<D, MODE>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  return launch_k(gdpa_fwd_kernel<D, ACT, WIN, KS>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
+  return launch_k(gdpa_fwd_kernel<D, ACT, MODE>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
                   device, attr_done, &mu);
 }
 
-// Two query tiles per work item (full attention).
-template <int D, int ACT>
+template <int D>
+gdpa_status_t launch_single(int act, int mode, const FwdParams& prm, int grid, cudaStream_t s, int device) {
+  const bool gelu = act == GDPA_ACT_GELU_TANH;
+  switch (mode) {
+    case kModeFull:
+      return gelu ? launch_t<D, kActGelu, kModeFull>(prm, grid, s, device)
+                  : launch_t<D, kActSoftmax, kModeFull>(prm, grid, s, device);
+    case kModeWindow:  // softmax only (validated on entry)
+      return launch_t<D, kActSoftmax, kModeWindow>(prm, grid, s, device);
+    default:
+      return GDPA_ERR_INVALID_ARG;
+  }
+}
+
+// Two query tiles per work item (full attention or block window).
+template <int D, int ACT, bool WIN>
 gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
   using C = PairCfg<D>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
-  return launch_k(gdpa_fwd_pair_kernel<D, ACT>, C::THREADS, C::SMEM_BYTES, 0, prm, grid, stream, device, attr_done,
-                  &mu);
+  return launch_k(gdpa_fwd_pair_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid, stream,
+                  device, attr_done, &mu);
 }
 
 // Evaluates the activation exactly as the kernels do: GELU two arguments at
@@ -191,35 +205,33 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks > 0;
   if (a.rows_per_item == 256) {
-    if (win) return GDPA_ERR_INVALID_ARG;
+    if (win) {  // softmax only (validated on entry)
+      if (a.D == 128) return launch_pair<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
+      if (a.D == 64) return launch_pair<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
+      return GDPA_ERR_UNSUPPORTED;
+    }
     if (a.D == 128)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<128, kActGelu>(prm, a.num_ctas, s, device)
-                                         : launch_pair<128, kActSoftmax>(prm, a.num_ctas, s, device);
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<128, kActGelu, false>(prm, a.num_ctas, s, device)
+                                         : launch_pair<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
     if (a.D == 64)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<64, kActGelu>(prm, a.num_ctas, s, device)
-                                         : launch_pair<64, kActSoftmax>(prm, a.num_ctas, s, device);
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<64, kActGelu, false>(prm, a.num_ctas, s, device)
+                                         : launch_pair<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
     return GDPA_ERR_UNSUPPORTED;
   }
   if (key_split) {
     if (win || a.D != 64) return GDPA_ERR_INVALID_ARG;
-    return a.act == GDPA_ACT_GELU_TANH ? launch_t<64, kActGelu, false, true>(prm, a.num_ctas, s, device)
-                                       : launch_t<64, kActSoftmax, false, true>(prm, a.num_ctas, s, device);
+    return a.act == GDPA_ACT_GELU_TANH ? launch_t<64, kActGelu, kModeKeySplit>(prm, a.num_ctas, s, device)
+                                       : launch_t<64, kActSoftmax, kModeKeySplit>(prm, a.num_ctas, s, device);
   }
-  if (a.rows_per_item != 128) return GDPA_ERR_INVALID_ARG;
-  if (a.D == 128) {
-    if (a.act == GDPA_ACT_GELU_TANH) return launch_t<128, kActGelu, false>(prm, a.num_ctas, s, device);
-    return win ? launch_t<128, kActSoftmax, true>(prm, a.num_ctas, s, device)
-               : launch_t<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
-  }
-  if (a.D == 64) {
-    if (a.act == GDPA_ACT_GELU_TANH) return launch_t<64, kActGelu, false>(prm, a.num_ctas, s, device);
-    return win ? launch_t<64, kActSoftmax, true>(prm, a.num_ctas, s, device)
-               : launch_t<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
-  }
+  if (a.rows_per_item != kBlockM) return GDPA_ERR_INVALID_ARG;
+  const int mode = win ? kModeWindow : kModeFull;
+  if (a.D == 128) return launch_single<128>(a.act, mode, prm, a.num_ctas, s, device);
+  if (a.D == 64) return launch_single<64>(a.act, mode, prm, a.num_ctas, s, device);
   return GDPA_ERR_UNSUPPORTED;
 }
 
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream) {
+  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH) return GDPA_ERR_INVALID_ARG;
   if (n <= 0) return GDPA_OK;
   const int threads = 256;
   const int64_t want = (n + threads - 1) / threads;

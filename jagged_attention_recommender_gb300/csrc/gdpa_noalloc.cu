@@ -49,8 +49,6 @@ static NoAllocHost g_host;
 static std::mutex g_mu;
 static void* g_dev_scratch[64];
 
-int64_t na_item_cost(int64_t kv_len) { return kv_len <= 0 ? 8 : ((kv_len + 15) / 16) * 16 + 96; }
-
 // The planner of gdpa_plan.cpp restated over fixed arrays: same items, same
 // cost model, same longest-processing-time-first order and CTA choice.
 gdpa_status_t na_plan(const int32_t* qo, const int32_t* ko, int B, int H, int window_blocks, int rows_per_item,
@@ -59,15 +57,8 @@ gdpa_status_t na_plan(const int32_t* qo, const int32_t* ko, int B, int H, int wi
   for (int b = 0; b < B; ++b) {
     const int64_t Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
     for (int64_t q0 = 0; q0 < Lq; q0 += rows_per_item) {
-      int64_t kv0 = 0, kv_end = Lkv;
-      if (window_blocks > 0) {
-        const int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
-        kv0 = blk > 0 ? blk * kWindowBlock : 0;
-        kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
-      }
-      if (kv_end < kv0) kv_end = kv0;
-      const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM);
-      const int64_t c = tiles * na_item_cost(kv_end - kv0);
+      const int64_t kv0 = window_blocks > 0 ? window_start(q0, window_blocks) : 0;
+      const int64_t c = plan_item_cost(q0, Lq, Lkv, window_blocks, rows_per_item);
       for (int h = 0; h < H; ++h) {
         if (n >= kNaMaxItems) return GDPA_ERR_NO_MEMORY;
         g_host.items[n] = gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0};

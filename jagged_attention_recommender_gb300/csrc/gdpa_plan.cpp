@@ -8,11 +8,12 @@
 // (LPT) list scheduling over a min-heap of per-CTA loads, which bounds the
 // finish time by 4/3 of optimal and subsumes the zigzag order.
 //
-// Work unit: 128 query rows (or 256, two tiles sharing every K/V tile, for
-// full attention over sequences that average more than 128 queries) of one
-// (sequence, head), against its key range [kv0, kv_end):
-//   full attention : kv0 = 0, kv_end = Lkv
-//   block window W : kv0 = 64 * max(0, q0/64 - (W-1)), kv_end = min(L, q0 + 128)
+// Work unit (chosen per batch by choose_rows_per_item): 32, 128
+// or 256 query rows of one (sequence, head) against its key range:
+//   full attention : keys [0, Lkv)
+//   block window W : keys [64 * max(0, q0/64 - (W-1)), min(L, q0 + rows)),
+//                    each 128-row tile of a 256-row item attending to its
+//                    own window inside that range
 // Items whose key range is empty (Lkv = 0) are still emitted (cheap) because
 // their output rows must be zero-filled.
 #include "gdpa_internal.h"
@@ -52,16 +53,40 @@ static int64_t item_cost(int64_t kv_len) {
   return ((kv_len + 15) / 16) * 16 + 96;
 }
 
+int64_t window_start(int64_t q0, int window_blocks) {
+  const int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
+  return blk > 0 ? blk * kWindowBlock : 0;
+}
+
+// Cost of one item: each of its (one or two) 128-row query tiles pays for
+// the keys it attends to -- the whole key range, or its own block window.
+int64_t plan_item_cost(int64_t q0, int64_t Lq, int64_t Lkv, int window_blocks, int rows_per_item) {
+  const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM);
+  int64_t c = 0;
+  for (int64_t x = 0; x < tiles; ++x) {
+    const int64_t qt = q0 + kBlockM * x;
+    int64_t lo = 0, hi = Lkv;
+    if (window_blocks > 0) {
+      lo = window_start(qt, window_blocks);
+      hi = std::min<int64_t>(Lkv, qt + kBlockM);
+    }
+    c += item_cost(hi > lo ? hi - lo : 0);
+  }
+  return c;
+}
+
 int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks) {
-  if (window_blocks > 0 || B <= 0) return kBlockM;
+  if (B <= 0) return kBlockM;
+  if (window_blocks > 0) return 2 * kBlockM;  // both tiles share the overlapping windows' keys
   int64_t busy = 0, max_lq = 0;
   for (int b = 0; b < B; ++b) {
     const int64_t lq = q_off[b + 1] - q_off[b];
     busy += lq > 0 ? 1 : 0;
     max_lq = std::max<int64_t>(max_lq, lq);
   }
-  if (busy > 0 && D == 64 && max_lq <= kKeySplitRows) return kKeySplitRows;
-  return (busy > 0 && q_off[B] > (int64_t)kBlockM * busy) ? 2 * kBlockM : kBlockM;
+  if (busy == 0) return kBlockM;
+  if (D == 64 && max_lq <= kKeySplitRows) return kKeySplitRows;
+  return q_off[B] > (int64_t)kBlockM * busy ? 2 * kBlockM : kBlockM;
 }
 
 int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item) {
@@ -74,8 +99,9 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
                          int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items_out,
                          std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
   if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
-  if (rows_per_item != kBlockM && !((rows_per_item == 2 * kBlockM || rows_per_item == kKeySplitRows) && window_blocks == 0))
-    return GDPA_ERR_INVALID_ARG;
+  const bool ok_rows = rows_per_item == kBlockM || rows_per_item == 2 * kBlockM ||
+                       (rows_per_item == kKeySplitRows && window_blocks == 0);
+  if (!ok_rows) return GDPA_ERR_INVALID_ARG;
   std::vector<gdpa_work_item_t> items;
   std::vector<int64_t> cost;
   const int64_t n = count_plan_items(q_off, B, H, rows_per_item);
@@ -85,16 +111,8 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
     const int64_t Lq = q_off[b + 1] - q_off[b];
     const int64_t Lkv = kv_off[b + 1] - kv_off[b];
     for (int64_t q0 = 0; q0 < Lq; q0 += rows_per_item) {
-      int64_t kv0 = 0, kv_end = Lkv;
-      if (window_blocks > 0) {
-        int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
-        kv0 = blk > 0 ? blk * kWindowBlock : 0;
-        kv_end = std::min<int64_t>(Lkv, q0 + kBlockM);
-      }
-      if (kv_end < kv0) kv_end = kv0;
-      // query tiles the item's K/V feeds: 1 or 2 (a key-split item is one tile)
-      const int64_t tiles = std::max<int64_t>(1, std::min<int64_t>(rows_per_item, Lq - q0 + kBlockM - 1) / kBlockM);
-      const int64_t c = tiles * item_cost(kv_end - kv0);
+      const int64_t kv0 = window_blocks > 0 ? window_start(q0, window_blocks) : 0;
+      const int64_t c = plan_item_cost(q0, Lq, Lkv, window_blocks, rows_per_item);
       for (int h = 0; h < H; ++h) {
         items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});
         cost.push_back(c);

@@ -187,6 +187,24 @@ def test_cross_softmax_long_kv(D):
     assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "pma-like D=%d" % D)
 
 
+# Short key ranges (every sequence at most 64 keys, one partial K/V tile):
+# key counts around the 16-key MMA granule and the 32-column chunks, query
+# counts around the 128-row tile and the 256-row item.
+SK_LQ = [1, 127, 128, 129, 300, 1000, 40, 77, 5]
+SK_LKV = [1, 15, 16, 17, 33, 63, 64, 0, 48]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_GELU_TANH])
+def test_short_kv_edges(D, act):
+    rng = np.random.default_rng(3400 + D + act)
+    gelu = act == ACT_GELU_TANH
+    b = small_batch(rng, np.array(SK_LQ), np.array(SK_LKV), 3, D, act=act, qk_norm=gelu,
+                    scale=1.0 if gelu else None)
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "short kv D=%d act=%d" % (D, act),
+                  bf16_scaled=gelu)
+
+
 # Key-split items (D = 64, every sequence at most 32 queries): the four
 # activation warps share the queries and split each K/V tile into 32-key
 # blocks; key counts around the block and tile edges, and query counts below

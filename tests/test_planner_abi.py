@@ -73,7 +73,10 @@ def check_plan(Lq, Lkv, H, wb, num_ctas):
     items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas, with_rows=True)
     n = len(items)
     busy = Lq[Lq > 0]
-    expect_R = 256 if (wb == 0 and busy.size and busy.sum() > 128 * busy.size) else 128
+    if wb > 0:
+        expect_R = 256 if busy.size else 128  # the two tiles' windows overlap
+    else:
+        expect_R = 256 if (busy.size and busy.sum() > 128 * busy.size) else 128
     assert R == expect_R
     # CSR over CTAs
     assert cta[0] == 0 and cta[-1] == n and np.all(np.diff(cta) >= 0)
@@ -127,7 +130,7 @@ def test_plan_empty_sequences():
 
 def test_short_query_batches_take_key_split_items():
     # D = 64, full attention, every sequence at most 32 queries: one 32-row
-    # item per (sequence, head); otherwise the 128/256-row rule applies
+    # item per (sequence, head); otherwise the window / 128 / 256-row rules
     qo, ko = offsets_of(np.array([32, 0, 5, 32])), offsets_of(np.array([900, 40, 0, 3000]))
     items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, 4, 3, 64, 0, 0, 5, with_rows=True)
     assert R == 32
@@ -136,10 +139,10 @@ def test_short_query_batches_take_key_split_items():
     # cost grows with the key range
     by_seq = {int(b): c for (b, _, _, _), c in zip(items, cost)}
     assert by_seq[3] > by_seq[0] > by_seq[2]
-    for D, wb, lq in ((128, 0, 32), (64, 2, 32), (64, 0, 33)):
+    for D, wb, lq, R_want in ((128, 0, 32, 128), (64, 2, 32, 256), (64, 0, 33, 128), (64, 0, 300, 256)):
         q2 = offsets_of(np.array([lq, lq]))
         _, _, _, R2 = gdpa.gdpa_plan_enumerate(q2, q2, 2, 1, D, 0, wb, 4, with_rows=True)
-        assert R2 == 128
+        assert R2 == R_want
 
 
 def test_plan_balances_the_long_jagged_workload():
