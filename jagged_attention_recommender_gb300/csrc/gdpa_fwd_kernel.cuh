@@ -331,6 +331,8 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float sl = p.score_scale;
+  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
+  if (ACT == kActGelu) gelu_scale_consts(sl, gA2, gC2);
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
@@ -430,7 +432,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               float a, b;
-              gelu_tanh_alu2(__uint_as_float(sr[2 * u]) * sl, __uint_as_float(sr[2 * u + 1]) * sl, a, b);
+              gelu_tanh_alu2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1]), gA2, gC2, a, b);
               if (!full) {
                 a = cb + 2 * u < ncols ? a : 0.0f;
                 b = cb + 2 * u + 1 < ncols ? b : 0.0f;
@@ -563,7 +565,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
               for (int u = 0; u < 16; ++u) {
                 const int c = 32 * ch + 2 * u;
                 float a, b;
-                gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, a, b);
+                gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, a, b);
                 if (!full) {
                   a = col_ok(c, c_lo, c_hi) ? a : 0.0f;
                   b = col_ok(c + 1, c_lo, c_hi) ? b : 0.0f;
@@ -650,7 +652,7 @@ __device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, FwdBars<D
     }
     w = den > 0.0f ? own / den : 0.0f;
   } else {
-    w = 1.0f / static_cast<float>(t.Lkv);
+    w = p.score_scale / static_cast<float>(t.Lkv);  // the GELU's folded scale, then 1/Lkv
   }
   bool ok = ptx::mbar_wait(&B.o_full[ob], ph, p.timeout_ns, abort);
   if (!__all_sync(0xffffffffu, ok)) return false;
@@ -752,7 +754,7 @@ __device__ void run_epilogue(const FwdParams& p, FwdBars<D, MODE>& B, const floa
       ptx::mbar_arrive(&B.l_empty[ob]);
       inv = l > 0.0f ? 1.0f / l : 0.0f;
     } else {
-      inv = 1.0f / static_cast<float>(t.Lkv);
+      inv = p.score_scale / static_cast<float>(t.Lkv);  // the GELU's folded scale, then 1/Lkv
     }
     ok = ptx::mbar_wait(&B.o_full[ob], ph, p.timeout_ns, abort);
     ok = __all_sync(0xffffffffu, ok);

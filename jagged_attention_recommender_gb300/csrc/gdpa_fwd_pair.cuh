@@ -318,6 +318,8 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
   const uint32_t s_addr = tmem + lane_off + C::tm_s(x);
   const uint32_t o_addr = tmem + lane_off + C::tm_o(x);
   const float sl = p.score_scale;
+  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
+  if (ACT == kActGelu) gelu_scale_consts(sl, gA2, gC2);
   const int H = p.H;
   uint32_t gx = 0;
   bool ok = true;
@@ -344,7 +346,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     }
     const int j0 = x ? t.t0[1] : t.t0[0], j1 = x ? t.t1[1] : t.t1[0];  // this side's K/V tiles
     const int kv0 = t.kv0, kv_end = t.kv_end;
-    const float inv_lkv = 1.0f / static_cast<float>(max(t.Lkv, 1));
+    const float inv_lkv = sl / static_cast<float>(max(t.Lkv, 1));  // the GELU's folded scale, then 1/Lkv
     for (int j = j0; j < j1; ++j, ++gx) {
       ok = ptx::mbar_wait(&B.s_full[x], gx & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
@@ -481,7 +483,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             for (int u = 0; u < 16; ++u) {
               const int c = 32 * ch + 2 * u;
               float e0, e1;
-              gelu_tanh_alu2(__uint_as_float(sr[c]) * sl, __uint_as_float(sr[c + 1]) * sl, e0, e1);
+              gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, e0, e1);
               if (!full) {
                 e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
                 e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;

@@ -139,7 +139,9 @@ __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __r
        i += 2 * (int64_t)gridDim.x * blockDim.x) {
     if (act == kActGelu) {
       float a, b;
-      gelu_tanh_alu2(x[i], i + 1 < n ? x[i + 1] : 0.0f, a, b);
+      uint64_t A2, C2;
+      gelu_scale_consts(1.0f, A2, C2);
+      gelu_tanh_alu2(x[i], i + 1 < n ? x[i + 1] : 0.0f, A2, C2, a, b);
       y[i] = a;
       if (i + 1 < n) y[i + 1] = b;
     } else {
