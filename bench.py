@@ -83,6 +83,7 @@ def load_peaks():
 # its own); the hash keys the committed ncu traffic figure to the kernel.
 KERNEL_SOURCES = {
     "gdpa_fwd_pair_kernel": ["gdpa_fwd_common.cuh", "sm103_ptx.cuh", "gelu_alu.cuh", "gdpa_fwd_pair.cuh"],
+    "gdpa_fwd_pair64_kernel": ["gdpa_fwd_common.cuh", "sm103_ptx.cuh", "gelu_alu.cuh", "gdpa_fwd_pair64.cuh"],
     "gdpa_fwd_kernel": ["gdpa_fwd_common.cuh", "sm103_ptx.cuh", "gelu_alu.cuh", "gdpa_fwd_kernel.cuh"],
 }
 
@@ -96,11 +97,14 @@ def kernel_hash(kernel: str) -> str:
 
 
 def kernel_for(batch, gdpa_mod, num_ctas: int) -> str:
-    """The kernel the planner picks for this batch (256-row items: the pair kernel)."""
+    """The kernel the planner picks for this batch: 256-row items take a pair
+    kernel (64- or 128-key K/V tiles), the rest the single-tile kernel."""
     w = batch.workload
-    _, _, _, rows = gdpa_mod.gdpa_plan_enumerate(batch.q_offsets, batch.kv_offsets, batch.B, w.H, w.D, w.act,
-                                                 w.window_blocks, num_ctas, with_rows=True)
-    return "gdpa_fwd_pair_kernel" if rows == 256 else "gdpa_fwd_kernel"
+    _, _, _, rows, kv_tile = gdpa_mod.gdpa_plan_enumerate(batch.q_offsets, batch.kv_offsets, batch.B, w.H, w.D,
+                                                          w.act, w.window_blocks, num_ctas, with_rows=True)
+    if rows != 256:
+        return "gdpa_fwd_kernel"
+    return "gdpa_fwd_pair64_kernel" if kv_tile == 64 else "gdpa_fwd_pair_kernel"
 
 
 def traffic_per_launch(workload: str, kernel: str):

@@ -173,13 +173,15 @@ gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const void* h_v, c
  * `items` (capacity `capacity`) grouped by CTA and `cta_begin` [num_ctas+1]
  * (items of CTA c are items[cta_begin[c] .. cta_begin[c+1])); `cost` (may be
  * NULL) receives each item's estimated cost; `rows_per_item` (may be NULL)
- * receives R.  *n_items always receives the required count;
+ * receives R; `kv_tile` (may be NULL) receives the keys per K/V tile the
+ * kernel stages (64 for block windows and short key ranges on 256-row
+ * items, else 128).  *n_items always receives the required count;
  * GDPA_ERR_NO_MEMORY if it exceeds `capacity`.
  */
 gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
                                   int D, int act, int window_blocks, int num_ctas,
                                   gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
-                                  int64_t* cost, int64_t* n_items, int32_t* rows_per_item);
+                                  int64_t* cost, int64_t* n_items, int32_t* rows_per_item, int32_t* kv_tile);
 
 /*
  * gdpa_act_eval -- evaluates the kernel's device activation elementwise:

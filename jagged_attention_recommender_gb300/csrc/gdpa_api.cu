@@ -14,7 +14,7 @@
 struct gdpa_plan {
   int B, H, D, act, window_blocks;
   int num_ctas;
-  int rows_per_item;
+  int rows_per_item, kv_tile;
   int device;
   int64_t n_items, Tq, Tkv;
   void* d_buf;  // work items followed by cta_begin
@@ -120,11 +120,12 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // buffer into c.d_work (both guarded by events against earlier calls).
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
                               int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
-                              int64_t* n_items) {
+                              int* kv_tile, int64_t* n_items) {
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
   const int rpi = choose_rows_per_item(h_q_off, B, D, window_blocks);
   *rows_per_item = rpi;
+  *kv_tile = choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
   const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *n_items = n;
   if (n == 0) {
@@ -160,9 +161,10 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
                               const int32_t* d_q_off, const int32_t* d_kv_off, int64_t Tq, int64_t Tkv, int H, int D,
                               int act, int window_blocks, float scale, int num_ctas, int rows_per_item,
-                              int64_t n_items, cudaStream_t stream) {
+                              int kv_tile, int64_t n_items, cudaStream_t stream) {
   LaunchArgs a;
   a.rows_per_item = rows_per_item;
+  a.kv_tile = kv_tile;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -228,12 +230,12 @@ extern "C" gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, c
   if ((st = check_tensors(q, k, v, out, Tq, Tkv)) != GDPA_OK) return st;
   if (Tq == 0) return GDPA_OK;
   int num_ctas = 0;
-  int rpi = 0;
+  int rpi = 0, kvt = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, hq, hk, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &n_items)) != GDPA_OK)
+  if ((st = plan_and_upload(c, hq, hk, B, H, D, window_blocks, sms, s, &num_ctas, &rpi, &kvt, &n_items)) != GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                         rpi, n_items, s);
+                         rpi, kvt, n_items, s);
 }
 
 extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
@@ -255,13 +257,13 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
   if ((st = c.init()) != GDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int num_ctas = 0;
-  int rpi = 0;
+  int rpi = 0, kvt = 0;
   int64_t n_items = 0;
   if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi,
-                            &n_items)) != GDPA_OK)
+                            &kvt, &n_items)) != GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                         rpi, n_items, s);
+                         rpi, kvt, n_items, s);
 }
 
 extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
@@ -289,6 +291,7 @@ extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int3
   P->d_items = nullptr;
   P->d_cta_begin = nullptr;
   P->rows_per_item = choose_rows_per_item(h_q_offsets, B, D, window_blocks);
+  P->kv_tile = choose_kv_tile(h_q_offsets, h_kv_offsets, B, window_blocks, P->rows_per_item);
   const int64_t n = B > 0 ? count_plan_items(h_q_offsets, B, H, P->rows_per_item) : 0;
   P->n_items = n;
   P->num_ctas = (int)(n < sms ? n : sms);
@@ -350,6 +353,7 @@ extern "C" gdpa_status_t gdpa_fwd_planned(const gdpa_plan_t* plan, const void* q
   a.cta_begin = plan->d_cta_begin;
   a.num_ctas = plan->num_ctas;
   a.rows_per_item = plan->rows_per_item;
+  a.kv_tile = plan->kv_tile;
   a.Tq = plan->Tq;
   a.Tkv = plan->Tkv;
   a.H = plan->H;
@@ -418,7 +422,7 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
   // per-chunk sizes of the rebased offsets and work lists
   int64_t n_items[kMaxChunks];
   int ctas[kMaxChunks];
-  int rpi[kMaxChunks];
+  int rpi[kMaxChunks], kvt[kMaxChunks];
   size_t off_at[kMaxChunks], work_at[kMaxChunks], item_bytes[kMaxChunks];
   size_t meta = 0;
   for (int i = 0; i < C; ++i) {
@@ -427,6 +431,11 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
     std::vector<int32_t> tmp(nb + 1);
     for (int b = 0; b <= nb; ++b) tmp[b] = qo[cut[i] + b] - qo[cut[i]];
     rpi[i] = choose_rows_per_item(tmp.data(), nb, D, window_blocks);
+    {
+      std::vector<int32_t> tmpk(nb + 1);
+      for (int b = 0; b <= nb; ++b) tmpk[b] = ko[cut[i] + b] - ko[cut[i]];
+      kvt[i] = choose_kv_tile(tmp.data(), tmpk.data(), nb, window_blocks, rpi[i]);
+    }
     const int64_t n = count_plan_items(tmp.data(), nb, H, rpi[i]);
     n_items[i] = n;
     ctas[i] = (int)(n < sms ? n : sms);
@@ -521,6 +530,7 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
       a.cta_begin = reinterpret_cast<const int32_t*>(dmeta + work_at[i] + item_bytes[i]);
       a.num_ctas = ctas[i];
       a.rows_per_item = rpi[i];
+      a.kv_tile = kvt[i];
       a.Tq = Tq_i;
       a.Tkv = Tkv_i;
       a.H = H;

@@ -1,0 +1,628 @@
+// gdpa_fwd_pair64.cuh -- jagged GDPA forward, two query tiles per work item,
+// 64-key K/V tiles with the scores double-buffered (block windows and short
+// key ranges; long key ranges take gdpa_fwd_pair.cuh).
+//
+// A work item is 256 query rows of one (sequence, head) -- tile A = rows
+// [q0, q0+128), tile B = [q0+128, q0+256), B may be empty -- against the
+// sequence's whole key range (full attention) or against the keys of the
+// two tiles' block windows, each tile taking only the K/V tiles its rows
+// may see (window).  Every K/V tile staged in shared memory feeds both
+// tiles' MMAs, which halves the K/V traffic per FLOP against one tile per
+// item.
+//
+// K/V tiles are 64 keys, and each side has two S buffers in tensor memory,
+// so the MMA thread issues S_x(t+1) = Q_x K(t+1)^T before O_x += P_x(t) V(t)
+// (the P of tile t sits in the other buffer): when a side's activation has
+// finished tile t its next scores are already there, and the activations of
+// both sides run back to back while the tensor core works off the queue:
+//
+//   MMA thread, per K/V tile g:  S_A(g), S_B(g)            (buffers g & 1)
+//                                O_A += P_A(g-1) V(g-1),  O_B += P_B(g-1) V(g-1)
+//
+// This look-ahead also crosses item boundaries (the next item's Q is double
+// buffered), which is what a one-tile key range needs (the "outer loop"
+// pipelining of the GDPA section of the techfeed summary of "GEM Training").
+// With 64-key tiles a block window's 64-key blocks are whole tiles, so each
+// side skips every block outside its window.
+//
+// Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
+// and K (warp 0), the MMA issuer + TMEM owner (warp 1) and the TMA producer
+// for V (warp 2), and hands its registers to warpgroups 1 and 2, the
+// activation/epilogue of tiles A and B.  TMEM (512 columns): S_A buffers 0
+// and 64, S_B buffers 128 and 192, O_A 256, O_B 384.  An activation thread
+// holds one query row; it reads its 64 scores of a tile from TMEM at once.
+#pragma once
+
+#include "gdpa_fwd_common.cuh"
+
+namespace gdpa {
+
+template <int D>
+struct Pair64Cfg {
+  static constexpr int BN = 64;                           // keys per K/V tile
+  static constexpr int KCH = D / 64;
+  static constexpr int Q_CHUNK = 128 * 128;               // Q: 128 rows x 128 bytes per 64-column chunk
+  static constexpr int Q_TILE = KCH * Q_CHUNK;
+  static constexpr int KV_CHUNK = BN * 128;               // K/V: 64 rows x 128 bytes per chunk
+  static constexpr int KV_TILE = KCH * KV_CHUNK;
+  static constexpr int NQS = 2;                           // Q stages per query tile
+  static constexpr int NK = (D == 64) ? 6 : 3;
+  static constexpr int NV = (D == 64) ? 6 : 3;
+  static constexpr int OFF_QA = 0;
+  static constexpr int OFF_QB = OFF_QA + NQS * Q_TILE;
+  static constexpr int OFF_K = OFF_QB + NQS * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NK * KV_TILE;
+  static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
+  __host__ __device__ static constexpr uint32_t tm_s(int x, int b) { return 128u * x + 64u * b; }  // S_x buffer b
+  __host__ __device__ static constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }           // O_A, O_B
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 384;  // 3 warpgroups
+  // Registers per thread after reallocation: the control warpgroup hands
+  // registers to the two activation warpgroups (the split that compiled
+  // without spills for each activation).  Each SM sub-partition holds one
+  // warp of each, so the launch count R must satisfy
+  // regs_ctrl + 2 regs_act <= 3 R.
+  __host__ __device__ static constexpr int regs_ctrl(int act) { return act == kActGelu ? 120 : 88; }
+  __host__ __device__ static constexpr int regs_act(int act) { return act == kActGelu ? 192 : 208; }
+  static constexpr int MIN_LAUNCH_REGS = 168;
+  static_assert(regs_ctrl(kActGelu) + 2 * regs_act(kActGelu) <= 3 * MIN_LAUNCH_REGS, "register split");
+  static_assert(regs_ctrl(kActSoftmax) + 2 * regs_act(kActSoftmax) <= 3 * MIN_LAUNCH_REGS, "register split");
+  static_assert(384 + D <= TM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int D>
+struct Pair64Bars {
+  uint64_t q_full[2][Pair64Cfg<D>::NQS], q_empty[2][Pair64Cfg<D>::NQS];
+  uint64_t k_full[Pair64Cfg<D>::NK], k_empty[Pair64Cfg<D>::NK];
+  uint64_t v_full[Pair64Cfg<D>::NV], v_empty[Pair64Cfg<D>::NV];
+  uint64_t s_full[2][2], p_full[2][2];  // per side and S buffer
+  uint64_t o_done[2], o_empty[2];
+  uint64_t mma_drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct Pair64Item {
+  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
+  int rows[2];       // valid rows of tile A and tile B (B may be 0)
+  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each query tile attends to
+};
+
+// Full attention: both tiles attend to every K/V tile of the item.  Block
+// window: the item's keys run from the first key tile A's rows may see to
+// the last query of tile B; each tile takes the 64-key blocks of its own
+// window (blocks are K/V tiles).
+template <bool WIN>
+__device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx) {
+  constexpr int BN = 64;
+  const int4 it = __ldg(p.items + idx);
+  Pair64Item v;
+  const int b = it.x;
+  v.h = it.y;
+  v.q0 = it.z;
+  v.kv0 = WIN ? it.w : 0;
+  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
+  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
+  v.q_tok = qs + v.q0;
+  v.kv_tok = ks;
+  v.Lkv = ke - ks;
+  const int left = qe - qs - v.q0;
+  v.rows[0] = min(128, left);
+  v.rows[1] = max(0, min(128, left - 128));
+  v.kv_end = WIN ? min(v.Lkv, v.q0 + v.rows[0] + v.rows[1]) : v.Lkv;
+  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;
+  v.t0[0] = 0;
+  v.t1[0] = v.n_kv;
+  v.t0[1] = 0;
+  v.t1[1] = v.rows[1] > 0 ? v.n_kv : 0;
+  if (WIN) {
+    const int end_a = min(v.Lkv, v.q0 + 128);
+    v.t1[0] = end_a > v.kv0 ? (end_a - v.kv0 + BN - 1) / BN : 0;
+    const int blk = (v.q0 + 128) / 64 - (p.window_blocks - 1);
+    const int lo_b = blk > 0 ? blk * 64 : 0;
+    v.t0[1] = (lo_b - v.kv0) / BN;
+  }
+  return v;
+}
+
+// ------------------------------------------------------------------ producer
+
+// Two producer threads: one stages Q and K, the other V, so that a K load
+// never waits behind a V slot.
+template <int D, bool WIN, bool LOAD_V>
+__device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, int ibeg, int iend) {
+  using C = Pair64Cfg<D>;
+  volatile int* abort = &B.abort;
+  int qn[2] = {0, 0};
+  uint32_t g = 0;
+  bool ok = true;
+  int q_armed[2][C::NQS], k_armed[C::NK], v_armed[C::NV];
+  for (int t = 0; t < 2; ++t)
+    for (int s = 0; s < C::NQS; ++s) q_armed[t][s] = -1;
+  for (int s = 0; s < C::NK; ++s) k_armed[s] = -1;
+  for (int s = 0; s < C::NV; ++s) v_armed[s] = -1;
+  if (LOAD_V) {
+    ptx::prefetch_tensormap(&p.tm_v);
+  } else {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+  }
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    if (t.n_kv == 0) continue;
+    if (!LOAD_V) {
+      for (int x = 0; x < 2 && ok; ++x) {
+        if (t.rows[x] == 0) continue;
+        const int s = qn[x] % C::NQS;
+        const uint32_t ph = (qn[x] / C::NQS) & 1;
+        ok = ptx::mbar_wait(&B.q_empty[x][s], ph ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.q_full[x][s], C::Q_TILE);
+        q_armed[x][s] = (int)ph;
+        uint8_t* sq = sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::Q_TILE;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(sq + c * C::Q_CHUNK, &p.tm_q, &B.q_full[x][s], t.h * D + 64 * c, t.q_tok + 128 * x);
+        ++qn[x];
+      }
+    }
+    for (int j = 0; j < t.n_kv && ok; ++j, ++g) {
+      const int y = t.kv_tok + t.kv0 + C::BN * j;
+      if (!LOAD_V) {
+        const int sk = g % C::NK;
+        const uint32_t phk = (g / C::NK) & 1;
+        ok = ptx::mbar_wait(&B.k_empty[sk], phk ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.k_full[sk], C::KV_TILE);
+        uint8_t* dk = sm + C::OFF_K + sk * C::KV_TILE;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dk + c * C::KV_CHUNK, &p.tm_k, &B.k_full[sk], t.h * D + 64 * c, y);
+        k_armed[sk] = (int)phk;
+      } else {
+        const int sv = g % C::NV;
+        const uint32_t phv = (g / C::NV) & 1;
+        ok = ptx::mbar_wait(&B.v_empty[sv], phv ^ 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&B.v_full[sv], C::KV_TILE);
+        uint8_t* dv = sm + C::OFF_V + sv * C::KV_TILE;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          ptx::tma_load_2d(dv + c * C::KV_CHUNK, &p.tm_v, &B.v_full[sv], t.h * D + 64 * c, y);
+        v_armed[sv] = (int)phv;
+      }
+    }
+  }
+  if (!ok) report_failure(p, abort, kStatusProducer);
+  const int never = 0;
+  const unsigned long long drain_ns = 100000000ull;
+  for (int x = 0; x < 2; ++x)
+    for (int s = 0; s < C::NQS; ++s)
+      if (q_armed[x][s] >= 0) ptx::mbar_wait(&B.q_full[x][s], (uint32_t)q_armed[x][s], drain_ns, &never);
+  for (int s = 0; s < C::NK; ++s)
+    if (k_armed[s] >= 0) ptx::mbar_wait(&B.k_full[s], (uint32_t)k_armed[s], drain_ns, &never);
+  for (int s = 0; s < C::NV; ++s)
+    if (v_armed[s] >= 0) ptx::mbar_wait(&B.v_full[s], (uint32_t)v_armed[s], drain_ns, &never);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+struct Pair64PV {
+  uint32_t gx;  // this side's tile counter (selects the S buffer)
+  uint32_t g;   // K/V tile counter (selects the V stage)
+  int item;     // this side's item counter (O buffer use count)
+  int first, n16;
+};
+
+template <int D>
+__device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int x,
+                                              const Pair64PV& P) {
+  using C = Pair64Cfg<D>;
+  volatile int* abort = &B.abort;
+  const int b = P.gx & 1;
+  if (!ptx::mbar_wait(&B.p_full[x][b], (P.gx >> 1) & 1, p.timeout_ns, abort)) return false;
+  if (P.first && !ptx::mbar_wait(&B.o_empty[x], (P.item & 1) ^ 1, p.timeout_ns, abort)) return false;
+  const int sv = P.g % C::NV;
+  if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
+  ptx::tc_fence_after();
+  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::KV_TILE);
+  constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
+  for (int kk = 0; kk < P.n16; ++kk) {
+    // B = V tile, MN-major: 16 keys = two 8-row groups (SBO = 1024 B apart);
+    // the two 64-column halves of D sit one chunk apart (LBO).
+    const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK, 1024);
+    ptx::mma_ts(tmem + C::tm_o(x), tmem + C::tm_s(x, b) + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
+  }
+  ptx::mma_commit(&B.o_done[x]);
+  return true;
+}
+
+template <int D, bool WIN>
+__device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend) {
+  using C = Pair64Cfg<D>;
+  volatile int* abort = &B.abort;
+  int qn[2] = {0, 0};       // items seen by each side (Q stage and O buffer use counts)
+  uint32_t gx[2] = {0, 0};  // tiles processed by each side (S buffers)
+  uint32_t g = 0;
+  bool ok = true;
+  bool pend[2] = {false, false};
+  Pair64PV pv[2] = {{0, 0, 0, 0, 0}, {0, 0, 0, 0, 0}};
+  bool pend_v = false;
+  uint32_t pend_v_g = 0;
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    if (t.n_kv == 0) continue;
+    const bool has[2] = {t.rows[0] > 0, t.rows[1] > 0};
+    uint32_t q_base[2] = {0, 0};
+    for (int x = 0; x < 2 && ok; ++x) {
+      if (!has[x]) continue;
+      const int s = qn[x] % C::NQS;
+      ok = ptx::mbar_wait(&B.q_full[x][s], (qn[x] / C::NQS) & 1, p.timeout_ns, abort);
+      q_base[x] = ptx::smem_u32(sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::Q_TILE);
+    }
+    if (!ok) break;
+    for (int j = 0; j < t.n_kv; ++j, ++g) {
+      const int sk = g % C::NK;
+      ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
+      const int n16 = (ncols + 15) >> 4;
+      const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + sk * C::KV_TILE);
+      bool act[2];
+      // S_x(g) goes into the buffer that held P_x two tiles ago, whose P V
+      // was issued in an earlier iteration (the tensor core runs them in order).
+      for (int x = 0; x < 2; ++x) {
+        act[x] = has[x] && j >= t.t0[x] && j < t.t1[x];
+        if (!act[x]) continue;
+        const uint32_t s_col = C::tm_s(x, gx[x] & 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
+          const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+          ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base[x] + qoff, 16, 1024),
+                      ptx::sdesc_sw128(k_base + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&B.s_full[x][gx[x] & 1]);
+      }
+      ptx::mma_commit(&B.k_empty[sk]);
+      if (j == t.n_kv - 1) {
+        for (int x = 0; x < 2; ++x)
+          if (has[x]) ptx::mma_commit(&B.q_empty[x][qn[x] % C::NQS]);
+      }
+      // Then O_x += P_x V for each side's previous tile (issued here even
+      // when this tile has no S_x, so that every P V of the previous K/V
+      // tile is issued now and its V stage can be released).
+      for (int x = 0; x < 2 && ok; ++x) {
+        if (!pend[x]) continue;
+        ok = pair64_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
+        pend[x] = false;
+      }
+      if (!ok) break;
+      if (pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);
+      for (int x = 0; x < 2; ++x) {
+        if (!act[x]) continue;
+        pv[x] = Pair64PV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
+        pend[x] = true;
+        ++gx[x];
+      }
+      pend_v = true;
+      pend_v_g = g;
+    }
+    for (int x = 0; x < 2; ++x)
+      if (has[x]) ++qn[x];
+  }
+  for (int x = 0; x < 2 && ok; ++x)
+    if (pend[x]) ok = pair64_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
+  if (ok && pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);
+  if (!ok) report_failure(p, abort, kStatusMma);
+  ptx::mma_commit(&B.mma_drain);
+  const int never = 0;
+  ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
+}
+
+// ------------------------------------------------------------------ activation + epilogue
+
+template <int D, int ACT, bool WIN>
+__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend, int x,
+                                int warp, int lane) {
+  using C = Pair64Cfg<D>;
+  volatile int* abort = &B.abort;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t o_addr = tmem + lane_off + C::tm_o(x);
+  const float sl = p.score_scale;
+  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
+  if (ACT == kActGelu) gelu_scale_consts(sl, gA2, gC2);
+  const int H = p.H;
+  uint32_t gx = 0;
+  bool ok = true;
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    const int rows = x ? t.rows[1] : t.rows[0];
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
+    if (t.n_kv == 0) {  // no keys: zero output rows
+      if (row < rows) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    if (rows == 0) continue;  // this side has no tile in the item
+    const bool rows_live = __any_sync(0xffffffffu, row < rows);
+    float m_run = -INFINITY, l_run = 0.0f;
+    const int i_seq = t.q0 + 128 * x + row;  // query index inside its sequence
+    int win_lo = 0;
+    if (WIN) {
+      const int blk = i_seq / 64 - (p.window_blocks - 1);
+      win_lo = blk > 0 ? blk * 64 : 0;
+    }
+    const int j0 = x ? t.t0[1] : t.t0[0], j1 = x ? t.t1[1] : t.t1[0];  // this side's K/V tiles
+    const int kv0 = t.kv0, kv_end = t.kv_end;
+    const float inv_lkv = sl / static_cast<float>(max(t.Lkv, 1));  // the GELU's folded scale, then 1/Lkv
+    for (int j = j0; j < j1; ++j, ++gx) {
+      const int sb = gx & 1;
+      ok = ptx::mbar_wait(&B.s_full[x][sb], (gx >> 1) & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t s_addr = tmem + lane_off + C::tm_s(x, sb);
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (rows_live) {
+        // valid key columns of this row: [c_lo, c_hi] (tile-relative)
+        const int kv_t0 = kv0 + C::BN * j;
+        const int ncols = min(C::BN, kv_end - kv_t0);  // the tile's key extent
+        int c_lo = 0, c_hi = ncols - 1;
+        if (WIN) {
+          c_lo = max(0, win_lo - kv_t0);
+          c_hi = min(c_hi, i_seq - kv_t0);
+        }
+        const int nch = (ncols + 31) >> 5;  // chunks P V reads
+        // chunk classes agreed on by the warp: bit ch of `fullm` = every key
+        // of chunk ch is valid for all 32 rows; bit ch of `livem` = some row
+        // has a valid key in it.  Full attention masks only the ragged end
+        // of the last tile, the same for every row.
+        uint32_t fullm, livem;
+        if (WIN) {
+          fullm = 0;
+          livem = 0;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int lo = 32 * ch, hi = 32 * ch + 31;
+            if (__all_sync(0xffffffffu, lo >= c_lo && hi <= c_hi)) fullm |= 1u << ch;
+            if (__any_sync(0xffffffffu, ch < nch && hi >= c_lo && lo <= c_hi)) livem |= 1u << ch;
+          }
+        } else {
+          livem = (1u << nch) - 1u;
+          fullm = (1u << (ncols >> 5)) - 1u;
+        }
+        // The tile's 64 scores of this row in registers, one TMEM round trip.
+        uint32_t sr[64];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
+        ptx::tmem_wait_ld();
+        if (ACT == kActSoftmax) {
+          // Scores in log2 units: x = s * scale * log2(e); masked columns
+          // become -inf.  With scale > 0 the scaling is folded into the
+          // exponent's FMA; otherwise it is applied first.
+          const bool fold = sl > 0.0f;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            if (!((livem >> ch) & 1u)) continue;
+            if (((fullm >> ch) & 1u) && fold) {
+#pragma unroll
+              for (int u = 0; u < 32; u += 8) {
+                const int c = 32 * ch + u;
+                m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+              }
+            } else {  // ragged end / window edge / diagonal chunk, or scale <= 0
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const int c = 32 * ch + u;
+                float v = __uint_as_float(sr[c]);
+                if (!fold) v *= sl;
+                if (c < c_lo || c > c_hi) v = -INFINITY;
+                sr[c] = __float_as_uint(v);
+                m4[u & 3] = fmaxf(m4[u & 3], v);
+              }
+            }
+          }
+          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          if (fold) mx *= sl;
+          const float m_new = fmaxf(m_run, mx);
+          if (j == j0) {
+            m_run = m_new;
+          } else if (m_new > m_run + 8.0f) {  // lazy rescale: only when the max grew by more than 2^8
+            alpha = ptx::ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            rescale = true;
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+          // masked entries hold -inf and give exactly 0; with scale > 0 the
+          // entries are still unscaled and take the scale in the packed FMA
+          const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
+          const uint64_t neg2 = ptx::f2_splat(-m_use);
+          uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
+#pragma unroll
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c = 32 * ch + 2 * u;
+              const uint64_t x2 =
+                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
+              float e0, e1;
+              ptx::f2_unpack(x2, e0, e1);
+              e0 = ptx::ex2_approx(e0);
+              e1 = ptx::ex2_approx(e1);
+              acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(e0, e1));
+              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);  // P overwrites scores already consumed
+            }
+          }
+          const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+          float sa, sb2;
+          ptx::f2_unpack(acc01, sa, sb2);
+          l_run += sa + sb2;
+        } else {  // GELU
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            if (ch >= nch) continue;
+            if (!((livem >> ch) & 1u)) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              continue;
+            }
+            const bool full = (fullm >> ch) & 1u;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c = 32 * ch + 2 * u;
+              float e0, e1;
+              gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, e0, e1);
+              if (!full) {
+                e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
+                e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;
+              }
+              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);
+            }
+          }
+        }
+        // P (bf16 pairs, 32 columns) over the first columns of this S
+        // buffer; P V reads no column beyond 8 * n16.
+        ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_wait_st();
+      }
+      // O_x += P_x(t-1) V has landed once this wait returns (it was issued
+      // after S_x(t), so the S barrier does not imply it); the wait also
+      // keeps this side's view of the barrier phase exact.
+      if (gx >= 1) {
+        ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(o_addr + 32 * c, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          ptx::tmem_st32(o_addr + 32 * c, r);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.p_full[x][sb]);
+    }
+    if (!ok) break;
+    ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);  // the item's last P V
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : inv_lkv;
+    if (rows_live) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld32(o_addr + 32 * c, r);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        if (row < rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&B.o_empty[x]);
+  }
+  if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D, int ACT, bool WIN>
+__global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_constant__ FwdParams p) {
+  using C = Pair64Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+  Pair64Bars<D>& B = *reinterpret_cast<Pair64Bars<D>*>(sm + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ibeg = p.cta_begin[blockIdx.x];
+  const int iend = p.cta_begin[blockIdx.x + 1];
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      for (int s = 0; s < C::NQS; ++s) {
+        ptx::mbar_init(&B.q_full[x][s], 1);
+        ptx::mbar_init(&B.q_empty[x][s], 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(&B.s_full[x][b], 1);
+        ptx::mbar_init(&B.p_full[x][b], 128);
+      }
+      ptx::mbar_init(&B.o_done[x], 1);
+      ptx::mbar_init(&B.o_empty[x], 128);
+    }
+    for (int s = 0; s < C::NK; ++s) {
+      ptx::mbar_init(&B.k_full[s], 1);
+      ptx::mbar_init(&B.k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      ptx::mbar_init(&B.v_full[s], 1);
+      ptx::mbar_init(&B.v_empty[s], 1);
+    }
+    ptx::mbar_init(&B.mma_drain, 1);
+    B.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&B.tmem_slot, C::TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = B.tmem_slot;
+  if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
+    ptx::regs_dec<C::regs_ctrl(ACT)>();
+    if (warp == 0) {
+      if (lane == 0) pair64_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+    } else if (warp == 2) {
+      if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+    } else if (warp == 1) {
+      if (lane == 0) pair64_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+    }
+  } else {  // warpgroups 1 and 2: tiles A and B
+    ptx::regs_inc<C::regs_act(ACT)>();
+    pair64_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp < 8 ? 0 : 1, warp, lane);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace gdpa

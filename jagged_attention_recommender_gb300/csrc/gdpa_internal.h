@@ -37,6 +37,14 @@ gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int 
 //   otherwise                                128
 int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks);
 
+// Keys per K/V tile for 256-row items: 64 (the scores double-buffered, so
+// the next tile's S is computed while the current one is activated; block
+// windows, whose 64-key blocks become whole tiles, and key ranges averaging
+// at most kShortRange keys) or 128 (long key ranges, where the wider tile
+// halves the per-tile overheads).  128 for every other item shape.
+constexpr int kShortRange = 256;
+int choose_kv_tile(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks, int rows_per_item);
+
 // First key of the block window of a query tile starting at q0.
 int64_t window_start(int64_t q0, int window_blocks);
 
@@ -62,6 +70,7 @@ struct LaunchArgs {
   const int32_t* cta_begin;       // device [num_ctas + 1]
   int num_ctas;
   int rows_per_item;      // 128: one query tile per item; 256: two; 32: key split
+  int kv_tile;            // keys per K/V tile (64 or 128, see choose_kv_tile)
   int64_t Tq, Tkv;
   int H, D, act, window_blocks;
   float scale;

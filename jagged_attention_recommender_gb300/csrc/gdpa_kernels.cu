@@ -8,6 +8,7 @@
 
 #include "gdpa_fwd_kernel.cuh"
 #include "gdpa_fwd_pair.cuh"
+#include "gdpa_fwd_pair64.cuh"
 #include "gdpa_internal.h"
 
 namespace gdpa {
@@ -97,6 +98,17 @@ gdpa_status_t launch_k(Kernel kernel, int threads, int smem, int min_regs, const
   return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
+// Two query tiles per work item, 64-key K/V tiles with the scores
+// double-buffered (block windows, short key ranges).
+template <int D, int ACT, bool WIN>
+gdpa_status_t launch_pair64(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
+  using C = Pair64Cfg<D>;
+  static std::mutex mu;
+  static bool attr_done[kMaxDevices] = {};
+  return launch_k(gdpa_fwd_pair64_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid,
+                  stream, device, attr_done, &mu);
+}
+
 // One query tile per work item; MODE: full attention, block window or key
 // split (at most 32 queries, the key range split over the four warps).
 template <int D, int ACT, int MODE>
@@ -122,7 +134,7 @@ gdpa_status_t launch_single(int act, int mode, const FwdParams& prm, int grid, c
   }
 }
 
-// Two query tiles per work item (full attention or block window).
+// Two query tiles per work item, 128-key K/V tiles (long key ranges).
 template <int D, int ACT, bool WIN>
 gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
   using C = PairCfg<D>;
@@ -191,8 +203,10 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   const void* kb = a.Tkv > 0 ? a.k : a.q;
   const void* vb = a.Tkv > 0 ? a.v : a.q;
   const int64_t kv_rows = a.Tkv > 0 ? a.Tkv : a.Tq;
-  if ((st = encode_rows(&prm.tm_k, kb, kv_rows, a.H, a.D)) != GDPA_OK) return st;
-  if ((st = encode_rows(&prm.tm_v, vb, kv_rows, a.H, a.D)) != GDPA_OK) return st;
+  if (a.kv_tile != kBlockN && !(a.kv_tile == kBlockN / 2 && a.rows_per_item == 2 * kBlockM)) return GDPA_ERR_INVALID_ARG;
+  const int kv_box = a.kv_tile;  // rows of a K/V tile the kernel stages
+  if ((st = encode_rows(&prm.tm_k, kb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
+  if ((st = encode_rows(&prm.tm_v, vb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
   prm.items = reinterpret_cast<const int4*>(a.items);
   prm.cta_begin = a.cta_begin;
   prm.q_off = a.q_off;
@@ -206,12 +220,22 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks > 0;
-  if (a.rows_per_item == 256) {
+  if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {
     if (win) {  // softmax only (validated on entry)
-      if (a.D == 128) return launch_pair<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
-      if (a.D == 64) return launch_pair<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
+      if (a.D == 128) return launch_pair64<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
+      if (a.D == 64) return launch_pair64<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
       return GDPA_ERR_UNSUPPORTED;
     }
+    if (a.D == 128)
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair64<128, kActGelu, false>(prm, a.num_ctas, s, device)
+                                         : launch_pair64<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
+    if (a.D == 64)
+      return a.act == GDPA_ACT_GELU_TANH ? launch_pair64<64, kActGelu, false>(prm, a.num_ctas, s, device)
+                                         : launch_pair64<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
+    return GDPA_ERR_UNSUPPORTED;
+  }
+  if (a.rows_per_item == 256) {
+    if (win) return GDPA_ERR_INVALID_ARG;  // windows take 64-key tiles
     if (a.D == 128)
       return a.act == GDPA_ACT_GELU_TANH ? launch_pair<128, kActGelu, false>(prm, a.num_ctas, s, device)
                                          : launch_pair<128, kActSoftmax, false>(prm, a.num_ctas, s, device);

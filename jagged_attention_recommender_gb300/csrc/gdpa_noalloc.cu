@@ -172,6 +172,7 @@ extern "C" gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const vo
   a.cta_begin = reinterpret_cast<const int32_t*>(dev + kNaItemBytes);
   a.num_ctas = num_ctas;
   a.rows_per_item = rpi;
+  a.kv_tile = choose_kv_tile(hq, hk, B, window_blocks, rpi);
   a.Tq = Tq;
   a.Tkv = Tkv;
   a.H = H;

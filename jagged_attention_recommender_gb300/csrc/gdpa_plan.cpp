@@ -89,6 +89,18 @@ int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks) 
   return q_off[B] > (int64_t)kBlockM * busy ? 2 * kBlockM : kBlockM;
 }
 
+int choose_kv_tile(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks, int rows_per_item) {
+  if (rows_per_item != 2 * kBlockM) return kBlockN;
+  if (window_blocks > 0) return kBlockN / 2;
+  int64_t busy = 0, keys = 0;
+  for (int b = 0; b < B; ++b)
+    if (q_off[b + 1] > q_off[b]) {
+      ++busy;
+      keys += kv_off[b + 1] - kv_off[b];
+    }
+  return (busy > 0 && keys <= (int64_t)kShortRange * busy) ? kBlockN / 2 : kBlockN;
+}
+
 int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item) {
   int64_t n = 0;
   for (int b = 0; b < B; ++b) n += (int64_t)((q_off[b + 1] - q_off[b] + rows_per_item - 1) / rows_per_item) * H;
@@ -181,7 +193,8 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
 extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B,
                                              int H, int D, int act, int window_blocks, int num_ctas,
                                              gdpa_work_item_t* items, int64_t capacity, int32_t* cta_begin,
-                                             int64_t* cost, int64_t* n_items, int32_t* rows_per_item) {
+                                             int64_t* cost, int64_t* n_items, int32_t* rows_per_item,
+                                             int32_t* kv_tile) {
   if (n_items) *n_items = 0;
   gdpa_status_t st = gdpa::validate_shape(B, H, D, act, window_blocks);
   if (st != GDPA_OK) return st;
@@ -194,6 +207,7 @@ extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const i
   std::vector<int64_t> c;
   const int rpi = gdpa::choose_rows_per_item(h_q_offsets, B, D, window_blocks);
   if (rows_per_item) *rows_per_item = rpi;
+  if (kv_tile) *kv_tile = gdpa::choose_kv_tile(h_q_offsets, h_kv_offsets, B, window_blocks, rpi);
   try {
     st = gdpa::plan_items(h_q_offsets, h_kv_offsets, B, H, window_blocks, rpi, num_ctas, v, cb, &c);
   } catch (...) {

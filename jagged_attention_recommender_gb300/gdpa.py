@@ -66,7 +66,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_plan_num_ctas.argtypes = [P]
     L.gdpa_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
     L.gdpa_plan_enumerate.argtypes = [P, P, I, I, I, I, I, I, P, I64, P, P, ctypes.POINTER(I64),
-                                      ctypes.POINTER(ctypes.c_int32)]
+                                      ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     L.gdpa_act_eval.argtypes = [I, P, P, I64, P]
     L.gdpa_device_status.argtypes = [P]
     L.gdpa_wait_selftest.argtypes = [I, P]
@@ -191,24 +191,26 @@ def gdpa_fwd_host(h_q, h_k, h_v, h_q_offsets, h_kv_offsets, B, H, D, act, window
 
 def gdpa_plan_enumerate(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, num_ctas, with_rows=False):
     """Host planner only: returns (items [n, 4] int32, cta_begin [num_ctas+1], cost [n])
-    (and the query rows per item when ``with_rows``)."""
+    (and, when ``with_rows``, the query rows per item and the keys per K/V tile)."""
     qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
     n = ctypes.c_int64(0)
     rows = ctypes.c_int32(0)
+    kvt = ctypes.c_int32(0)
     cta = np.zeros(num_ctas + 1, dtype=np.int32)
     code = lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
                                      int(window_blocks), int(num_ctas), None, 0, cta.ctypes.data, None,
-                                     ctypes.byref(n), ctypes.byref(rows))
+                                     ctypes.byref(n), ctypes.byref(rows), ctypes.byref(kvt))
     if code not in (GDPA_OK, GDPA_ERR_NO_MEMORY):
         raise GdpaError(code, "gdpa_plan_enumerate")
     items = np.zeros((max(n.value, 1), 4), dtype=np.int32)
     cost = np.zeros(max(n.value, 1), dtype=np.int64)
     _check(lib().gdpa_plan_enumerate(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
                                      int(window_blocks), int(num_ctas), items.ctypes.data, n.value,
-                                     cta.ctypes.data, cost.ctypes.data, ctypes.byref(n), ctypes.byref(rows)),
+                                     cta.ctypes.data, cost.ctypes.data, ctypes.byref(n), ctypes.byref(rows),
+                                     ctypes.byref(kvt)),
            "gdpa_plan_enumerate")
     if with_rows:
-        return items[:n.value], cta, cost[:n.value], rows.value
+        return items[:n.value], cta, cost[:n.value], rows.value, kvt.value
     return items[:n.value], cta, cost[:n.value]
 
 

@@ -205,6 +205,28 @@ def test_short_kv_edges(D, act):
                   bf16_scaled=gelu)
 
 
+# Two-tile (256-row) items with 128-key K/V tiles (long key ranges) and with
+# 64-key tiles (short key ranges): query counts around the 128/256-row edges,
+# key counts around both tile sizes.
+PAIR_LQ = [256, 257, 511, 300, 700, 129, 1000, 383]
+PAIR_KV = {128: [256, 257, 511, 300, 700, 129, 1000, 383],
+           64: [64, 65, 200, 1, 255, 129, 500, 0]}
+
+
+@pytest.mark.parametrize("kv_tile", [128, 64])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_GELU_TANH])
+def test_pair_items(kv_tile, D, act):
+    rng = np.random.default_rng(3600 + kv_tile + D + act)
+    gelu = act == ACT_GELU_TANH
+    b = small_batch(rng, np.array(PAIR_LQ), np.array(PAIR_KV[kv_tile]), 2, D, act=act, qk_norm=gelu,
+                    scale=1.0 if gelu else None)
+    _, _, _, rows, kvt = gdpa.gdpa_plan_enumerate(b.q_offsets, b.kv_offsets, b.B, 2, D, act, 0, 8, with_rows=True)
+    assert (rows, kvt) == (256, kv_tile)
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "pair kv_tile=%d D=%d act=%d"
+                  % (kv_tile, D, act), bf16_scaled=gelu)
+
+
 # Key-split items (D = 64, every sequence at most 32 queries): the four
 # activation warps share the queries and split each K/V tile into 32-key
 # blocks; key counts around the block and tile edges, and query counts below
@@ -217,7 +239,7 @@ KS_LKV = [1, 31, 32, 33, 95, 96, 97, 127, 128, 129, 255, 256, 0, 1000]
 def test_key_split_edges_softmax(H):
     rng = np.random.default_rng(3100 + H)
     b = small_batch(rng, np.array(KS_LQ), np.array(KS_LKV), H, 64)
-    items, _, _, rows = gdpa.gdpa_plan_enumerate(b.q_offsets, b.kv_offsets, b.B, H, 64, 0, 0, 8, with_rows=True)
+    items, _, _, rows, _ = gdpa.gdpa_plan_enumerate(b.q_offsets, b.kv_offsets, b.B, H, 64, 0, 0, 8, with_rows=True)
     assert rows == 32
     assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "key split H=%d" % H)
 

@@ -70,14 +70,23 @@ def test_enumerate_rejects_bad_offsets():
 def check_plan(Lq, Lkv, H, wb, num_ctas):
     qo, ko = offsets_of(Lq), offsets_of(Lkv)
     B = len(Lq)
-    items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas, with_rows=True)
+    items, cta, cost, R, kvt = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, wb, num_ctas, with_rows=True)
     n = len(items)
-    busy = Lq[Lq > 0]
+    busy = Lq > 0
     if wb > 0:
-        expect_R = 256 if busy.size else 128  # the two tiles' windows overlap
+        expect_R = 256 if busy.any() else 128  # the two tiles' windows overlap
     else:
-        expect_R = 256 if (busy.size and busy.sum() > 128 * busy.size) else 128
+        expect_R = 256 if (busy.any() and Lq[busy].sum() > 128 * busy.sum()) else 128
     assert R == expect_R
+    # 256-row items stage 64-key tiles for windows and short key ranges
+    # (at most 256 keys per busy sequence on average), 128-key tiles otherwise
+    if R != 256:
+        expect_kvt = 128
+    elif wb > 0 or Lkv[busy].sum() <= 256 * busy.sum():
+        expect_kvt = 64
+    else:
+        expect_kvt = 128
+    assert kvt == expect_kvt
     # CSR over CTAs
     assert cta[0] == 0 and cta[-1] == n and np.all(np.diff(cta) >= 0)
     # every (sequence, head, query row) is covered exactly once
@@ -132,7 +141,7 @@ def test_short_query_batches_take_key_split_items():
     # D = 64, full attention, every sequence at most 32 queries: one 32-row
     # item per (sequence, head); otherwise the window / 128 / 256-row rules
     qo, ko = offsets_of(np.array([32, 0, 5, 32])), offsets_of(np.array([900, 40, 0, 3000]))
-    items, cta, cost, R = gdpa.gdpa_plan_enumerate(qo, ko, 4, 3, 64, 0, 0, 5, with_rows=True)
+    items, cta, cost, R, _ = gdpa.gdpa_plan_enumerate(qo, ko, 4, 3, 64, 0, 0, 5, with_rows=True)
     assert R == 32
     assert sorted(map(tuple, items[:, :3].tolist())) == sorted((b, h, 0) for b in (0, 2, 3) for h in range(3))
     assert np.all(items[:, 3] == 0) and cta[-1] == len(items)
@@ -141,7 +150,7 @@ def test_short_query_batches_take_key_split_items():
     assert by_seq[3] > by_seq[0] > by_seq[2]
     for D, wb, lq, R_want in ((128, 0, 32, 128), (64, 2, 32, 256), (64, 0, 33, 128), (64, 0, 300, 256)):
         q2 = offsets_of(np.array([lq, lq]))
-        _, _, _, R2 = gdpa.gdpa_plan_enumerate(q2, q2, 2, 1, D, 0, wb, 4, with_rows=True)
+        _, _, _, R2, _ = gdpa.gdpa_plan_enumerate(q2, q2, 2, 1, D, 0, wb, 4, with_rows=True)
         assert R2 == R_want
 
 
