@@ -9,10 +9,11 @@
 //     warp 0    TMA producer for the Q tile (2 stages) and K tiles (NK
 //               stages); warp 2 TMA producer for V tiles (NV stages); all
 //               128-byte swizzled; K is released after Q K^T, V after P V;
-//     warp 1    MMA issuer (one thread): S = Q K^T into tensor memory
+//     warp 1    MMA issuer (the whole warp runs the loop, one elected
+//               lane issues): S = Q K^T into tensor memory
 //               (two S buffers), then O += P V with P read straight from
 //               tensor memory (two O buffers, one per in-flight item);
-//   warpgroup 1 (240 registers a thread): activation, one query row per
+//   warpgroup 1 (248 registers a thread): activation, one query row per
 //               thread: reads its whole row of S from TMEM at once, masks the
 //               ragged edge / window, applies the online softmax (running max
 //               with lazy rescaling of O) or the ALU-only GELU, and writes P
@@ -82,7 +83,7 @@ struct FwdCfg {
   // warpgroup; the epilogue keeps the launch count.  Each SM sub-partition
   // holds one warp of each warpgroup, so the launch count R must satisfy
   // REGS_CTRL + REGS_ACT + R <= 3 R.
-  static constexpr int REGS_CTRL = 56;
+  static constexpr int REGS_CTRL = 88;
   static constexpr int REGS_ACT = 248;
   static constexpr int MIN_LAUNCH_REGS = (REGS_CTRL + REGS_ACT + 1) / 2;
   static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
@@ -252,11 +253,11 @@ __device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, FwdBar
     // B = V tile, MN-major: 16 keys = two 8-row groups (SBO = 1024 B apart);
     // the two 64-column halves of D sit one chunk apart (LBO).
     const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK_BYTES, 1024);
-    ptx::mma_ts(tmem + o_col, tmem + p_col + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
+    ptx::mma_ts_elect(tmem + o_col, tmem + p_col + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
   }
-  ptx::mma_commit(&B.v_empty[sv]);
-  ptx::mma_commit(&B.o_done);
-  if (P.last) ptx::mma_commit(&B.o_full[P.ob]);
+  ptx::mma_commit_elect(&B.v_empty[sv]);
+  ptx::mma_commit_elect(&B.o_done);
+  if (P.last) ptx::mma_commit_elect(&B.o_full[P.ob]);
   return true;
 }
 
@@ -292,12 +293,12 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, ui
         // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
         const uint32_t qoff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
         const uint32_t koff = (kk >> 2) * C::KV_CHUNK_BYTES + (kk & 3) * 32;
-        ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024), ptx::sdesc_sw128(k_base + koff, 16, 1024),
+        ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024), ptx::sdesc_sw128(k_base + koff, 16, 1024),
                     idesc, kk > 0 ? 1u : 0u);
       }
-      ptx::mma_commit(&B.s_full[sb]);
-      ptx::mma_commit(&B.k_empty[s]);
-      if (j == t.n_kv - 1) ptx::mma_commit(&B.q_empty[qs]);
+      ptx::mma_commit_elect(&B.s_full[sb]);
+      ptx::mma_commit_elect(&B.k_empty[s]);
+      if (j == t.n_kv - 1) ptx::mma_commit_elect(&B.q_empty[qs]);
       if (have_prev) {
         ok = issue_pv<D, MODE>(p, sm, B, tmem, prev);
         if (!ok) break;
@@ -310,7 +311,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, ui
   if (ok && have_prev) ok = issue_pv<D, MODE>(p, sm, B, tmem, prev);
   if (!ok) report_failure(p, abort, kStatusMma);
   // Every MMA this thread issued is complete once this commit lands.
-  ptx::mma_commit(&B.mma_drain);
+  ptx::mma_commit_elect(&B.mma_drain);
   const int never = 0;
   ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
 }
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
     } else if (warp == 2) {
       if (lane == 0) run_producer<D, MODE, true>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
-      if (lane == 0) run_mma<D, MODE>(p, sm, B, tmem, ibeg, iend);
+      run_mma<D, MODE>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
     }
   } else if (warp < 8) {  // warpgroup 1: activation, a whole row of scores in registers
     ptx::regs_inc<C::REGS_ACT>();

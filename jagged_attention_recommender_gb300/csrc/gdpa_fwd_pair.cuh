@@ -15,11 +15,12 @@
 //   the other way round.
 //
 // Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
-// and K (warp 0), the MMA issuer + TMEM owner (warp 1) and the TMA producer
-// for V (warp 2), and hands its registers to warpgroups 1 and 2, the
-// activation/epilogue of tiles A and B (216 registers a thread, so a whole
-// row of 128 scores stays in registers: S is read from TMEM once).  TMEM
-// (512 columns): S_A 0, S_B 128, O_A 256, O_B 384.
+// and K (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
+// the issue loop and one elected lane issues) and the TMA producer for V
+// (warp 2), and hands registers to warpgroups 1 and 2, the activation /
+// epilogue of tiles A and B (200 registers a thread, so a whole row of 128
+// scores stays in registers: S is read from TMEM once).  TMEM (512
+// columns): S_A 0, S_B 128, O_A 256, O_B 384.
 #pragma once
 
 #include "gdpa_fwd_common.cuh"
@@ -49,8 +50,8 @@ struct PairCfg {
   // registers to the two activation warpgroups.  Each SM sub-partition holds
   // one warp of each, so the launch count R must satisfy
   // REGS_CTRL + 2 REGS_ACT <= 3 R.
-  static constexpr int REGS_CTRL = 72;
-  static constexpr int REGS_ACT = 216;
+  static constexpr int REGS_CTRL = 104;
+  static constexpr int REGS_ACT = 200;
   static constexpr int MIN_LAUNCH_REGS = (REGS_CTRL + 2 * REGS_ACT + 2) / 3;
   static_assert(384 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -208,13 +209,20 @@ __device__ __forceinline__ bool pair_issue_pv(const FwdParams& p, uint8_t* sm, P
   const int sv = P.g % C::NV;
   if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
-  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::TILE_BYTES);
+  // One descriptor, advanced by 16 keys (2048 bytes, 128 in the address
+  // field) per MMA: the V stage lies below 256 KB, so the 14-bit field
+  // never carries.  A whole tile takes the unrolled path.
+  const uint64_t bd0 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_V + sv * C::TILE_BYTES), C::CHUNK_BYTES, 1024);
   constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
-  for (int kk = 0; kk < P.n16; ++kk) {
-    const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::CHUNK_BYTES, 1024);
-    ptx::mma_ts(tmem + C::tm_o(x), tmem + C::tm_s(x) + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
+  const uint32_t d_tm = tmem + C::tm_o(x), a_tm = tmem + C::tm_s(x);
+  const uint32_t acc0 = P.first ? 0u : 1u;
+  if (P.n16 == 8) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
+  } else {
+    for (int kk = 0; kk < P.n16; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
   }
-  ptx::mma_commit(&B.o_done[x]);
+  ptx::mma_commit_elect(&B.o_done[x]);
   return true;
 }
 
@@ -269,20 +277,22 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
         }
         act[x] = has[x] && j >= t.t0[x] && j < t.t1[x];
         if (!act[x]) continue;
+        // descriptors advanced in their address field (16-byte units)
+        const uint64_t qd = ptx::sdesc_sw128(q_base[x], 16, 1024), kd = ptx::sdesc_sw128(k_base, 16, 1024);
+        const uint32_t d_tm = tmem + C::tm_s(x);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + C::tm_s(x), ptx::sdesc_sw128(q_base[x] + off, 16, 1024),
-                      ptx::sdesc_sw128(k_base + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+          ptx::mma_ss_elect(d_tm, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&B.s_full[x]);
+        ptx::mma_commit_elect(&B.s_full[x]);
       }
       if (!ok) break;
-      if (pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);  // both P V of the previous tile issued
-      ptx::mma_commit(&B.k_empty[sk]);
+      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);  // both P V of the previous tile issued
+      ptx::mma_commit_elect(&B.k_empty[sk]);
       if (j == t.n_kv - 1) {
         for (int x = 0; x < 2; ++x)
-          if (has[x]) ptx::mma_commit(&B.q_empty[x][qn[x] % C::NQS]);
+          if (has[x]) ptx::mma_commit_elect(&B.q_empty[x][qn[x] % C::NQS]);
       }
       for (int x = 0; x < 2; ++x) {
         if (!act[x]) continue;
@@ -298,9 +308,9 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
-  if (ok && pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);
+  if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
-  ptx::mma_commit(&B.mma_drain);
+  ptx::mma_commit_elect(&B.mma_drain);
   const int never = 0;
   ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
 }
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_cons
     } else if (warp == 2) {
       if (lane == 0) pair_producer<D, WIN, true>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
-      if (lane == 0) pair_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+      pair_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
     }
   } else {  // warpgroups 1 and 2: tiles A and B, a whole row of scores in registers
     ptx::regs_inc<C::REGS_ACT>();

@@ -26,8 +26,9 @@
 // side skips every block outside its window.
 //
 // Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
-// and K (warp 0), the MMA issuer + TMEM owner (warp 1) and the TMA producer
-// for V (warp 2), and hands its registers to warpgroups 1 and 2, the
+// and K (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
+// the issue loop and one elected lane issues) and the TMA producer for V
+// (warp 2), and hands its registers to warpgroups 1 and 2, the
 // activation/epilogue of tiles A and B.  TMEM (512 columns): S_A buffers 0
 // and 64, S_B buffers 128 and 192, O_A 256, O_B 384.  An activation thread
 // holds one query row; it reads its 64 scores of a tile from TMEM at once.
@@ -234,9 +235,9 @@ __device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm,
     // B = V tile, MN-major: 16 keys = two 8-row groups (SBO = 1024 B apart);
     // the two 64-column halves of D sit one chunk apart (LBO).
     const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK, 1024);
-    ptx::mma_ts(tmem + C::tm_o(x), tmem + C::tm_s(x, b) + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
+    ptx::mma_ts_elect(tmem + C::tm_o(x), tmem + C::tm_s(x, b) + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
   }
-  ptx::mma_commit(&B.o_done[x]);
+  ptx::mma_commit_elect(&B.o_done[x]);
   return true;
 }
 
@@ -285,15 +286,15 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
           // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
           const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          ptx::mma_ss(tmem + s_col, ptx::sdesc_sw128(q_base[x] + qoff, 16, 1024),
+          ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base[x] + qoff, 16, 1024),
                       ptx::sdesc_sw128(k_base + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&B.s_full[x][gx[x] & 1]);
+        ptx::mma_commit_elect(&B.s_full[x][gx[x] & 1]);
       }
-      ptx::mma_commit(&B.k_empty[sk]);
+      ptx::mma_commit_elect(&B.k_empty[sk]);
       if (j == t.n_kv - 1) {
         for (int x = 0; x < 2; ++x)
-          if (has[x]) ptx::mma_commit(&B.q_empty[x][qn[x] % C::NQS]);
+          if (has[x]) ptx::mma_commit_elect(&B.q_empty[x][qn[x] % C::NQS]);
       }
       // Then O_x += P_x V for each side's previous tile (issued here even
       // when this tile has no S_x, so that every P V of the previous K/V
@@ -304,7 +305,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
         pend[x] = false;
       }
       if (!ok) break;
-      if (pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);
+      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
       for (int x = 0; x < 2; ++x) {
         if (!act[x]) continue;
         pv[x] = Pair64PV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
@@ -319,9 +320,9 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair64_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
-  if (ok && pend_v) ptx::mma_commit(&B.v_empty[pend_v_g % C::NV]);
+  if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
-  ptx::mma_commit(&B.mma_drain);
+  ptx::mma_commit_elect(&B.mma_drain);
   const int never = 0;
   ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
 }
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
     } else if (warp == 2) {
       if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
-      if (lane == 0) pair64_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);
+      pair64_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
     }
   } else {  // warpgroups 1 and 2: tiles A and B
     ptx::regs_inc<C::regs_act(ACT)>();
