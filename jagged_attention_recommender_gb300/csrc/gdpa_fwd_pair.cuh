@@ -394,24 +394,44 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
         }
         // The whole row of scores in registers, one TMEM round trip.
         uint32_t sr[128];
+        // A whole tile of valid keys (softmax, scale > 0): the second half
+        // of the row loads while the first half's maximum is taken.
+        const bool split_ld = !WIN && ACT == kActSoftmax && fullm == 0xFu && sl > 0.0f;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (split_ld) {
+          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          ptx::tmem_wait_ld_r64(&sr[0]);
+          ptx::tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+          ptx::tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
-        ptx::tmem_wait_ld();
+          for (int c = 0; c < 64; c += 8) {
+            m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+          ptx::tmem_wait_ld_r64(&sr[64]);
+#pragma unroll
+          for (int c = 64; c < 128; c += 8) {
+            m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
+          ptx::tmem_wait_ld();
+        }
         if (ACT == kActSoftmax) {
           // Scores in log2 units: x = s * scale * log2(e); masked columns
           // become -inf.  With scale > 0 the scaling is folded into the
           // exponent's FMA; otherwise it is applied first.
           const bool fold = sl > 0.0f;
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (!WIN && fullm == 0xFu && fold) {
-#pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-              m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-              m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-              m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-              m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-            }
+          if (split_ld) {
+            // maximum taken with the loads
           } else
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
