@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the jagged GDPA forward pass -- TEST INFRASTRUCTURE.
+"""fp64 CPU oracle for the jagged GDPA forward and backward passes -- TEST INFRASTRUCTURE.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product library never loads it and
@@ -38,6 +38,11 @@ def _load():
         lib.oracle_gdpa_fwd.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int]
         lib.oracle_gdpa_fwd.restype = ctypes.c_int
+        lib.oracle_gdpa_bwd.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int]
+        lib.oracle_gdpa_bwd.restype = ctypes.c_int
+        lib.oracle_gelu_tanh_grad.argtypes = [ctypes.c_double]
+        lib.oracle_gelu_tanh_grad.restype = ctypes.c_double
         lib.oracle_gelu_tanh.argtypes = [ctypes.c_double]
         lib.oracle_gelu_tanh.restype = ctypes.c_double
         lib.oracle_num_cpus.restype = ctypes.c_int
@@ -75,6 +80,43 @@ def gdpa_fwd_batch(batch, nthreads: int = 0) -> np.ndarray:
     w = batch.workload
     return gdpa_fwd(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, w.H, w.D, w.act,
                     w.window_blocks, w.scale, nthreads)
+
+
+def gdpa_bwd(q, k, v, dout, q_offsets, kv_offsets, H: int, D: int, act: int, window_blocks: int,
+             scale: float, nthreads: int = 0):
+    """Oracle gradients ``(dq, dk, dv, lse)`` in fp64 for the upstream gradient ``dout``.
+
+    ``dout`` is uint16 bf16 bits ``[Tq, H, D]`` like ``q``; ``lse`` is ``[Tq, H]``
+    (natural log; -inf for an empty key set, 0 for GELU rows).
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    do = np.ascontiguousarray(dout, dtype=np.uint16)
+    qo = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ko = np.ascontiguousarray(kv_offsets, dtype=np.int32)
+    B = len(qo) - 1
+    Tq, Tkv = int(qo[-1]), int(ko[-1])
+    dq = np.zeros((Tq, H, D), dtype=np.float64)
+    dk = np.zeros((Tkv, H, D), dtype=np.float64)
+    dv = np.zeros((Tkv, H, D), dtype=np.float64)
+    lse = np.zeros((Tq, H), dtype=np.float64)
+    rc = lib.oracle_gdpa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(qo), _ptr(ko), B, H, D, act,
+                             window_blocks, float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gdpa_bwd returned %d" % rc)
+    return dq, dk, dv, lse
+
+
+def gdpa_bwd_batch(batch, dout, nthreads: int = 0):
+    w = batch.workload
+    return gdpa_bwd(batch.q, batch.k, batch.v, dout, batch.q_offsets, batch.kv_offsets, w.H, w.D, w.act,
+                    w.window_blocks, w.scale, nthreads)
+
+
+def gelu_tanh_grad(x: float) -> float:
+    return _load().oracle_gelu_tanh_grad(float(x))
 
 
 def gelu_tanh(x: float) -> float:

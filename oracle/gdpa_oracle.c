@@ -36,6 +36,21 @@
  * The oracle follows that definition literally: it loops over sequences,
  * heads, queries and keys, in fp64, with libm's exp and tanh.  There is no
  * tiling, no online (running-max) rescaling and no reordering.
+ *
+ * Backward (oracle_gdpa_bwd): the gradients of the same forward for an
+ * upstream gradient dO -- the training step the techfeed summary's JFA
+ * section measures for this attention (its backward parallelises dQ, dK,
+ * dV).  The formulas are the chain rule written out for one query row i,
+ * with P_ij the weight of key j in o_i and dP_ij = <dO_i, v_j>:
+ *
+ *   dv_j  = sum_i P_ij dO_i
+ *   softmax:  P_ij = exp(s_ij - lse_i),  lse_i = log sum_j exp(s_ij),
+ *             dS_ij = P_ij (dP_ij - sum_j' P_ij' dP_ij')
+ *   GELU:     P_ij = gelu(s_ij) / Lkv_b,  dS_ij = gelu'(s_ij) dP_ij / Lkv_b
+ *   dq_i  = scale * sum_j dS_ij k_j,   dk_j = scale * sum_i dS_ij q_i
+ *
+ * It also returns lse_i (natural log; -inf for an empty key set, 0 for GELU
+ * rows), which a forward that keeps it for the backward must reproduce.
  */
 #include <math.h>
 #include <pthread.h>
@@ -59,6 +74,13 @@ static double bf16_to_double(uint16_t bits) {
 double oracle_gelu_tanh(double x) {
   const double c = sqrt(2.0 / M_PI);
   return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+/* d/dx of oracle_gelu_tanh. */
+double oracle_gelu_tanh_grad(double x) {
+  const double c = sqrt(2.0 / M_PI);
+  const double t = tanh(c * (x + 0.044715 * x * x * x));
+  return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * x * x);
 }
 
 /* Is key j in the key set of query i (both counted from the sequence start)? */
@@ -186,6 +208,151 @@ int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   if (started == 0) { /* no thread could start: run on this one */
     failed = worker(&J) != NULL;
   }
+  for (int t = 0; t < started; ++t) {
+    void* r = NULL;
+    pthread_join(th[t], &r);
+    if (r) failed = 1;
+  }
+  free(th);
+  return failed ? 2 : 0;
+}
+
+/* ------------------------------------------------------------------ backward */
+
+typedef struct {
+  const uint16_t *q, *k, *v, *dout;
+  const int32_t *q_off, *kv_off;
+  int B, H, D, act, window_blocks;
+  double scale;
+  double *dq, *dk, *dv, *lse;
+  int64_t next_task;
+} bjob_t;
+
+typedef struct {
+  double *kbuf, *vbuf, *qrow, *drow, *s, *p, *dp;
+} bscratch_t;
+
+static void run_bwd_task(const bjob_t* J, int b, int h, const bscratch_t* W) {
+  const int H = J->H, D = J->D;
+  const int64_t q0 = J->q_off[b], Lq = J->q_off[b + 1] - q0;
+  const int64_t k0 = J->kv_off[b], Lkv = J->kv_off[b + 1] - k0;
+  for (int64_t j = 0; j < Lkv; ++j)
+    for (int d = 0; d < D; ++d) {
+      W->kbuf[j * D + d] = bf16_to_double(J->k[((k0 + j) * H + h) * D + d]);
+      W->vbuf[j * D + d] = bf16_to_double(J->v[((k0 + j) * H + h) * D + d]);
+      J->dk[((k0 + j) * H + h) * (int64_t)D + d] = 0.0;
+      J->dv[((k0 + j) * H + h) * (int64_t)D + d] = 0.0;
+    }
+  for (int64_t i = 0; i < Lq; ++i) {
+    double* dqi = J->dq + ((q0 + i) * H + h) * (int64_t)D;
+    for (int d = 0; d < D; ++d) {
+      W->qrow[d] = bf16_to_double(J->q[((q0 + i) * H + h) * D + d]);
+      W->drow[d] = bf16_to_double(J->dout[((q0 + i) * H + h) * D + d]);
+      dqi[d] = 0.0;
+    }
+    double* lse_i = J->lse + (q0 + i) * H + h;
+    *lse_i = J->act == ORACLE_ACT_SOFTMAX ? -INFINITY : 0.0;
+    int any = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Lkv; ++j) {
+      if (!key_in_set(i, j, J->window_blocks)) continue;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += W->qrow[d] * W->kbuf[j * D + d];
+      W->s[j] = J->scale * dot;
+      if (W->s[j] > m) m = W->s[j];
+      any = 1;
+    }
+    if (!any) continue; /* empty key set: no gradient flows */
+    /* P_ij and dP_ij = <dO_i, v_j> over the key set */
+    double den = 0.0;
+    if (J->act == ORACLE_ACT_SOFTMAX) {
+      for (int64_t j = 0; j < Lkv; ++j)
+        if (key_in_set(i, j, J->window_blocks)) den += exp(W->s[j] - m);
+      *lse_i = m + log(den);
+    }
+    double dsum = 0.0; /* sum_j P_ij dP_ij (softmax) */
+    for (int64_t j = 0; j < Lkv; ++j) {
+      if (!key_in_set(i, j, J->window_blocks)) continue;
+      W->p[j] = J->act == ORACLE_ACT_SOFTMAX ? exp(W->s[j] - *lse_i) : oracle_gelu_tanh(W->s[j]) / (double)Lkv;
+      double dp = 0.0;
+      for (int d = 0; d < D; ++d) dp += W->drow[d] * W->vbuf[j * D + d];
+      W->dp[j] = dp;
+      dsum += W->p[j] * dp;
+    }
+    for (int64_t j = 0; j < Lkv; ++j) {
+      if (!key_in_set(i, j, J->window_blocks)) continue;
+      const double ds = J->act == ORACLE_ACT_SOFTMAX ? W->p[j] * (W->dp[j] - dsum)
+                                                     : oracle_gelu_tanh_grad(W->s[j]) * W->dp[j] / (double)Lkv;
+      double* dkj = J->dk + ((k0 + j) * H + h) * (int64_t)D;
+      double* dvj = J->dv + ((k0 + j) * H + h) * (int64_t)D;
+      for (int d = 0; d < D; ++d) {
+        dqi[d] += J->scale * ds * W->kbuf[j * D + d];
+        dkj[d] += J->scale * ds * W->qrow[d];
+        dvj[d] += W->p[j] * W->drow[d];
+      }
+    }
+  }
+}
+
+static void* bwd_worker(void* arg) {
+  bjob_t* J = (bjob_t*)arg;
+  int64_t max_kv = 0;
+  for (int b = 0; b < J->B; ++b) {
+    int64_t L = J->kv_off[b + 1] - J->kv_off[b];
+    if (L > max_kv) max_kv = L;
+  }
+  bscratch_t W;
+  W.kbuf = (double*)malloc(sizeof(double) * (size_t)(max_kv * J->D + 1));
+  W.vbuf = (double*)malloc(sizeof(double) * (size_t)(max_kv * J->D + 1));
+  W.qrow = (double*)malloc(sizeof(double) * (size_t)J->D);
+  W.drow = (double*)malloc(sizeof(double) * (size_t)J->D);
+  W.s = (double*)malloc(sizeof(double) * (size_t)(max_kv + 1));
+  W.p = (double*)malloc(sizeof(double) * (size_t)(max_kv + 1));
+  W.dp = (double*)malloc(sizeof(double) * (size_t)(max_kv + 1));
+  void* rc = NULL;
+  if (!W.kbuf || !W.vbuf || !W.qrow || !W.drow || !W.s || !W.p || !W.dp) {
+    rc = (void*)1;
+  } else {
+    const int64_t ntask = (int64_t)J->B * J->H;
+    for (;;) {
+      int64_t t = __atomic_fetch_add(&J->next_task, 1, __ATOMIC_RELAXED);
+      if (t >= ntask) break;
+      run_bwd_task(J, (int)(t / J->H), (int)(t % J->H), &W);
+    }
+  }
+  free(W.kbuf); free(W.vbuf); free(W.qrow); free(W.drow); free(W.s); free(W.p); free(W.dp);
+  return rc;
+}
+
+/*
+ * Gradients of oracle_gdpa_fwd for the upstream gradient dout (bf16 bits
+ * [Tq, H, D]).  dq: fp64 [Tq, H, D]; dk, dv: fp64 [Tkv, H, D]; lse: fp64
+ * [Tq, H]; all fully written (keys no query sees get zero gradients).
+ * Arguments and return codes as oracle_gdpa_fwd.
+ */
+int oracle_gdpa_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                    const int32_t* q_off, const int32_t* kv_off, int B, int H, int D, int act, int window_blocks,
+                    double scale, double* dq, double* dk, double* dv, double* lse, int nthreads) {
+  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH)) return 1;
+  if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
+  for (int b = 0; b < B; ++b) {
+    if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;
+    if (window_blocks > 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
+  }
+  if (B == 0) return 0;
+  if ((q_off[B] > 0 && (!q || !dout || !dq || !lse)) || (kv_off[B] > 0 && (!k || !v || !dk || !dv))) return 1;
+  bjob_t J = {q, k, v, dout, q_off, kv_off, B, H, D, act, window_blocks, scale, dq, dk, dv, lse, 0};
+  if (nthreads <= 0) nthreads = oracle_num_cpus();
+  if (nthreads > B * H) nthreads = B * H;
+  if (nthreads < 1) nthreads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return 2;
+  int started = 0, failed = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, bwd_worker, &J) != 0) break;
+    ++started;
+  }
+  if (started == 0) failed = bwd_worker(&J) != NULL;
   for (int t = 0; t < started; ++t) {
     void* r = NULL;
     pthread_join(th[t], &r);
