@@ -107,6 +107,45 @@ gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void* v, const 
                              void* stream);
 
 /*
+ * gdpa_fwd_lse -- gdpa_fwd_async that also keeps, for the backward pass, the
+ * row logsumexp of every softmax query row: lse[t * H + h] =
+ * ln sum_j exp(scale <q_t, k_j>) over the row's key set (natural log; -inf
+ * for a row whose sequence has no keys).  lse: device fp32 [Tq, H], 4-byte
+ * aligned, written in full for softmax and not touched for GELU (may be
+ * NULL then).  Every other argument, layout and result as gdpa_fwd_async.
+ * The row logsumexp is the quantity the backward needs to rebuild the
+ * softmax weights tile by tile (techfeed summary of "GEM Training", JFA
+ * section: the forward of a training step feeds its backward).
+ */
+gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                           const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets, int B,
+                           int H, int D, int act, int window_blocks, float scale, void* out, float* lse,
+                           void* stream);
+
+/*
+ * gdpa_bwd -- gradients of the forward for an upstream gradient dout:
+ *   dq = dL/dq, dk = dL/dk, dv = dL/dv for L = sum(dout * out), computed by
+ * the chain rule of the forward's definition (techfeed summary of "GEM
+ * Training", JFA section: a backward over batch x heads without atomics):
+ *   softmax: P_ij = exp(scale <q_i,k_j> - lse_i), dS_ij = P_ij (<dO_i,v_j> - <dO_i,o_i>)
+ *   GELU:    P_ij = gelu(scale <q_i,k_j>) / Lkv,  dS_ij = gelu'(...) <dO_i,v_j> / Lkv
+ *   dv_j = sum_i P_ij dO_i,  dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i
+ * q, k, v, out, dout: device bf16 [tokens, H, D] (out and lse from
+ * gdpa_fwd_lse on the same inputs); lse: device fp32 [Tq, H] (softmax only;
+ * may be NULL for GELU); offsets twice, host (h_*, read during the call) and
+ * device, as gdpa_fwd_async; dq: device bf16 [Tq, H, D]; dk, dv: device bf16
+ * [Tkv, H, D]; all written in full (keys no query sees get zero gradients).
+ * Tensors 16-byte aligned.  Full attention only: window_blocks > 0 returns
+ * GDPA_ERR_UNSUPPORTED.  Asynchronous on `stream`; the library keeps a
+ * grow-only device buffer for the work lists and 8 Tq H bytes of scratch.
+ * Errors as gdpa_fwd (a wait that runs out shows in gdpa_device_status).
+ */
+gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                       const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                       const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                       int window_blocks, float scale, void* dq, void* dk, void* dv, void* stream);
+
+/*
  * gdpa_fwd_noalloc -- gdpa_fwd for callers that must not allocate memory.
  * The pages describe no such entry point; it exists for users of this
  * library.  Some callers cannot allocate where they run attention: a serving

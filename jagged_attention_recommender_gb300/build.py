@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libgdpa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdpa_kernels.cu", "gdpa_api.cu", "gdpa_plan.cpp", "gdpa_noalloc.cu"]
+SOURCES = ["gdpa_kernels.cu", "gdpa_bwd.cu", "gdpa_api.cu", "gdpa_plan.cpp", "gdpa_noalloc.cu"]
 
 
 def _nvcc() -> str:

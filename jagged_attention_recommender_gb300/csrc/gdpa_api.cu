@@ -81,6 +81,10 @@ struct DeviceCtx {
   cudaEvent_t stage_free = nullptr;  // host staging buffer may be overwritten
   cudaEvent_t work_free = nullptr;   // device buffers no longer read by an earlier launch
   bool events_ok = false;
+  // gdpa_bwd: device work lists + scratch, pinned staging, and their events
+  Buf d_bwd;
+  Buf h_bwd{nullptr, 0, true};
+  cudaEvent_t bwd_stage_free = nullptr, bwd_free = nullptr;
   // gdpa_fwd_host pipeline: copy-in and copy-out streams, per-chunk events
   cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaEvent_t ev_start = nullptr, ev_meta = nullptr, ev_in[kMaxChunks] = {}, ev_done[kMaxChunks] = {};
@@ -102,7 +106,10 @@ struct DeviceCtx {
     if (events_ok) return GDPA_OK;
     if (cudaEventCreateWithFlags(&stage_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
     if (cudaEventCreateWithFlags(&work_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
-    if (cudaEventRecord(stage_free, 0) != cudaSuccess || cudaEventRecord(work_free, 0) != cudaSuccess)
+    if (cudaEventCreateWithFlags(&bwd_stage_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&bwd_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaEventRecord(stage_free, 0) != cudaSuccess || cudaEventRecord(work_free, 0) != cudaSuccess ||
+        cudaEventRecord(bwd_stage_free, 0) != cudaSuccess || cudaEventRecord(bwd_free, 0) != cudaSuccess)
       return GDPA_ERR_CUDA;
     events_ok = true;
     return GDPA_OK;
@@ -161,8 +168,9 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
                               const int32_t* d_q_off, const int32_t* d_kv_off, int64_t Tq, int64_t Tkv, int H, int D,
                               int act, int window_blocks, float scale, int num_ctas, int rows_per_item,
-                              int kv_tile, int64_t n_items, cudaStream_t stream) {
+                              int kv_tile, int64_t n_items, cudaStream_t stream, float* lse = nullptr) {
   LaunchArgs a;
+  a.lse = lse;
   a.rows_per_item = rows_per_item;
   a.kv_tile = kv_tile;
   a.q = q;
@@ -264,6 +272,112 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
                          rpi, kvt, n_items, s);
+}
+
+extern "C" gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                                      const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
+                                      int B, int H, int D, int act, int window_blocks, float scale, void* out,
+                                      float* lse, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  if (B == 0) return GDPA_OK;
+  int64_t Tq = 0, Tkv = 0;
+  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window_blocks, &Tq, &Tkv)) != GDPA_OK) return st;
+  if ((st = check_tensors(q, k, v, out, Tq, Tkv)) != GDPA_OK) return st;
+  if (Tq == 0) return GDPA_OK;
+  if (!q_offsets || !kv_offsets) return GDPA_ERR_INVALID_ARG;
+  if (act == GDPA_ACT_SOFTMAX && (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)) return GDPA_ERR_INVALID_ARG;
+  int device = 0, sms = 0;
+  if ((st = num_sms(&device, &sms)) != GDPA_OK) return st;
+  DeviceCtx& c = ctx(device);
+  std::lock_guard<std::mutex> lock(c.mu);
+  if ((st = c.init()) != GDPA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int num_ctas = 0;
+  int rpi = 0, kvt = 0;
+  int64_t n_items = 0;
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi,
+                            &kvt, &n_items)) != GDPA_OK)
+    return st;
+  return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
+                         rpi, kvt, n_items, s, act == GDPA_ACT_SOFTMAX ? lse : nullptr);
+}
+
+extern "C" gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                  const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                                  const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                                  int window_blocks, float scale, void* dq, void* dk, void* dv, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  if (window_blocks > 0) return GDPA_ERR_UNSUPPORTED;
+  if (B == 0) return GDPA_OK;
+  int64_t Tq = 0, Tkv = 0;
+  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, 0, &Tq, &Tkv)) != GDPA_OK) return st;
+  if (Tq >= (int64_t)1 << 31 || Tkv >= (int64_t)1 << 31) return GDPA_ERR_UNSUPPORTED;
+  if (Tq > 0 && (!q || !dq || !aligned16(q) || !aligned16(dq))) return GDPA_ERR_INVALID_ARG;
+  if (Tq > 0 && Tkv > 0 && (!out || !dout || !aligned16(out) || !aligned16(dout))) return GDPA_ERR_INVALID_ARG;
+  if (Tq > 0 && Tkv > 0 && act == GDPA_ACT_SOFTMAX && (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)))
+    return GDPA_ERR_INVALID_ARG;
+  if (!q_offsets || !kv_offsets) return GDPA_ERR_INVALID_ARG;
+  if (Tq == 0 && Tkv == 0) return GDPA_OK;
+  int device = 0, sms = 0;
+  if ((st = num_sms(&device, &sms)) != GDPA_OK) return st;
+  DeviceCtx& c = ctx(device);
+  std::lock_guard<std::mutex> lock(c.mu);
+  if ((st = c.init()) != GDPA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t> dq_items, kv_items;
+  try {
+    plan_backward(h_q_offsets, h_kv_offsets, B, H, dq_items, kv_items);
+  } catch (const std::bad_alloc&) {
+    return GDPA_ERR_NO_MEMORY;
+  }
+  const size_t dq_bytes = dq_items.size() * sizeof(int32_t), kv_bytes = kv_items.size() * sizeof(int32_t);
+  const size_t lists = align_up(dq_bytes, 16) + align_up(kv_bytes, 16);
+  const size_t scratch = (size_t)Tq * H * 2 * sizeof(float);
+  const size_t total = lists + scratch + 16;
+  // the device buffer may still be read by an earlier backward on another stream
+  if (cudaStreamWaitEvent(s, c.bwd_free, 0) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (c.d_bwd.cap < total) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;
+    if ((st = c.d_bwd.ensure(total)) != GDPA_OK) return st;
+  }
+  if (cudaEventSynchronize(c.bwd_stage_free) != cudaSuccess) return GDPA_ERR_CUDA;
+  if ((st = c.h_bwd.ensure(lists + 16)) != GDPA_OK) return st;
+  char* h = static_cast<char*>(c.h_bwd.p);
+  if (dq_bytes) std::memcpy(h, dq_items.data(), dq_bytes);
+  if (kv_bytes) std::memcpy(h + align_up(dq_bytes, 16), kv_items.data(), kv_bytes);
+  char* d = static_cast<char*>(c.d_bwd.p);
+  if (lists && cudaMemcpyAsync(d, h, lists, cudaMemcpyHostToDevice, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (cudaEventRecord(c.bwd_stage_free, s) != cudaSuccess) return GDPA_ERR_CUDA;
+  BwdLaunchArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.q_off = q_offsets;
+  a.kv_off = kv_offsets;
+  a.dq_items = d;
+  a.n_dq = (int64_t)(dq_items.size() / 4);
+  a.kv_items = d + align_up(dq_bytes, 16);
+  a.n_kv = (int64_t)(kv_items.size() / 4);
+  a.scratch = reinterpret_cast<float*>(d + lists);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.Tq = Tq;
+  a.Tkv = Tkv;
+  a.H = H;
+  a.D = D;
+  a.act = act;
+  a.scale = scale;
+  a.stream = stream;
+  if ((st = launch_backward(a)) != GDPA_OK) return st;
+  return cudaEventRecord(c.bwd_free, s) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
 extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,

@@ -1,0 +1,533 @@
+// gdpa_bwd.cuh -- jagged GDPA backward on sm_103a: dQ, dK and dV.
+//
+// The gradients of the forward for an upstream gradient dO, per (sequence,
+// head), with s_ij = <q_i, k_j>, x_ij = scale s_ij and dP_ij = <dO_i, v_j>:
+//
+//   softmax: P_ij = 2^(x_ij log2(e) - lse2_i),  dS_ij = P_ij (dP_ij - Dv_i),
+//            Dv_i = <dO_i, O_i>,  lse2_i the forward's row logsumexp, log2 units
+//   GELU:    P_ij = gelu(x_ij) / Lkv,             dS_ij = gelu'(x_ij) dP_ij / Lkv
+//   dV = P^T dO,   dQ = scale dS K,   dK = scale dS^T Q
+//
+// (the backward the techfeed summary of "GEM Training" describes in its JFA
+// section: dQ, dK and dV computed without atomics, parallel over batch and
+// heads.)  Two kernels, one CTA per work item, each output written once:
+//
+//   gdpa_bwd_dq_kernel    item = 128 query rows of one (sequence, head); it
+//     walks the sequence's 128-key K/V tiles: S = Q K^T and dP = dO V^T into
+//     tensor memory, the activation warps turn them into dS (bf16, written
+//     over S), then dQ += dS K with dS read straight from tensor memory.
+//   gdpa_bwd_dkdv_kernel  item = 128 keys of one (sequence, head); it walks
+//     the sequence's 128-row query tiles: S^T = K Q^T and dP^T = V dO^T, the
+//     activation warps write P^T over S^T and dS^T over dP^T, then
+//     dV += P^T dO and dK += dS^T Q.
+//
+// Threads (192): warp 0 the TMA producer, warp 1 the MMA issuer (the whole
+// warp runs the loop, one elected lane issues), warps 2-5 the activation and
+// the epilogue (warp w owns tensor-memory lanes 32 (w mod 4) .. +31, one row
+// of S each).  Tensor memory (512 columns): S 0, dP 128, accumulators from
+// 256 (dQ; or dV then dK).  Shared memory (D = 128): the item's two resident
+// tiles (Q and dO, or K and V) and two stages of the two streamed ones.
+// Rows past a sequence's end are masked to P = dS = 0 in the activation, so
+// whatever the TMA box brought in for them never reaches an accumulator.
+#pragma once
+
+#include "gdpa_fwd_common.cuh"
+
+namespace gdpa {
+
+struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
+  CUtensorMap tm_q;   // 2-D views [T, H*D] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const int4* items;  // {sequence, head, first row of the item in its sequence, 0}
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  const float* lse2;  // [Tq, H]: row logsumexp of the forward, log2 units (softmax)
+  const float* dvec;  // [Tq, H]: <dO_i, O_i> (softmax)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  unsigned long long timeout_ns;
+  int H;
+  float score_scale;  // softmax: scale * log2(e); GELU: scale
+  float scale;
+  int align32;        // dq, dk and dv all 32-byte aligned: 32-byte stores allowed
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KCH = D / 64;
+  static constexpr int CHUNK_BYTES = 128 * 128;        // 128 rows x 64 bf16 columns
+  static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;  // 128 rows x D
+  static constexpr int OFF_R1 = 0;                      // resident: Q (dq) or K (dkdv)
+  static constexpr int OFF_R2 = OFF_R1 + TILE_BYTES;    // resident: dO (dq) or V (dkdv)
+  static constexpr int OFF_S1 = OFF_R2 + TILE_BYTES;    // streamed, 2 stages: K (dq) or Q (dkdv)
+  static constexpr int OFF_S2 = OFF_S1 + 2 * TILE_BYTES;  // streamed, 2 stages: V (dq) or dO (dkdv)
+  static constexpr int OFF_VEC = OFF_S2 + 2 * TILE_BYTES;  // dkdv: lse2 and Dv of a query tile, 2 buffers
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * 128 * 4;
+  static constexpr int BAR_BYTES = 256;
+  // at least 117 KB so that one CTA fits per SM (each allocates 512 TMEM columns)
+  static constexpr int SMEM_BYTES = (OFF_BAR + BAR_BYTES + 1024) > 119808 ? (OFF_BAR + BAR_BYTES + 1024) : 119808;
+  static constexpr uint32_t TM_S = 0, TM_P = 128, TM_A1 = 256, TM_A2 = 256 + D;
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 192;
+  static_assert(256 + 2 * D <= TM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct BwdBars {
+  uint64_t res_full;                 // the item's resident tiles landed
+  uint64_t st_full[2], st_empty[2];  // streamed stages
+  uint64_t mma_full;                 // S and dP of the current tile are in TMEM
+  uint64_t act_full;                 // P / dS of the current tile are in TMEM
+  uint64_t acc_full;                 // every MMA of the item completed
+  uint64_t vec_full[2];              // dkdv: lse2 / Dv of a query tile staged by the activation warps
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
+
+__device__ __forceinline__ void bwd_failure(const BwdParams& p, volatile int* abort, int bit) {
+  *abort = 1;
+  atomicOr(p.status, bit);
+}
+
+// The item's sequence geometry.
+struct BwdItem {
+  int b, h, row0, q_tok, kv_tok, Lq, Lkv;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
+  const int4 it = __ldg(p.items + blockIdx.x);
+  BwdItem t;
+  t.b = it.x;
+  t.h = it.y;
+  t.row0 = it.z;
+  t.q_tok = __ldg(p.q_off + t.b);
+  t.Lq = __ldg(p.q_off + t.b + 1) - t.q_tok;
+  t.kv_tok = __ldg(p.kv_off + t.b);
+  t.Lkv = __ldg(p.kv_off + t.b + 1) - t.kv_tok;
+  return t;
+}
+
+// ------------------------------------------------------------------ producer
+
+// Loads the two resident tiles at rows r_row (maps r1, r2), then n tiles of
+// the two streamed maps at rows s_row + 128 t into the two stages.
+template <int D>
+__device__ void bwd_producer(const BwdParams& p, uint8_t* sm, BwdBars& B, int h, const CUtensorMap* r1,
+                             const CUtensorMap* r2, int r_row, const CUtensorMap* s1, const CUtensorMap* s2,
+                             int s_row, int n) {
+  using C = BwdCfg<D>;
+  volatile int* abort = &B.abort;
+  ptx::mbar_arrive_expect_tx(&B.res_full, 2 * C::TILE_BYTES);
+#pragma unroll
+  for (int c = 0; c < C::KCH; ++c) {
+    ptx::tma_load_2d(sm + C::OFF_R1 + c * C::CHUNK_BYTES, r1, &B.res_full, h * D + 64 * c, r_row);
+    ptx::tma_load_2d(sm + C::OFF_R2 + c * C::CHUNK_BYTES, r2, &B.res_full, h * D + 64 * c, r_row);
+  }
+  int armed[2] = {-1, -1};
+  bool ok = true;
+  for (int t = 0; t < n; ++t) {
+    const int s = t & 1;
+    const uint32_t ph = (t >> 1) & 1;
+    ok = ptx::mbar_wait(&B.st_empty[s], ph ^ 1, p.timeout_ns, abort);
+    if (!ok) break;
+    ptx::mbar_arrive_expect_tx(&B.st_full[s], 2 * C::TILE_BYTES);
+    armed[s] = (int)ph;
+#pragma unroll
+    for (int c = 0; c < C::KCH; ++c) {
+      ptx::tma_load_2d(sm + C::OFF_S1 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, s1, &B.st_full[s], h * D + 64 * c,
+                       s_row + 128 * t);
+      ptx::tma_load_2d(sm + C::OFF_S2 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, s2, &B.st_full[s], h * D + 64 * c,
+                       s_row + 128 * t);
+    }
+  }
+  if (!ok) bwd_failure(p, abort, kStatusProducer);
+  // no copy may be in flight when the CTA exits
+  const int never = 0;
+  const unsigned long long drain_ns = 100000000ull;
+  ptx::mbar_wait(&B.res_full, 0, drain_ns, &never);
+  for (int s = 0; s < 2; ++s)
+    if (armed[s] >= 0) ptx::mbar_wait(&B.st_full[s], (uint32_t)armed[s], drain_ns, &never);
+}
+
+// ------------------------------------------------------------------ MMA issuer (whole warp)
+
+// Per streamed tile t (n tiles; `len` rows in all, so the last tile may be
+// partial): S = R1 S1^T and dP = R2 S2^T with both operands K-major; then,
+// once the activation has written its bf16 operands over S and dP, the
+// accumulating MMAs with the operand from tensor memory and the streamed
+// tile read MN-major (16 rows per MMA): dQ += dS K, or dV += P^T dO and
+// dK += dS^T Q.
+template <int D, bool DKDV>
+__device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int n, int len) {
+  using C = BwdCfg<D>;
+  volatile int* abort = &B.abort;
+  bool ok = ptx::mbar_wait(&B.res_full, 0, p.timeout_ns, abort);
+  ptx::tc_fence_after();
+  const uint64_t r1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R1), 16, 1024);
+  const uint64_t r2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R2), 16, 1024);
+  constexpr uint32_t idesc_acc = ptx::idesc_bf16(128, D, 1);
+  for (int t = 0; t < n && ok; ++t) {
+    const int s = t & 1;
+    ok = ptx::mbar_wait(&B.st_full[s], (t >> 1) & 1, p.timeout_ns, abort);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    const int cols = min(128, len - 128 * t);
+    const int n16 = (cols + 15) >> 4;
+    const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+    const uint32_t s1_addr = ptx::smem_u32(sm + C::OFF_S1 + s * C::TILE_BYTES);
+    const uint32_t s2_addr = ptx::smem_u32(sm + C::OFF_S2 + s * C::TILE_BYTES);
+    const uint64_t s1 = ptx::sdesc_sw128(s1_addr, 16, 1024), s2 = ptx::sdesc_sw128(s2_addr, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {  // S (or S^T): K-dimension D, 16 per MMA
+      const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+      ptx::mma_ss_elect(tmem + C::TM_S, r1 + off, s1 + off, idesc, kk > 0 ? 1u : 0u);
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {  // dP (or dP^T)
+      const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+      ptx::mma_ss_elect(tmem + C::TM_P, r2 + off, s2 + off, idesc, kk > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit_elect(&B.mma_full);
+    ok = ptx::mbar_wait(&B.act_full, t & 1, p.timeout_ns, abort);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    if (DKDV) {
+      // dV += P^T dO and dK += dS^T Q: B operands are the streamed dO and Q
+      // tiles, MN-major, 16 query rows (2048 bytes) per MMA
+      const uint64_t x1 = ptx::sdesc_sw128(s2_addr, C::CHUNK_BYTES, 1024);
+      const uint64_t x2 = ptx::sdesc_sw128(s1_addr, C::CHUNK_BYTES, 1024);
+      for (int kk = 0; kk < n16; ++kk)
+        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::TM_S + 8 * kk, x1 + 128u * kk, idesc_acc,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < n16; ++kk)
+        ptx::mma_ts_elect(tmem + C::TM_A2, tmem + C::TM_P + 8 * kk, x2 + 128u * kk, idesc_acc,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+    } else {
+      // dQ += dS K: B operand is the streamed K tile, MN-major, 16 keys per MMA
+      const uint64_t x1 = ptx::sdesc_sw128(s1_addr, C::CHUNK_BYTES, 1024);
+      for (int kk = 0; kk < n16; ++kk)
+        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::TM_S + 8 * kk, x1 + 128u * kk, idesc_acc,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+    }
+    ptx::mma_commit_elect(&B.st_empty[s]);  // the stage is free once these MMAs complete
+  }
+  if (!ok) bwd_failure(p, abort, kStatusMma);
+  ptx::mma_commit_elect(&B.acc_full);
+  // no MMA may be in flight when tensor memory is released
+  const int never = 0;
+  ptx::mbar_wait(&B.acc_full, 0, 100000000ull, &never);
+}
+
+// ------------------------------------------------------------------ activation
+
+// 32 columns of S and dP (one chunk) -> 16 packed bf16 words of P and of dS.
+// lse2/dv: per column (dkdv: one value per query) or per row (dq: the same
+// value in every column); `nvalid`: columns >= nvalid get P = dS = 0.
+template <int ACT, bool PER_COL>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2c,
+                                          const float* dvc, float lse2r, float dvr, int c0, int nvalid,
+                                          bool row_ok, float sl, float inv_l, uint64_t gA2, uint64_t gC2,
+                                          uint32_t (&pk_p)[16], uint32_t (&pk_ds)[16]) {
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int c = 2 * u;
+    const float s0 = __uint_as_float(sr[c]), s1 = __uint_as_float(sr[c + 1]);
+    const float d0 = __uint_as_float(dr[c]), d1 = __uint_as_float(dr[c + 1]);
+    float p0, p1, g0, g1;
+    if (ACT == kActSoftmax) {
+      float l0 = lse2r, l1 = lse2r, v0 = dvr, v1 = dvr;
+      if (PER_COL) {
+        l0 = lse2c[c];
+        l1 = lse2c[c + 1];
+        v0 = dvc[c];
+        v1 = dvc[c + 1];
+      }
+      p0 = ptx::ex2_approx(fmaf(s0, sl, -l0));
+      p1 = ptx::ex2_approx(fmaf(s1, sl, -l1));
+      g0 = p0 * (d0 - v0);
+      g1 = p1 * (d1 - v1);
+    } else {
+      float y0, y1;
+      gelu_tanh_alu2(s0, s1, gA2, gC2, y0, y1);  // gelu(x) / scale
+      p0 = y0 * sl * inv_l;
+      p1 = y1 * sl * inv_l;
+      gelu_tanh_grad_alu2(s0, s1, gA2, gC2, g0, g1);
+      g0 *= d0 * inv_l;
+      g1 *= d1 * inv_l;
+    }
+    const bool ok0 = row_ok && c0 + c < nvalid, ok1 = row_ok && c0 + c + 1 < nvalid;
+    pk_p[u] = ptx::pack_bf16x2(ok0 ? p0 : 0.0f, ok1 ? p1 : 0.0f);
+    pk_ds[u] = ptx::pack_bf16x2(ok0 ? g0 : 0.0f, ok1 ? g1 : 0.0f);
+  }
+}
+
+// Stores one 128 x D fp32 accumulator row (times `mul`) as bf16 to dst.
+template <int D>
+__device__ __forceinline__ void bwd_store_row(uint32_t taddr, float mul, __nv_bfloat16* dst, bool store, bool v8) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(taddr + 32 * c, r);
+    ptx::tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (store) store_row32(dst + 32 * c, pk, v8);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void zero_row(__nv_bfloat16* dst) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ------------------------------------------------------------------ kernels
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+  BwdBars& B = *reinterpret_cast<BwdBars*>(sm + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdItem t = bwd_item(p);
+  const int rows = min(128, t.Lq - t.row0);
+  const int n_kv = (t.Lkv + 127) >> 7;
+  if (n_kv == 0) {  // no keys: no gradient reaches these queries
+    if (warp >= 2) {
+      const int row = ((warp & 3) << 5) + lane;
+      if (row < rows) zero_row<D>(p.dq + (static_cast<size_t>(t.q_tok + t.row0 + row) * p.H + t.h) * D);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&B.res_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&B.st_full[s], 1);
+      ptx::mbar_init(&B.st_empty[s], 1);
+    }
+    ptx::mbar_init(&B.mma_full, 1);
+    ptx::mbar_init(&B.act_full, 128);
+    ptx::mbar_init(&B.acc_full, 1);
+    B.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&B.tmem_slot, C::TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = B.tmem_slot;
+  volatile int* abort = &B.abort;
+  if (warp == 0) {
+    if (lane == 0)
+      bwd_producer<D>(p, sm, B, t.h, &p.tm_q, &p.tm_do, t.q_tok + t.row0, &p.tm_k, &p.tm_v, t.kv_tok, n_kv);
+  } else if (warp == 1) {
+    bwd_mma<D, false>(p, sm, B, tmem, n_kv, t.Lkv);
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool row_ok = row < rows;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const size_t ri = static_cast<size_t>(t.q_tok + t.row0 + row) * p.H + t.h;
+    float lse2 = 0.0f, dvr = 0.0f;
+    if (ACT == kActSoftmax && row_ok) {
+      lse2 = __ldg(p.lse2 + ri);
+      dvr = __ldg(p.dvec + ri);
+    }
+    uint64_t gA2 = 0, gC2 = 0;
+    if (ACT == kActGelu) gelu_scale_consts(p.score_scale, gA2, gC2);
+    const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
+    bool ok = true;
+    for (int g = 0; g < n_kv && ok; ++g) {
+      ok = ptx::mbar_wait(&B.mma_full, g & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int ncols = min(128, t.Lkv - 128 * g);
+      const int nch = (ncols + 31) >> 5;
+      for (int ch = 0; ch < nch; ++ch) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tmem + lane_off + C::TM_S + 32 * ch, sr);
+        ptx::tmem_ld32(tmem + lane_off + C::TM_P + 32 * ch, dr);
+        ptx::tmem_wait_ld();
+        uint32_t pk_p[16], pk_ds[16];
+        bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, ncols, row_ok, p.score_scale, inv_l,
+                              gA2, gC2, pk_p, pk_ds);
+        ptx::tmem_st16(tmem + lane_off + C::TM_S + 16 * ch, pk_ds);  // dS over consumed S columns
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.act_full);
+    }
+    if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      ptx::tc_fence_after();
+      bwd_store_row<D>(tmem + lane_off + C::TM_A1, p.scale, p.dq + ri * D, row_ok, p.align32 != 0);
+    } else if (lane == 0) {
+      bwd_failure(p, abort, kStatusActivation);
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+  BwdBars& B = *reinterpret_cast<BwdBars*>(sm + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdItem t = bwd_item(p);
+  const int keys = min(128, t.Lkv - t.row0);
+  const int n_q = (t.Lq + 127) >> 7;
+  if (n_q == 0) {  // no queries: these keys receive no gradient
+    if (warp >= 2) {
+      const int row = ((warp & 3) << 5) + lane;
+      if (row < keys) {
+        const size_t ri = static_cast<size_t>(t.kv_tok + t.row0 + row) * p.H + t.h;
+        zero_row<D>(p.dk + ri * D);
+        zero_row<D>(p.dv + ri * D);
+      }
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&B.res_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&B.st_full[s], 1);
+      ptx::mbar_init(&B.st_empty[s], 1);
+    }
+    ptx::mbar_init(&B.mma_full, 1);
+    ptx::mbar_init(&B.act_full, 128);
+    ptx::mbar_init(&B.acc_full, 1);
+    for (int s = 0; s < 2; ++s) ptx::mbar_init(&B.vec_full[s], 128);
+    B.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&B.tmem_slot, C::TM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = B.tmem_slot;
+  volatile int* abort = &B.abort;
+  if (warp == 0) {
+    if (lane == 0)
+      bwd_producer<D>(p, sm, B, t.h, &p.tm_k, &p.tm_v, t.kv_tok + t.row0, &p.tm_q, &p.tm_do, t.q_tok, n_q);
+  } else if (warp == 1) {
+    bwd_mma<D, true>(p, sm, B, tmem, n_q, t.Lq);
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row of the item
+    const int tid = (warp - 2) * 32 + lane;  // 0..127 over the four warps
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC);  // [2 buffers][lse2, Dv][128]
+    uint64_t gA2 = 0, gC2 = 0;
+    if (ACT == kActGelu) gelu_scale_consts(p.score_scale, gA2, gC2);
+    const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
+    bool ok = true;
+    for (int u = 0; u < n_q && ok; ++u) {
+      const int nq = min(128, t.Lq - 128 * u);
+      float* vb = vec + (u & 1) * 256;
+      if (ACT == kActSoftmax) {
+        // lse2 and Dv of the tile's queries, one per thread.  The buffer of
+        // tile u - 2 is free: this thread waited for every thread's arrival
+        // at tile u - 1, which each made after finishing tile u - 2.
+        float l = 0.0f, d = 0.0f;
+        if (tid < nq) {
+          const size_t qi = static_cast<size_t>(t.q_tok + 128 * u + tid) * p.H + t.h;
+          l = __ldg(p.lse2 + qi);
+          d = __ldg(p.dvec + qi);
+        }
+        vb[tid] = l;
+        vb[128 + tid] = d;
+        ptx::mbar_arrive(&B.vec_full[u & 1]);
+        ok = ptx::mbar_wait(&B.vec_full[u & 1], (u >> 1) & 1, p.timeout_ns, abort);
+      }
+      if (ok) ok = ptx::mbar_wait(&B.mma_full, u & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int nch = (nq + 31) >> 5;
+      for (int ch = 0; ch < nch; ++ch) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(tmem + lane_off + C::TM_S + 32 * ch, sr);
+        ptx::tmem_ld32(tmem + lane_off + C::TM_P + 32 * ch, dr);
+        ptx::tmem_wait_ld();
+        uint32_t pk_p[16], pk_ds[16];
+        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + 128 + 32 * ch, 0.0f, 0.0f, 32 * ch, nq, true,
+                             p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
+        ptx::tmem_st16(tmem + lane_off + C::TM_S + 16 * ch, pk_p);   // P^T over consumed S^T columns
+        ptx::tmem_st16(tmem + lane_off + C::TM_P + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.act_full);
+    }
+    if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      ptx::tc_fence_after();
+      const size_t ri = static_cast<size_t>(t.kv_tok + t.row0 + row) * p.H + t.h;
+      const bool store = row < keys;
+      bwd_store_row<D>(tmem + lane_off + C::TM_A1, 1.0f, p.dv + ri * D, store, p.align32 != 0);
+      bwd_store_row<D>(tmem + lane_off + C::TM_A2, p.scale, p.dk + ri * D, store, p.align32 != 0);
+    } else if (lane == 0) {
+      bwd_failure(p, abort, kStatusActivation);
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// Dv_i = <dO_i, O_i> and lse2_i = lse_i log2(e), one warp per (token, head) row.
+template <int D>
+__global__ void __launch_bounds__(256) gdpa_bwd_prep_kernel(const __nv_bfloat16* out, const __nv_bfloat16* dout,
+                                                            const float* lse, float* lse2, float* dvec,
+                                                            int64_t rows) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  constexpr int PER = D / 32;  // bf16 values per lane (2 or 4)
+  const __nv_bfloat16* o = out + r * D + lane * PER;
+  const __nv_bfloat16* d = dout + r * D + lane * PER;
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + i);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(d + i);
+    acc = fmaf(__low2float(a), __low2float(b), acc);
+    acc = fmaf(__high2float(a), __high2float(b), acc);
+  }
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (lane == 0) {
+    dvec[r] = acc;
+    lse2[r] = lse[r] * 1.4426950408889634f;
+  }
+}
+
+}  // namespace gdpa

@@ -26,6 +26,7 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   int window_blocks;
   float score_scale;         // softmax: scale * log2(e); GELU: scale
   int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
+  float* lse;                // optional [Tq, H]: softmax row logsumexp (natural log) for the backward
 };
 
 enum : int { kActSoftmax = 0, kActGelu = 1 };
@@ -47,6 +48,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 #pragma unroll
     for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
   }
+}
+
+// Natural-log row logsumexp from the log2-domain running max m and sum l
+// (sum_j 2^(x_j - m) = l): ln 2 (m + log2 l); -inf for an empty row.
+__device__ __forceinline__ float row_lse(float m, float l) {
+  return l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
 }
 
 __device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {

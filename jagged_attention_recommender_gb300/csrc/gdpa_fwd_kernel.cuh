@@ -611,6 +611,8 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
       l_buf[ob * 128 + row] = l_run;
       if (KS) m_buf[ob * 128 + row] = m_run;
       ptx::mbar_arrive(&B.l_full[ob]);
+      if (!KS && p.lse && row < t.q_rows)
+        p.lse[static_cast<size_t>(t.q_tok + row) * p.H + t.h] = row_lse(m_run, l_run);
     }
     ++qi;
   }
@@ -652,6 +654,8 @@ __device__ __forceinline__ bool epilogue_key_split(const FwdParams& p, FwdBars<D
       if (k == quarter) own = e;
     }
     w = den > 0.0f ? own / den : 0.0f;
+    if (quarter == 0 && p.lse && lane < t.q_rows)  // sum_j 2^(x_j - M) = den
+      p.lse[static_cast<size_t>(t.q_tok + lane) * p.H + t.h] = row_lse(M, den);
   } else {
     w = p.score_scale / static_cast<float>(t.Lkv);  // the GELU's folded scale, then 1/Lkv
   }
@@ -733,6 +737,7 @@ __device__ void run_epilogue(const FwdParams& p, FwdBars<D, MODE>& B, const floa
     if (t.n_kv == 0) {  // no keys: the output rows are zero
       if (KS ? (quarter == 0 && lane < t.q_rows) : row < t.q_rows) {
         if (KS) orow = p.out + (static_cast<size_t>(t.q_tok + lane) * H + t.h) * D;
+        if (ACT == kActSoftmax && p.lse) p.lse[static_cast<size_t>(t.q_tok + (KS ? lane : row)) * H + t.h] = -INFINITY;
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);

@@ -339,6 +339,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: zero output rows
       if (row < rows) {
+        if (ACT == kActSoftmax && p.lse) p.lse[static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h] = -INFINITY;
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -559,6 +560,8 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     if (!ok) break;
     ptx::tc_fence_after();
     const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : inv_lkv;
+    if (ACT == kActSoftmax && p.lse && row < rows)
+      p.lse[static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h] = row_lse(m_run, l_run);
     if (rows_live) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -75,10 +75,37 @@ struct LaunchArgs {
   int H, D, act, window_blocks;
   float scale;
   void* stream;
+  float* lse = nullptr;   // optional: softmax row logsumexp [Tq, H]
+};
+
+// Backward launch: work lists of int4 {sequence, head, first row, 0} on the
+// device (dq: 128-row query tiles; dkdv: 128-key tiles), scratch [Tq, H]
+// fp32 x 2 (log2-domain lse, then Dv).
+struct BwdLaunchArgs {
+  const void *q, *k, *v, *out, *dout;
+  const float* lse;
+  const int32_t* q_off;   // device
+  const int32_t* kv_off;  // device
+  const void* dq_items;
+  int64_t n_dq;
+  const void* kv_items;
+  int64_t n_kv;
+  float* scratch;
+  void *dq, *dk, *dv;
+  int64_t Tq, Tkv;
+  int H, D, act;
+  float scale;
+  void* stream;
 };
 
 // Defined in gdpa_kernels.cu.
 gdpa_status_t launch_forward(const LaunchArgs& a);
+// Defined in gdpa_bwd.cu.
+gdpa_status_t launch_backward(const BwdLaunchArgs& a);
+// Backward work lists (host): query tiles ordered by their key count, key
+// tiles by their query count, longest first.
+void plan_backward(const int32_t* q_off, const int32_t* kv_off, int B, int H, std::vector<int32_t>& dq_items,
+                   std::vector<int32_t>& kv_items);
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
 gdpa_status_t read_and_clear_device_status(void* stream);
 gdpa_status_t launch_wait_selftest(int timeout_ms, void* stream);

@@ -178,6 +178,13 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
 
 }  // namespace
 
+// Shared with the backward launcher (gdpa_bwd.cu).
+gdpa_status_t encode_rows_2d(CUtensorMap* m, const void* base, int64_t rows, int H, int D, int box_rows) {
+  return encode_rows(m, base, rows, H, D, box_rows);
+}
+int* device_status_word(int device) { return status_ptr(device); }
+unsigned long long bounded_wait_ns() { return wait_timeout_ns(); }
+
 gdpa_status_t launch_wait_selftest(int timeout_ms, void* stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GDPA_ERR_CUDA;
@@ -218,6 +225,7 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.window_blocks = a.window_blocks;
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
   prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
+  prm.lse = a.lse;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks > 0;
   if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {

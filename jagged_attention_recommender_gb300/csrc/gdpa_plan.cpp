@@ -221,3 +221,34 @@ extern "C" gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const i
   if (cost && !c.empty()) std::memcpy(cost, c.data(), c.size() * sizeof(int64_t));
   return GDPA_OK;
 }
+
+namespace gdpa {
+
+// Backward work lists: every 128-row query tile (dq) and every 128-key tile
+// (dk/dv) of every (sequence, head), as {sequence, head, first row, 0}.  A
+// query tile's work grows with its sequence's key count and a key tile's with
+// its query count, so each list is ordered longest first (the GPU hands the
+// next CTA slot to the next item in order, a greedy longest-first schedule).
+void plan_backward(const int32_t* q_off, const int32_t* kv_off, int B, int H, std::vector<int32_t>& dq_items,
+                   std::vector<int32_t>& kv_items) {
+  std::vector<int> by_keys(B), by_queries(B);
+  for (int b = 0; b < B; ++b) by_keys[b] = by_queries[b] = b;
+  std::stable_sort(by_keys.begin(), by_keys.end(),
+                   [&](int a, int b) { return kv_off[a + 1] - kv_off[a] > kv_off[b + 1] - kv_off[b]; });
+  std::stable_sort(by_queries.begin(), by_queries.end(),
+                   [&](int a, int b) { return q_off[a + 1] - q_off[a] > q_off[b + 1] - q_off[b]; });
+  dq_items.clear();
+  kv_items.clear();
+  for (int b : by_keys) {
+    const int Lq = q_off[b + 1] - q_off[b];
+    for (int h = 0; h < H; ++h)
+      for (int q0 = 0; q0 < Lq; q0 += kBlockM) dq_items.insert(dq_items.end(), {b, h, q0, 0});
+  }
+  for (int b : by_queries) {
+    const int Lkv = kv_off[b + 1] - kv_off[b];
+    for (int h = 0; h < H; ++h)
+      for (int k0 = 0; k0 < Lkv; k0 += kBlockN) kv_items.insert(kv_items.end(), {b, h, k0, 0});
+  }
+}
+
+}  // namespace gdpa

@@ -75,6 +75,49 @@ __device__ __forceinline__ void gelu_tanh_alu2(float s0, float s1, uint64_t A2, 
   ptx::f2_unpack(ptx::f2_mul(s, ptx::f2_mul(inv, sel)), y0, y1);
 }
 
+// Derivative for the backward: with x = scale * s and z = s (A + C s^2),
+// gelu'(x) = sigma(z) + sigma(z) sigma(-z) s (A + 3 C s^2), where
+// sigma(z) sigma(-z) = e^-a sigma(a)^2 (a = |z|) is formed without the
+// cancellation of sigma(1 - sigma).  Same evaluation of e^-a and sigma(a)
+// as gelu_tanh_alu2; returns gelu'(x) for each lane.
+__device__ __forceinline__ void gelu_tanh_grad_alu2(float s0, float s1, uint64_t A2, uint64_t C2, float& g0, float& g1) {
+  const uint64_t s = ptx::f2_pack(s0, s1);
+  const uint64_t ss = ptx::f2_mul(s, s);
+  const uint64_t z = ptx::f2_mul(s, ptx::f2_fma(C2, ss, A2));
+  float z0, z1;
+  ptx::f2_unpack(z, z0, z1);
+  const uint64_t a = ptx::f2_pack(fminf(fabsf(z0), 18.0f), fminf(fabsf(z1), 18.0f));
+  const uint64_t magic = ptx::f2_splat(12582912.0f);  // 1.5 * 2^23: round to nearest integer
+  const uint64_t t = ptx::f2_fma(a, ptx::f2_splat(1.4426950408889634f), magic);
+  const uint64_t kf = ptx::f2_sub(t, magic);
+  uint64_t r = ptx::f2_fma(kf, ptx::f2_splat(-0.693145751953125f), a);
+  r = ptx::f2_fma(kf, ptx::f2_splat(-1.4286068203094173e-06f), r);
+  uint64_t p = ptx::f2_fma(ptx::f2_splat(1.0f / 720.0f), r, ptx::f2_splat(-1.0f / 120.0f));
+  p = ptx::f2_fma(p, r, ptx::f2_splat(1.0f / 24.0f));
+  p = ptx::f2_fma(p, r, ptx::f2_splat(-1.0f / 6.0f));
+  p = ptx::f2_fma(p, r, ptx::f2_splat(0.5f));
+  p = ptx::f2_fma(p, r, ptx::f2_splat(-1.0f));
+  p = ptx::f2_fma(p, r, ptx::f2_splat(1.0f));
+  float t0, t1;
+  ptx::f2_unpack(t, t0, t1);
+  const int k0 = __float_as_int(t0) - 0x4B400000, k1 = __float_as_int(t1) - 0x4B400000;
+  const uint64_t e = ptx::f2_mul(ptx::f2_pack(__int_as_float((127 - k0) << 23), __int_as_float((127 - k1) << 23)), p);
+  const uint64_t nd = ptx::f2_fma(e, ptx::f2_splat(-1.0f), ptx::f2_splat(-1.0f));
+  uint64_t inv = ptx::f2_fma(ptx::f2_fma(ptx::f2_splat(0.3232244551181793f), nd, ptx::f2_splat(1.4545105695724487f)), nd,
+                             ptx::f2_splat(2.1211774349212646f));
+  const uint64_t one = ptx::f2_splat(1.0f);
+  uint64_t err = ptx::f2_fma(nd, inv, one);
+  inv = ptx::f2_fma(inv, err, inv);
+  err = ptx::f2_fma(nd, inv, one);
+  inv = ptx::f2_fma(inv, err, inv);
+  float e0, e1;
+  ptx::f2_unpack(e, e0, e1);
+  const uint64_t sig = ptx::f2_mul(inv, ptx::f2_pack(z0 >= 0.0f ? 1.0f : e0, z1 >= 0.0f ? 1.0f : e1));
+  const uint64_t sig2 = ptx::f2_mul(e, ptx::f2_mul(inv, inv));                       // sigma(z) sigma(-z)
+  const uint64_t dz = ptx::f2_mul(s, ptx::f2_fma(ptx::f2_mul(C2, ptx::f2_splat(3.0f)), ss, A2));  // s (A + 3 C s^2)
+  ptx::f2_unpack(ptx::f2_fma(sig2, dz, sig), g0, g1);
+}
+
 // The folded-scale constants A and C of gelu_tanh_alu2, both lanes.
 __device__ __forceinline__ void gelu_scale_consts(float scale, uint64_t& A2, uint64_t& C2) {
   const float A = 1.5957691216057308f * scale;  // 2 sqrt(2/pi) scale
