@@ -12,6 +12,11 @@ Prints one JSON line (rank 0).  ``value`` is useful TFLOPS: 4*D*H per
 unmasked (query, key) pair, summed over all ranks, over the max-over-ranks
 time.  ``--impl reference`` times the fp64 CPU oracle instead (the slow
 baseline arm) on a bounded sample of the same workload.
+
+``--pass backward`` times the training backward instead (``gdpa_bwd``: dq,
+dk, dv from the forward's output and row logsumexp, which are computed once
+before the timed region); its useful FLOPs are the five products of the
+backward, 10*D*H per unmasked pair (2.5 times the forward's).
 """
 from __future__ import annotations
 
@@ -36,6 +41,7 @@ from jagged_attention_recommender_gb300.metrics import algorithmic_bytes, useful
 from jagged_attention_recommender_gb300.workloads import WORKLOADS, make_batch  # noqa: E402
 
 METRIC = "jagged GDPA fwd useful TFLOPS (unpadded) & % of GB300 roofline, 1 GPU"
+METRIC_BWD = "jagged GDPA bwd useful TFLOPS (unpadded, 10*D*H per pair) & % of GB300 roofline, 1 GPU"
 DEFAULT_WORKLOAD = "self_long"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -59,6 +65,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
     return ap.parse_args()
 
 
@@ -392,11 +399,161 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def backward_bytes(batch) -> float:
+    """Read Q, K, V, O, dO once, write dq, dk, dv once (bf16), plus the fp32 lse."""
+    Tq, Tkv = int(batch.q_offsets[-1]), int(batch.kv_offsets[-1])
+    return 2.0 * batch.H * batch.D * (4 * Tq + 4 * Tkv) + 4.0 * batch.H * Tq
+
+
+def run_backward(args, rank, world, local):
+    import torch
+
+    from jagged_attention_recommender_gb300 import build as gbuild
+    from jagged_attention_recommender_gb300 import gdpa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    gbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = WORKLOADS[args.workload]
+    if w.window_blocks > 0:
+        raise SystemExit("the backward covers full attention only")
+    batch = make_batch(args.workload, seed=w.seed + 1000 * rank)
+    flops = 2.5 * useful_flops(batch)
+    nbytes = backward_bytes(batch)
+    H, D, B = w.H, w.D, batch.B
+    Tq, Tkv = int(batch.q_offsets[-1]), int(batch.kv_offsets[-1])
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v = dev(batch.q), dev(batch.k), dev(batch.v)
+    g = torch.Generator(device="cuda").manual_seed(w.seed + 17)
+    dout = torch.randn((Tq, H, D), device="cuda", generator=g).to(torch.bfloat16)
+    qo = torch.from_numpy(batch.q_offsets).cuda()
+    ko = torch.from_numpy(batch.kv_offsets).cuda()
+    out = torch.empty((Tq, H, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Tq, H), dtype=torch.float32, device="cuda")
+    dq = torch.empty_like(out)
+    dk = torch.empty((Tkv, H, D), dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty_like(dk)
+    h_qo, h_ko = batch.q_offsets, batch.kv_offsets
+    stream = torch.cuda.current_stream()
+    gdpa.gdpa_fwd_lse(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, 0, w.scale, out, lse, stream)
+
+    def step():
+        gdpa.gdpa_bwd(q, k, v, out, dout, lse, h_qo, h_ko, qo, ko, B, H, D, w.act, 0, w.scale, dq, dk, dv, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = gdpa.gdpa_device_status()
+    if st != gdpa.GDPA_OK:
+        raise SystemExit("device status after warm-up: " + gdpa.gdpa_status_string(st))
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    st = gdpa.gdpa_device_status()
+    if st != gdpa.GDPA_OK:
+        raise SystemExit("device status after timing: " + gdpa.gdpa_status_string(st))
+    elapsed_ms = e0.elapsed_time(e1)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if dist:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    value = flops * world * K / (elapsed_ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    bound = BOUND[args.workload]
+    if bound == "tensor":
+        achieved, peak, unit = flops / (launch_ms / 1e3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = nbytes / (launch_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": None, "peak_source": peak_src + (" (burst)" if bound == "tensor" else ""),
+                "launch_ms": launch_ms, "useful_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+                "kernel": "gdpa_bwd step (prep + dq + dkdv kernels)"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        rng = np.random.default_rng(2024)
+        order = [int(s_) for s_ in rng.permutation(B)]
+        do_bits = dout.view(torch.int16).cpu().numpy().view(np.uint16)
+
+        def dout_of(seqs):
+            return np.concatenate([do_bits[batch.q_offsets[s_]:batch.q_offsets[s_ + 1]] for s_ in seqs])
+
+        # calibrate on one sequence (at most H threads busy), then time one
+        # call over a sample sized for about --cpu-seconds on every core
+        probe = batch.subset(order[:1])
+        t0 = time.perf_counter()
+        oracle.gdpa_bwd_batch(probe, dout_of(order[:1]))
+        rate = useful_flops(probe) / max(time.perf_counter() - t0, 1e-3)
+        rate *= max(1.0, min(oracle.num_cpus(), 4 * H) / H)
+        seqs, acc = [], 0.0
+        for s_ in order:
+            seqs.append(s_)
+            acc += useful_flops(batch.subset([s_]))
+            if acc >= rate * args.cpu_seconds:
+                break
+        sub = batch.subset(seqs)
+        t0 = time.perf_counter()
+        oracle.gdpa_bwd_batch(sub, dout_of(seqs))
+        spent = time.perf_counter() - t0
+        cpu = {"value": 2.5 * useful_flops(sub) / spent / 1e12, "unit": "TFLOPS", "cores": oracle.num_cpus(),
+               "kind": "oracle", "sample": "%d of %d sequences (seeded), all %d heads, %.1f s" % (
+                   len(seqs), B, H, spent)}
+    if rank == 0:
+        line = {
+            "metric": METRIC_BWD, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
+                       "pass": "backward", "global_batch": B * world, "tokens_q": Tq, "tokens_kv": Tkv,
+                       "l2": "inputs %.2f GB > 126 MB L2; no flush" % (
+                           (q.numel() + k.numel() + v.numel() + out.numel() + dout.numel()) * 2 / 1e9),
+                       "parallelism": "dp%d (independent batches, no collective)" % world,
+                       "entry": "gdpa_bwd (host work lists + upload + 3 kernels per step)"},
+            "clocks": clocks,
+            "e2e": None,
+            "gpu_launches": 3 * K,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.pass_ == "backward":
+        return run_backward(args, rank, world, local)
     return run_ours(args, rank, world, local)
 
 

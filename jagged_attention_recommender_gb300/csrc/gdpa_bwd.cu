@@ -72,10 +72,12 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a) {
   const void* vb = a.Tkv > 0 ? a.v : a.q;
   const int64_t qr = a.Tq > 0 ? a.Tq : a.Tkv, kr = a.Tkv > 0 ? a.Tkv : a.Tq;
   gdpa_status_t st;
-  if ((st = encode_rows_2d(&prm.tm_q, qb, qr, a.H, a.D, 128)) != GDPA_OK) return st;
-  if ((st = encode_rows_2d(&prm.tm_do, dob, qr, a.H, a.D, 128)) != GDPA_OK) return st;
-  if ((st = encode_rows_2d(&prm.tm_k, kb, kr, a.H, a.D, 128)) != GDPA_OK) return st;
-  if ((st = encode_rows_2d(&prm.tm_v, vb, kr, a.H, a.D, 128)) != GDPA_OK) return st;
+  // boxes of 64 rows: a streamed tile is one box, a resident 128-row tile two
+  constexpr int box = BwdCfg<128>::BN;
+  if ((st = encode_rows_2d(&prm.tm_q, qb, qr, a.H, a.D, box)) != GDPA_OK) return st;
+  if ((st = encode_rows_2d(&prm.tm_do, dob, qr, a.H, a.D, box)) != GDPA_OK) return st;
+  if ((st = encode_rows_2d(&prm.tm_k, kb, kr, a.H, a.D, box)) != GDPA_OK) return st;
+  if ((st = encode_rows_2d(&prm.tm_v, vb, kr, a.H, a.D, box)) != GDPA_OK) return st;
   prm.q_off = a.q_off;
   prm.kv_off = a.kv_off;
   prm.lse2 = a.scratch;

@@ -13,20 +13,26 @@
 // heads.)  Two kernels, one CTA per work item, each output written once:
 //
 //   gdpa_bwd_dq_kernel    item = 128 query rows of one (sequence, head); it
-//     walks the sequence's 128-key K/V tiles: S = Q K^T and dP = dO V^T into
+//     walks the sequence's 64-key K/V tiles: S = Q K^T and dP = dO V^T into
 //     tensor memory, the activation warps turn them into dS (bf16, written
 //     over S), then dQ += dS K with dS read straight from tensor memory.
 //   gdpa_bwd_dkdv_kernel  item = 128 keys of one (sequence, head); it walks
-//     the sequence's 128-row query tiles: S^T = K Q^T and dP^T = V dO^T, the
+//     the sequence's 64-row query tiles: S^T = K Q^T and dP^T = V dO^T, the
 //     activation warps write P^T over S^T and dS^T over dP^T, then
 //     dV += P^T dO and dK += dS^T Q.
+//
+// S and dP are double-buffered in tensor memory and the MMA issuer runs one
+// tile ahead: it issues S, dP of tile t+1 before the accumulating MMAs of
+// tile t, so the tensor core works while the activation warps turn tile t's
+// scores into P and dS.
 //
 // Threads (192): warp 0 the TMA producer, warp 1 the MMA issuer (the whole
 // warp runs the loop, one elected lane issues), warps 2-5 the activation and
 // the epilogue (warp w owns tensor-memory lanes 32 (w mod 4) .. +31, one row
-// of S each).  Tensor memory (512 columns): S 0, dP 128, accumulators from
-// 256 (dQ; or dV then dK).  Shared memory (D = 128): the item's two resident
-// tiles (Q and dO, or K and V) and two stages of the two streamed ones.
+// each).  Tensor memory (512 columns): S0 0, dP0 64, S1 128, dP1 192,
+// accumulators from 256 (dQ; or dV then dK).  Shared memory (D = 128): the
+// item's two resident 128-row tiles (Q and dO, or K and V) and three stages
+// of the two streamed 64-row ones.
 // Rows past a sequence's end are masked to P = dS = 0 in the activation, so
 // whatever the TMA box brought in for them never reaches an accumulator.
 #pragma once
@@ -36,7 +42,7 @@
 namespace gdpa {
 
 struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
-  CUtensorMap tm_q;   // 2-D views [T, H*D] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_q;   // 2-D views [T, H*D] bf16, box 64 columns x 64 rows, 128-byte swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
@@ -59,18 +65,24 @@ struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
 template <int D>
 struct BwdCfg {
   static constexpr int KCH = D / 64;
-  static constexpr int CHUNK_BYTES = 128 * 128;        // 128 rows x 64 bf16 columns
-  static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;  // 128 rows x D
+  static constexpr int BN = 64;                         // rows of a streamed tile
+  static constexpr int NS = 3;                          // stages of the streamed tiles
+  static constexpr int RCHUNK = 128 * 128;              // resident: 128 rows x 64 bf16 columns
+  static constexpr int RTILE = KCH * RCHUNK;            // resident: 128 rows x D
+  static constexpr int SCHUNK = BN * 128;               // streamed: 64 rows x 64 bf16 columns
+  static constexpr int STILE = KCH * SCHUNK;            // streamed: 64 rows x D
   static constexpr int OFF_R1 = 0;                      // resident: Q (dq) or K (dkdv)
-  static constexpr int OFF_R2 = OFF_R1 + TILE_BYTES;    // resident: dO (dq) or V (dkdv)
-  static constexpr int OFF_S1 = OFF_R2 + TILE_BYTES;    // streamed, 2 stages: K (dq) or Q (dkdv)
-  static constexpr int OFF_S2 = OFF_S1 + 2 * TILE_BYTES;  // streamed, 2 stages: V (dq) or dO (dkdv)
-  static constexpr int OFF_VEC = OFF_S2 + 2 * TILE_BYTES;  // dkdv: lse2 and Dv of a query tile, 2 buffers
-  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * 128 * 4;
+  static constexpr int OFF_R2 = OFF_R1 + RTILE;         // resident: dO (dq) or V (dkdv)
+  static constexpr int OFF_S1 = OFF_R2 + RTILE;         // streamed stages: K (dq) or Q (dkdv)
+  static constexpr int OFF_S2 = OFF_S1 + NS * STILE;    // streamed stages: V (dq) or dO (dkdv)
+  static constexpr int OFF_VEC = OFF_S2 + NS * STILE;   // dkdv: lse2 and Dv of a query tile, 2 buffers
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
   static constexpr int BAR_BYTES = 256;
   // at least 117 KB so that one CTA fits per SM (each allocates 512 TMEM columns)
   static constexpr int SMEM_BYTES = (OFF_BAR + BAR_BYTES + 1024) > 119808 ? (OFF_BAR + BAR_BYTES + 1024) : 119808;
-  static constexpr uint32_t TM_S = 0, TM_P = 128, TM_A1 = 256, TM_A2 = 256 + D;
+  __host__ __device__ static constexpr uint32_t tm_s(int b) { return 128u * b; }       // S (or S^T) buffers
+  __host__ __device__ static constexpr uint32_t tm_p(int b) { return 128u * b + 64u; } // dP (or dP^T) buffers
+  static constexpr uint32_t TM_A1 = 256, TM_A2 = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int THREADS = 192;
   static_assert(256 + 2 * D <= TM_COLS, "TMEM budget");
@@ -79,9 +91,9 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t res_full;                 // the item's resident tiles landed
-  uint64_t st_full[2], st_empty[2];  // streamed stages
-  uint64_t mma_full;                 // S and dP of the current tile are in TMEM
-  uint64_t act_full;                 // P / dS of the current tile are in TMEM
+  uint64_t st_full[3], st_empty[3];  // streamed stages
+  uint64_t mma_full[2];              // S and dP of a tile are in TMEM buffer b
+  uint64_t act_full[2];              // P / dS of a tile are in TMEM buffer b
   uint64_t acc_full;                 // every MMA of the item completed
   uint64_t vec_full[2];              // dkdv: lse2 / Dv of a query tile staged by the activation warps
   uint32_t tmem_slot;
@@ -114,35 +126,40 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
 
 // ------------------------------------------------------------------ producer
 
-// Loads the two resident tiles at rows r_row (maps r1, r2), then n tiles of
-// the two streamed maps at rows s_row + 128 t into the two stages.
+// Loads the two resident 128-row tiles at rows r_row (maps r1, r2, boxes of
+// 64 rows), then n 64-row tiles of the two streamed maps at rows
+// s_row + 64 t into the stages.
 template <int D>
 __device__ void bwd_producer(const BwdParams& p, uint8_t* sm, BwdBars& B, int h, const CUtensorMap* r1,
                              const CUtensorMap* r2, int r_row, const CUtensorMap* s1, const CUtensorMap* s2,
                              int s_row, int n) {
   using C = BwdCfg<D>;
   volatile int* abort = &B.abort;
-  ptx::mbar_arrive_expect_tx(&B.res_full, 2 * C::TILE_BYTES);
+  ptx::mbar_arrive_expect_tx(&B.res_full, 2 * C::RTILE);
 #pragma unroll
-  for (int c = 0; c < C::KCH; ++c) {
-    ptx::tma_load_2d(sm + C::OFF_R1 + c * C::CHUNK_BYTES, r1, &B.res_full, h * D + 64 * c, r_row);
-    ptx::tma_load_2d(sm + C::OFF_R2 + c * C::CHUNK_BYTES, r2, &B.res_full, h * D + 64 * c, r_row);
-  }
-  int armed[2] = {-1, -1};
+  for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int off = c * C::RCHUNK + half * C::SCHUNK;  // rows 64 half .. +63 of the chunk
+      ptx::tma_load_2d(sm + C::OFF_R1 + off, r1, &B.res_full, h * D + 64 * c, r_row + 64 * half);
+      ptx::tma_load_2d(sm + C::OFF_R2 + off, r2, &B.res_full, h * D + 64 * c, r_row + 64 * half);
+    }
+  int armed[C::NS];
+  for (int s = 0; s < C::NS; ++s) armed[s] = -1;
   bool ok = true;
   for (int t = 0; t < n; ++t) {
-    const int s = t & 1;
-    const uint32_t ph = (t >> 1) & 1;
+    const int s = t % C::NS;
+    const uint32_t ph = (t / C::NS) & 1;
     ok = ptx::mbar_wait(&B.st_empty[s], ph ^ 1, p.timeout_ns, abort);
     if (!ok) break;
-    ptx::mbar_arrive_expect_tx(&B.st_full[s], 2 * C::TILE_BYTES);
+    ptx::mbar_arrive_expect_tx(&B.st_full[s], 2 * C::STILE);
     armed[s] = (int)ph;
 #pragma unroll
     for (int c = 0; c < C::KCH; ++c) {
-      ptx::tma_load_2d(sm + C::OFF_S1 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, s1, &B.st_full[s], h * D + 64 * c,
-                       s_row + 128 * t);
-      ptx::tma_load_2d(sm + C::OFF_S2 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, s2, &B.st_full[s], h * D + 64 * c,
-                       s_row + 128 * t);
+      ptx::tma_load_2d(sm + C::OFF_S1 + s * C::STILE + c * C::SCHUNK, s1, &B.st_full[s], h * D + 64 * c,
+                       s_row + C::BN * t);
+      ptx::tma_load_2d(sm + C::OFF_S2 + s * C::STILE + c * C::SCHUNK, s2, &B.st_full[s], h * D + 64 * c,
+                       s_row + C::BN * t);
     }
   }
   if (!ok) bwd_failure(p, abort, kStatusProducer);
@@ -150,18 +167,49 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* sm, BwdBars& B, int h,
   const int never = 0;
   const unsigned long long drain_ns = 100000000ull;
   ptx::mbar_wait(&B.res_full, 0, drain_ns, &never);
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < C::NS; ++s)
     if (armed[s] >= 0) ptx::mbar_wait(&B.st_full[s], (uint32_t)armed[s], drain_ns, &never);
 }
 
 // ------------------------------------------------------------------ MMA issuer (whole warp)
 
-// Per streamed tile t (n tiles; `len` rows in all, so the last tile may be
-// partial): S = R1 S1^T and dP = R2 S2^T with both operands K-major; then,
-// once the activation has written its bf16 operands over S and dP, the
+// S (or S^T) = R1 S1^T and dP (or dP^T) = R2 S2^T for streamed tile t into
+// TMEM buffer t & 1, both operands K-major; `len` rows in all, so the last
+// tile may be partial.
+template <int D>
+__device__ __forceinline__ bool bwd_issue_sdp(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int t,
+                                              int len, uint64_t r1, uint64_t r2, volatile int* abort) {
+  using C = BwdCfg<D>;
+  const int s = t % C::NS;
+  if (!ptx::mbar_wait(&B.st_full[s], (t / C::NS) & 1, p.timeout_ns, abort)) return false;
+  ptx::tc_fence_after();
+  const int n16 = (min(C::BN, len - C::BN * t) + 15) >> 4;
+  const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+  const uint64_t s1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_S1 + s * C::STILE), 16, 1024);
+  const uint64_t s2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_S2 + s * C::STILE), 16, 1024);
+  const int b = t & 1;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {  // K-dimension D, 16 per MMA
+    const uint32_t off_r = ((kk >> 2) * C::RCHUNK + (kk & 3) * 32) >> 4;
+    const uint32_t off_s = ((kk >> 2) * C::SCHUNK + (kk & 3) * 32) >> 4;
+    ptx::mma_ss_elect(tmem + C::tm_s(b), r1 + off_r, s1 + off_s, idesc, kk > 0 ? 1u : 0u);
+  }
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off_r = ((kk >> 2) * C::RCHUNK + (kk & 3) * 32) >> 4;
+    const uint32_t off_s = ((kk >> 2) * C::SCHUNK + (kk & 3) * 32) >> 4;
+    ptx::mma_ss_elect(tmem + C::tm_p(b), r2 + off_r, s2 + off_s, idesc, kk > 0 ? 1u : 0u);
+  }
+  ptx::mma_commit_elect(&B.mma_full[b]);
+  return true;
+}
+
+// Per streamed tile t: S, dP of tile t+1 first (look-ahead), then, once the
+// activation has written its bf16 operands over tile t's S and dP, the
 // accumulating MMAs with the operand from tensor memory and the streamed
 // tile read MN-major (16 rows per MMA): dQ += dS K, or dV += P^T dO and
-// dK += dS^T Q.
+// dK += dS^T Q.  S/dP of tile t+2 reuse tile t's buffer only after these
+// (the tensor core runs one thread's MMAs in order).
 template <int D, bool DKDV>
 __device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int n, int len) {
   using C = BwdCfg<D>;
@@ -171,47 +219,35 @@ __device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tm
   const uint64_t r1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R1), 16, 1024);
   const uint64_t r2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R2), 16, 1024);
   constexpr uint32_t idesc_acc = ptx::idesc_bf16(128, D, 1);
+  if (ok && n > 0) ok = bwd_issue_sdp<D>(p, sm, B, tmem, 0, len, r1, r2, abort);
   for (int t = 0; t < n && ok; ++t) {
-    const int s = t & 1;
-    ok = ptx::mbar_wait(&B.st_full[s], (t >> 1) & 1, p.timeout_ns, abort);
+    if (t + 1 < n) {
+      ok = bwd_issue_sdp<D>(p, sm, B, tmem, t + 1, len, r1, r2, abort);
+      if (!ok) break;
+    }
+    const int b = t & 1, s = t % C::NS;
+    ok = ptx::mbar_wait(&B.act_full[b], (t >> 1) & 1, p.timeout_ns, abort);
     if (!ok) break;
     ptx::tc_fence_after();
-    const int cols = min(128, len - 128 * t);
-    const int n16 = (cols + 15) >> 4;
-    const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
-    const uint32_t s1_addr = ptx::smem_u32(sm + C::OFF_S1 + s * C::TILE_BYTES);
-    const uint32_t s2_addr = ptx::smem_u32(sm + C::OFF_S2 + s * C::TILE_BYTES);
-    const uint64_t s1 = ptx::sdesc_sw128(s1_addr, 16, 1024), s2 = ptx::sdesc_sw128(s2_addr, 16, 1024);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {  // S (or S^T): K-dimension D, 16 per MMA
-      const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-      ptx::mma_ss_elect(tmem + C::TM_S, r1 + off, s1 + off, idesc, kk > 0 ? 1u : 0u);
-    }
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {  // dP (or dP^T)
-      const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-      ptx::mma_ss_elect(tmem + C::TM_P, r2 + off, s2 + off, idesc, kk > 0 ? 1u : 0u);
-    }
-    ptx::mma_commit_elect(&B.mma_full);
-    ok = ptx::mbar_wait(&B.act_full, t & 1, p.timeout_ns, abort);
-    if (!ok) break;
-    ptx::tc_fence_after();
+    const int n16 = (min(C::BN, len - C::BN * t) + 15) >> 4;
+    const uint32_t s1_addr = ptx::smem_u32(sm + C::OFF_S1 + s * C::STILE);
+    const uint32_t s2_addr = ptx::smem_u32(sm + C::OFF_S2 + s * C::STILE);
     if (DKDV) {
       // dV += P^T dO and dK += dS^T Q: B operands are the streamed dO and Q
       // tiles, MN-major, 16 query rows (2048 bytes) per MMA
-      const uint64_t x1 = ptx::sdesc_sw128(s2_addr, C::CHUNK_BYTES, 1024);
-      const uint64_t x2 = ptx::sdesc_sw128(s1_addr, C::CHUNK_BYTES, 1024);
+      const uint64_t x1 = ptx::sdesc_sw128(s2_addr, C::SCHUNK, 1024);
+      const uint64_t x2 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
       for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::TM_S + 8 * kk, x1 + 128u * kk, idesc_acc,
+        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
                           (t > 0 || kk > 0) ? 1u : 0u);
       for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A2, tmem + C::TM_P + 8 * kk, x2 + 128u * kk, idesc_acc,
+        ptx::mma_ts_elect(tmem + C::TM_A2, tmem + C::tm_p(b) + 8 * kk, x2 + 128u * kk, idesc_acc,
                           (t > 0 || kk > 0) ? 1u : 0u);
     } else {
       // dQ += dS K: B operand is the streamed K tile, MN-major, 16 keys per MMA
-      const uint64_t x1 = ptx::sdesc_sw128(s1_addr, C::CHUNK_BYTES, 1024);
+      const uint64_t x1 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
       for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::TM_S + 8 * kk, x1 + 128u * kk, idesc_acc,
+        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
                           (t > 0 || kk > 0) ? 1u : 0u);
     }
     ptx::mma_commit_elect(&B.st_empty[s]);  // the stage is free once these MMAs complete
@@ -301,7 +337,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdItem t = bwd_item(p);
   const int rows = min(128, t.Lq - t.row0);
-  const int n_kv = (t.Lkv + 127) >> 7;
+  const int n_kv = (t.Lkv + C::BN - 1) / C::BN;
   if (n_kv == 0) {  // no keys: no gradient reaches these queries
     if (warp >= 2) {
       const int row = ((warp & 3) << 5) + lane;
@@ -311,12 +347,14 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   }
   if (threadIdx.x == 0) {
     ptx::mbar_init(&B.res_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NS; ++s) {
       ptx::mbar_init(&B.st_full[s], 1);
       ptx::mbar_init(&B.st_empty[s], 1);
     }
-    ptx::mbar_init(&B.mma_full, 1);
-    ptx::mbar_init(&B.act_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&B.mma_full[b], 1);
+      ptx::mbar_init(&B.act_full[b], 128);
+    }
     ptx::mbar_init(&B.acc_full, 1);
     B.abort = 0;
     ptx::fence_mbar_init();
@@ -351,25 +389,26 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
     const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
     for (int g = 0; g < n_kv && ok; ++g) {
-      ok = ptx::mbar_wait(&B.mma_full, g & 1, p.timeout_ns, abort);
+      const int b = g & 1;
+      ok = ptx::mbar_wait(&B.mma_full[b], (g >> 1) & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int ncols = min(128, t.Lkv - 128 * g);
+      const int ncols = min(C::BN, t.Lkv - C::BN * g);
       const int nch = (ncols + 31) >> 5;
       for (int ch = 0; ch < nch; ++ch) {
         uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tmem + lane_off + C::TM_S + 32 * ch, sr);
-        ptx::tmem_ld32(tmem + lane_off + C::TM_P + 32 * ch, dr);
+        ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
+        ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
         ptx::tmem_wait_ld();
         uint32_t pk_p[16], pk_ds[16];
         bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, ncols, row_ok, p.score_scale, inv_l,
                               gA2, gC2, pk_p, pk_ds);
-        ptx::tmem_st16(tmem + lane_off + C::TM_S + 16 * ch, pk_ds);  // dS over consumed S columns
+        ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_ds);  // dS over consumed S columns
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&B.act_full);
+      ptx::mbar_arrive(&B.act_full[b]);
     }
     if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
     ok = __all_sync(0xffffffffu, ok);
@@ -397,7 +436,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdItem t = bwd_item(p);
   const int keys = min(128, t.Lkv - t.row0);
-  const int n_q = (t.Lq + 127) >> 7;
+  const int n_q = (t.Lq + C::BN - 1) / C::BN;
   if (n_q == 0) {  // no queries: these keys receive no gradient
     if (warp >= 2) {
       const int row = ((warp & 3) << 5) + lane;
@@ -411,12 +450,14 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
   }
   if (threadIdx.x == 0) {
     ptx::mbar_init(&B.res_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NS; ++s) {
       ptx::mbar_init(&B.st_full[s], 1);
       ptx::mbar_init(&B.st_empty[s], 1);
     }
-    ptx::mbar_init(&B.mma_full, 1);
-    ptx::mbar_init(&B.act_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&B.mma_full[b], 1);
+      ptx::mbar_init(&B.act_full[b], 128);
+    }
     ptx::mbar_init(&B.acc_full, 1);
     for (int s = 0; s < 2; ++s) ptx::mbar_init(&B.vec_full[s], 128);
     B.abort = 0;
@@ -441,48 +482,51 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
     const int row = quarter * 32 + lane;  // key row of the item
     const int tid = (warp - 2) * 32 + lane;  // 0..127 over the four warps
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC);  // [2 buffers][lse2, Dv][128]
+    float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC);  // [2 buffers][lse2, Dv][64]
     uint64_t gA2 = 0, gC2 = 0;
     if (ACT == kActGelu) gelu_scale_consts(p.score_scale, gA2, gC2);
     const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
     for (int u = 0; u < n_q && ok; ++u) {
-      const int nq = min(128, t.Lq - 128 * u);
-      float* vb = vec + (u & 1) * 256;
+      const int nq = min(C::BN, t.Lq - C::BN * u);
+      const int b = u & 1;
+      float* vb = vec + b * 2 * C::BN;
       if (ACT == kActSoftmax) {
         // lse2 and Dv of the tile's queries, one per thread.  The buffer of
         // tile u - 2 is free: this thread waited for every thread's arrival
         // at tile u - 1, which each made after finishing tile u - 2.
-        float l = 0.0f, d = 0.0f;
-        if (tid < nq) {
-          const size_t qi = static_cast<size_t>(t.q_tok + 128 * u + tid) * p.H + t.h;
-          l = __ldg(p.lse2 + qi);
-          d = __ldg(p.dvec + qi);
+        if (tid < C::BN) {
+          float l = 0.0f, d = 0.0f;
+          if (tid < nq) {
+            const size_t qi = static_cast<size_t>(t.q_tok + C::BN * u + tid) * p.H + t.h;
+            l = __ldg(p.lse2 + qi);
+            d = __ldg(p.dvec + qi);
+          }
+          vb[tid] = l;
+          vb[C::BN + tid] = d;
         }
-        vb[tid] = l;
-        vb[128 + tid] = d;
         ptx::mbar_arrive(&B.vec_full[u & 1]);
         ok = ptx::mbar_wait(&B.vec_full[u & 1], (u >> 1) & 1, p.timeout_ns, abort);
       }
-      if (ok) ok = ptx::mbar_wait(&B.mma_full, u & 1, p.timeout_ns, abort);
+      if (ok) ok = ptx::mbar_wait(&B.mma_full[b], (u >> 1) & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
       const int nch = (nq + 31) >> 5;
       for (int ch = 0; ch < nch; ++ch) {
         uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tmem + lane_off + C::TM_S + 32 * ch, sr);
-        ptx::tmem_ld32(tmem + lane_off + C::TM_P + 32 * ch, dr);
+        ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
+        ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
         ptx::tmem_wait_ld();
         uint32_t pk_p[16], pk_ds[16];
-        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + 128 + 32 * ch, 0.0f, 0.0f, 32 * ch, nq, true,
+        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, nq, true,
                              p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
-        ptx::tmem_st16(tmem + lane_off + C::TM_S + 16 * ch, pk_p);   // P^T over consumed S^T columns
-        ptx::tmem_st16(tmem + lane_off + C::TM_P + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
+        ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_p);   // P^T over consumed S^T columns
+        ptx::tmem_st16(tmem + lane_off + C::tm_p(b) + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&B.act_full);
+      ptx::mbar_arrive(&B.act_full[b]);
     }
     if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
     ok = __all_sync(0xffffffffu, ok);
