@@ -344,6 +344,33 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
   const int H = p.H;
   uint32_t gx = 0;
   bool ok = true;
+  // The epilogue of an item waits for its last P V.  With full attention it
+  // is deferred until the next item's first P is stored, so that wait
+  // overlaps that activation (short key ranges: an item is one or two
+  // tiles).  Window items hold several tiles per side, and there holding
+  // back the next item's first P V stalls the MMA issuer: no deferral.
+  bool pend = false, pend_live = false, pend_row_ok = false;
+  float pend_inv = 0.0f;
+  __nv_bfloat16* pend_orow = nullptr;
+  auto epilogue = [&]() {
+    ptx::tc_fence_after();
+    if (pend_live) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld32(o_addr + 32 * c, r);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * pend_inv, __uint_as_float(r[2 * i + 1]) * pend_inv);
+        if (pend_row_ok) store_row32(pend_orow + 32 * c, pk, p.out_align32 != 0);
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&B.o_empty[x]);
+    pend = false;
+  };
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const Pair64Item t = decode_pair64<WIN>(p, idx);
     const int rows = x ? t.rows[1] : t.rows[0];
@@ -408,18 +435,43 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
         }
         // The tile's 64 scores of this row in registers, one TMEM round trip.
         uint32_t sr[64];
+        // A whole tile of valid keys (full attention, softmax, scale > 0):
+        // the second half of the row loads while the first half's maximum is
+        // taken.  (Window tiles keep one load: the split measured slower there.)
+        const bool split_ld = !WIN && ACT == kActSoftmax && fullm == 0x3u && sl > 0.0f;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (split_ld) {
+          ptx::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          ptx::tmem_wait_ld_r32(&sr[0]);
+          ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch)
-          if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
-        ptx::tmem_wait_ld();
+          for (int c = 0; c < 32; c += 8) {
+            m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+          ptx::tmem_wait_ld_r32(&sr[32]);
+#pragma unroll
+          for (int c = 32; c < 64; c += 8) {
+            m4[0] = ptx::max3(m4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            m4[1] = ptx::max3(m4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            m4[2] = ptx::max3(m4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            m4[3] = ptx::max3(m4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch)
+            if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
+          ptx::tmem_wait_ld();
+        }
         if (ACT == kActSoftmax) {
           // Scores in log2 units: x = s * scale * log2(e); masked columns
           // become -inf.  With scale > 0 the scaling is folded into the
           // exponent's FMA; otherwise it is applied first.
           const bool fold = sl > 0.0f;
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
+          for (int ch = 0; ch < 2 && !split_ld; ++ch) {
             if (!((livem >> ch) & 1u)) continue;
             if (((fullm >> ch) & 1u) && fold) {
 #pragma unroll
@@ -520,6 +572,9 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
+      if constexpr (!WIN) {
+        if (pend) epilogue();  // the previous item's last P V has landed
+      }
       if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
         ptx::tc_fence_after();
 #pragma unroll
@@ -537,28 +592,43 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
       ptx::mbar_arrive(&B.p_full[x][sb]);
     }
     if (!ok) break;
-    ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);  // the item's last P V
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    ptx::tc_fence_after();
-    const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : inv_lkv;
     if (ACT == kActSoftmax && p.lse && row < rows)
       p.lse[static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h] = row_lse(m_run, l_run);
-    if (rows_live) {
+    const float inv = (ACT == kActSoftmax) ? (l_run > 0.0f ? 1.0f / l_run : 0.0f) : inv_lkv;
+    if constexpr (WIN) {  // no deferral: the epilogue now
+      ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);  // the item's last P V
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (rows_live) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(o_addr + 32 * c, r);
-        ptx::tmem_wait_ld();
-        uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(o_addr + 32 * c, r);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        if (row < rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          if (row < rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
+        }
       }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.o_empty[x]);
+    } else {
+      pend = true;
+      pend_live = rows_live;
+      pend_row_ok = row < rows;
+      pend_inv = inv;
+      pend_orow = orow;
     }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&B.o_empty[x]);
+  }
+  if constexpr (!WIN) {
+    if (ok && pend) {  // the last item's epilogue
+      ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) epilogue();
+    }
   }
   if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
 }
