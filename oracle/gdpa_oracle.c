@@ -17,6 +17,8 @@
  *
  * with j over the key set K(i):
  *   full attention:  every key j < Lkv_b of the same sequence;
+ *   sliding window of W tokens (window_blocks = -W < 0): the keys j with
+ *                    i - W < j <= i (causal, W tokens wide);
  *   block window W:  blocks of 64 tokens counted from the sequence start,
  *                    beta(t) = floor(t / 64); keys of the W-1 previous blocks
  *                    and keys j <= i of the query's own block.
@@ -29,6 +31,9 @@
  * the remio.ai commentary, section on model/system co-design; 64-token
  * block-aligned windows, window a whole number of blocks -- techfeed summary,
  * BlockAttention section, and the aigeeknews translation, co-design section.
+ * The token-granular sliding window is the causal window the BlockAttention
+ * section names as the step before block-aligned attention (techfeed
+ * summary); its width W in tokens is this project's parameter.
  * The output normalisation 1/Lkv of the GELU form and the window-of-blocks
  * semantics (own block causal plus the previous W-1 blocks, one softmax over
  * the union) are this project's readings of those passages.
@@ -85,7 +90,8 @@ double oracle_gelu_tanh_grad(double x) {
 
 /* Is key j in the key set of query i (both counted from the sequence start)? */
 static int key_in_set(int64_t i, int64_t j, int window_blocks) {
-  if (window_blocks <= 0) return 1;
+  if (window_blocks < 0) return j <= i && j > i + window_blocks; /* W = -window_blocks tokens */
+  if (window_blocks == 0) return 1;
   int64_t bi = i / ORACLE_BLOCK, bj = j / ORACLE_BLOCK;
   if (bj == bi) return j <= i;                        /* own block, causal */
   return bj < bi && bj >= bi - (window_blocks - 1);   /* W-1 previous blocks */
@@ -180,7 +186,8 @@ int oracle_num_cpus(void) {
 /*
  * q: bf16 bits [Tq, H, D]; k, v: bf16 bits [Tkv, H, D]; q_off, kv_off: int32
  * [B+1] prefix sums starting at 0; out: fp64 [Tq, H, D] (fully written).
- * window_blocks > 0 needs q_off == kv_off.  nthreads <= 0 uses every online
+ * window_blocks != 0 needs q_off == kv_off (> 0: block window of that many
+ * 64-token blocks; < 0: sliding window of -window_blocks tokens).  nthreads <= 0 uses every online
  * CPU.  Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
  */
 int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
@@ -190,7 +197,7 @@ int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
   for (int b = 0; b < B; ++b) {
     if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;
-    if (window_blocks > 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
+    if (window_blocks != 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
   }
   if (B == 0 || q_off[B] == 0) return 0;
   if (!q || !out || (kv_off[B] > 0 && (!k || !v))) return 1;
@@ -337,7 +344,7 @@ int oracle_gdpa_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
   for (int b = 0; b < B; ++b) {
     if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;
-    if (window_blocks > 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
+    if (window_blocks != 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
   }
   if (B == 0) return 0;
   if ((q_off[B] > 0 && (!q || !dout || !dq || !lse)) || (kv_off[B] > 0 && (!k || !v || !dk || !dv))) return 1;

@@ -30,7 +30,7 @@ def small_batch(rng, Lq, Lkv, H, D, act=0, window_blocks=0, scale=None, name="cu
     if qk_norm:
         q = 4 * q / np.linalg.norm(q, axis=-1, keepdims=True)
         k = 4 * k / np.linalg.norm(k, axis=-1, keepdims=True)
-    kind = "window" if window_blocks > 0 else "self"
+    kind = "window" if window_blocks != 0 else "self"
     w = Workload(name, 0, len(Lq), H, D, act, window_blocks, scale, kind)
     return JaggedBatch(w, bits(q), bits(k), bits(v), offsets_of(Lq), offsets_of(Lkv))
 
@@ -73,6 +73,9 @@ def padded_dense(batch: JaggedBatch, causal_only=False) -> np.ndarray:
             m &= j <= i
         elif w.window_blocks > 0:
             m &= (j <= i) & ((i // BLOCK) - (j // BLOCK) <= w.window_blocks - 1)
+        elif w.window_blocks < 0:  # sliding window of W tokens: a band of W diagonals
+            W = -w.window_blocks
+            m &= np.tril(np.ones((Mq, Mk), dtype=bool)) & np.triu(np.ones((Mq, Mk), dtype=bool), -(W - 1))
         mask[b, 0] = m
     if w.act == 0:
         Sm = np.where(mask, S, -np.inf)

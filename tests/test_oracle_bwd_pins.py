@@ -51,6 +51,8 @@ def torch_grads(batch, dout):
         mask = torch.ones((Lq, Lkv), dtype=torch.bool)
         if w.window_blocks > 0:
             mask = (j <= i) & ((i // BLOCK) - (j // BLOCK) <= w.window_blocks - 1)
+        elif w.window_blocks < 0:  # sliding window of W tokens
+            mask = (j <= i) & (i - j < -w.window_blocks)
         rows = mask.any(dim=1)
         if w.act == ACT_SOFTMAX:
             Sm = S.masked_fill(~mask, -torch.inf)

@@ -70,6 +70,42 @@ def test_full_window_is_causal_attention():
     np.testing.assert_allclose(run(b), padded_dense(b, causal_only=True), rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("W", [1, 2, 63, 64, 65, 130])
+def test_sliding_window_matches_padded_dense(W):
+    rng = np.random.default_rng(30 + W)
+    L = [150, 1, 64, 65, 0, 129]
+    b = small_batch(rng, L, L, 2, 8, window_blocks=-W)
+    np.testing.assert_allclose(run(b), padded_dense(b), rtol=1e-11, atol=1e-12)
+
+
+def test_sliding_window_of_one_token_returns_own_value():
+    rng = np.random.default_rng(40)
+    L = [7, 33]
+    b = small_batch(rng, L, L, 2, 8, window_blocks=-1)
+    np.testing.assert_array_equal(run(b), bf16_bits_to_f64(b.v))
+
+
+def test_wide_sliding_window_is_causal_attention():
+    rng = np.random.default_rng(41)
+    L = [150, 90]
+    b = small_batch(rng, L, L, 2, 8, window_blocks=-150)
+    np.testing.assert_allclose(run(b), padded_dense(b, causal_only=True), rtol=1e-11, atol=1e-12)
+
+
+def test_sliding_window_backward_matches_torch_autograd():
+    from tests.test_oracle_bwd_pins import assert_close, rand_dout, torch_grads
+    rng = np.random.default_rng(42)
+    L = [130, 64, 65, 1]
+    b = small_batch(rng, L, L, 1, 8, window_blocks=-40)
+    do = rand_dout(rng, b)
+    dq, dk, dv, lse = oracle.gdpa_bwd_batch(b, do, nthreads=2)
+    rq, rk, rv, rl = torch_grads(b, do)
+    assert_close(dq, rq, "dq")
+    assert_close(dk, rk, "dk")
+    assert_close(dv, rv, "dv")
+    assert np.allclose(lse, rl, atol=1e-12)
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_single_key_softmax_returns_v0_exactly():
