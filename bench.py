@@ -51,8 +51,10 @@ RECIPES = {
     "cross_gelu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, GELU-tanh (ALU), scale=1, /Lkv",
     "pma": "B=256 H=8 D=64, 32 shared seed queries per sample, Lkv=clip(round(lognormal(7.6,1.0)),100,16384), softmax",
     "block_window": "B=64 H=4 D=128, L=64*U{8..512}, 64-token blocks, window 4 blocks (own causal + 3 previous), softmax",
+    "sliding_window": "B=64 H=4 D=128, L~U{512..32768}, causal sliding window of 256 tokens, softmax",
 }
-BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm"}
+BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm",
+         "sliding_window": "hbm"}
 
 
 def parse_args():
@@ -107,6 +109,8 @@ def kernel_for(batch, gdpa_mod, num_ctas: int) -> str:
     """The kernel the planner picks for this batch: 256-row items take a pair
     kernel (64- or 128-key K/V tiles), the rest the single-tile kernel."""
     w = batch.workload
+    if w.window_blocks < 0:  # sliding windows: 256-row items on the 64-key pair kernel
+        return "gdpa_fwd_pair64_kernel"
     _, _, _, rows, kv_tile = gdpa_mod.gdpa_plan_enumerate(batch.q_offsets, batch.kv_offsets, batch.B, w.H, w.D,
                                                           w.act, w.window_blocks, num_ctas, with_rows=True)
     if rows != 256:
@@ -287,7 +291,11 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        gdpa.gdpa_fwd_async(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, out, stream)
+        if w.window_blocks < 0:
+            gdpa.gdpa_fwd_sliding(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, -w.window_blocks, w.scale, out, None,
+                                  stream)
+        else:
+            gdpa.gdpa_fwd_async(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, out, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -327,27 +335,32 @@ def run_ours(args, rank, world, local):
     total_flops = flops * world
     value = total_flops * K / (elapsed_ms / 1e3) / 1e12
 
-    # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step)
-    hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
-    hk = torch.from_numpy(batch.k.view(np.int16)).pin_memory()
-    hv = torch.from_numpy(batch.v.view(np.int16)).pin_memory()
-    ho = torch.empty((Tq, H, D), dtype=torch.int16).pin_memory()
-    h2d = int(hq.numel() + hk.numel() + hv.numel()) * 2 + 2 * 4 * (B + 1)
-    d2h = int(ho.numel()) * 2
-    gdpa.gdpa_fwd_host(hq, hk, hv, h_qo, h_ko, B, H, D, w.act, w.window_blocks, w.scale, ho, stream)
-    e2e_t = []
-    for _ in range(max(1, args.e2e_steps)):
-        if dist:
-            dist.barrier()
-        t0 = time.perf_counter()
+    # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step);
+    # the host-buffer entry point takes block windows only, so a sliding window has none
+    e2e = None
+    if w.window_blocks >= 0:
+        hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
+        hk = torch.from_numpy(batch.k.view(np.int16)).pin_memory()
+        hv = torch.from_numpy(batch.v.view(np.int16)).pin_memory()
+        ho = torch.empty((Tq, H, D), dtype=torch.int16).pin_memory()
+        h2d = int(hq.numel() + hk.numel() + hv.numel()) * 2 + 2 * 4 * (B + 1)
+        d2h = int(ho.numel()) * 2
         gdpa.gdpa_fwd_host(hq, hk, hv, h_qo, h_ko, B, H, D, w.act, w.window_blocks, w.scale, ho, stream)
-        e2e_t.append(time.perf_counter() - t0)
-    e2e_s = statistics.mean(e2e_t)
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = total_flops / e2e_s / 1e12
+        e2e_t = []
+        for _ in range(max(1, args.e2e_steps)):
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            gdpa.gdpa_fwd_host(hq, hk, hv, h_qo, h_ko, B, H, D, w.act, w.window_blocks, w.scale, ho, stream)
+            e2e_t.append(time.perf_counter() - t0)
+        e2e_s = statistics.mean(e2e_t)
+        if dist:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e_value = total_flops / e2e_s / 1e12
+        e2e = {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3, "entry": "gdpa_fwd_host"}
 
     peaks, peak_src = load_peaks()
     bound = BOUND[args.workload]
@@ -387,8 +400,7 @@ def run_ours(args, rank, world, local):
                        "parallelism": "dp%d (independent batches, no collective)" % world,
                        "entry": "gdpa_fwd_async (host plan + upload + kernel per step)"},
             "clocks": clocks,
-            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_s * 1e3, "entry": "gdpa_fwd_host"},
+            "e2e": e2e,
             "gpu_launches": K,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -123,6 +123,22 @@ gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* v, const in
                            void* stream);
 
 /*
+ * gdpa_fwd_sliding -- the forward with a causal sliding window of
+ * window_tokens tokens instead of block windows: query i of a sequence sees
+ * the keys i - window_tokens < j <= i of its own sequence (the token-granular
+ * window the BlockAttention section of the techfeed summary of "GEM
+ * Training" names as the step before block-aligned attention).  Softmax only
+ * (GDPA_ERR_UNSUPPORTED for GELU), self attention (q and kv offsets equal),
+ * window_tokens >= 1.  lse: optional (may be NULL) device fp32 [Tq, H], as
+ * gdpa_fwd_lse.  Offsets twice (host and device) and everything else as
+ * gdpa_fwd_async; asynchronous on `stream`.
+ */
+gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                               const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
+                               int B, int H, int D, int act, int window_tokens, float scale, void* out, float* lse,
+                               void* stream);
+
+/*
  * gdpa_bwd -- gradients of the forward for an upstream gradient dout:
  *   dq = dL/dq, dk = dL/dk, dv = dL/dv for L = sum(dout * out), computed by
  * the chain rule of the forward's definition (techfeed summary of "GEM

@@ -274,19 +274,21 @@ extern "C" gdpa_status_t gdpa_fwd_async(const void* q, const void* k, const void
                          rpi, kvt, n_items, s);
 }
 
-extern "C" gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
-                                      const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
-                                      int B, int H, int D, int act, int window_blocks, float scale, void* out,
-                                      float* lse, void* stream) {
-  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
-  if (st != GDPA_OK) return st;
-  if (B == 0) return GDPA_OK;
+namespace gdpa {
+namespace {
+
+// gdpa_fwd_async with an optional logsumexp output and the internal window
+// code (> 0: block window, < 0: sliding window of -window tokens).
+gdpa_status_t fwd_async_impl(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                             const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets, int B,
+                             int H, int D, int act, int window, float scale, void* out, float* lse, void* stream) {
   int64_t Tq = 0, Tkv = 0;
-  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window_blocks, &Tq, &Tkv)) != GDPA_OK) return st;
+  gdpa_status_t st;
+  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window, &Tq, &Tkv)) != GDPA_OK) return st;
   if ((st = check_tensors(q, k, v, out, Tq, Tkv)) != GDPA_OK) return st;
   if (Tq == 0) return GDPA_OK;
   if (!q_offsets || !kv_offsets) return GDPA_ERR_INVALID_ARG;
-  if (act == GDPA_ACT_SOFTMAX && (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)) return GDPA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GDPA_ERR_INVALID_ARG;
   int device = 0, sms = 0;
   if ((st = num_sms(&device, &sms)) != GDPA_OK) return st;
   DeviceCtx& c = ctx(device);
@@ -296,11 +298,38 @@ extern "C" gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* 
   int num_ctas = 0;
   int rpi = 0, kvt = 0;
   int64_t n_items = 0;
-  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window_blocks, sms, s, &num_ctas, &rpi,
-                            &kvt, &n_items)) != GDPA_OK)
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window, sms, s, &num_ctas, &rpi, &kvt,
+                            &n_items)) != GDPA_OK)
     return st;
-  return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window_blocks, scale, num_ctas,
-                         rpi, kvt, n_items, s, act == GDPA_ACT_SOFTMAX ? lse : nullptr);
+  return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window, scale, num_ctas, rpi,
+                         kvt, n_items, s, act == GDPA_ACT_SOFTMAX ? lse : nullptr);
+}
+
+}  // namespace
+}  // namespace gdpa
+
+extern "C" gdpa_status_t gdpa_fwd_lse(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                                      const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
+                                      int B, int H, int D, int act, int window_blocks, float scale, void* out,
+                                      float* lse, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  if (B == 0) return GDPA_OK;
+  if (act == GDPA_ACT_SOFTMAX && !lse) return GDPA_ERR_INVALID_ARG;
+  return fwd_async_impl(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, window_blocks,
+                        scale, out, lse, stream);
+}
+
+extern "C" gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
+                                          const int32_t* h_kv_offsets, const int32_t* q_offsets,
+                                          const int32_t* kv_offsets, int B, int H, int D, int act, int window_tokens,
+                                          float scale, void* out, float* lse, void* stream) {
+  if (window_tokens < 1) return GDPA_ERR_INVALID_ARG;
+  gdpa_status_t st = validate_shape(B, H, D, act, 1);  // as a window: softmax only
+  if (st != GDPA_OK) return st;
+  if (B == 0) return GDPA_OK;
+  return fwd_async_impl(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, -window_tokens,
+                        scale, out, lse, stream);
 }
 
 extern "C" gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,

@@ -122,8 +122,14 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
   if (WIN) {
     const int end_a = min(v.Lkv, v.q0 + 128);
     v.t1[0] = end_a > v.kv0 ? (end_a - v.kv0 + BN - 1) / BN : 0;
-    const int blk = (v.q0 + 128) / 64 - (p.window_blocks - 1);
-    const int lo_b = blk > 0 ? blk * 64 : 0;
+    int lo_b;  // first key any row of tile B may see, rounded down to its tile
+    if (p.window_blocks < 0) {  // sliding window of -window_blocks tokens
+      const int lo = v.q0 + 128 + p.window_blocks + 1;
+      lo_b = lo > 0 ? lo / BN * BN : 0;
+    } else {
+      const int blk = (v.q0 + 128) / 64 - (p.window_blocks - 1);
+      lo_b = blk > 0 ? blk * 64 : 0;
+    }
     v.t0[1] = (lo_b - v.kv0) / BN;
   }
   return v;
@@ -389,9 +395,13 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
     float m_run = -INFINITY, l_run = 0.0f;
     const int i_seq = t.q0 + 128 * x + row;  // query index inside its sequence
     int win_lo = 0;
-    if (WIN) {
-      const int blk = i_seq / 64 - (p.window_blocks - 1);
-      win_lo = blk > 0 ? blk * 64 : 0;
+    if (WIN) {  // first key of this row's window
+      if (p.window_blocks < 0) {
+        win_lo = max(0, i_seq + p.window_blocks + 1);
+      } else {
+        const int blk = i_seq / 64 - (p.window_blocks - 1);
+        win_lo = blk > 0 ? blk * 64 : 0;
+      }
     }
     const int j0 = x ? t.t0[1] : t.t0[0], j1 = x ? t.t1[1] : t.t1[0];  // this side's K/V tiles
     const int kv0 = t.kv0, kv_end = t.kv_end;

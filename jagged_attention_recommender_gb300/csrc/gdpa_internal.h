@@ -45,7 +45,10 @@ int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks);
 constexpr int kShortRange = 256;
 int choose_kv_tile(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks, int rows_per_item);
 
-// First key of the block window of a query tile starting at q0.
+// First key of the window of a query tile starting at q0: window_blocks > 0
+// is a block window of that many 64-token blocks, window_blocks < 0 (internal
+// only, gdpa_fwd_sliding) a causal sliding window of -window_blocks tokens,
+// whose first key is rounded down to its 64-key tile.
 int64_t window_start(int64_t q0, int window_blocks);
 
 // Planner cost of an item (units of key columns of a 128-row tile).

@@ -227,7 +227,9 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   prm.lse = a.lse;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
-  const bool win = a.window_blocks > 0;
+  const bool win = a.window_blocks != 0;
+  // sliding windows (window_blocks < 0) exist only in the 64-key pair kernel
+  if (a.window_blocks < 0 && !(a.rows_per_item == 256 && a.kv_tile == kBlockN / 2)) return GDPA_ERR_INVALID_ARG;
   if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {
     if (win) {  // softmax only (validated on entry)
       if (a.D == 128) return launch_pair64<128, kActSoftmax, true>(prm, a.num_ctas, s, device);

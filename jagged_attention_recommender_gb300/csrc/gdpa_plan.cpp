@@ -37,7 +37,7 @@ gdpa_status_t validate_offsets(const int32_t* q_off, const int32_t* kv_off, int 
   if (q_off[0] != 0 || kv_off[0] != 0) return GDPA_ERR_INVALID_ARG;
   for (int b = 0; b < B; ++b) {
     if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return GDPA_ERR_INVALID_ARG;
-    if (window_blocks > 0 && (q_off[b + 1] != kv_off[b + 1])) return GDPA_ERR_INVALID_ARG;
+    if (window_blocks != 0 && (q_off[b + 1] != kv_off[b + 1])) return GDPA_ERR_INVALID_ARG;
   }
   *Tq = q_off[B];
   *Tkv = kv_off[B];
@@ -54,6 +54,10 @@ static int64_t item_cost(int64_t kv_len) {
 }
 
 int64_t window_start(int64_t q0, int window_blocks) {
+  if (window_blocks < 0) {  // sliding window of W tokens, from the 64-key tile holding q0 - W + 1
+    const int64_t lo = q0 + window_blocks + 1;
+    return lo > 0 ? lo / kWindowBlock * kWindowBlock : 0;
+  }
   const int64_t blk = q0 / kWindowBlock - (window_blocks - 1);
   return blk > 0 ? blk * kWindowBlock : 0;
 }
@@ -66,7 +70,7 @@ int64_t plan_item_cost(int64_t q0, int64_t Lq, int64_t Lkv, int window_blocks, i
   for (int64_t x = 0; x < tiles; ++x) {
     const int64_t qt = q0 + kBlockM * x;
     int64_t lo = 0, hi = Lkv;
-    if (window_blocks > 0) {
+    if (window_blocks != 0) {
       lo = window_start(qt, window_blocks);
       hi = std::min<int64_t>(Lkv, qt + kBlockM);
     }
@@ -77,7 +81,7 @@ int64_t plan_item_cost(int64_t q0, int64_t Lq, int64_t Lkv, int window_blocks, i
 
 int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks) {
   if (B <= 0) return kBlockM;
-  if (window_blocks > 0) return 2 * kBlockM;  // both tiles share the overlapping windows' keys
+  if (window_blocks != 0) return 2 * kBlockM;  // both tiles share the overlapping windows' keys
   int64_t busy = 0, max_lq = 0;
   for (int b = 0; b < B; ++b) {
     const int64_t lq = q_off[b + 1] - q_off[b];
@@ -91,7 +95,7 @@ int choose_rows_per_item(const int32_t* q_off, int B, int D, int window_blocks) 
 
 int choose_kv_tile(const int32_t* q_off, const int32_t* kv_off, int B, int window_blocks, int rows_per_item) {
   if (rows_per_item != 2 * kBlockM) return kBlockN;
-  if (window_blocks > 0) return kBlockN / 2;
+  if (window_blocks != 0) return kBlockN / 2;
   int64_t busy = 0, keys = 0;
   for (int b = 0; b < B; ++b)
     if (q_off[b + 1] > q_off[b]) {
@@ -123,7 +127,7 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
     const int64_t Lq = q_off[b + 1] - q_off[b];
     const int64_t Lkv = kv_off[b + 1] - kv_off[b];
     for (int64_t q0 = 0; q0 < Lq; q0 += rows_per_item) {
-      const int64_t kv0 = window_blocks > 0 ? window_start(q0, window_blocks) : 0;
+      const int64_t kv0 = window_blocks != 0 ? window_start(q0, window_blocks) : 0;
       const int64_t c = plan_item_cost(q0, Lq, Lkv, window_blocks, rows_per_item);
       for (int h = 0; h < H; ++h) {
         items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});

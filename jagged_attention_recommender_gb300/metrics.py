@@ -12,7 +12,11 @@ from .workloads import BLOCK, JaggedBatch
 
 def key_count(Lq: int, Lkv: int, window_blocks: int) -> int:
     """Number of (query, key) pairs a sequence attends over (useful pairs)."""
-    if window_blocks <= 0:
+    if window_blocks < 0:  # sliding window of W tokens: query i sees min(i + 1, W) keys
+        W, L = -window_blocks, int(Lq)
+        m = min(W, L)
+        return m * (m + 1) // 2 + (L - m) * W
+    if window_blocks == 0:
         return int(Lq) * int(Lkv)
     # own block causal + (window_blocks - 1) full previous blocks, clipped at 0
     total = 0

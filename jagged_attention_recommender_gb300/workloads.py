@@ -25,6 +25,8 @@ pma             B=256, H=8, D=64, 32 seed queries shared by every sample
                 100, 16384); softmax; scale 1/sqrt(D)
 block_window    B=64, H=4, D=128, L = 64 * U{8..512}; window of 4 blocks of 64
                 (own block causal + 3 previous); softmax; scale 1/sqrt(D)
+sliding_window  B=64, H=4, D=128, L ~ U{512..32768}; causal sliding window of
+                256 tokens (window_blocks = -256); softmax; scale 1/sqrt(D)
 ==============  ====================================================================
 
 Draw order (fixed): lengths first, then one 63-bit sub-seed per value tensor
@@ -68,6 +70,8 @@ WORKLOADS = {
     "cross_gelu": Workload("cross_gelu", 2, 512, 4, 128, ACT_GELU_TANH, 0, 1.0, "cross"),
     "pma": Workload("pma", 3, 256, 8, 64, ACT_SOFTMAX, 0, 1.0 / math.sqrt(64), "pma"),
     "block_window": Workload("block_window", 4, 64, 4, 128, ACT_SOFTMAX, 4, 1.0 / math.sqrt(128), "window"),
+    # window_blocks < 0: a causal sliding window of -window_blocks tokens
+    "sliding_window": Workload("sliding_window", 5, 64, 4, 128, ACT_SOFTMAX, -256, 1.0 / math.sqrt(128), "window"),
 }
 
 PMA_SEEDS = 32
@@ -103,6 +107,9 @@ def draw_lengths(w: Workload, rng: np.random.Generator, B: int | None = None):
         return np.full(B, PMA_SEEDS, dtype=np.int64), Lkv
     if w.name == "block_window":
         L = BLOCK * rng.integers(8, 512, size=B, endpoint=True)
+        return L, L
+    if w.name == "sliding_window":
+        L = rng.integers(512, 32768, size=B, endpoint=True)
         return L, L
     raise KeyError(w.name)
 

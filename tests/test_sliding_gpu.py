@@ -1,0 +1,108 @@
+"""GPU parity of the causal sliding window (gdpa_fwd_sliding) against the
+fp64 oracle (window_blocks = -W in the oracle: keys i - W < j <= i).
+
+The forward workloads' bar, max |d| <= 1e-2 and rel-L2 <= 5e-3, with the
+absolute part grown by 2^-7 |o| as for the other few-key edge cases: the
+first rows of a sequence average only a handful of keys, so |o| reaches
+|v| ~ 4, and P (rounded to bf16, up to 2^-9 relative) and the bf16 output
+(up to half an ulp, 2^-9 |o|) legitimately move such an output by about
+1.5 * 2^-8 |o|, more than 1e-2 once |o| > 2.6.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from jagged_attention_recommender_gb300 import build as gbuild, gdpa
+from jagged_attention_recommender_gb300.workloads import ACT_GELU_TANH, ACT_SOFTMAX, make_batch
+from tests.helpers import small_batch
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+REL_L2 = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gbuild.build()
+    yield
+
+
+def dev(bits_arr):
+    return torch.from_numpy(np.ascontiguousarray(bits_arr).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run_sliding(batch, W, guard=3, with_lse=False):
+    w = batch.workload
+    H, D, B = w.H, w.D, len(batch.q_offsets) - 1
+    Tq = int(batch.q_offsets[-1])
+    q, k, v = dev(batch.q), dev(batch.k), dev(batch.v)
+    qo = torch.from_numpy(batch.q_offsets).cuda()
+    ko = torch.from_numpy(batch.kv_offsets).cuda()
+    full = torch.full((Tq + 2 * guard, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = full[guard:guard + Tq]
+    lse = torch.full((Tq, H), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    gdpa.gdpa_fwd_sliding(q, k, v, batch.q_offsets, batch.kv_offsets, qo, ko, B, H, D, w.act, W, w.scale, out, lse)
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_OK
+    torch.cuda.synchronize()
+    if guard:
+        g = torch.cat([full[:guard], full[guard + Tq:]])
+        assert torch.isnan(g.float()).all(), "kernel wrote outside its output rows"
+    res = out.float().cpu().numpy().astype(np.float64)
+    if with_lse:
+        return res, lse.cpu().numpy().astype(np.float64)
+    return res
+
+
+def assert_parity(got, ref, what):
+    assert np.isfinite(got).all(), what
+    d = np.abs(got - ref)
+    bar = MAX_ABS + np.abs(ref) * 2.0 ** -7
+    assert np.all(d <= bar), "%s: max |d| - bar %.3e" % (what, (d - bar).max())
+    rl2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rl2 <= REL_L2, "%s: rel L2 %.3e" % (what, rl2)
+
+
+LENGTHS = [1, 64, 65, 200, 640, 1000, 257, 256]
+
+
+@pytest.mark.parametrize("W", [1, 17, 64, 65, 200, 1000])
+def test_sliding_window_parity(W):
+    rng = np.random.default_rng(8000 + W)
+    L = np.array(LENGTHS)
+    b = small_batch(rng, L, L, 2, 128, window_blocks=-W)
+    assert_parity(run_sliding(b, W), oracle.gdpa_fwd_batch(b), "W=%d" % W)
+
+
+def test_sliding_window_d64_and_lse():
+    rng = np.random.default_rng(8100)
+    L = np.array([300, 129, 512, 3])
+    b = small_batch(rng, L, L, 4, 64, window_blocks=-100)
+    out, lse = run_sliding(b, 100, with_lse=True)
+    assert_parity(out, oracle.gdpa_fwd_batch(b), "D=64")
+    rl = oracle.gdpa_bwd_batch(b, np.zeros_like(b.q))[3]
+    assert np.abs(lse - rl).max() <= 2e-3
+
+
+def test_sliding_window_full_workload_sampled():
+    batch = make_batch("sliding_window")
+    w = batch.workload
+    got = run_sliding(batch, -w.window_blocks, guard=0)
+    qo = batch.q_offsets
+    for b in [0, int(np.argmax(np.diff(qo))), len(qo) - 2]:
+        sub = batch.subset([b])
+        sl = slice(qo[b], qo[b + 1])
+        assert_parity(got[sl], oracle.gdpa_fwd_batch(sub), "sequence %d" % b)
+
+
+def test_sliding_window_rejects_bad_arguments():
+    qo = np.array([0, 64], np.int32)
+    for act, W, ko, code in ((ACT_GELU_TANH, 8, qo, gdpa.GDPA_ERR_UNSUPPORTED),
+                             (ACT_SOFTMAX, 0, qo, gdpa.GDPA_ERR_INVALID_ARG),
+                             (ACT_SOFTMAX, 8, np.array([0, 65], np.int32), gdpa.GDPA_ERR_INVALID_ARG)):
+        with pytest.raises(gdpa.GdpaError) as e:
+            gdpa.gdpa_fwd_sliding(0, 0, 0, qo, ko, 0, 0, 1, 1, 64, act, W, 1.0, 0)
+        assert e.value.code == code
