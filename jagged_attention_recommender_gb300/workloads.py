@@ -47,6 +47,7 @@ import numpy as np
 
 ACT_SOFTMAX = 0
 ACT_GELU_TANH = 1
+ACT_SILU = 2
 
 CHUNK_TOKENS = 16384
 

@@ -43,6 +43,10 @@ def _load():
         lib.oracle_gdpa_bwd.restype = ctypes.c_int
         lib.oracle_gelu_tanh_grad.argtypes = [ctypes.c_double]
         lib.oracle_gelu_tanh_grad.restype = ctypes.c_double
+        lib.oracle_silu.argtypes = [ctypes.c_double]
+        lib.oracle_silu.restype = ctypes.c_double
+        lib.oracle_silu_grad.argtypes = [ctypes.c_double]
+        lib.oracle_silu_grad.restype = ctypes.c_double
         lib.oracle_gelu_tanh.argtypes = [ctypes.c_double]
         lib.oracle_gelu_tanh.restype = ctypes.c_double
         lib.oracle_num_cpus.restype = ctypes.c_int
@@ -117,6 +121,14 @@ def gdpa_bwd_batch(batch, dout, nthreads: int = 0):
 
 def gelu_tanh_grad(x: float) -> float:
     return _load().oracle_gelu_tanh_grad(float(x))
+
+
+def silu(x: float) -> float:
+    return _load().oracle_silu(float(x))
+
+
+def silu_grad(x: float) -> float:
+    return _load().oracle_silu_grad(float(x))
 
 
 def gelu_tanh(x: float) -> float:

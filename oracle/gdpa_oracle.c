@@ -14,6 +14,9 @@
  *   GELU:     o_i = (1 / Lkv_b) * sum_j gelu(s_ij) v_j,
  *             gelu(x) = x/2 * (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))),
  *             o_i = 0 when Lkv_b = 0
+ *   SiLU:     o_i = (1 / Lkv_b) * sum_j silu(s_ij) v_j,  silu(x) = x / (1 + e^-x)
+ *             (the same form with another activation: the remio.ai
+ *             commentary's "alternative activations" of GDPA)
  *
  * with j over the key set K(i):
  *   full attention:  every key j < Lkv_b of the same sequence;
@@ -66,6 +69,7 @@
 
 #define ORACLE_ACT_SOFTMAX 0
 #define ORACLE_ACT_GELU_TANH 1
+#define ORACLE_ACT_SILU 2
 #define ORACLE_BLOCK 64
 
 /* bf16 bit pattern -> exact double (bf16 is the top half of an IEEE float). */
@@ -79,6 +83,21 @@ static double bf16_to_double(uint16_t bits) {
 double oracle_gelu_tanh(double x) {
   const double c = sqrt(2.0 / M_PI);
   return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+double oracle_silu(double x) { return x / (1.0 + exp(-x)); }
+
+/* d/dx of oracle_silu: sigma(x) (1 + x (1 - sigma(x))). */
+double oracle_silu_grad(double x) {
+  const double sg = 1.0 / (1.0 + exp(-x));
+  return sg * (1.0 + x * (1.0 - sg));
+}
+
+/* The elementwise activation of the non-softmax forms and its derivative. */
+static double act_value(int act, double x) { return act == ORACLE_ACT_SILU ? oracle_silu(x) : oracle_gelu_tanh(x); }
+double oracle_gelu_tanh_grad(double x);
+static double act_grad(int act, double x) {
+  return act == ORACLE_ACT_SILU ? oracle_silu_grad(x) : oracle_gelu_tanh_grad(x);
 }
 
 /* d/dx of oracle_gelu_tanh. */
@@ -145,7 +164,7 @@ static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, d
     } else {
       for (int64_t j = 0; j < Lkv; ++j) {
         if (!key_in_set(i, j, J->window_blocks)) continue;
-        double g = oracle_gelu_tanh(s[j]);
+        double g = act_value(J->act, s[j]);
         for (int d = 0; d < D; ++d) o[d] += g * vbuf[j * D + d];
       }
       for (int d = 0; d < D; ++d) o[d] /= (double)Lkv;
@@ -193,7 +212,8 @@ int oracle_num_cpus(void) {
 int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
                     const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
                     double* out, int nthreads) {
-  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH)) return 1;
+  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH && act != ORACLE_ACT_SILU))
+    return 1;
   if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
   for (int b = 0; b < B; ++b) {
     if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;
@@ -280,7 +300,7 @@ static void run_bwd_task(const bjob_t* J, int b, int h, const bscratch_t* W) {
     double dsum = 0.0; /* sum_j P_ij dP_ij (softmax) */
     for (int64_t j = 0; j < Lkv; ++j) {
       if (!key_in_set(i, j, J->window_blocks)) continue;
-      W->p[j] = J->act == ORACLE_ACT_SOFTMAX ? exp(W->s[j] - *lse_i) : oracle_gelu_tanh(W->s[j]) / (double)Lkv;
+      W->p[j] = J->act == ORACLE_ACT_SOFTMAX ? exp(W->s[j] - *lse_i) : act_value(J->act, W->s[j]) / (double)Lkv;
       double dp = 0.0;
       for (int d = 0; d < D; ++d) dp += W->drow[d] * W->vbuf[j * D + d];
       W->dp[j] = dp;
@@ -289,7 +309,7 @@ static void run_bwd_task(const bjob_t* J, int b, int h, const bscratch_t* W) {
     for (int64_t j = 0; j < Lkv; ++j) {
       if (!key_in_set(i, j, J->window_blocks)) continue;
       const double ds = J->act == ORACLE_ACT_SOFTMAX ? W->p[j] * (W->dp[j] - dsum)
-                                                     : oracle_gelu_tanh_grad(W->s[j]) * W->dp[j] / (double)Lkv;
+                                                     : act_grad(J->act, W->s[j]) * W->dp[j] / (double)Lkv;
       double* dkj = J->dk + ((k0 + j) * H + h) * (int64_t)D;
       double* dvj = J->dv + ((k0 + j) * H + h) * (int64_t)D;
       for (int d = 0; d < D; ++d) {
@@ -340,7 +360,8 @@ static void* bwd_worker(void* arg) {
 int oracle_gdpa_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                     const int32_t* q_off, const int32_t* kv_off, int B, int H, int D, int act, int window_blocks,
                     double scale, double* dq, double* dk, double* dv, double* lse, int nthreads) {
-  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH)) return 1;
+  if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH && act != ORACLE_ACT_SILU))
+    return 1;
   if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
   for (int b = 0; b < B; ++b) {
     if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return 1;

@@ -87,7 +87,10 @@ def padded_dense(batch: JaggedBatch, causal_only=False) -> np.ndarray:
         den_t = np.transpose(den, (0, 2, 1, 3))  # [B, Mq, H, 1]
         O = np.where(den_t > 0, O / np.where(den_t > 0, den_t, 1.0), 0.0)
     else:
-        G = torch.nn.functional.gelu(torch.from_numpy(S), approximate="tanh").numpy()
+        if w.act == 2:  # SiLU
+            G = torch.nn.functional.silu(torch.from_numpy(S)).numpy()
+        else:
+            G = torch.nn.functional.gelu(torch.from_numpy(S), approximate="tanh").numpy()
         G = np.where(mask, G, 0.0)
         O = np.einsum("bhij,bjhd->bihd", G, V)
         div = np.where(Lkv > 0, Lkv, 1).astype(np.float64)

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from jagged_attention_recommender_gb300.workloads import (
-    ACT_GELU_TANH, ACT_SOFTMAX, BLOCK, bf16_bits_to_f64)
+    ACT_GELU_TANH, ACT_SILU, ACT_SOFTMAX, BLOCK, bf16_bits_to_f64)
 from tests.helpers import bits, small_batch, with_values
 
 
@@ -60,6 +60,8 @@ def torch_grads(batch, dout):
             P = torch.exp(Sm - torch.where(rows, l, torch.zeros_like(l))[..., None])
             P = torch.where(rows[:, None], P, torch.zeros_like(P))
             lse[qo[b]:qo[b + 1]] = torch.where(rows, l, torch.full_like(l, -torch.inf)).transpose(0, 1).detach()
+        elif w.act == ACT_SILU:
+            P = torch.nn.functional.silu(S) * mask / Lkv
         else:
             P = torch.nn.functional.gelu(S, approximate="tanh") * mask / Lkv
         O = torch.einsum("hij,hjd->hid", P, V)
@@ -86,6 +88,7 @@ CASES = [
     ([40, 3, 70], [7, 1, 19], 2, 16, ACT_GELU_TANH, 0, True),
     ([130, 64, 65], [130, 64, 65], 1, 8, ACT_SOFTMAX, 2, False),   # windows, partial blocks
     ([0, 9], [4, 0], 2, 8, ACT_GELU_TANH, 0, True),                 # all rows empty
+    ([40, 3, 70], [7, 1, 19], 2, 16, ACT_SILU, 0, True),              # SiLU cross
 ]
 
 
@@ -105,7 +108,7 @@ def test_oracle_bwd_matches_torch_autograd(case):
     assert np.allclose(lse[fin], rl[fin], rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_GELU_TANH])
+@pytest.mark.parametrize("act", [ACT_SOFTMAX, ACT_GELU_TANH, ACT_SILU])
 def test_oracle_bwd_matches_finite_differences_of_forward(act):
     # d/dx of L = sum(dO * O) by central differences of the forward oracle,
     # perturbing one bf16 input to its neighbours (exact bf16 values)
@@ -169,3 +172,14 @@ def test_gelu_grad_matches_central_difference():
         h = 1e-5
         fd = (oracle.gelu_tanh(x + h) - oracle.gelu_tanh(x - h)) / (2 * h)
         assert abs(oracle.gelu_tanh_grad(x) - fd) < 1e-8
+
+
+def test_silu_and_its_grad_closed_forms():
+    # silu(0) = 0, silu'(0) = 1/2; silu(x) -> x and silu'(x) -> 1 for large x;
+    # silu(-x) = silu(x) - x; central difference of the oracle's silu
+    assert oracle.silu(0.0) == 0.0 and oracle.silu_grad(0.0) == 0.5
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu_grad(40.0) - 1.0) < 1e-12
+    for x in np.linspace(-8, 8, 65):
+        assert abs(oracle.silu(-x) - (oracle.silu(x) - x)) < 1e-12
+        fd = (oracle.silu(x + 1e-5) - oracle.silu(x - 1e-5)) / 2e-5
+        assert abs(oracle.silu_grad(x) - fd) < 1e-8

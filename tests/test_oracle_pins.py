@@ -38,6 +38,7 @@ BRUTE_CASES = [
     ([5, 1, 37, 0, 12], [5, 1, 37, 0, 12], 2, 16, ACT_SOFTMAX, 0, False),
     ([40, 3, 70], [7, 0, 19], 3, 8, ACT_SOFTMAX, 0, False),           # cross, empty KV
     ([40, 3, 70], [7, 1, 19], 2, 16, ACT_GELU_TANH, 0, True),         # GELU cross
+    ([40, 3, 70], [7, 0, 19], 2, 16, 2, 0, True),                     # SiLU cross, empty KV
     ([0, 9, 33], [4, 0, 33], 2, 8, ACT_GELU_TANH, 0, True),           # empty Q and empty KV
     ([32, 32], [150, 7], 2, 8, ACT_SOFTMAX, 0, False),                # PMA-like
     ([200, 64, 130], [200, 64, 130], 1, 8, ACT_SOFTMAX, 4, False),    # window, partial tail block
