@@ -55,8 +55,11 @@ extern "C" {
 #endif
 
 typedef enum {
-  GDPA_ACT_SOFTMAX = 0,   /* online softmax */
-  GDPA_ACT_GELU_TANH = 1  /* (1/Lkv) * sum gelu_tanh(s) v, ALU-only polynomial */
+  GDPA_ACT_SOFTMAX = 0,    /* online softmax */
+  GDPA_ACT_GELU_TANH = 1,  /* (1/Lkv) * sum gelu_tanh(s) v, ALU-only polynomial */
+  GDPA_ACT_SILU = 2        /* (1/Lkv) * sum silu(s) v, silu(x) = x sigma(x), the same ALU sigma
+                              (an alternative activation of GDPA: remio.ai commentary,
+                              model/system co-design section); no windows */
 } gdpa_act_t;
 
 typedef enum {
@@ -241,6 +244,7 @@ gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_k
 /*
  * gdpa_act_eval -- evaluates the kernel's device activation elementwise:
  * y[i] = gelu(x[i]) with the ALU-only polynomial (act = GDPA_ACT_GELU_TANH),
+ * y[i] = silu(x[i]) with the same ALU sigma (act = GDPA_ACT_SILU),
  * or y[i] = 2^x[i] with the exponential the softmax path uses
  * (act = GDPA_ACT_SOFTMAX).  x, y: device fp32 [n].  For accuracy tests;
  * GDPA_ERR_INVALID_ARG for any other act.

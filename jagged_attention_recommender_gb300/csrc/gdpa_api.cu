@@ -695,7 +695,7 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
 }
 
 extern "C" gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* stream) {
-  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH) return GDPA_ERR_INVALID_ARG;
+  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH && act != GDPA_ACT_SILU) return GDPA_ERR_INVALID_ARG;
   if (n < 0 || (n > 0 && (!x || !y))) return GDPA_ERR_INVALID_ARG;
   return launch_act_eval(act, x, y, n, stream);
 }

@@ -94,7 +94,8 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a) {
                        reinterpret_cast<uintptr_t>(a.dv);
   prm.align32 = (al & 31u) == 0 ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
-  const bool gelu = a.act == GDPA_ACT_GELU_TANH;
+  const bool gelu = a.act != GDPA_ACT_SOFTMAX;  // the ALU activations
+  alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
   if (a.D == 128)
     return gelu ? launch_bwd_d<128, kActGelu>(a, prm, s, device) : launch_bwd_d<128, kActSoftmax>(a, prm, s, device);
   if (a.D == 64)

@@ -60,6 +60,7 @@ struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   float score_scale;  // softmax: scale * log2(e); GELU: scale
   float scale;
   int align32;        // dq, dk and dv all 32-byte aligned: 32-byte stores allowed
+  float act_a, act_c; // ALU activations: folded constants (alu_act_consts)
 };
 
 template <int D>
@@ -385,7 +386,10 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
       dvr = __ldg(p.dvec + ri);
     }
     uint64_t gA2 = 0, gC2 = 0;
-    if (ACT == kActGelu) gelu_scale_consts(p.score_scale, gA2, gC2);
+    if (ACT == kActGelu) {
+      gA2 = ptx::f2_splat(p.act_a);
+      gC2 = ptx::f2_splat(p.act_c);
+    }
     const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
     for (int g = 0; g < n_kv && ok; ++g) {
@@ -484,7 +488,10 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC);  // [2 buffers][lse2, Dv][64]
     uint64_t gA2 = 0, gC2 = 0;
-    if (ACT == kActGelu) gelu_scale_consts(p.score_scale, gA2, gC2);
+    if (ACT == kActGelu) {
+      gA2 = ptx::f2_splat(p.act_a);
+      gC2 = ptx::f2_splat(p.act_c);
+    }
     const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
     for (int u = 0; u < n_q && ok; ++u) {

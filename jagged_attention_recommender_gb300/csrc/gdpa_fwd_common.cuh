@@ -27,8 +27,11 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   float score_scale;         // softmax: scale * log2(e); GELU: scale
   int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
   float* lse;                // optional [Tq, H]: softmax row logsumexp (natural log) for the backward
+  float act_a, act_c;        // ALU activations: folded constants (alu_act_consts)
 };
 
+// kActGelu instantiates the ALU activations (tanh-GELU and SiLU, told apart
+// by the constants act_a / act_c the launcher passes).
 enum : int { kActSoftmax = 0, kActGelu = 1 };
 
 enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatusEpilogue = 8 };

@@ -333,7 +333,10 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float sl = p.score_scale;
   uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
-  if (ACT == kActGelu) gelu_scale_consts(sl, gA2, gC2);
+  if (ACT == kActGelu) {  // the ALU activation's folded constants
+    gA2 = ptx::f2_splat(p.act_a);
+    gC2 = ptx::f2_splat(p.act_c);
+  }
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;

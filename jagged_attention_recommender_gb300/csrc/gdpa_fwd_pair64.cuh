@@ -346,7 +346,10 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
   const uint32_t o_addr = tmem + lane_off + C::tm_o(x);
   const float sl = p.score_scale;
   uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
-  if (ACT == kActGelu) gelu_scale_consts(sl, gA2, gC2);
+  if (ACT == kActGelu) {  // the ALU activation's folded constants
+    gA2 = ptx::f2_splat(p.act_a);
+    gC2 = ptx::f2_splat(p.act_c);
+  }
   const int H = p.H;
   uint32_t gx = 0;
   bool ok = true;

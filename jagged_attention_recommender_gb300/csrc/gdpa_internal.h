@@ -16,7 +16,7 @@ constexpr int kKeySplitRows = 32; // query rows of a key-split item
 
 inline gdpa_status_t validate_shape(int B, int H, int D, int act, int window_blocks) {
   if (B < 0 || H <= 0 || window_blocks < 0) return GDPA_ERR_INVALID_ARG;
-  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH) return GDPA_ERR_INVALID_ARG;
+  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH && act != GDPA_ACT_SILU) return GDPA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return GDPA_ERR_UNSUPPORTED;
   if (window_blocks > 0 && act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
   if ((int64_t)H * D > (1 << 20)) return GDPA_ERR_UNSUPPORTED;

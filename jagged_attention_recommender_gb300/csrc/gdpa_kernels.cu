@@ -122,7 +122,7 @@ gdpa_status_t launch_t(const FwdParams& prm, int grid, cudaStream_t stream, int 
 
 template <int D>
 gdpa_status_t launch_single(int act, int mode, const FwdParams& prm, int grid, cudaStream_t s, int device) {
-  const bool gelu = act == GDPA_ACT_GELU_TANH;
+  const bool gelu = act != GDPA_ACT_SOFTMAX;  // the ALU activations
   switch (mode) {
     case kModeFull:
       return gelu ? launch_t<D, kActGelu, kModeFull>(prm, grid, s, device)
@@ -149,10 +149,10 @@ gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, i
 __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
   for (int64_t i = 2 * (blockIdx.x * (int64_t)blockDim.x + threadIdx.x); i < n;
        i += 2 * (int64_t)gridDim.x * blockDim.x) {
-    if (act == kActGelu) {
-      float a, b;
-      uint64_t A2, C2;
-      gelu_scale_consts(1.0f, A2, C2);
+    if (act != kActSoftmax) {
+      float a, b, A, C;
+      alu_act_consts(act == GDPA_ACT_SILU, 1.0f, A, C);
+      const uint64_t A2 = ptx::f2_splat(A), C2 = ptx::f2_splat(C);
       gelu_tanh_alu2(x[i], i + 1 < n ? x[i + 1] : 0.0f, A2, C2, a, b);
       y[i] = a;
       if (i + 1 < n) y[i + 1] = b;
@@ -226,6 +226,7 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
   prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   prm.lse = a.lse;
+  alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks != 0;
   // sliding windows (window_blocks < 0) exist only in the 64-key pair kernel
@@ -237,26 +238,26 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
       return GDPA_ERR_UNSUPPORTED;
     }
     if (a.D == 128)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair64<128, kActGelu, false>(prm, a.num_ctas, s, device)
+      return a.act != GDPA_ACT_SOFTMAX ? launch_pair64<128, kActGelu, false>(prm, a.num_ctas, s, device)
                                          : launch_pair64<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
     if (a.D == 64)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair64<64, kActGelu, false>(prm, a.num_ctas, s, device)
+      return a.act != GDPA_ACT_SOFTMAX ? launch_pair64<64, kActGelu, false>(prm, a.num_ctas, s, device)
                                          : launch_pair64<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
     return GDPA_ERR_UNSUPPORTED;
   }
   if (a.rows_per_item == 256) {
     if (win) return GDPA_ERR_INVALID_ARG;  // windows take 64-key tiles
     if (a.D == 128)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<128, kActGelu, false>(prm, a.num_ctas, s, device)
+      return a.act != GDPA_ACT_SOFTMAX ? launch_pair<128, kActGelu, false>(prm, a.num_ctas, s, device)
                                          : launch_pair<128, kActSoftmax, false>(prm, a.num_ctas, s, device);
     if (a.D == 64)
-      return a.act == GDPA_ACT_GELU_TANH ? launch_pair<64, kActGelu, false>(prm, a.num_ctas, s, device)
+      return a.act != GDPA_ACT_SOFTMAX ? launch_pair<64, kActGelu, false>(prm, a.num_ctas, s, device)
                                          : launch_pair<64, kActSoftmax, false>(prm, a.num_ctas, s, device);
     return GDPA_ERR_UNSUPPORTED;
   }
   if (key_split) {
     if (win || a.D != 64) return GDPA_ERR_INVALID_ARG;
-    return a.act == GDPA_ACT_GELU_TANH ? launch_t<64, kActGelu, kModeKeySplit>(prm, a.num_ctas, s, device)
+    return a.act != GDPA_ACT_SOFTMAX ? launch_t<64, kActGelu, kModeKeySplit>(prm, a.num_ctas, s, device)
                                        : launch_t<64, kActSoftmax, kModeKeySplit>(prm, a.num_ctas, s, device);
   }
   if (a.rows_per_item != kBlockM) return GDPA_ERR_INVALID_ARG;
@@ -267,7 +268,7 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
 }
 
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream) {
-  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH) return GDPA_ERR_INVALID_ARG;
+  if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH && act != GDPA_ACT_SILU) return GDPA_ERR_INVALID_ARG;
   if (n <= 0) return GDPA_OK;
   const int threads = 256;
   const int64_t want = (n + threads - 1) / threads;

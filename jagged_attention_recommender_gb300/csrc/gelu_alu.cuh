@@ -1,5 +1,6 @@
-// gelu_alu.cuh -- tanh-GELU evaluated with FMA-pipe and integer instructions
-// only (no special-function-unit instruction).
+// gelu_alu.cuh -- tanh-GELU (and SiLU, x sigma(x), through the same sigma
+// with other constants) evaluated with FMA-pipe and integer instructions only
+// (no special-function-unit instruction).
 //
 // The GDPA section of the techfeed summary of "GEM Training" replaces the tanh
 // inside GELU, a special-function-unit bottleneck, by a 6th-order Taylor
@@ -118,11 +119,14 @@ __device__ __forceinline__ void gelu_tanh_grad_alu2(float s0, float s1, uint64_t
   ptx::f2_unpack(ptx::f2_fma(sig2, dz, sig), g0, g1);
 }
 
-// The folded-scale constants A and C of gelu_tanh_alu2, both lanes.
-__device__ __forceinline__ void gelu_scale_consts(float scale, uint64_t& A2, uint64_t& C2) {
-  const float A = 1.5957691216057308f * scale;  // 2 sqrt(2/pi) scale
-  A2 = ptx::f2_splat(A);
-  C2 = ptx::f2_splat(A * 0.044715f * scale * scale);
+// The folded constants of the ALU activations, for which the routines above
+// return y = s sigma(s (A + C s^2)) = act(scale s) / scale:
+//   tanh-GELU: A = 2 sqrt(2/pi) scale, C = 0.044715 A scale^2
+//   SiLU:      A = scale, C = 0           (silu(x) = x sigma(x))
+// gelu_tanh_grad_alu2 then returns act'(scale s) for either.
+__host__ __device__ inline void alu_act_consts(bool silu, float scale, float& A, float& C) {
+  A = silu ? scale : 1.5957691216057308f * scale;
+  C = silu ? 0.0f : A * 0.044715f * scale * scale;
 }
 
 }  // namespace gdpa

@@ -245,7 +245,9 @@ def gdpa_plan_enumerate(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, 
     return items[:n.value], cta, cost[:n.value]
 
 
-def gdpa_act_eval(act, x, y, stream=None):
+def gdpa_act_eval(act, x, y, *, stream=None):
+    """y = act(x) elementwise on the device (``stream`` keyword-only: a stray
+    positional argument must not be taken for a stream handle)."""
     _check(lib().gdpa_act_eval(int(act), _addr(x), _addr(y), int(x.numel()), _stream(stream)), "gdpa_act_eval")
 
 

@@ -19,7 +19,7 @@ import torch
 import oracle
 from jagged_attention_recommender_gb300 import build as gbuild, gdpa
 from jagged_attention_recommender_gb300.workloads import (
-    ACT_GELU_TANH, ACT_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_batch)
+    ACT_GELU_TANH, ACT_SILU, ACT_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_batch)
 from tests.helpers import bits, small_batch
 
 pytestmark = pytest.mark.gpu
@@ -133,6 +133,14 @@ def test_bwd_gelu(D):
     Lq = np.array([129, 33, 300, 0, 64])
     Lkv = np.array([40, 200, 8, 9, 128])
     check(small_batch(rng, Lq, Lkv, 2, D, act=ACT_GELU_TANH, qk_norm=True, scale=1.0), 6500 + D)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bwd_silu(D):
+    rng = np.random.default_rng(6450 + D)
+    Lq = np.array([129, 33, 300, 0, 64])
+    Lkv = np.array([40, 200, 8, 9, 128])
+    check(small_batch(rng, Lq, Lkv, 2, D, act=ACT_SILU, qk_norm=True, scale=1.0), 6550 + D)
 
 
 def test_bwd_zero_scale_and_negative_scale():

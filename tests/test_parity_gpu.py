@@ -18,7 +18,7 @@ import oracle
 from jagged_attention_recommender_gb300 import build as gbuild
 from jagged_attention_recommender_gb300 import gdpa
 from jagged_attention_recommender_gb300.workloads import (
-    ACT_GELU_TANH, ACT_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_batch)
+    ACT_GELU_TANH, ACT_SILU, ACT_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_batch)
 from tests.helpers import rel_l2, small_batch
 
 pytestmark = pytest.mark.gpu
@@ -137,6 +137,18 @@ def test_oracle_gelu_agrees_with_device_polynomial_on_grid():
     assert np.abs(ref32 - ref).max() < 1e-5
 
 
+def test_alu_silu_matches_oracle_on_grid():
+    # the kernels' SiLU: the GELU's sigma evaluation with A = 1, C = 0
+    x = np.linspace(-20.0, 20.0, 8001).astype(np.float32)
+    xd = torch.from_numpy(x).cuda()
+    y = torch.empty_like(xd)
+    gdpa.gdpa_act_eval(ACT_SILU, xd, y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    ref = np.array([oracle.silu(float(v)) for v in x])
+    assert np.abs(got - ref).max() <= 1e-5 * np.maximum(1.0, np.abs(ref)).max()
+
+
 # ------------------------------------------------------------------ small cases, element by element
 
 SMALL = {
@@ -185,6 +197,21 @@ def test_cross_softmax_long_kv(D):
     Lkv = np.array([1000, 129, 4100, 0])
     b = small_batch(rng, Lq, Lkv, 3, D)
     assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "pma-like D=%d" % D)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_silu_cross_and_self(D):
+    rng = np.random.default_rng(2500 + D)
+    for Lq, Lkv in ((np.array([1, 129, 300, 0, 64, 77, 128]), np.array([0, 1, 8, 5, 64, 65, 300])),
+                    (np.array([300, 257, 129, 500]), np.array([300, 257, 129, 500]))):
+        b = small_batch(rng, Lq, Lkv, 2, D, act=ACT_SILU, qk_norm=True, scale=1.0)
+        assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "silu D=%d" % D, bf16_scaled=True)
+
+
+def test_silu_key_split():
+    rng = np.random.default_rng(2600)
+    b = small_batch(rng, np.array(KS_LQ), np.array(KS_LKV), 2, 64, act=ACT_SILU, qk_norm=True, scale=1.0)
+    assert_parity(run_gpu(b, guard_rows=3), oracle.gdpa_fwd_batch(b), "silu key split", bf16_scaled=True)
 
 
 # Short key ranges (every sequence at most 64 keys, one partial K/V tile):
