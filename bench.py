@@ -52,9 +52,10 @@ RECIPES = {
     "pma": "B=256 H=8 D=64, 32 shared seed queries per sample, Lkv=clip(round(lognormal(7.6,1.0)),100,16384), softmax",
     "block_window": "B=64 H=4 D=128, L=64*U{8..512}, 64-token blocks, window 4 blocks (own causal + 3 previous), softmax",
     "sliding_window": "B=64 H=4 D=128, L~U{512..32768}, causal sliding window of 256 tokens, softmax",
+    "cross_silu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, SiLU (ALU), scale=1, /Lkv",
 }
 BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm",
-         "sliding_window": "hbm"}
+         "sliding_window": "hbm", "cross_silu": "hbm"}
 
 
 def parse_args():

@@ -154,8 +154,9 @@ gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const void* v, cons
  * may be NULL for GELU); offsets twice, host (h_*, read during the call) and
  * device, as gdpa_fwd_async; dq: device bf16 [Tq, H, D]; dk, dv: device bf16
  * [Tkv, H, D]; all written in full (keys no query sees get zero gradients).
- * Tensors 16-byte aligned.  Full attention only: window_blocks > 0 returns
- * GDPA_ERR_UNSUPPORTED.  Asynchronous on `stream`; the library keeps a
+ * Tensors 16-byte aligned.  window_blocks > 0 (block windows, softmax, self
+ * attention) as in the forward: each query row's gradient runs over its
+ * window only.  Asynchronous on `stream`; the library keeps a
  * grow-only device buffer for the work lists and 8 Tq H bytes of scratch.
  * Errors as gdpa_fwd (a wait that runs out shows in gdpa_device_status).
  */
@@ -163,6 +164,17 @@ gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* 
                        const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
                        const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
                        int window_blocks, float scale, void* dq, void* dk, void* dv, void* stream);
+
+/*
+ * gdpa_bwd_sliding -- gdpa_bwd for the causal sliding window of
+ * window_tokens tokens (the forward of gdpa_fwd_sliding, whose out and lse
+ * it takes).  Softmax only, self attention, window_tokens >= 1; everything
+ * else as gdpa_bwd.
+ */
+gdpa_status_t gdpa_bwd_sliding(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                               const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                               const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                               int window_tokens, float scale, void* dq, void* dk, void* dv, void* stream);
 
 /*
  * gdpa_fwd_noalloc -- gdpa_fwd for callers that must not allocate memory.

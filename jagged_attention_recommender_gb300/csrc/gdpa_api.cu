@@ -332,16 +332,19 @@ extern "C" gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const vo
                         scale, out, lse, stream);
 }
 
-extern "C" gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
-                                  const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
-                                  const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
-                                  int window_blocks, float scale, void* dq, void* dk, void* dv, void* stream) {
-  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
-  if (st != GDPA_OK) return st;
-  if (window_blocks > 0) return GDPA_ERR_UNSUPPORTED;
+namespace gdpa {
+namespace {
+
+// The backward with the internal window code (0 full, > 0 block window,
+// < 0 sliding window of -window tokens); shape already validated.
+gdpa_status_t bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                       const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                       const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act, int window,
+                       float scale, void* dq, void* dk, void* dv, void* stream) {
+  gdpa_status_t st;
   if (B == 0) return GDPA_OK;
   int64_t Tq = 0, Tkv = 0;
-  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, 0, &Tq, &Tkv)) != GDPA_OK) return st;
+  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window, &Tq, &Tkv)) != GDPA_OK) return st;
   if (Tq >= (int64_t)1 << 31 || Tkv >= (int64_t)1 << 31) return GDPA_ERR_UNSUPPORTED;
   if (Tq > 0 && (!q || !dq || !aligned16(q) || !aligned16(dq))) return GDPA_ERR_INVALID_ARG;
   if (Tq > 0 && Tkv > 0 && (!out || !dout || !aligned16(out) || !aligned16(dout))) return GDPA_ERR_INVALID_ARG;
@@ -403,10 +406,36 @@ extern "C" gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, c
   a.H = H;
   a.D = D;
   a.act = act;
+  a.window = window;
   a.scale = scale;
   a.stream = stream;
   if ((st = launch_backward(a)) != GDPA_OK) return st;
   return cudaEventRecord(c.bwd_free, s) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdpa
+
+extern "C" gdpa_status_t gdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                  const float* lse, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                                  const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                                  int window_blocks, float scale, void* dq, void* dk, void* dv, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  return bwd_impl(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act,
+                  window_blocks, scale, dq, dk, dv, stream);
+}
+
+extern "C" gdpa_status_t gdpa_bwd_sliding(const void* q, const void* k, const void* v, const void* out,
+                                          const void* dout, const float* lse, const int32_t* h_q_offsets,
+                                          const int32_t* h_kv_offsets, const int32_t* q_offsets,
+                                          const int32_t* kv_offsets, int B, int H, int D, int act, int window_tokens,
+                                          float scale, void* dq, void* dk, void* dv, void* stream) {
+  if (window_tokens < 1) return GDPA_ERR_INVALID_ARG;
+  gdpa_status_t st = validate_shape(B, H, D, act, 1);  // as a window: softmax only
+  if (st != GDPA_OK) return st;
+  return bwd_impl(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act,
+                  -window_tokens, scale, dq, dk, dv, stream);
 }
 
 extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,

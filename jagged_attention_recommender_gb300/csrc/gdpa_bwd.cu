@@ -88,6 +88,7 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a) {
   prm.status = status;
   prm.timeout_ns = bounded_wait_ns();
   prm.H = a.H;
+  prm.window = a.window;
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
   prm.scale = a.scale;
   const uintptr_t al = reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |

@@ -61,7 +61,26 @@ struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   float scale;
   int align32;        // dq, dk and dv all 32-byte aligned: 32-byte stores allowed
   float act_a, act_c; // ALU activations: folded constants (alu_act_consts)
+  int window;         // 0 full; > 0 block window of that many 64-token blocks;
+                      // < 0 causal sliding window of -window tokens (self attention)
 };
+
+// First key of query i's window (both counted from the sequence start).
+__device__ __forceinline__ int win_key_lo(int i, int window) {
+  if (window > 0) {
+    const int blk = (i >> 6) - (window - 1);
+    return blk > 0 ? blk << 6 : 0;
+  }
+  const int lo = i + window + 1;  // i - W + 1
+  return lo > 0 ? lo : 0;
+}
+
+// Last query whose window holds key j: its window starts at or before j.
+__device__ __forceinline__ int win_query_hi(int j, int window) {
+  const long long hi = window > 0 ? (static_cast<long long>(j >> 6) + window) * 64 - 1  // block of j plus W - 1 blocks
+                                  : static_cast<long long>(j) - window - 1;           // j + W - 1
+  return hi < 0x7fffffffLL ? static_cast<int>(hi) : 0x7fffffff;
+}
 
 template <int D>
 struct BwdCfg {
@@ -264,11 +283,13 @@ __device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tm
 
 // 32 columns of S and dP (one chunk) -> 16 packed bf16 words of P and of dS.
 // lse2/dv: per column (dkdv: one value per query) or per row (dq: the same
-// value in every column); `nvalid`: columns >= nvalid get P = dS = 0.
+// value in every column); columns outside [c_lo, c_hi] (tile-relative: the
+// tile's ragged end, the window, or every column of a row past the end) get
+// P = dS = 0.
 template <int ACT, bool PER_COL>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2c,
-                                          const float* dvc, float lse2r, float dvr, int c0, int nvalid,
-                                          bool row_ok, float sl, float inv_l, uint64_t gA2, uint64_t gC2,
+                                          const float* dvc, float lse2r, float dvr, int c0, int c_lo, int c_hi,
+                                          float sl, float inv_l, uint64_t gA2, uint64_t gC2,
                                           uint32_t (&pk_p)[16], uint32_t (&pk_ds)[16]) {
 #pragma unroll
   for (int u = 0; u < 16; ++u) {
@@ -297,7 +318,7 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
       g0 *= d0 * inv_l;
       g1 *= d1 * inv_l;
     }
-    const bool ok0 = row_ok && c0 + c < nvalid, ok1 = row_ok && c0 + c + 1 < nvalid;
+    const bool ok0 = c0 + c >= c_lo && c0 + c <= c_hi, ok1 = c0 + c + 1 >= c_lo && c0 + c + 1 <= c_hi;
     pk_p[u] = ptx::pack_bf16x2(ok0 ? p0 : 0.0f, ok1 ? p1 : 0.0f);
     pk_ds[u] = ptx::pack_bf16x2(ok0 ? g0 : 0.0f, ok1 ? g1 : 0.0f);
   }
@@ -338,7 +359,14 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdItem t = bwd_item(p);
   const int rows = min(128, t.Lq - t.row0);
-  const int n_kv = (t.Lkv + C::BN - 1) / C::BN;
+  // keys the item's rows may see: all, or from the first row's window start
+  // (rounded down to a 64-key tile) to the last row (causal)
+  int kv_lo = 0, kv_hi = t.Lkv;
+  if (p.window != 0) {
+    kv_lo = win_key_lo(t.row0, p.window) / C::BN * C::BN;
+    kv_hi = min(t.Lkv, t.row0 + 128);
+  }
+  const int n_kv = kv_hi > kv_lo ? (kv_hi - kv_lo + C::BN - 1) / C::BN : 0;
   if (n_kv == 0) {  // no keys: no gradient reaches these queries
     if (warp >= 2) {
       const int row = ((warp & 3) << 5) + lane;
@@ -371,9 +399,9 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   volatile int* abort = &B.abort;
   if (warp == 0) {
     if (lane == 0)
-      bwd_producer<D>(p, sm, B, t.h, &p.tm_q, &p.tm_do, t.q_tok + t.row0, &p.tm_k, &p.tm_v, t.kv_tok, n_kv);
+      bwd_producer<D>(p, sm, B, t.h, &p.tm_q, &p.tm_do, t.q_tok + t.row0, &p.tm_k, &p.tm_v, t.kv_tok + kv_lo, n_kv);
   } else if (warp == 1) {
-    bwd_mma<D, false>(p, sm, B, tmem, n_kv, t.Lkv);
+    bwd_mma<D, false>(p, sm, B, tmem, n_kv, kv_hi - kv_lo);
   } else {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -398,16 +426,23 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int ncols = min(C::BN, t.Lkv - C::BN * g);
+      const int kv_t0 = kv_lo + C::BN * g;
+      const int ncols = min(C::BN, kv_hi - kv_t0);
       const int nch = (ncols + 31) >> 5;
+      int c_lo = 0, c_hi = row_ok ? ncols - 1 : -1;  // this row's valid columns of the tile
+      if (p.window != 0 && row_ok) {
+        const int i = t.row0 + row;
+        c_lo = win_key_lo(i, p.window) - kv_t0;
+        c_hi = min(c_hi, i - kv_t0);
+      }
       for (int ch = 0; ch < nch; ++ch) {
         uint32_t sr[32], dr[32];
         ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
         ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
         ptx::tmem_wait_ld();
         uint32_t pk_p[16], pk_ds[16];
-        bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, ncols, row_ok, p.score_scale, inv_l,
-                              gA2, gC2, pk_p, pk_ds);
+        bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, c_lo, c_hi, p.score_scale, inv_l, gA2,
+                              gC2, pk_p, pk_ds);
         ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_ds);  // dS over consumed S columns
       }
       ptx::tmem_wait_st();
@@ -440,7 +475,14 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdItem t = bwd_item(p);
   const int keys = min(128, t.Lkv - t.row0);
-  const int n_q = (t.Lq + C::BN - 1) / C::BN;
+  // queries that may see the item's keys: all, or from the first key (causal)
+  // to the last query whose window holds the item's last key
+  int q_lo = 0, q_hi = t.Lq;
+  if (p.window != 0) {
+    q_lo = t.row0;
+    q_hi = min(t.Lq, win_query_hi(t.row0 + keys - 1, p.window) + 1);
+  }
+  const int n_q = q_hi > q_lo ? (q_hi - q_lo + C::BN - 1) / C::BN : 0;
   if (n_q == 0) {  // no queries: these keys receive no gradient
     if (warp >= 2) {
       const int row = ((warp & 3) << 5) + lane;
@@ -478,9 +520,9 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
   volatile int* abort = &B.abort;
   if (warp == 0) {
     if (lane == 0)
-      bwd_producer<D>(p, sm, B, t.h, &p.tm_k, &p.tm_v, t.kv_tok + t.row0, &p.tm_q, &p.tm_do, t.q_tok, n_q);
+      bwd_producer<D>(p, sm, B, t.h, &p.tm_k, &p.tm_v, t.kv_tok + t.row0, &p.tm_q, &p.tm_do, t.q_tok + q_lo, n_q);
   } else if (warp == 1) {
-    bwd_mma<D, true>(p, sm, B, tmem, n_q, t.Lq);
+    bwd_mma<D, true>(p, sm, B, tmem, n_q, q_hi - q_lo);
   } else {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row of the item
@@ -494,8 +536,11 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
     }
     const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
+    const int j = t.row0 + row;  // this thread's key, counted from the sequence start
+    const int j_qhi = p.window != 0 ? win_query_hi(j, p.window) : 0x7fffffff;
     for (int u = 0; u < n_q && ok; ++u) {
-      const int nq = min(C::BN, t.Lq - C::BN * u);
+      const int u0 = q_lo + C::BN * u;  // the tile's first query
+      const int nq = min(C::BN, q_hi - u0);
       const int b = u & 1;
       float* vb = vec + b * 2 * C::BN;
       if (ACT == kActSoftmax) {
@@ -505,7 +550,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
         if (tid < C::BN) {
           float l = 0.0f, d = 0.0f;
           if (tid < nq) {
-            const size_t qi = static_cast<size_t>(t.q_tok + C::BN * u + tid) * p.H + t.h;
+            const size_t qi = static_cast<size_t>(t.q_tok + u0 + tid) * p.H + t.h;
             l = __ldg(p.lse2 + qi);
             d = __ldg(p.dvec + qi);
           }
@@ -520,13 +565,18 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
       if (!ok) break;
       ptx::tc_fence_after();
       const int nch = (nq + 31) >> 5;
+      int c_lo = 0, c_hi = nq - 1;  // this key row's valid query columns of the tile
+      if (p.window != 0) {
+        c_lo = j - u0;
+        c_hi = min(c_hi, j_qhi - u0);
+      }
       for (int ch = 0; ch < nch; ++ch) {
         uint32_t sr[32], dr[32];
         ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
         ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
         ptx::tmem_wait_ld();
         uint32_t pk_p[16], pk_ds[16];
-        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, nq, true,
+        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, c_lo, c_hi,
                              p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
         ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_p);   // P^T over consumed S^T columns
         ptx::tmem_st16(tmem + lane_off + C::tm_p(b) + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns

@@ -97,6 +97,7 @@ struct BwdLaunchArgs {
   void *dq, *dk, *dv;
   int64_t Tq, Tkv;
   int H, D, act;
+  int window;             // 0 full; > 0 block window (blocks); < 0 sliding window (-tokens)
   float scale;
   void* stream;
 };

@@ -27,7 +27,7 @@ GDPA_ERR_DEVICE_TIMEOUT = 4
 GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
-EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
            "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_fwd_lse.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
     L.gdpa_fwd_sliding.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
     L.gdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
+    L.gdpa_bwd_sliding.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
     L.gdpa_fwd_planned.argtypes = [P, P, P, P, P, P, F, P, P]
     L.gdpa_plan_destroy.argtypes = [P]
@@ -77,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_status_string.restype = ctypes.c_char_p
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
-    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
+    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
                  "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
@@ -164,6 +165,16 @@ def gdpa_bwd(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_o
                           ko.ctypes.data, _addr(q_offsets), _addr(kv_offsets), int(B), int(H), int(D), int(act),
                           int(window_blocks), float(scale), _addr(dq), _addr(dk), _addr(dv), _stream(stream)),
            "gdpa_bwd")
+
+
+def gdpa_bwd_sliding(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act,
+                     window_tokens, scale, dq, dk, dv, stream=None):
+    """gdpa_bwd for the causal sliding window of ``window_tokens`` tokens."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    _check(lib().gdpa_bwd_sliding(_addr(q), _addr(k), _addr(v), _addr(out), _addr(dout), _addr(lse), qo.ctypes.data,
+                                  ko.ctypes.data, _addr(q_offsets), _addr(kv_offsets), int(B), int(H), int(D),
+                                  int(act), int(window_tokens), float(scale), _addr(dq), _addr(dk), _addr(dv),
+                                  _stream(stream)), "gdpa_bwd_sliding")
 
 
 class Plan:

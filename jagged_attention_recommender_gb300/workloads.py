@@ -27,6 +27,7 @@ block_window    B=64, H=4, D=128, L = 64 * U{8..512}; window of 4 blocks of 64
                 (own block causal + 3 previous); softmax; scale 1/sqrt(D)
 sliding_window  B=64, H=4, D=128, L ~ U{512..32768}; causal sliding window of
                 256 tokens (window_blocks = -256); softmax; scale 1/sqrt(D)
+cross_silu      cross_gelu's shapes and QK-norm with SiLU instead of GELU
 ==============  ====================================================================
 
 Draw order (fixed): lengths first, then one 63-bit sub-seed per value tensor
@@ -71,6 +72,7 @@ WORKLOADS = {
     "cross_gelu": Workload("cross_gelu", 2, 512, 4, 128, ACT_GELU_TANH, 0, 1.0, "cross"),
     "pma": Workload("pma", 3, 256, 8, 64, ACT_SOFTMAX, 0, 1.0 / math.sqrt(64), "pma"),
     "block_window": Workload("block_window", 4, 64, 4, 128, ACT_SOFTMAX, 4, 1.0 / math.sqrt(128), "window"),
+    "cross_silu": Workload("cross_silu", 6, 512, 4, 128, ACT_SILU, 0, 1.0, "cross"),
     # window_blocks < 0: a causal sliding window of -window_blocks tokens
     "sliding_window": Workload("sliding_window", 5, 64, 4, 128, ACT_SOFTMAX, -256, 1.0 / math.sqrt(128), "window"),
 }
@@ -99,7 +101,7 @@ def draw_lengths(w: Workload, rng: np.random.Generator, B: int | None = None):
     if w.name == "self_long":
         L = np.clip(np.round(rng.lognormal(6.9, 0.8, size=B)), 100, 4096).astype(np.int64)
         return L, L
-    if w.name == "cross_gelu":
+    if w.name in ("cross_gelu", "cross_silu"):
         Lq = rng.integers(256, 4096, size=B, endpoint=True)
         Lkv = rng.integers(8, 64, size=B, endpoint=True)
         return Lq, Lkv
