@@ -433,8 +433,6 @@ def run_backward(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = WORKLOADS[args.workload]
-    if w.window_blocks > 0:
-        raise SystemExit("the backward covers full attention only")
     batch = make_batch(args.workload, seed=w.seed + 1000 * rank)
     flops = 2.5 * useful_flops(batch)
     nbytes = backward_bytes(batch)
@@ -456,10 +454,18 @@ def run_backward(args, rank, world, local):
     dv = torch.empty_like(dk)
     h_qo, h_ko = batch.q_offsets, batch.kv_offsets
     stream = torch.cuda.current_stream()
-    gdpa.gdpa_fwd_lse(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, 0, w.scale, out, lse, stream)
+    if w.window_blocks < 0:  # sliding window of -window_blocks tokens
+        gdpa.gdpa_fwd_sliding(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, -w.window_blocks, w.scale, out, lse, stream)
+    else:
+        gdpa.gdpa_fwd_lse(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, out, lse, stream)
 
     def step():
-        gdpa.gdpa_bwd(q, k, v, out, dout, lse, h_qo, h_ko, qo, ko, B, H, D, w.act, 0, w.scale, dq, dk, dv, stream)
+        if w.window_blocks < 0:
+            gdpa.gdpa_bwd_sliding(q, k, v, out, dout, lse, h_qo, h_ko, qo, ko, B, H, D, w.act, -w.window_blocks,
+                                  w.scale, dq, dk, dv, stream)
+        else:
+            gdpa.gdpa_bwd(q, k, v, out, dout, lse, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, dq,
+                          dk, dv, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
