@@ -18,11 +18,18 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Persistent: one CTA per SM (or per item, if fewer), each taking every
+// grid-th item of the list.
 template <typename Kernel>
-gdpa_status_t launch_bwd_kernel(Kernel kernel, int smem, const BwdParams& prm, int64_t grid, cudaStream_t stream,
+gdpa_status_t launch_bwd_kernel(Kernel kernel, int smem, BwdParams& prm, int64_t n_items, cudaStream_t stream,
                                 int device, bool* attr_done, std::mutex* mu) {
-  if (grid <= 0) return GDPA_OK;
-  if (grid > 0x7fffffffLL) return GDPA_ERR_UNSUPPORTED;
+  if (n_items <= 0) return GDPA_OK;
+  if (n_items > 0x7fffffffLL) return GDPA_ERR_UNSUPPORTED;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
+    return GDPA_ERR_CUDA;
+  prm.n_items = static_cast<int>(n_items);
+  const int64_t grid = n_items < sms ? n_items : sms;
   {
     std::lock_guard<std::mutex> lock(*mu);
     if (!attr_done[device]) {

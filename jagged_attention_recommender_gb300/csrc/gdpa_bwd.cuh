@@ -63,6 +63,7 @@ struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   float act_a, act_c; // ALU activations: folded constants (alu_act_consts)
   int window;         // 0 full; > 0 block window of that many 64-token blocks;
                       // < 0 causal sliding window of -window tokens (self attention)
+  int n_items;        // items in `items`; a persistent CTA takes every gridDim.x-th
 };
 
 // First key of query i's window (both counted from the sequence start).
@@ -91,9 +92,10 @@ struct BwdCfg {
   static constexpr int RTILE = KCH * RCHUNK;            // resident: 128 rows x D
   static constexpr int SCHUNK = BN * 128;               // streamed: 64 rows x 64 bf16 columns
   static constexpr int STILE = KCH * SCHUNK;            // streamed: 64 rows x D
-  static constexpr int OFF_R1 = 0;                      // resident: Q (dq) or K (dkdv)
-  static constexpr int OFF_R2 = OFF_R1 + RTILE;         // resident: dO (dq) or V (dkdv)
-  static constexpr int OFF_S1 = OFF_R2 + RTILE;         // streamed stages: K (dq) or Q (dkdv)
+  // resident tiles, two buffers (the next item's load overlaps this one):
+  // buffer b holds R1 (Q for dq, K for dkdv) and R2 (dO, or V)
+  __host__ __device__ static constexpr int off_r(int b, int which) { return (2 * b + which) * RTILE; }
+  static constexpr int OFF_S1 = 4 * RTILE;              // streamed stages: K (dq) or Q (dkdv)
   static constexpr int OFF_S2 = OFF_S1 + NS * STILE;    // streamed stages: V (dq) or dO (dkdv)
   static constexpr int OFF_VEC = OFF_S2 + NS * STILE;   // dkdv: lse2 and Dv of a query tile, 2 buffers
   static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
@@ -110,12 +112,14 @@ struct BwdCfg {
 };
 
 struct BwdBars {
-  uint64_t res_full;                 // the item's resident tiles landed
-  uint64_t st_full[3], st_empty[3];  // streamed stages
-  uint64_t mma_full[2];              // S and dP of a tile are in TMEM buffer b
-  uint64_t act_full[2];              // P / dS of a tile are in TMEM buffer b
-  uint64_t acc_full;                 // every MMA of the item completed
-  uint64_t vec_full[2];              // dkdv: lse2 / Dv of a query tile staged by the activation warps
+  uint64_t res_full[2], res_empty[2];  // resident buffers
+  uint64_t st_full[3], st_empty[3];    // streamed stages
+  uint64_t mma_full[2];                // S and dP of a tile are in TMEM buffer b
+  uint64_t act_full[2];                // P / dS of a tile are in TMEM buffer b
+  uint64_t acc_full;                   // an item's accumulating MMAs completed
+  uint64_t acc_empty;                  // the epilogue has read the accumulators
+  uint64_t vec_full[2];                // dkdv: lse2 / Dv of a query tile staged by the activation warps
+  uint64_t drain;                      // every MMA of the CTA completed
   uint32_t tmem_slot;
   int abort;
 };
@@ -126,13 +130,13 @@ __device__ __forceinline__ void bwd_failure(const BwdParams& p, volatile int* ab
   atomicOr(p.status, bit);
 }
 
-// The item's sequence geometry.
+// An item's sequence geometry.
 struct BwdItem {
   int b, h, row0, q_tok, kv_tok, Lq, Lkv;
 };
 
-__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
-  const int4 it = __ldg(p.items + blockIdx.x);
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int idx) {
+  const int4 it = __ldg(p.items + idx);
   BwdItem t;
   t.b = it.x;
   t.h = it.y;
@@ -144,70 +148,125 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
   return t;
 }
 
+// The streamed range of an item: dq streams the keys its rows may see, dk/dv
+// the queries that may see its keys (all of them, or the window's).
+struct BwdWork {
+  int r_row;  // first resident row (token index)
+  int s_row;  // first streamed row (token index)
+  int lo;     // first streamed row within the sequence
+  int len;    // streamed rows
+  int n;      // streamed 64-row tiles
+};
+
+template <bool DKDV>
+__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p, const BwdItem& t) {
+  BwdWork w;
+  int lo, hi;
+  if (!DKDV) {  // keys: all, or from the first row's window start (64-key tile) to the last row
+    lo = 0;
+    hi = t.Lkv;
+    if (p.window != 0) {
+      lo = win_key_lo(t.row0, p.window) / 64 * 64;
+      hi = min(t.Lkv, t.row0 + 128);
+    }
+    w.r_row = t.q_tok + t.row0;
+    w.s_row = t.kv_tok + lo;
+  } else {  // queries: all, or from the first key to the last query whose window holds the last key
+    lo = 0;
+    hi = t.Lq;
+    if (p.window != 0) {
+      lo = t.row0;
+      hi = min(t.Lq, win_query_hi(t.row0 + min(128, t.Lkv - t.row0) - 1, p.window) + 1);
+    }
+    w.r_row = t.kv_tok + t.row0;
+    w.s_row = t.q_tok + lo;
+  }
+  w.lo = lo;
+  w.len = hi > lo ? hi - lo : 0;
+  w.n = (w.len + 63) / 64;
+  return w;
+}
+
 // ------------------------------------------------------------------ producer
 
-// Loads the two resident 128-row tiles at rows r_row (maps r1, r2, boxes of
-// 64 rows), then n 64-row tiles of the two streamed maps at rows
-// s_row + 64 t into the stages.
-template <int D>
-__device__ void bwd_producer(const BwdParams& p, uint8_t* sm, BwdBars& B, int h, const CUtensorMap* r1,
-                             const CUtensorMap* r2, int r_row, const CUtensorMap* s1, const CUtensorMap* s2,
-                             int s_row, int n) {
+// Walks the CTA's items (blockIdx.x, + gridDim.x, ...) that have work: the
+// two resident 128-row tiles of item k into buffer k & 1 (boxes of 64 rows),
+// then its streamed 64-row tiles into the stages (a counter across items).
+template <int D, bool DKDV>
+__device__ void bwd_producer(const BwdParams& p, uint8_t* sm, BwdBars& B, int n_items) {
   using C = BwdCfg<D>;
   volatile int* abort = &B.abort;
-  ptx::mbar_arrive_expect_tx(&B.res_full, 2 * C::RTILE);
-#pragma unroll
-  for (int c = 0; c < C::KCH; ++c)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int off = c * C::RCHUNK + half * C::SCHUNK;  // rows 64 half .. +63 of the chunk
-      ptx::tma_load_2d(sm + C::OFF_R1 + off, r1, &B.res_full, h * D + 64 * c, r_row + 64 * half);
-      ptx::tma_load_2d(sm + C::OFF_R2 + off, r2, &B.res_full, h * D + 64 * c, r_row + 64 * half);
-    }
-  int armed[C::NS];
-  for (int s = 0; s < C::NS; ++s) armed[s] = -1;
+  const CUtensorMap* r1 = DKDV ? &p.tm_k : &p.tm_q;
+  const CUtensorMap* r2 = DKDV ? &p.tm_v : &p.tm_do;
+  const CUtensorMap* s1 = DKDV ? &p.tm_q : &p.tm_k;
+  const CUtensorMap* s2 = DKDV ? &p.tm_do : &p.tm_v;
+  int res_armed[2] = {-1, -1}, st_armed[C::NS];
+  for (int s = 0; s < C::NS; ++s) st_armed[s] = -1;
   bool ok = true;
-  for (int t = 0; t < n; ++t) {
-    const int s = t % C::NS;
-    const uint32_t ph = (t / C::NS) & 1;
-    ok = ptx::mbar_wait(&B.st_empty[s], ph ^ 1, p.timeout_ns, abort);
+  uint32_t k = 0, gt = 0;
+  for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    const BwdItem t = bwd_item(p, idx);
+    const BwdWork w = bwd_work<DKDV>(p, t);
+    if (w.n == 0) continue;
+    const int rb = k & 1;
+    const uint32_t rph = (k >> 1) & 1;
+    ok = ptx::mbar_wait(&B.res_empty[rb], rph ^ 1, p.timeout_ns, abort);
     if (!ok) break;
-    ptx::mbar_arrive_expect_tx(&B.st_full[s], 2 * C::STILE);
-    armed[s] = (int)ph;
+    ptx::mbar_arrive_expect_tx(&B.res_full[rb], 2 * C::RTILE);
+    res_armed[rb] = (int)rph;
 #pragma unroll
-    for (int c = 0; c < C::KCH; ++c) {
-      ptx::tma_load_2d(sm + C::OFF_S1 + s * C::STILE + c * C::SCHUNK, s1, &B.st_full[s], h * D + 64 * c,
-                       s_row + C::BN * t);
-      ptx::tma_load_2d(sm + C::OFF_S2 + s * C::STILE + c * C::SCHUNK, s2, &B.st_full[s], h * D + 64 * c,
-                       s_row + C::BN * t);
+    for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int off = c * C::RCHUNK + half * C::SCHUNK;  // rows 64 half .. +63 of the chunk
+        ptx::tma_load_2d(sm + C::off_r(rb, 0) + off, r1, &B.res_full[rb], t.h * D + 64 * c, w.r_row + 64 * half);
+        ptx::tma_load_2d(sm + C::off_r(rb, 1) + off, r2, &B.res_full[rb], t.h * D + 64 * c, w.r_row + 64 * half);
+      }
+    for (int j = 0; j < w.n; ++j, ++gt) {
+      const int s = gt % C::NS;
+      const uint32_t ph = (gt / C::NS) & 1;
+      ok = ptx::mbar_wait(&B.st_empty[s], ph ^ 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::mbar_arrive_expect_tx(&B.st_full[s], 2 * C::STILE);
+      st_armed[s] = (int)ph;
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) {
+        ptx::tma_load_2d(sm + C::OFF_S1 + s * C::STILE + c * C::SCHUNK, s1, &B.st_full[s], t.h * D + 64 * c,
+                         w.s_row + C::BN * j);
+        ptx::tma_load_2d(sm + C::OFF_S2 + s * C::STILE + c * C::SCHUNK, s2, &B.st_full[s], t.h * D + 64 * c,
+                         w.s_row + C::BN * j);
+      }
     }
+    ++k;
   }
   if (!ok) bwd_failure(p, abort, kStatusProducer);
   // no copy may be in flight when the CTA exits
   const int never = 0;
   const unsigned long long drain_ns = 100000000ull;
-  ptx::mbar_wait(&B.res_full, 0, drain_ns, &never);
+  for (int b = 0; b < 2; ++b)
+    if (res_armed[b] >= 0) ptx::mbar_wait(&B.res_full[b], (uint32_t)res_armed[b], drain_ns, &never);
   for (int s = 0; s < C::NS; ++s)
-    if (armed[s] >= 0) ptx::mbar_wait(&B.st_full[s], (uint32_t)armed[s], drain_ns, &never);
+    if (st_armed[s] >= 0) ptx::mbar_wait(&B.st_full[s], (uint32_t)st_armed[s], drain_ns, &never);
 }
 
 // ------------------------------------------------------------------ MMA issuer (whole warp)
 
-// S (or S^T) = R1 S1^T and dP (or dP^T) = R2 S2^T for streamed tile t into
-// TMEM buffer t & 1, both operands K-major; `len` rows in all, so the last
-// tile may be partial.
+// S (or S^T) = R1 S1^T and dP (or dP^T) = R2 S2^T for streamed tile gt (the
+// CTA's tile counter; t-th tile of its item, `len` streamed rows in all)
+// into TMEM buffer gt & 1, both operands K-major.
 template <int D>
-__device__ __forceinline__ bool bwd_issue_sdp(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int t,
-                                              int len, uint64_t r1, uint64_t r2, volatile int* abort) {
+__device__ __forceinline__ bool bwd_issue_sdp(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem,
+                                              uint32_t gt, int t, int len, uint64_t r1, uint64_t r2,
+                                              volatile int* abort) {
   using C = BwdCfg<D>;
-  const int s = t % C::NS;
-  if (!ptx::mbar_wait(&B.st_full[s], (t / C::NS) & 1, p.timeout_ns, abort)) return false;
+  const int s = gt % C::NS;
+  if (!ptx::mbar_wait(&B.st_full[s], (gt / C::NS) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
   const int n16 = (min(C::BN, len - C::BN * t) + 15) >> 4;
   const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
   const uint64_t s1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_S1 + s * C::STILE), 16, 1024);
   const uint64_t s2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_S2 + s * C::STILE), 16, 1024);
-  const int b = t & 1;
+  const int b = gt & 1;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {  // K-dimension D, 16 per MMA
     const uint32_t off_r = ((kk >> 2) * C::RCHUNK + (kk & 3) * 32) >> 4;
@@ -224,59 +283,74 @@ __device__ __forceinline__ bool bwd_issue_sdp(const BwdParams& p, uint8_t* sm, B
   return true;
 }
 
-// Per streamed tile t: S, dP of tile t+1 first (look-ahead), then, once the
-// activation has written its bf16 operands over tile t's S and dP, the
-// accumulating MMAs with the operand from tensor memory and the streamed
-// tile read MN-major (16 rows per MMA): dQ += dS K, or dV += P^T dO and
-// dK += dS^T Q.  S/dP of tile t+2 reuse tile t's buffer only after these
-// (the tensor core runs one thread's MMAs in order).
+// Per item: S, dP of tile t+1 first (look-ahead), then, once the activation
+// has written its bf16 operands over tile t's S and dP, the accumulating
+// MMAs with the operand from tensor memory and the streamed tile read
+// MN-major (16 rows per MMA): dQ += dS K, or dV += P^T dO and dK += dS^T Q.
+// S/dP of tile t+2 reuse tile t's buffer only after these (the tensor core
+// runs one thread's MMAs in order).  An item's first accumulating MMA waits
+// until the epilogue has read the previous item's accumulators.
 template <int D, bool DKDV>
-__device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int n, int len) {
+__device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tmem, int n_items) {
   using C = BwdCfg<D>;
   volatile int* abort = &B.abort;
-  bool ok = ptx::mbar_wait(&B.res_full, 0, p.timeout_ns, abort);
-  ptx::tc_fence_after();
-  const uint64_t r1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R1), 16, 1024);
-  const uint64_t r2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_R2), 16, 1024);
   constexpr uint32_t idesc_acc = ptx::idesc_bf16(128, D, 1);
-  if (ok && n > 0) ok = bwd_issue_sdp<D>(p, sm, B, tmem, 0, len, r1, r2, abort);
-  for (int t = 0; t < n && ok; ++t) {
-    if (t + 1 < n) {
-      ok = bwd_issue_sdp<D>(p, sm, B, tmem, t + 1, len, r1, r2, abort);
-      if (!ok) break;
-    }
-    const int b = t & 1, s = t % C::NS;
-    ok = ptx::mbar_wait(&B.act_full[b], (t >> 1) & 1, p.timeout_ns, abort);
+  bool ok = true;
+  uint32_t k = 0, gt = 0;
+  for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    const BwdItem t = bwd_item(p, idx);
+    const BwdWork w = bwd_work<DKDV>(p, t);
+    if (w.n == 0) continue;
+    const int rb = k & 1;
+    ok = ptx::mbar_wait(&B.res_full[rb], (k >> 1) & 1, p.timeout_ns, abort);
     if (!ok) break;
     ptx::tc_fence_after();
-    const int n16 = (min(C::BN, len - C::BN * t) + 15) >> 4;
-    const uint32_t s1_addr = ptx::smem_u32(sm + C::OFF_S1 + s * C::STILE);
-    const uint32_t s2_addr = ptx::smem_u32(sm + C::OFF_S2 + s * C::STILE);
-    if (DKDV) {
-      // dV += P^T dO and dK += dS^T Q: B operands are the streamed dO and Q
-      // tiles, MN-major, 16 query rows (2048 bytes) per MMA
-      const uint64_t x1 = ptx::sdesc_sw128(s2_addr, C::SCHUNK, 1024);
-      const uint64_t x2 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
-      for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-      for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A2, tmem + C::tm_p(b) + 8 * kk, x2 + 128u * kk, idesc_acc,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-    } else {
-      // dQ += dS K: B operand is the streamed K tile, MN-major, 16 keys per MMA
-      const uint64_t x1 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
-      for (int kk = 0; kk < n16; ++kk)
-        ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
-                          (t > 0 || kk > 0) ? 1u : 0u);
+    const uint64_t r1 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::off_r(rb, 0)), 16, 1024);
+    const uint64_t r2 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::off_r(rb, 1)), 16, 1024);
+    ok = bwd_issue_sdp<D>(p, sm, B, tmem, gt, 0, w.len, r1, r2, abort);
+    for (int j = 0; j < w.n && ok; ++j, ++gt) {
+      if (j + 1 < w.n) {
+        ok = bwd_issue_sdp<D>(p, sm, B, tmem, gt + 1, j + 1, w.len, r1, r2, abort);
+        if (!ok) break;
+      }
+      const int b = gt & 1, s = gt % C::NS;
+      ok = ptx::mbar_wait(&B.act_full[b], (gt >> 1) & 1, p.timeout_ns, abort);
+      if (ok && j == 0 && k > 0) ok = ptx::mbar_wait(&B.acc_empty, (k - 1) & 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int n16 = (min(C::BN, w.len - C::BN * j) + 15) >> 4;
+      const uint32_t s1_addr = ptx::smem_u32(sm + C::OFF_S1 + s * C::STILE);
+      const uint32_t s2_addr = ptx::smem_u32(sm + C::OFF_S2 + s * C::STILE);
+      if (DKDV) {
+        // dV += P^T dO and dK += dS^T Q: B operands are the streamed dO and Q
+        // tiles, MN-major, 16 query rows (2048 bytes) per MMA
+        const uint64_t x1 = ptx::sdesc_sw128(s2_addr, C::SCHUNK, 1024);
+        const uint64_t x2 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
+        for (int kk = 0; kk < n16; ++kk)
+          ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < n16; ++kk)
+          ptx::mma_ts_elect(tmem + C::TM_A2, tmem + C::tm_p(b) + 8 * kk, x2 + 128u * kk, idesc_acc,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+      } else {
+        // dQ += dS K: B operand is the streamed K tile, MN-major, 16 keys per MMA
+        const uint64_t x1 = ptx::sdesc_sw128(s1_addr, C::SCHUNK, 1024);
+        for (int kk = 0; kk < n16; ++kk)
+          ptx::mma_ts_elect(tmem + C::TM_A1, tmem + C::tm_s(b) + 8 * kk, x1 + 128u * kk, idesc_acc,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit_elect(&B.st_empty[s]);  // the stage is free once these MMAs complete
     }
-    ptx::mma_commit_elect(&B.st_empty[s]);  // the stage is free once these MMAs complete
+    if (!ok) break;
+    ptx::mma_commit_elect(&B.res_empty[rb]);  // the resident buffer too
+    ptx::mma_commit_elect(&B.acc_full);       // the item's accumulators are final
+    ++k;
   }
   if (!ok) bwd_failure(p, abort, kStatusMma);
-  ptx::mma_commit_elect(&B.acc_full);
   // no MMA may be in flight when tensor memory is released
+  ptx::mma_commit_elect(&B.drain);
   const int never = 0;
-  ptx::mbar_wait(&B.acc_full, 0, 100000000ull, &never);
+  ptx::mbar_wait(&B.drain, 0, 100000000ull, &never);
 }
 
 // ------------------------------------------------------------------ activation
@@ -349,42 +423,30 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst) {
 
 // ------------------------------------------------------------------ kernels
 
-template <int D, int ACT>
-__global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+// Barriers, tensor memory and the three roles; `activation` runs on warps 2-5.
+template <int D, bool DKDV, typename Activation>
+__device__ __forceinline__ void bwd_kernel_body(const BwdParams& p, Activation&& activation) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
   BwdBars& B = *reinterpret_cast<BwdBars*>(sm + C::OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdItem t = bwd_item(p);
-  const int rows = min(128, t.Lq - t.row0);
-  // keys the item's rows may see: all, or from the first row's window start
-  // (rounded down to a 64-key tile) to the last row (causal)
-  int kv_lo = 0, kv_hi = t.Lkv;
-  if (p.window != 0) {
-    kv_lo = win_key_lo(t.row0, p.window) / C::BN * C::BN;
-    kv_hi = min(t.Lkv, t.row0 + 128);
-  }
-  const int n_kv = kv_hi > kv_lo ? (kv_hi - kv_lo + C::BN - 1) / C::BN : 0;
-  if (n_kv == 0) {  // no keys: no gradient reaches these queries
-    if (warp >= 2) {
-      const int row = ((warp & 3) << 5) + lane;
-      if (row < rows) zero_row<D>(p.dq + (static_cast<size_t>(t.q_tok + t.row0 + row) * p.H + t.h) * D);
-    }
-    return;
-  }
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&B.res_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&B.res_full[b], 1);
+      ptx::mbar_init(&B.res_empty[b], 1);
+      ptx::mbar_init(&B.mma_full[b], 1);
+      ptx::mbar_init(&B.act_full[b], 128);
+      ptx::mbar_init(&B.vec_full[b], 128);
+    }
     for (int s = 0; s < C::NS; ++s) {
       ptx::mbar_init(&B.st_full[s], 1);
       ptx::mbar_init(&B.st_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&B.mma_full[b], 1);
-      ptx::mbar_init(&B.act_full[b], 128);
-    }
     ptx::mbar_init(&B.acc_full, 1);
+    ptx::mbar_init(&B.acc_empty, 128);
+    ptx::mbar_init(&B.drain, 1);
     B.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -396,67 +458,12 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = B.tmem_slot;
-  volatile int* abort = &B.abort;
   if (warp == 0) {
-    if (lane == 0)
-      bwd_producer<D>(p, sm, B, t.h, &p.tm_q, &p.tm_do, t.q_tok + t.row0, &p.tm_k, &p.tm_v, t.kv_tok + kv_lo, n_kv);
+    if (lane == 0) bwd_producer<D, DKDV>(p, sm, B, p.n_items);
   } else if (warp == 1) {
-    bwd_mma<D, false>(p, sm, B, tmem, n_kv, kv_hi - kv_lo);
+    bwd_mma<D, DKDV>(p, sm, B, tmem, p.n_items);
   } else {
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const bool row_ok = row < rows;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const size_t ri = static_cast<size_t>(t.q_tok + t.row0 + row) * p.H + t.h;
-    float lse2 = 0.0f, dvr = 0.0f;
-    if (ACT == kActSoftmax && row_ok) {
-      lse2 = __ldg(p.lse2 + ri);
-      dvr = __ldg(p.dvec + ri);
-    }
-    uint64_t gA2 = 0, gC2 = 0;
-    if (ACT == kActGelu) {
-      gA2 = ptx::f2_splat(p.act_a);
-      gC2 = ptx::f2_splat(p.act_c);
-    }
-    const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
-    bool ok = true;
-    for (int g = 0; g < n_kv && ok; ++g) {
-      const int b = g & 1;
-      ok = ptx::mbar_wait(&B.mma_full[b], (g >> 1) & 1, p.timeout_ns, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const int kv_t0 = kv_lo + C::BN * g;
-      const int ncols = min(C::BN, kv_hi - kv_t0);
-      const int nch = (ncols + 31) >> 5;
-      int c_lo = 0, c_hi = row_ok ? ncols - 1 : -1;  // this row's valid columns of the tile
-      if (p.window != 0 && row_ok) {
-        const int i = t.row0 + row;
-        c_lo = win_key_lo(i, p.window) - kv_t0;
-        c_hi = min(c_hi, i - kv_t0);
-      }
-      for (int ch = 0; ch < nch; ++ch) {
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
-        ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
-        ptx::tmem_wait_ld();
-        uint32_t pk_p[16], pk_ds[16];
-        bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, c_lo, c_hi, p.score_scale, inv_l, gA2,
-                              gC2, pk_p, pk_ds);
-        ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_ds);  // dS over consumed S columns
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&B.act_full[b]);
-    }
-    if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      ptx::tc_fence_after();
-      bwd_store_row<D>(tmem + lane_off + C::TM_A1, p.scale, p.dq + ri * D, row_ok, p.align32 != 0);
-    } else if (lane == 0) {
-      bwd_failure(p, abort, kStatusActivation);
-    }
+    activation(sm, B, tmem, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -465,67 +472,87 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
   if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
 }
 
+// Persistent: CTA c takes items c, c + gridDim.x, ... of the list.
+template <int D, int ACT>
+__global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  bwd_kernel_body<D, false>(p, [&](uint8_t* sm, BwdBars& B, uint32_t tmem, int warp, int lane) {
+    volatile int* abort = &B.abort;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint64_t gA2 = 0, gC2 = 0;
+    if (ACT == kActGelu) {
+      gA2 = ptx::f2_splat(p.act_a);
+      gC2 = ptx::f2_splat(p.act_c);
+    }
+    bool ok = true;
+    uint32_t k = 0, gt = 0;
+    for (int idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+      const BwdItem t = bwd_item(p, idx);
+      const BwdWork w = bwd_work<false>(p, t);
+      const bool row_ok = row < min(128, t.Lq - t.row0);
+      const size_t ri = static_cast<size_t>(t.q_tok + t.row0 + row) * p.H + t.h;
+      if (w.n == 0) {  // no keys: no gradient reaches these queries
+        if (row_ok) zero_row<D>(p.dq + ri * D);
+        continue;
+      }
+      float lse2 = 0.0f, dvr = 0.0f;
+      if (ACT == kActSoftmax && row_ok) {
+        lse2 = __ldg(p.lse2 + ri);
+        dvr = __ldg(p.dvec + ri);
+      }
+      const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
+      for (int j = 0; j < w.n && ok; ++j, ++gt) {
+        const int b = gt & 1;
+        ok = ptx::mbar_wait(&B.mma_full[b], (gt >> 1) & 1, p.timeout_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int kv_t0 = w.lo + C::BN * j;
+        const int ncols = min(C::BN, w.len - C::BN * j);
+        const int nch = (ncols + 31) >> 5;
+        int c_lo = 0, c_hi = row_ok ? ncols - 1 : -1;  // this row's valid columns of the tile
+        if (p.window != 0 && row_ok) {
+          const int i = t.row0 + row;
+          c_lo = win_key_lo(i, p.window) - kv_t0;
+          c_hi = min(c_hi, i - kv_t0);
+        }
+        for (int ch = 0; ch < nch; ++ch) {
+          uint32_t sr[32], dr[32];
+          ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
+          ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
+          ptx::tmem_wait_ld();
+          uint32_t pk_p[16], pk_ds[16];
+          bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, c_lo, c_hi, p.score_scale, inv_l,
+                                gA2, gC2, pk_p, pk_ds);
+          ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_ds);  // dS over consumed S columns
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&B.act_full[b]);
+      }
+      if (!ok) break;
+      ok = ptx::mbar_wait(&B.acc_full, k & 1, p.timeout_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      bwd_store_row<D>(tmem + lane_off + C::TM_A1, p.scale, p.dq + ri * D, row_ok, p.align32 != 0);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.acc_empty);
+      ++k;
+    }
+    if (!ok && lane == 0) bwd_failure(p, abort, kStatusActivation);
+  });
+}
+
 template <int D, int ACT>
 __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
-  uint8_t* sm = smem_raw + pad;
-  BwdBars& B = *reinterpret_cast<BwdBars*>(sm + C::OFF_BAR);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdItem t = bwd_item(p);
-  const int keys = min(128, t.Lkv - t.row0);
-  // queries that may see the item's keys: all, or from the first key (causal)
-  // to the last query whose window holds the item's last key
-  int q_lo = 0, q_hi = t.Lq;
-  if (p.window != 0) {
-    q_lo = t.row0;
-    q_hi = min(t.Lq, win_query_hi(t.row0 + keys - 1, p.window) + 1);
-  }
-  const int n_q = q_hi > q_lo ? (q_hi - q_lo + C::BN - 1) / C::BN : 0;
-  if (n_q == 0) {  // no queries: these keys receive no gradient
-    if (warp >= 2) {
-      const int row = ((warp & 3) << 5) + lane;
-      if (row < keys) {
-        const size_t ri = static_cast<size_t>(t.kv_tok + t.row0 + row) * p.H + t.h;
-        zero_row<D>(p.dk + ri * D);
-        zero_row<D>(p.dv + ri * D);
-      }
-    }
-    return;
-  }
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(&B.res_full, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      ptx::mbar_init(&B.st_full[s], 1);
-      ptx::mbar_init(&B.st_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&B.mma_full[b], 1);
-      ptx::mbar_init(&B.act_full[b], 128);
-    }
-    ptx::mbar_init(&B.acc_full, 1);
-    for (int s = 0; s < 2; ++s) ptx::mbar_init(&B.vec_full[s], 128);
-    B.abort = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&B.tmem_slot, C::TM_COLS);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = B.tmem_slot;
-  volatile int* abort = &B.abort;
-  if (warp == 0) {
-    if (lane == 0)
-      bwd_producer<D>(p, sm, B, t.h, &p.tm_k, &p.tm_v, t.kv_tok + t.row0, &p.tm_q, &p.tm_do, t.q_tok + q_lo, n_q);
-  } else if (warp == 1) {
-    bwd_mma<D, true>(p, sm, B, tmem, n_q, q_hi - q_lo);
-  } else {
+  bwd_kernel_body<D, true>(p, [&](uint8_t* sm, BwdBars& B, uint32_t tmem, int warp, int lane) {
+    volatile int* abort = &B.abort;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // key row of the item
+    const int row = quarter * 32 + lane;     // key row of the item
     const int tid = (warp - 2) * 32 + lane;  // 0..127 over the four warps
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float* vec = reinterpret_cast<float*>(sm + C::OFF_VEC);  // [2 buffers][lse2, Dv][64]
@@ -534,74 +561,84 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
       gA2 = ptx::f2_splat(p.act_a);
       gC2 = ptx::f2_splat(p.act_c);
     }
-    const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
     bool ok = true;
-    const int j = t.row0 + row;  // this thread's key, counted from the sequence start
-    const int j_qhi = p.window != 0 ? win_query_hi(j, p.window) : 0x7fffffff;
-    for (int u = 0; u < n_q && ok; ++u) {
-      const int u0 = q_lo + C::BN * u;  // the tile's first query
-      const int nq = min(C::BN, q_hi - u0);
-      const int b = u & 1;
-      float* vb = vec + b * 2 * C::BN;
-      if (ACT == kActSoftmax) {
-        // lse2 and Dv of the tile's queries, one per thread.  The buffer of
-        // tile u - 2 is free: this thread waited for every thread's arrival
-        // at tile u - 1, which each made after finishing tile u - 2.
-        if (tid < C::BN) {
-          float l = 0.0f, d = 0.0f;
-          if (tid < nq) {
-            const size_t qi = static_cast<size_t>(t.q_tok + u0 + tid) * p.H + t.h;
-            l = __ldg(p.lse2 + qi);
-            d = __ldg(p.dvec + qi);
-          }
-          vb[tid] = l;
-          vb[C::BN + tid] = d;
+    uint32_t k = 0, gt = 0;
+    for (int idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+      const BwdItem t = bwd_item(p, idx);
+      const BwdWork w = bwd_work<true>(p, t);
+      const int keys = min(128, t.Lkv - t.row0);
+      const size_t ri = static_cast<size_t>(t.kv_tok + t.row0 + row) * p.H + t.h;
+      if (w.n == 0) {  // no queries: these keys receive no gradient
+        if (row < keys) {
+          zero_row<D>(p.dk + ri * D);
+          zero_row<D>(p.dv + ri * D);
         }
-        ptx::mbar_arrive(&B.vec_full[u & 1]);
-        ok = ptx::mbar_wait(&B.vec_full[u & 1], (u >> 1) & 1, p.timeout_ns, abort);
+        continue;
       }
-      if (ok) ok = ptx::mbar_wait(&B.mma_full[b], (u >> 1) & 1, p.timeout_ns, abort);
+      const float inv_l = 1.0f / static_cast<float>(max(t.Lkv, 1));
+      const int jk = t.row0 + row;  // this thread's key, counted from the sequence start
+      const int j_qhi = p.window != 0 ? win_query_hi(jk, p.window) : 0x7fffffff;
+      for (int u = 0; u < w.n && ok; ++u, ++gt) {
+        const int b = gt & 1;
+        const int u0 = w.lo + C::BN * u;  // the tile's first query
+        const int nq = min(C::BN, w.len - C::BN * u);
+        float* vb = vec + b * 2 * C::BN;
+        if (ACT == kActSoftmax) {
+          // lse2 and Dv of the tile's queries, one per thread.  The buffer of
+          // tile gt - 2 is free: this thread waited for every thread's
+          // arrival at tile gt - 1, which each made after finishing gt - 2.
+          if (tid < C::BN) {
+            float l = 0.0f, d = 0.0f;
+            if (tid < nq) {
+              const size_t qi = static_cast<size_t>(t.q_tok + u0 + tid) * p.H + t.h;
+              l = __ldg(p.lse2 + qi);
+              d = __ldg(p.dvec + qi);
+            }
+            vb[tid] = l;
+            vb[C::BN + tid] = d;
+          }
+          ptx::mbar_arrive(&B.vec_full[b]);
+          ok = ptx::mbar_wait(&B.vec_full[b], (gt >> 1) & 1, p.timeout_ns, abort);
+        }
+        if (ok) ok = ptx::mbar_wait(&B.mma_full[b], (gt >> 1) & 1, p.timeout_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int nch = (nq + 31) >> 5;
+        int c_lo = 0, c_hi = nq - 1;  // this key row's valid query columns of the tile
+        if (p.window != 0) {
+          c_lo = jk - u0;
+          c_hi = min(c_hi, j_qhi - u0);
+        }
+        for (int ch = 0; ch < nch; ++ch) {
+          uint32_t sr[32], dr[32];
+          ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
+          ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
+          ptx::tmem_wait_ld();
+          uint32_t pk_p[16], pk_ds[16];
+          bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, c_lo, c_hi,
+                               p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
+          ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_p);   // P^T over consumed S^T columns
+          ptx::tmem_st16(tmem + lane_off + C::tm_p(b) + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&B.act_full[b]);
+      }
+      if (!ok) break;
+      ok = ptx::mbar_wait(&B.acc_full, k & 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int nch = (nq + 31) >> 5;
-      int c_lo = 0, c_hi = nq - 1;  // this key row's valid query columns of the tile
-      if (p.window != 0) {
-        c_lo = j - u0;
-        c_hi = min(c_hi, j_qhi - u0);
-      }
-      for (int ch = 0; ch < nch; ++ch) {
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(tmem + lane_off + C::tm_s(b) + 32 * ch, sr);
-        ptx::tmem_ld32(tmem + lane_off + C::tm_p(b) + 32 * ch, dr);
-        ptx::tmem_wait_ld();
-        uint32_t pk_p[16], pk_ds[16];
-        bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, c_lo, c_hi,
-                             p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
-        ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_p);   // P^T over consumed S^T columns
-        ptx::tmem_st16(tmem + lane_off + C::tm_p(b) + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&B.act_full[b]);
-    }
-    if (ok) ok = ptx::mbar_wait(&B.acc_full, 0, p.timeout_ns, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      ptx::tc_fence_after();
-      const size_t ri = static_cast<size_t>(t.kv_tok + t.row0 + row) * p.H + t.h;
       const bool store = row < keys;
       bwd_store_row<D>(tmem + lane_off + C::TM_A1, 1.0f, p.dv + ri * D, store, p.align32 != 0);
       bwd_store_row<D>(tmem + lane_off + C::TM_A2, p.scale, p.dk + ri * D, store, p.align32 != 0);
-    } else if (lane == 0) {
-      bwd_failure(p, abort, kStatusActivation);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.acc_empty);
+      ++k;
     }
-  }
-  __syncwarp();
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+    if (!ok && lane == 0) bwd_failure(p, abort, kStatusActivation);
+  });
 }
 
 // Dv_i = <dO_i, O_i> and lse2_i = lse_i log2(e), one warp per (token, head) row.
