@@ -1,6 +1,6 @@
 /*
- * gdpa.h -- C ABI of libgdpa: forward pass of jagged Generalized Dot-Product
- * Attention (GDPA) on NVIDIA GB300 (sm_103a).
+ * gdpa.h -- C ABI of libgdpa: forward and backward passes of jagged
+ * Generalized Dot-Product Attention (GDPA) on NVIDIA GB300 (sm_103a).
  *
  * The operation (techfeed summary of "GEM Training", sections "JFA" and
  * "GDPA"; remio.ai commentary, section on model/system co-design): attention
@@ -13,10 +13,16 @@
  *   s_ij = scale * <q_i, k_j>                                  j in K(i)
  *   softmax : o_i = sum_j exp(s_ij - max s) v_j / sum_j exp(s_ij - max s)
  *   GELU    : o_i = (1/Lkv_b) * sum_j gelu_tanh(s_ij) v_j
+ *   SiLU    : o_i = (1/Lkv_b) * sum_j silu(s_ij) v_j        (GDPA_ACT_SILU)
  *
  *   K(i) = all keys j < Lkv_b of sequence b            (window_blocks == 0)
  *        = keys j <= i with floor(i/64) - floor(j/64) <= window_blocks - 1
  *                                                      (window_blocks  > 0)
+ *        = keys i - W < j <= i   (gdpa_fwd_sliding / gdpa_bwd_sliding, W tokens)
+ *
+ * The training entry points keep the softmax row logsumexp in the forward
+ * (gdpa_fwd_lse, gdpa_fwd_sliding) and return dq, dk, dv in the backward
+ * (gdpa_bwd, gdpa_bwd_sliding).
  *
  * An empty key set gives o_i = 0.  The GELU is evaluated on the ALU only: the
  * tanh is rewritten as a logistic function whose exponential is a range-reduced
@@ -30,8 +36,8 @@
  *   out  bf16 [Tq,  H, D]   every row is written (zeros for empty key sets)
  *   q_offsets, kv_offsets  int32 [B+1], offsets[0] = 0, non-decreasing
  * q, k, v and out must be 16-byte aligned.  D must be 64 or 128.  Tq and Tkv
- * must be below 2^31.  window_blocks > 0 requires q_offsets == kv_offsets and
- * act == GDPA_ACT_SOFTMAX.
+ * must be below 2^31.  Windows (block or sliding) require q_offsets ==
+ * kv_offsets and act == GDPA_ACT_SOFTMAX.
  *
  * Ownership: the caller owns every buffer it passes; the library never frees
  * them and keeps no reference after the call returns (the GPU may still be
