@@ -53,9 +53,10 @@ RECIPES = {
     "block_window": "B=64 H=4 D=128, L=64*U{8..512}, 64-token blocks, window 4 blocks (own causal + 3 previous), softmax",
     "sliding_window": "B=64 H=4 D=128, L~U{512..32768}, causal sliding window of 256 tokens, softmax",
     "cross_silu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, SiLU (ALU), scale=1, /Lkv",
+    "pffn": "B=256 H=4 D=128, Lq~U{256..4096}, 512 hidden units per sample as keys/values, GELU (ALU), scale=1/sqrt(D)",
 }
 BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm",
-         "sliding_window": "hbm", "cross_silu": "hbm"}
+         "sliding_window": "hbm", "cross_silu": "hbm", "pffn": "tensor"}
 
 
 def parse_args():

@@ -28,6 +28,9 @@ block_window    B=64, H=4, D=128, L = 64 * U{8..512}; window of 4 blocks of 64
 sliding_window  B=64, H=4, D=128, L ~ U{512..32768}; causal sliding window of
                 256 tokens (window_blocks = -256); softmax; scale 1/sqrt(D)
 cross_silu      cross_gelu's shapes and QK-norm with SiLU instead of GELU
+pffn            B=256, H=4, D=128, Lq ~ U{256..4096}, Lkv = 512: a per-sample FFN
+                gelu(x W1^T) W2 as GDPA (K = W1, V = W2, 512 hidden units per
+                sample); GELU; scale 1/sqrt(D); no QK-norm
 ==============  ====================================================================
 
 Draw order (fixed): lengths first, then one 63-bit sub-seed per value tensor
@@ -63,7 +66,7 @@ class Workload:
     act: int
     window_blocks: int
     scale: float
-    kind: str  # "self", "cross", "pma", "window"
+    kind: str  # "self", "cross", "pma", "window", "ffn"
 
 
 WORKLOADS = {
@@ -73,6 +76,7 @@ WORKLOADS = {
     "pma": Workload("pma", 3, 256, 8, 64, ACT_SOFTMAX, 0, 1.0 / math.sqrt(64), "pma"),
     "block_window": Workload("block_window", 4, 64, 4, 128, ACT_SOFTMAX, 4, 1.0 / math.sqrt(128), "window"),
     "cross_silu": Workload("cross_silu", 6, 512, 4, 128, ACT_SILU, 0, 1.0, "cross"),
+    "pffn": Workload("pffn", 7, 256, 4, 128, ACT_GELU_TANH, 0, 1.0 / math.sqrt(128), "ffn"),
     # window_blocks < 0: a causal sliding window of -window_blocks tokens
     "sliding_window": Workload("sliding_window", 5, 64, 4, 128, ACT_SOFTMAX, -256, 1.0 / math.sqrt(128), "window"),
 }
@@ -114,6 +118,8 @@ def draw_lengths(w: Workload, rng: np.random.Generator, B: int | None = None):
     if w.name == "sliding_window":
         L = rng.integers(512, 32768, size=B, endpoint=True)
         return L, L
+    if w.name == "pffn":
+        return rng.integers(256, 4096, size=B, endpoint=True), np.full(B, 512, dtype=np.int64)
     raise KeyError(w.name)
 
 

@@ -289,3 +289,22 @@ def test_golden_hand_cases():
         got = out[rows] if rows is not None else out
         np.testing.assert_allclose(got.reshape(-1), np.array(c["out"], dtype=np.float64), rtol=1e-12,
                                    atol=1e-14, err_msg=c["name"])
+
+
+@pytest.mark.parametrize("act", [ACT_GELU_TANH, 2])
+def test_pffn_is_gdpa_with_weights_as_keys_and_values(act):
+    # A per-sample FFN, act(x W1^T) W2 (W1, W2: [hidden, D]), is GDPA with
+    # K = W1, V = W2 and the ALU activation: o = (1/hidden) act(x W1^T) W2.
+    # Brute force with torch's activation on plain matrices, per sample.
+    rng = np.random.default_rng(60 + act)
+    Lq, hidden = np.array([5, 17, 1]), np.array([24, 24, 24])
+    b = small_batch(rng, Lq, hidden, 1, 16, act=act, scale=0.25)
+    got = run(b)
+    qf, kf, vf = bf16_bits_to_f64(b.q), bf16_bits_to_f64(b.k), bf16_bits_to_f64(b.v)
+    f = (lambda z: torch.nn.functional.gelu(z, approximate="tanh")) if act == ACT_GELU_TANH else torch.nn.functional.silu
+    for i in range(len(Lq)):
+        x = torch.from_numpy(qf[b.q_offsets[i]:b.q_offsets[i + 1], 0])
+        W1 = torch.from_numpy(kf[b.kv_offsets[i]:b.kv_offsets[i + 1], 0])
+        W2 = torch.from_numpy(vf[b.kv_offsets[i]:b.kv_offsets[i + 1], 0])
+        ffn = (f(0.25 * x @ W1.T) @ W2).numpy()
+        np.testing.assert_allclose(got[b.q_offsets[i]:b.q_offsets[i + 1], 0] * hidden[i], ffn, rtol=1e-11, atol=1e-11)

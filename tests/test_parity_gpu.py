@@ -154,6 +154,7 @@ def test_alu_silu_matches_oracle_on_grid():
 SMALL = {
     # name: (B override) -- same distributions as the full workloads, several tiles and ragged tails
     "tiny": None,
+    "pffn": 3,
     "self_long": 6,
     "cross_gelu": 5,
     "pma": 12,
