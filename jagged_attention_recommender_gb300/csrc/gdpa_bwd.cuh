@@ -10,14 +10,17 @@
 //
 // (the backward the techfeed summary of "GEM Training" describes in its JFA
 // section: dQ, dK and dV computed without atomics, parallel over batch and
-// heads.)  Two kernels, one CTA per work item, each output written once:
+// heads.)  Two persistent kernels (one CTA per SM walking every gridDim.x-th
+// item of a longest-first list), each output row written once:
 //
 //   gdpa_bwd_dq_kernel    item = 128 query rows of one (sequence, head); it
-//     walks the sequence's 64-key K/V tiles: S = Q K^T and dP = dO V^T into
+//     walks the 64-key K/V tiles its rows may see (all, or the window's):
+//     S = Q K^T and dP = dO V^T into
 //     tensor memory, the activation warps turn them into dS (bf16, written
 //     over S), then dQ += dS K with dS read straight from tensor memory.
 //   gdpa_bwd_dkdv_kernel  item = 128 keys of one (sequence, head); it walks
-//     the sequence's 64-row query tiles: S^T = K Q^T and dP^T = V dO^T, the
+//     the 64-row query tiles that may see its keys: S^T = K Q^T and
+//     dP^T = V dO^T, the
 //     activation warps write P^T over S^T and dS^T over dP^T, then
 //     dV += P^T dO and dK += dS^T Q.
 //
@@ -30,9 +33,10 @@
 // warp runs the loop, one elected lane issues), warps 2-5 the activation and
 // the epilogue (warp w owns tensor-memory lanes 32 (w mod 4) .. +31, one row
 // each).  Tensor memory (512 columns): S0 0, dP0 64, S1 128, dP1 192,
-// accumulators from 256 (dQ; or dV then dK).  Shared memory (D = 128): the
-// item's two resident 128-row tiles (Q and dO, or K and V) and three stages
-// of the two streamed 64-row ones.
+// accumulators from 256 (dQ; or dV then dK).  Shared memory (D = 128): two
+// buffers of the item's two resident 128-row tiles (Q and dO, or K and V;
+// the next item's load overlaps the current one) and three stages of the
+// two streamed 64-row ones.
 // Rows past a sequence's end are masked to P = dS = 0 in the activation, so
 // whatever the TMA box brought in for them never reaches an accumulator.
 #pragma once
