@@ -31,6 +31,10 @@ cross_silu      cross_gelu's shapes and QK-norm with SiLU instead of GELU
 pffn            B=256, H=4, D=128, Lq ~ U{256..4096}, Lkv = 512: a per-sample FFN
                 gelu(x W1^T) W2 as GDPA (K = W1, V = W2, 512 hidden units per
                 sample); GELU; scale 1/sqrt(D); no QK-norm
+self_long_mx    self_long's lengths and values with Q and K in MXFP8: e4m3
+                elements, one E8M0 scale per 32 coordinates (OCP MX recipe:
+                scale 2^(floor(log2 amax) - 8), elements rounded to nearest
+                even and clamped to +-448); V bf16
 ==============  ====================================================================
 
 Draw order (fixed): lengths first, then one 63-bit sub-seed per value tensor
@@ -67,6 +71,7 @@ class Workload:
     window_blocks: int
     scale: float
     kind: str  # "self", "cross", "pma", "window", "ffn"
+    mx: bool = False  # Q and K also drawn as MXFP8 (e4m3 codes + E8M0 block scales)
 
 
 WORKLOADS = {
@@ -79,7 +84,10 @@ WORKLOADS = {
     "pffn": Workload("pffn", 7, 256, 4, 128, ACT_GELU_TANH, 0, 1.0 / math.sqrt(128), "ffn"),
     # window_blocks < 0: a causal sliding window of -window_blocks tokens
     "sliding_window": Workload("sliding_window", 5, 64, 4, 128, ACT_SOFTMAX, -256, 1.0 / math.sqrt(128), "window"),
+    "self_long_mx": Workload("self_long_mx", 1, 256, 4, 128, ACT_SOFTMAX, 0, 1.0 / math.sqrt(128), "self", mx=True),
 }
+
+MX_BLOCK = 32
 
 PMA_SEEDS = 32
 BLOCK = 64
@@ -92,6 +100,26 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + bias) >> 16).astype(np.uint16)
 
 
+def to_mx(x: np.ndarray):
+    """OCP MX quantisation of float32 ``[T, H, D]`` rows in blocks of 32
+    coordinates: returns (e4m3 codes uint8 ``[T, H, D]``, E8M0 scale codes
+    uint8 ``[T, H, D // 32]``).  The block scale is 2^(floor(log2 amax) - 8)
+    (8 = the largest e4m3 exponent), elements are x / scale clamped to +-448
+    and rounded to nearest even by torch's float8_e4m3fn conversion; an
+    all-zero block takes scale 1."""
+    import torch
+
+    T, H, D = x.shape
+    xb = np.ascontiguousarray(x, dtype=np.float32).reshape(T, H, D // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(xb).max(axis=-1)
+    _, ex = np.frexp(amax)  # amax = m 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = np.where(amax > 0, ex - 1 - 8, 0).clip(-127, 127).astype(np.int32)
+    sf = (e + 127).astype(np.uint8)
+    y = np.clip(xb * np.ldexp(np.float32(1.0), -e)[..., None].astype(np.float32), -448.0, 448.0)
+    codes = torch.from_numpy(np.ascontiguousarray(y.reshape(T, H, D))).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy(), sf
+
+
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -102,7 +130,7 @@ def draw_lengths(w: Workload, rng: np.random.Generator, B: int | None = None):
     if w.name == "tiny":
         L = rng.integers(1, 128, size=B, endpoint=True)
         return L, L
-    if w.name == "self_long":
+    if w.name in ("self_long", "self_long_mx"):
         L = np.clip(np.round(rng.lognormal(6.9, 0.8, size=B)), 100, 4096).astype(np.int64)
         return L, L
     if w.name in ("cross_gelu", "cross_silu"):
@@ -165,6 +193,12 @@ class JaggedBatch:
     v: np.ndarray          # uint16 bf16 bits [Tkv, H, D]
     q_offsets: np.ndarray  # int32 [B+1]
     kv_offsets: np.ndarray  # int32 [B+1]
+    # MXFP8 workloads: e4m3 codes [T, H, D] and E8M0 scales [T, H, D/32] of
+    # Q and K (q, k then hold the unquantised values, rounded to bf16)
+    q8: np.ndarray | None = None
+    q_sf: np.ndarray | None = None
+    k8: np.ndarray | None = None
+    k_sf: np.ndarray | None = None
 
     @property
     def B(self) -> int:
@@ -188,10 +222,17 @@ class JaggedBatch:
         q = np.concatenate([self.q[qo[s]:qo[s + 1]] for s in seqs]) if seqs else self.q[:0]
         k = np.concatenate([self.k[ko[s]:ko[s + 1]] for s in seqs]) if seqs else self.k[:0]
         v = np.concatenate([self.v[ko[s]:ko[s + 1]] for s in seqs]) if seqs else self.v[:0]
+
+        def rows(a, off):
+            if a is None:
+                return None
+            return np.ascontiguousarray(np.concatenate([a[off[s]:off[s + 1]] for s in seqs]) if seqs else a[:0])
+
         return JaggedBatch(self.workload, np.ascontiguousarray(q), np.ascontiguousarray(k),
                            np.ascontiguousarray(v),
                            offsets_of([qo[s + 1] - qo[s] for s in seqs]),
-                           offsets_of([ko[s + 1] - ko[s] for s in seqs]))
+                           offsets_of([ko[s + 1] - ko[s] for s in seqs]),
+                           rows(self.q8, qo), rows(self.q_sf, qo), rows(self.k8, ko), rows(self.k_sf, ko))
 
 
 def make_batch(name: str, B: int | None = None, seed: int | None = None,
@@ -226,9 +267,13 @@ def make_batch(name: str, B: int | None = None, seed: int | None = None,
     if w.kind == "cross":
         qf = _qk_norm_x4(qf)
         kf = _qk_norm_x4(kf)
+    mx = (to_mx(qf), to_mx(kf)) if w.mx else None
     q = f32_to_bf16_bits(qf)
     del qf
     k = f32_to_bf16_bits(kf)
     del kf
     v = f32_to_bf16_bits(_normal_chunked(subs[2], Tkv, H, D, threads))
-    return JaggedBatch(w, q, k, v, offsets_of(Lq), offsets_of(Lkv))
+    b = JaggedBatch(w, q, k, v, offsets_of(Lq), offsets_of(Lkv))
+    if mx is not None:
+        (b.q8, b.q_sf), (b.k8, b.k_sf) = mx
+    return b

@@ -50,6 +50,13 @@ def _load():
         lib.oracle_gelu_tanh.argtypes = [ctypes.c_double]
         lib.oracle_gelu_tanh.restype = ctypes.c_double
         lib.oracle_num_cpus.restype = ctypes.c_int
+        lib.oracle_gdpa_fwd_mx.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int]
+        lib.oracle_gdpa_fwd_mx.restype = ctypes.c_int
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_to_double.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -84,6 +91,41 @@ def gdpa_fwd_batch(batch, nthreads: int = 0) -> np.ndarray:
     w = batch.workload
     return gdpa_fwd(batch.q, batch.k, batch.v, batch.q_offsets, batch.kv_offsets, w.H, w.D, w.act,
                     w.window_blocks, w.scale, nthreads)
+
+
+def gdpa_fwd_mx(q8, q_sf, k8, k_sf, v, q_offsets, kv_offsets, H: int, D: int, act: int,
+                window_blocks: int, scale: float, nthreads: int = 0) -> np.ndarray:
+    """Oracle output, fp64 ``[Tq, H, D]``, for MXFP8 Q and K.
+
+    ``q8``, ``k8``: uint8 e4m3 codes ``[tokens, H, D]``; ``q_sf``, ``k_sf``:
+    uint8 E8M0 scales ``[tokens, H, D // 32]``; ``v``: uint16 bf16 bits.
+    """
+    lib = _load()
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (q8, q_sf, k8, k_sf)]
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    qo = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ko = np.ascontiguousarray(kv_offsets, dtype=np.int32)
+    B = len(qo) - 1
+    out = np.zeros((int(qo[-1]), H, D), dtype=np.float64)
+    rc = lib.oracle_gdpa_fwd_mx(*[_ptr(a) for a in arrs], _ptr(v), _ptr(qo), _ptr(ko), B, H, D, act,
+                                window_blocks, float(scale), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gdpa_fwd_mx returned %d" % rc)
+    return out
+
+
+def gdpa_fwd_mx_batch(batch, nthreads: int = 0) -> np.ndarray:
+    w = batch.workload
+    return gdpa_fwd_mx(batch.q8, batch.q_sf, batch.k8, batch.k_sf, batch.v, batch.q_offsets, batch.kv_offsets,
+                       w.H, w.D, w.act, w.window_blocks, w.scale, nthreads)
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().oracle_e4m3_to_double(int(code))
+
+
+def e8m0_to_double(code: int) -> float:
+    return _load().oracle_e8m0_to_double(int(code))
 
 
 def gdpa_bwd(q, k, v, dout, q_offsets, kv_offsets, H: int, D: int, act: int, window_blocks: int,

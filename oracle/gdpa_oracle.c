@@ -59,6 +59,21 @@
  *
  * It also returns lse_i (natural log; -inf for an empty key set, 0 for GELU
  * rows), which a forward that keeps it for the backward must reproduce.
+ *
+ * MXFP8 score operands (oracle_gdpa_fwd_mx): q and k arrive as OCP
+ * microscaling values -- an e4m3 element per coordinate and one E8M0 scale
+ * per 32 consecutive coordinates of a (token, head) row -- and the forward
+ * above runs on their values
+ *
+ *   q_id = e4m3(q8_id) * 2^(qs_i,floor(d/32) - 127)    (k likewise; v stays bf16)
+ *
+ * e4m3: 1 sign, 4 exponent (bias 7) and 3 mantissa bits, subnormal below
+ * exponent 1, no infinities, S.1111.111 is NaN; E8M0: 2^(e - 127), 0xFF NaN.
+ * Source: MXFP8 applied to attention -- techfeed summary of "GEM Training",
+ * section on MXFP8 ultra-low-precision training, and the aigeeknews
+ * translation, section on compute efficiency ("MXFP8 attention").  Which
+ * operands are quantised is not stated there; this oracle quantises the two
+ * operands of the score product along their contraction (head) dimension.
  */
 #include <math.h>
 #include <pthread.h>
@@ -79,6 +94,17 @@ static double bf16_to_double(uint16_t bits) {
   memcpy(&f, &u, sizeof f);
   return (double)f;
 }
+
+/* OCP e4m3 ("E4M3FN") element code -> exact double. */
+double oracle_e4m3_to_double(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10); /* m/8 * 2^-6, (1 + m/8) 2^(e-7) */
+  return (c & 0x80) ? -mag : mag;
+}
+
+/* OCP E8M0 scale code -> 2^(c - 127); 0xFF is NaN. */
+double oracle_e8m0_to_double(uint8_t c) { return c == 0xFF ? NAN : ldexp(1.0, (int)c - 127); }
 
 double oracle_gelu_tanh(double x) {
   const double c = sqrt(2.0 / M_PI);
@@ -123,7 +149,19 @@ typedef struct {
   double scale;
   double* out;
   int64_t next_task; /* shared counter over (b, h) tasks */
+  /* MXFP8 q and k (used instead of q, k when q8 is set): e4m3 codes
+   * [T, H, D] and E8M0 scales [T, H, D/32] */
+  const uint8_t *q8, *q_sf, *k8, *k_sf;
 } job_t;
+
+/* Element d of the (token t, head h) row of q or k, as a double. */
+static double qk_value(const job_t* J, int is_k, int64_t t, int h, int d) {
+  const int64_t e = (t * J->H + h) * J->D + d;
+  if (!J->q8) return bf16_to_double(is_k ? J->k[e] : J->q[e]);
+  const uint8_t* codes = is_k ? J->k8 : J->q8;
+  const uint8_t* sf = is_k ? J->k_sf : J->q_sf;
+  return oracle_e4m3_to_double(codes[e]) * oracle_e8m0_to_double(sf[(t * J->H + h) * (J->D / 32) + d / 32]);
+}
 
 static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, double* qrow, double* s) {
   const int H = J->H, D = J->D;
@@ -131,13 +169,13 @@ static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, d
   const int64_t k0 = J->kv_off[b], Lkv = J->kv_off[b + 1] - k0;
   for (int64_t j = 0; j < Lkv; ++j)
     for (int d = 0; d < D; ++d) {
-      kbuf[j * D + d] = bf16_to_double(J->k[((k0 + j) * H + h) * D + d]);
+      kbuf[j * D + d] = qk_value(J, 1, k0 + j, h, d);
       vbuf[j * D + d] = bf16_to_double(J->v[((k0 + j) * H + h) * D + d]);
     }
   for (int64_t i = 0; i < Lq; ++i) {
     double* o = J->out + ((q0 + i) * H + h) * (int64_t)D;
     for (int d = 0; d < D; ++d) {
-      qrow[d] = bf16_to_double(J->q[((q0 + i) * H + h) * D + d]);
+      qrow[d] = qk_value(J, 0, q0 + i, h, d);
       o[d] = 0.0;
     }
     /* scores over the key set */
@@ -209,9 +247,9 @@ int oracle_num_cpus(void) {
  * 64-token blocks; < 0: sliding window of -window_blocks tokens).  nthreads <= 0 uses every online
  * CPU.  Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
  */
-int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
-                    const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
-                    double* out, int nthreads) {
+static int run_fwd(job_t* J, int nthreads) {
+  const int B = J->B, H = J->H, D = J->D, act = J->act, window_blocks = J->window_blocks;
+  const int32_t *q_off = J->q_off, *kv_off = J->kv_off;
   if (B < 0 || H <= 0 || D <= 0 || (act != ORACLE_ACT_SOFTMAX && act != ORACLE_ACT_GELU_TANH && act != ORACLE_ACT_SILU))
     return 1;
   if (!q_off || !kv_off || q_off[0] != 0 || kv_off[0] != 0) return 1;
@@ -220,8 +258,9 @@ int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
     if (window_blocks != 0 && q_off[b + 1] != kv_off[b + 1]) return 1;
   }
   if (B == 0 || q_off[B] == 0) return 0;
-  if (!q || !out || (kv_off[B] > 0 && (!k || !v))) return 1;
-  job_t J = {q, k, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0};
+  const int mx = J->q8 != NULL;
+  if (!J->out || (mx ? !J->q_sf : !J->q)) return 1;
+  if (kv_off[B] > 0 && (!J->v || (mx ? (!J->k8 || !J->k_sf) : !J->k))) return 1;
   if (nthreads <= 0) nthreads = oracle_num_cpus();
   if (nthreads > B * H) nthreads = B * H;
   if (nthreads < 1) nthreads = 1;
@@ -229,11 +268,11 @@ int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   if (!th) return 2;
   int started = 0, failed = 0;
   for (int t = 0; t < nthreads; ++t) {
-    if (pthread_create(&th[t], NULL, worker, &J) != 0) break;
+    if (pthread_create(&th[t], NULL, worker, J) != 0) break;
     ++started;
   }
   if (started == 0) { /* no thread could start: run on this one */
-    failed = worker(&J) != NULL;
+    failed = worker(J) != NULL;
   }
   for (int t = 0; t < started; ++t) {
     void* r = NULL;
@@ -242,6 +281,33 @@ int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   }
   free(th);
   return failed ? 2 : 0;
+}
+
+/*
+ * q: bf16 bits [Tq, H, D]; k, v: bf16 bits [Tkv, H, D]; q_off, kv_off: int32
+ * [B+1] prefix sums starting at 0; out: fp64 [Tq, H, D] (fully written).
+ * window_blocks != 0 needs q_off == kv_off (> 0: block window of that many
+ * 64-token blocks; < 0: sliding window of -window_blocks tokens).  nthreads <= 0 uses every online
+ * CPU.  Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
+                    const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
+                    double* out, int nthreads) {
+  job_t J = {q, k, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, NULL, NULL, NULL, NULL};
+  return run_fwd(&J, nthreads);
+}
+
+/*
+ * The same forward with MXFP8 q and k: q8 / k8 e4m3 codes [T, H, D], q_sf /
+ * k_sf E8M0 scales [T, H, D/32] (D a multiple of 32); v bf16 bits.  Full
+ * attention or a window exactly as oracle_gdpa_fwd.
+ */
+int oracle_gdpa_fwd_mx(const uint8_t* q8, const uint8_t* q_sf, const uint8_t* k8, const uint8_t* k_sf,
+                       const uint16_t* v, const int32_t* q_off, const int32_t* kv_off, int B, int H, int D, int act,
+                       int window_blocks, double scale, double* out, int nthreads) {
+  if (!q8 || D % 32 != 0) return 1;
+  job_t J = {NULL, NULL, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, q8, q_sf, k8, k_sf};
+  return run_fwd(&J, nthreads);
 }
 
 /* ------------------------------------------------------------------ backward */

@@ -1,0 +1,118 @@
+"""Pins of the oracle's MXFP8 path (CPU only).
+
+The MX decode is pinned element by element to torch's own float8 types, and
+the MX forward to the (separately pinned) bf16 forward: an e4m3 element
+times a power-of-two scale is exactly a bf16 value, so decoding the codes
+with torch, rounding to bf16 (checked exact) and running the bf16 oracle must
+give the MX oracle's output bit for bit.  Scales that differ per 32-element
+block make a wrong block index, a swapped operand or a dropped scale fail.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from jagged_attention_recommender_gb300.workloads import (ACT_GELU_TANH, ACT_SILU, ACT_SOFTMAX,
+                                                          f32_to_bf16_bits, offsets_of, to_mx)
+
+
+def test_e4m3_decode_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in codes])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    assert np.isnan(got).sum() == 2  # S.1111.111
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_e8m0_decode_matches_torch():
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without float8_e8m0fnu")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([oracle.e8m0_to_double(c) for c in codes])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert got[127] == 1.0 and got[128] == 2.0
+
+
+def _torch_dequant_bf16(codes, sf):
+    """MX -> bf16 bits through torch's float8 types (exactness checked)."""
+    T, H, D = codes.shape
+    x = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32)
+    s = torch.pow(torch.tensor(2.0, dtype=torch.float64), torch.from_numpy(sf.astype(np.int64) - 127)).float()
+    y = (x.reshape(T, H, D // 32, 32) * s[..., None]).reshape(T, H, D).numpy()
+    bits = f32_to_bf16_bits(y)
+    back = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(back, y), "MX value not exact in bf16"
+    return bits
+
+
+def _random_mx(rng, T, H, D):
+    """N(0, 1) rows quantised, every block's scale then moved by -2..+2
+    (values of order one, scales that differ from block to block), and one
+    element in 16 replaced by a code from the whole non-NaN range."""
+    codes, sf = to_mx(rng.standard_normal((T, H, D)).astype(np.float32))
+    sf = (sf.astype(np.int64) + rng.integers(-2, 2, size=sf.shape, endpoint=True)).astype(np.uint8)
+    wild = rng.integers(0, 256, size=codes.shape, dtype=np.uint8)
+    wild[(wild & 0x7F) == 0x7F] = 0x38
+    pick = rng.random(codes.shape) < 1.0 / 16
+    codes = np.where(pick, wild >> 2 | (wild & 0x80), codes).astype(np.uint8)  # wild codes kept below 2^1
+    return codes, sf
+
+
+@pytest.mark.parametrize("act,window,D", [(ACT_SOFTMAX, 0, 128), (ACT_GELU_TANH, 0, 128), (ACT_SILU, 0, 64),
+                                          (ACT_SOFTMAX, 2, 128), (ACT_SOFTMAX, -40, 64)])
+def test_mx_forward_equals_bf16_forward_on_torch_dequantised_inputs(act, window, D):
+    rng = np.random.default_rng(900 + D + 7 * act + window)
+    H = 2
+    L = np.array([1, 70, 130, 5, 0, 200]) if window == 0 else np.array([1, 70, 130, 5, 200])
+    Lkv = np.array([3, 200, 1, 64, 9, 130]) if window == 0 else L
+    qo, ko = offsets_of(L), offsets_of(Lkv)
+    q8, qs = _random_mx(rng, int(qo[-1]), H, D)
+    k8, ks = _random_mx(rng, int(ko[-1]), H, D)
+    v = f32_to_bf16_bits(rng.standard_normal((int(ko[-1]), H, D)).astype(np.float32))
+    scale = 1.0 / np.sqrt(D) if act == ACT_SOFTMAX else 0.05
+    got = oracle.gdpa_fwd_mx(q8, qs, k8, ks, v, qo, ko, H, D, act, window, scale)
+    ref = oracle.gdpa_fwd(_torch_dequant_bf16(q8, qs), _torch_dequant_bf16(k8, ks), v, qo, ko, H, D, act, window,
+                          scale)
+    assert np.array_equal(got, ref)
+    # and the scales matter: one block's scale doubled changes exactly the
+    # rows that read it
+    qs2 = qs.copy()
+    qs2[qo[1] + 3, 1, 1] += 1
+    got2 = oracle.gdpa_fwd_mx(q8, qs2, k8, ks, v, qo, ko, H, D, act, window, scale)
+    changed = np.argwhere(np.any(got2 != got, axis=-1))
+    assert [tuple(r) for r in changed] == [(qo[1] + 3, 1)]
+
+
+def test_mx_forward_rejects_bad_block_size():
+    q8 = np.zeros((1, 1, 48), np.uint8)
+    sf = np.full((1, 1, 1), 127, np.uint8)
+    v = np.zeros((1, 1, 48), np.uint16)
+    o = np.array([0, 1], np.int32)
+    with pytest.raises(ValueError):
+        oracle.gdpa_fwd_mx(q8, sf, q8, sf, v, o, o, 1, 48, ACT_SOFTMAX, 0, 1.0)
+
+
+def test_to_mx_is_the_ocp_recipe():
+    """The input generator's quantiser: block scale 2^(floor(log2 amax) - 8),
+    every element within half an e4m3 step of x / scale (clamped to 448)."""
+    rng = np.random.default_rng(77)
+    x = (rng.standard_normal((50, 3, 64)) * np.exp(rng.uniform(-6, 6, size=(50, 3, 1)))).astype(np.float32)
+    x[0, 0, :32] = 0.0
+    codes, sf = to_mx(x)
+    xb = x.reshape(50, 3, 2, 32).astype(np.float64)
+    amax = np.abs(xb).max(-1)
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1))) - 8, 0).astype(np.int64)
+    assert np.array_equal(sf.astype(np.int64) - 127, e.astype(np.int64))
+    dec = np.vectorize(oracle.e4m3_to_double)(codes).reshape(50, 3, 2, 32) * np.ldexp(1.0, e)[..., None]
+    y = np.clip(xb / np.ldexp(1.0, e)[..., None], -448, 448)
+    # e4m3 spacing at |y|: 2^(floor(log2|y|) - 3), at least 2^-9 (subnormals)
+    ulp = np.ldexp(1.0, np.maximum(np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -9))) - 3, -9).astype(np.int64))
+    assert np.all(np.abs(dec / np.ldexp(1.0, e)[..., None] - y) <= ulp / 2)
