@@ -54,9 +54,14 @@ RECIPES = {
     "sliding_window": "B=64 H=4 D=128, L~U{512..32768}, causal sliding window of 256 tokens, softmax",
     "cross_silu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, SiLU (ALU), scale=1, /Lkv",
     "pffn": "B=256 H=4 D=128, Lq~U{256..4096}, 512 hidden units per sample as keys/values, GELU (ALU), scale=1/sqrt(D)",
+    "self_long_mx": "self_long with Q, K in MXFP8 (e4m3, E8M0 scale per 32 of D; block-scaled QK^T MMA), V/P/O bf16",
 }
 BOUND = {"tiny": "hbm", "self_long": "tensor", "cross_gelu": "hbm", "pma": "hbm", "block_window": "hbm",
-         "sliding_window": "hbm", "cross_silu": "hbm", "pffn": "tensor"}
+         "sliding_window": "hbm", "cross_silu": "hbm", "pffn": "tensor", "self_long_mx": "tensor"}
+# MXFP8 forward: Q K^T on the e4m3 tensor core (nominally twice the bf16
+# rate), P V in bf16, equal FLOPs in each: the peak of the mix is
+# 1 / (0.5 / 2 + 0.5) = 4/3 of the bf16 peak
+MX_PEAK_FACTOR = 4.0 / 3.0
 
 
 def parse_args():
@@ -113,6 +118,8 @@ def kernel_for(batch, gdpa_mod, num_ctas: int) -> str:
     w = batch.workload
     if w.window_blocks < 0:  # sliding windows: 256-row items on the 64-key pair kernel
         return "gdpa_fwd_pair64_kernel"
+    if w.mx:  # MXFP8: single-tile items
+        return "gdpa_fwd_kernel"
     _, _, _, rows, kv_tile = gdpa_mod.gdpa_plan_enumerate(batch.q_offsets, batch.kv_offsets, batch.B, w.H, w.D,
                                                           w.act, w.window_blocks, num_ctas, with_rows=True)
     if rows != 256:
@@ -192,6 +199,12 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def oracle_fwd(batch):
+    import oracle
+
+    return oracle.gdpa_fwd_mx_batch(batch) if batch.workload.mx else oracle.gdpa_fwd_batch(batch)
+
+
 def oracle_sample(batch, target_s: float, seed: int = 2024):
     """A seeded subset of whole sequences sized for ~target_s of oracle CPU time."""
     import oracle
@@ -202,7 +215,7 @@ def oracle_sample(batch, target_s: float, seed: int = 2024):
     probe = [int(order[0])]
     sub = batch.subset(probe)
     t0 = time.perf_counter()
-    oracle.gdpa_fwd_batch(sub)
+    oracle_fwd(sub)
     dt = max(time.perf_counter() - t0, 1e-3)
     rate = useful_flops(sub) / dt  # single-sequence rate: at most H threads busy
     cores = oracle.num_cpus()
@@ -224,7 +237,7 @@ def time_oracle(sample, reps=1):
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
-        oracle.gdpa_fwd_batch(sample)
+        oracle_fwd(sample)
         times.append(time.perf_counter() - t0)
     return times
 
@@ -292,10 +305,16 @@ def run_ours(args, rank, world, local):
     h_qo, h_ko = batch.q_offsets, batch.kv_offsets
     stream = torch.cuda.current_stream()
 
+    if w.mx:
+        q8, qsf, k8, ksf = (torch.from_numpy(np.ascontiguousarray(a)).cuda()
+                            for a in (batch.q8, batch.q_sf, batch.k8, batch.k_sf))
+
     def step():
         if w.window_blocks < 0:
             gdpa.gdpa_fwd_sliding(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, -w.window_blocks, w.scale, out, None,
                                   stream)
+        elif w.mx:
+            gdpa.gdpa_fwd_mx(q8, qsf, k8, ksf, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.scale, out, None, stream)
         else:
             gdpa.gdpa_fwd_async(q, k, v, h_qo, h_ko, qo, ko, B, H, D, w.act, w.window_blocks, w.scale, out, stream)
 
@@ -338,9 +357,10 @@ def run_ours(args, rank, world, local):
     value = total_flops * K / (elapsed_ms / 1e3) / 1e12
 
     # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step);
-    # the host-buffer entry point takes block windows only, so a sliding window has none
+    # the host-buffer entry point takes bf16 inputs and block windows only, so a sliding window
+    # and the MXFP8 forward have none
     e2e = None
-    if w.window_blocks >= 0:
+    if w.window_blocks >= 0 and not w.mx:
         hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
         hk = torch.from_numpy(batch.k.view(np.int16)).pin_memory()
         hv = torch.from_numpy(batch.v.view(np.int16)).pin_memory()
@@ -368,7 +388,7 @@ def run_ours(args, rank, world, local):
     bound = BOUND[args.workload]
     if bound == "tensor":
         achieved = flops / (launch_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        peak = peaks["bf16_tflops"] * (MX_PEAK_FACTOR if w.mx else 1.0)
         unit = "TFLOP/s"
     else:
         achieved = nbytes / (launch_ms / 1e3) / 1e9
@@ -376,8 +396,11 @@ def run_ours(args, rank, world, local):
         unit = "GB/s"
     kernel = kernel_for(batch, gdpa, torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
     traffic = traffic_per_launch(args.workload, kernel)
+    peak_note = " (burst)" if bound == "tensor" else ""
+    if w.mx:
+        peak_note = " (burst bf16 x 4/3: Q K^T at the nominal e4m3 rate of 2x bf16, P V at bf16)"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": traffic, "peak_source": peak_src + (" (burst)" if bound == "tensor" else ""),
+                "traffic": traffic, "peak_source": peak_src + peak_note,
                 "launch_ms": launch_ms, "useful_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
                 "kernel": kernel, "kernel_hash": kernel_hash(kernel)}
 
@@ -395,12 +418,14 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 (Q, K) + bf16" if w.mx else "bf16",
+            "data": "synthetic",
             "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
                        "global_batch": B * world, "tokens_q": Tq, "tokens_kv": int(batch.kv_offsets[-1]),
                        "l2": "inputs %.2f GB > 126 MB L2; no flush" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
                        "parallelism": "dp%d (independent batches, no collective)" % world,
-                       "entry": "gdpa_fwd_async (host plan + upload + kernel per step)"},
+                       "entry": ("gdpa_fwd_mx" if w.mx else "gdpa_fwd_async")
+                                + " (host plan + upload + kernel per step)"},
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": K,

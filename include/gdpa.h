@@ -22,7 +22,7 @@
  *
  * The training entry points keep the softmax row logsumexp in the forward
  * (gdpa_fwd_lse, gdpa_fwd_sliding) and return dq, dk, dv in the backward
- * (gdpa_bwd, gdpa_bwd_sliding).
+ * (gdpa_bwd, gdpa_bwd_sliding).  gdpa_fwd_mx takes q and k in MXFP8.
  *
  * An empty key set gives o_i = 0.  The GELU is evaluated on the ALU only: the
  * tanh is rewritten as a logistic function whose exponential is a range-reduced
@@ -146,6 +146,32 @@ gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const void* v, cons
                                const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets,
                                int B, int H, int D, int act, int window_tokens, float scale, void* out, float* lse,
                                void* stream);
+
+/*
+ * gdpa_fwd_mx -- the forward (full attention) with q and k in MXFP8, the
+ * microscaling FP8 format the techfeed summary of "GEM Training" (section on
+ * MXFP8 ultra-low-precision training) and the aigeeknews translation
+ * (compute-efficiency section, "MXFP8 attention") apply to attention:
+ *
+ *   q8, k8  uint8 [T, H, D]     OCP e4m3 element codes ("E4M3FN": no
+ *                               infinities, S.1111.111 NaN)
+ *   q_sf, k_sf uint8 [T, H, D/32]  OCP E8M0 scale codes, 2^(e - 127): code b
+ *                               of a (token, head) row scales its elements
+ *                               [32 b, 32 b + 32)
+ *   q_id = e4m3(q8_id) * 2^(q_sf_i,floor(d/32) - 127), k likewise
+ *
+ * The score product runs on the block-scaled e4m3 tensor-core MMA with fp32
+ * accumulation; v and out stay bf16, and everything after the scores is
+ * gdpa_fwd_lse's (softmax, GELU or SiLU; lse optional, may be NULL).  D must
+ * be 128 (GDPA_ERR_UNSUPPORTED otherwise), no windows.  q8, k8, v and out
+ * 16-byte aligned, q_sf and k_sf 4-byte aligned (each row's four codes are
+ * read as one 32-bit word).  Offsets twice (host and device) as
+ * gdpa_fwd_async; asynchronous on `stream`.  The buffers stay the caller's.
+ */
+gdpa_status_t gdpa_fwd_mx(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v,
+                          const int32_t* h_q_offsets, const int32_t* h_kv_offsets, const int32_t* q_offsets,
+                          const int32_t* kv_offsets, int B, int H, int D, int act, float scale, void* out, float* lse,
+                          void* stream);
 
 /*
  * gdpa_bwd -- gradients of the forward for an upstream gradient dout:

@@ -125,14 +125,16 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Plans on the host and uploads the work list through the pinned staging
 // buffer into c.d_work (both guarded by events against earlier calls).
+// `single_tile`: one 128-row query tile and 128-key tiles per item whatever
+// the shapes (the MXFP8 kernel's item kind).
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
                               int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
-                              int* kv_tile, int64_t* n_items) {
+                              int* kv_tile, int64_t* n_items, bool single_tile = false) {
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
-  const int rpi = choose_rows_per_item(h_q_off, B, D, window_blocks);
+  const int rpi = single_tile ? kBlockM : choose_rows_per_item(h_q_off, B, D, window_blocks);
   *rows_per_item = rpi;
-  *kv_tile = choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
+  *kv_tile = single_tile ? kBlockN : choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
   const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *n_items = n;
   if (n == 0) {
@@ -168,9 +170,12 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
                               const int32_t* d_q_off, const int32_t* d_kv_off, int64_t Tq, int64_t Tkv, int H, int D,
                               int act, int window_blocks, float scale, int num_ctas, int rows_per_item,
-                              int kv_tile, int64_t n_items, cudaStream_t stream, float* lse = nullptr) {
+                              int kv_tile, int64_t n_items, cudaStream_t stream, float* lse = nullptr,
+                              const void* q_sf = nullptr, const void* k_sf = nullptr) {
   LaunchArgs a;
   a.lse = lse;
+  a.q_sf = q_sf;
+  a.k_sf = k_sf;
   a.rows_per_item = rows_per_item;
   a.kv_tile = kv_tile;
   a.q = q;
@@ -279,9 +284,12 @@ namespace {
 
 // gdpa_fwd_async with an optional logsumexp output and the internal window
 // code (> 0: block window, < 0: sliding window of -window tokens).
+// With q_sf set, q and k are MXFP8 codes with those scale words (full
+// attention, D = 128, single-tile items).
 gdpa_status_t fwd_async_impl(const void* q, const void* k, const void* v, const int32_t* h_q_offsets,
                              const int32_t* h_kv_offsets, const int32_t* q_offsets, const int32_t* kv_offsets, int B,
-                             int H, int D, int act, int window, float scale, void* out, float* lse, void* stream) {
+                             int H, int D, int act, int window, float scale, void* out, float* lse, void* stream,
+                             const void* q_sf = nullptr, const void* k_sf = nullptr) {
   int64_t Tq = 0, Tkv = 0;
   gdpa_status_t st;
   if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window, &Tq, &Tkv)) != GDPA_OK) return st;
@@ -299,10 +307,10 @@ gdpa_status_t fwd_async_impl(const void* q, const void* k, const void* v, const 
   int rpi = 0, kvt = 0;
   int64_t n_items = 0;
   if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, window, sms, s, &num_ctas, &rpi, &kvt,
-                            &n_items)) != GDPA_OK)
+                            &n_items, q_sf != nullptr)) != GDPA_OK)
     return st;
   return launch_with_ctx(c, q, k, v, out, q_offsets, kv_offsets, Tq, Tkv, H, D, act, window, scale, num_ctas, rpi,
-                         kvt, n_items, s, act == GDPA_ACT_SOFTMAX ? lse : nullptr);
+                         kvt, n_items, s, act == GDPA_ACT_SOFTMAX ? lse : nullptr, q_sf, k_sf);
 }
 
 }  // namespace
@@ -330,6 +338,22 @@ extern "C" gdpa_status_t gdpa_fwd_sliding(const void* q, const void* k, const vo
   if (B == 0) return GDPA_OK;
   return fwd_async_impl(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, -window_tokens,
                         scale, out, lse, stream);
+}
+
+extern "C" gdpa_status_t gdpa_fwd_mx(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                     const void* v, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                                     const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                                     float scale, void* out, float* lse, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, 0);
+  if (st != GDPA_OK) return st;
+  if (D != 128) return GDPA_ERR_UNSUPPORTED;
+  if (B == 0) return GDPA_OK;
+  const bool any_q = h_q_offsets && h_q_offsets[B] > 0, any_kv = h_kv_offsets && h_kv_offsets[B] > 0;
+  if (any_q && (!q_sf || (reinterpret_cast<uintptr_t>(q_sf) & 3u) != 0)) return GDPA_ERR_INVALID_ARG;
+  if (any_kv && (!k_sf || (reinterpret_cast<uintptr_t>(k_sf) & 3u) != 0)) return GDPA_ERR_INVALID_ARG;
+  // with no keys k_sf is never read
+  return fwd_async_impl(q8, k8, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, 0, scale, out, lse,
+                        stream, q_sf, k_sf ? k_sf : q_sf);
 }
 
 namespace gdpa {

@@ -45,8 +45,14 @@ namespace gdpa {
 // Item kinds, one kernel instantiation each:
 //   full      128 query rows against the whole key range in 128-key tiles;
 //   window    128 query rows against their block window;
-//   key split at most 32 queries, each warp owns a 32-key block of every tile.
-enum : int { kModeFull = 0, kModeWindow = 1, kModeKeySplit = 2 };
+//   key split at most 32 queries, each warp owns a 32-key block of every tile;
+//   full MX   full attention with MXFP8 Q and K (D = 128): e4m3 tiles, one
+//             E8M0 scale per 32 elements of a row, S = Q K^T by the
+//             block-scaled MMA (32 elements of D per instruction, the scales
+//             read from TMEM); P V stays bf16.  The activation warps put the
+//             next tile's scale words into TMEM while they work on the
+//             current one; the second O buffer gives its columns to them.
+enum : int { kModeFull = 0, kModeWindow = 1, kModeKeySplit = 2, kModeFullMx = 3 };
 
 template <int D, int MODE = kModeFull>
 struct FwdCfg {
@@ -62,10 +68,15 @@ struct FwdCfg {
   static constexpr int NQ = 2;                                // Q stages
   static constexpr int NK = (D == 64) ? 4 : 3;                // K stages
   static constexpr int NV = (D == 64) ? 4 : 2;                // V stages
+  static constexpr bool MX = MODE == kModeFullMx;
+  // staged tile sizes: an e4m3 row of D = 128 is one 128-byte swizzle row
+  static constexpr int Q_BYTES = MX ? BM * D : TILE_BYTES;
+  static constexpr int K_BYTES = MX ? BN * D : KV_TILE_BYTES;
+  static constexpr int V_BYTES = KV_TILE_BYTES;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NK * KV_TILE_BYTES;
-  static constexpr int OFF_L = OFF_V + NV * KV_TILE_BYTES;  // row sums, 2 x 128 floats
+  static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_BYTES;
+  static constexpr int OFF_L = OFF_V + NV * V_BYTES;  // row sums, 2 x 128 floats
   // Key split only: row maxima (2 x 128 floats) and the exchange buffer in
   // which the four warps' partial output rows meet (4 x 32 rows of 64
   // floats, rows padded to 68 floats so that 16-byte accesses by a warp are
@@ -76,7 +87,12 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_X + (KS ? 4 * 32 * X_STRIDE * 4 : 0);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + slack for 1024-byte alignment
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  // O buffers: two (an item's epilogue overlaps the next item), one with MX
+  static constexpr int NOB = MX ? 1 : 2;
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = MX ? 256 : 256 + D;
+  // MX scale words (4 columns a slot, slots 32 columns apart): Q of items
+  // qi & 1, K of tiles g & 1
+  static constexpr uint32_t TM_SFA = 256 + D, TM_SFB = 256 + D + 64;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int THREADS = 384;  // 3 warpgroups
   // Registers per thread after reallocation: control warpgroup, activation
@@ -89,6 +105,7 @@ struct FwdCfg {
   static_assert(TM_O1 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!KS || D == 64, "key split is built for D = 64");
+  static_assert(!MX || (D == 128 && TM_SFB + 32 + 4 <= TM_COLS), "MXFP8 is built for D = 128");
 };
 
 // Shared-memory barrier block.
@@ -102,6 +119,7 @@ struct Bars {
   uint64_t o_empty[2];          // the epilogue has drained O[b] (MMA)
   uint64_t l_full[2], l_empty[2];  // row sums of the item using O[b] (activation <-> epilogue)
   uint64_t x_full, x_empty;     // key split: partial rows written / read (epilogue warps)
+  uint64_t sf_full[2];          // MX: scale words of tile g (and of its item's Q) in TMEM (activation)
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort;
@@ -171,10 +189,12 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& 
       const uint32_t qph = (qi / C::NQ) & 1;
       ok = ptx::mbar_wait(&B.q_empty[qs], qph ^ 1, p.timeout_ns, abort);
       if (!ok) break;
-      ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::TILE_BYTES);
+      ptx::mbar_arrive_expect_tx(&B.q_full[qs], C::Q_BYTES);
       q_armed[qs] = (int)qph;
-      uint8_t* sq = sm + C::OFF_Q + qs * C::TILE_BYTES;
-      if (KS) {  // the (at most) 32 queries in each lane quarter: the Q map's box is 32 rows
+      uint8_t* sq = sm + C::OFF_Q + qs * C::Q_BYTES;
+      if (C::MX) {  // e4m3: the whole row of D = 128 bytes in one box
+        ptx::tma_load_2d(sq, &p.tm_q, &B.q_full[qs], t.h * D, t.q_tok);
+      } else if (KS) {  // the (at most) 32 queries in each lane quarter: the Q map's box is 32 rows
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
@@ -193,19 +213,23 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& 
         const uint32_t ph = (g / C::NK) & 1;
         ok = ptx::mbar_wait(&B.k_empty[si], ph ^ 1, p.timeout_ns, abort);
         if (!ok) break;
-        uint8_t* dst = sm + C::OFF_K + si * C::KV_TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(&B.k_full[si], C::KV_TILE_BYTES);
+        uint8_t* dst = sm + C::OFF_K + si * C::K_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.k_full[si], C::K_BYTES);
+        if (C::MX) {
+          ptx::tma_load_2d(dst, &p.tm_k, &B.k_full[si], t.h * D, y);
+        } else {
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          ptx::tma_load_2d(dst + c * C::KV_CHUNK_BYTES, &p.tm_k, &B.k_full[si], t.h * D + 64 * c, y);
+          for (int c = 0; c < C::KCH; ++c)
+            ptx::tma_load_2d(dst + c * C::KV_CHUNK_BYTES, &p.tm_k, &B.k_full[si], t.h * D + 64 * c, y);
+        }
         k_armed[si] = (int)ph;
       } else {  // V is released once its P V is done
         const int si = g % C::NV;
         const uint32_t ph = (g / C::NV) & 1;
         ok = ptx::mbar_wait(&B.v_empty[si], ph ^ 1, p.timeout_ns, abort);
         if (!ok) break;
-        uint8_t* dst = sm + C::OFF_V + si * C::KV_TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(&B.v_full[si], C::KV_TILE_BYTES);
+        uint8_t* dst = sm + C::OFF_V + si * C::V_BYTES;
+        ptx::mbar_arrive_expect_tx(&B.v_full[si], C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
           ptx::tma_load_2d(dst + c * C::KV_CHUNK_BYTES, &p.tm_v, &B.v_full[si], t.h * D + 64 * c, y);
@@ -241,11 +265,11 @@ __device__ __forceinline__ bool issue_pv(const FwdParams& p, uint8_t* sm, FwdBar
   using C = FwdCfg<D, MODE>;
   volatile int* abort = &B.abort;
   if (!ptx::mbar_wait(&B.p_full[P.sb], (P.g >> 1) & 1, p.timeout_ns, abort)) return false;
-  if (P.first && !ptx::mbar_wait(&B.o_empty[P.ob], ((P.qi >> 1) & 1) ^ 1, p.timeout_ns, abort)) return false;
+  if (P.first && !ptx::mbar_wait(&B.o_empty[P.ob], ((P.qi / C::NOB) & 1) ^ 1, p.timeout_ns, abort)) return false;
   const int sv = P.g % C::NV;
   if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
-  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::KV_TILE_BYTES);
+  const uint32_t v_base = ptx::smem_u32(sm + C::OFF_V + sv * C::V_BYTES);
   const uint32_t o_col = P.ob ? C::TM_O1 : C::TM_O0;
   const uint32_t p_col = P.sb ? C::TM_S1 : C::TM_S0;
   constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
@@ -276,25 +300,38 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, ui
     const int qs = qi % C::NQ;
     ok = ptx::mbar_wait(&B.q_full[qs], (qi / C::NQ) & 1, p.timeout_ns, abort);
     if (!ok) break;
-    const uint32_t q_base = ptx::smem_u32(sm + C::OFF_Q + qs * C::TILE_BYTES);
+    const uint32_t q_base = ptx::smem_u32(sm + C::OFF_Q + qs * C::Q_BYTES);
     for (int j = 0; j < t.n_kv; ++j, ++g) {
       const int s = g % C::NK;
       ok = ptx::mbar_wait(&B.k_full[s], (g / C::NK) & 1, p.timeout_ns, abort);
+      const int sb = g & 1;
+      if (C::MX && ok) ok = ptx::mbar_wait(&B.sf_full[sb], (g >> 1) & 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::tc_fence_after();
       const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
       const int n16 = (ncols + 15) >> 4;
-      const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
-      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + s * C::KV_TILE_BYTES);
-      const int sb = g & 1;
+      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + s * C::K_BYTES);
       const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
+      if constexpr (C::MX) {
+        // 32 e4m3 elements of D = 32 bytes of the 128-byte swizzle row per
+        // MMA, scale byte kk of each row's word; all 128 key columns (the
+        // ragged end's extra columns are masked by the activation).
+        const uint32_t sfa = tmem + C::TM_SFA + 32u * (qi & 1), sfb = tmem + C::TM_SFB + 32u * sb;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
-        const uint32_t qoff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-        const uint32_t koff = (kk >> 2) * C::KV_CHUNK_BYTES + (kk & 3) * 32;
-        ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024), ptx::sdesc_sw128(k_base + koff, 16, 1024),
-                    idesc, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_mx_elect(tmem + s_col, ptx::sdesc_sw128(q_base + 32 * kk, 16, 1024),
+                            ptx::sdesc_sw128(k_base + 32 * kk, 16, 1024), ptx::idesc_mx_e4m3(128, 128, kk), sfa, sfb,
+                            kk > 0 ? 1u : 0u);
+      } else {
+        const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
+          const uint32_t qoff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * C::KV_CHUNK_BYTES + (kk & 3) * 32;
+          ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024),
+                            ptx::sdesc_sw128(k_base + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
       }
       ptx::mma_commit_elect(&B.s_full[sb]);
       ptx::mma_commit_elect(&B.k_empty[s]);
@@ -303,7 +340,7 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, ui
         ok = issue_pv<D, MODE>(p, sm, B, tmem, prev);
         if (!ok) break;
       }
-      prev = PendingPV{g, sb, qi & 1, qi, j == 0 ? 1 : 0, j == t.n_kv - 1 ? 1 : 0, n16};
+      prev = PendingPV{g, sb, qi % C::NOB, qi, j == 0 ? 1 : 0, j == t.n_kv - 1 ? 1 : 0, n16};
       have_prev = true;
     }
     ++qi;
@@ -317,6 +354,43 @@ __device__ void run_mma(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& B, ui
 }
 
 // ------------------------------------------------------------------ activation
+
+// MX: where the activation warps stand in the CTA's tile sequence when they
+// stage scale words -- item index, tile of the item, non-empty item count.
+template <int MODE>
+struct MxCursor {
+  int idx, j, qi;
+  ItemView t;
+  bool valid;
+  __device__ __forceinline__ void seek(const FwdParams& p, int iend) {  // first non-empty item from idx on
+    for (valid = false; idx < iend; ++idx) {
+      t = decode_item<MODE>(p, idx);
+      if (t.n_kv > 0) {
+        valid = true;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void advance(const FwdParams& p, int iend) {
+    if (++j < t.n_kv) return;
+    j = 0;
+    ++qi;
+    ++idx;
+    seek(p, iend);
+  }
+  // This thread's four scale words of the tile (keys 128 j + 32 c + lane) and,
+  // at an item's first tile, of its Q (rows 32 c + lane); scale 1 (0x7F) past
+  // the end.
+  __device__ __forceinline__ void load(const FwdParams& p, int lane, uint32_t (&wk)[4], uint32_t (&wq)[4]) const {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int key = 128 * j + 32 * c + lane, row = 32 * c + lane;
+      wk[c] = key < t.Lkv ? __ldg(p.k_sf + static_cast<size_t>(t.kv_tok + key) * p.H + t.h) : 0x7F7F7F7Fu;
+      wq[c] = (j == 0 && row < t.q_rows) ? __ldg(p.q_sf + static_cast<size_t>(t.q_tok + row) * p.H + t.h)
+                                         : 0x7F7F7F7Fu;
+    }
+  }
+};
 
 // Per-element validity of score column c (tile-relative) for this row.
 __device__ __forceinline__ bool col_ok(int c, int c_lo, int c_hi) { return c >= c_lo && c <= c_hi; }
@@ -340,10 +414,31 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
+  // MX: the scale words of tile 0 go to TMEM now, those of tile g + 1 at the
+  // start of tile g (S(g) complete, so S(g - 1) and the previous item's
+  // Q K^T, the slots' last readers, are too); their loads run a tile ahead.
+  MxCursor<MODE> cur;
+  uint32_t wk[4], wq[4];
+  if constexpr (C::MX) {
+    cur.idx = ibeg;
+    cur.j = 0;
+    cur.qi = 0;
+    cur.seek(p, iend);
+    if (cur.valid) {
+      cur.load(p, lane, wk, wq);
+      ptx::tmem_st4(tmem + lane_off + C::TM_SFB, wk[0], wk[1], wk[2], wk[3]);
+      ptx::tmem_st4(tmem + lane_off + C::TM_SFA, wq[0], wq[1], wq[2], wq[3]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&B.sf_full[0]);
+      cur.advance(p, iend);
+      if (cur.valid) cur.load(p, lane, wk, wq);
+    }
+  }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const ItemView t = decode_item<MODE>(p, idx);
     if (t.n_kv == 0) continue;  // the epilogue writes the zero rows
-    const int ob = qi & 1;
+    const int ob = qi % C::NOB;
     const uint32_t o_addr = tmem + lane_off + (ob ? C::TM_O1 : C::TM_O0);
     float m_run = -INFINITY, l_run = 0.0f;
     const int i_seq = t.q0 + row;  // query index inside its sequence
@@ -361,6 +456,19 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
+      if constexpr (C::MX) {
+        if (cur.valid) {  // tile g + 1: its K scales, and its item's Q scales if it starts one
+          const uint32_t nb = (g + 1) & 1;
+          ptx::tmem_st4(tmem + lane_off + C::TM_SFB + 32 * nb, wk[0], wk[1], wk[2], wk[3]);
+          if (cur.j == 0)
+            ptx::tmem_st4(tmem + lane_off + C::TM_SFA + 32 * (cur.qi & 1), wq[0], wq[1], wq[2], wq[3]);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&B.sf_full[nb]);
+          cur.advance(p, iend);
+          if (cur.valid) cur.load(p, lane, wk, wq);
+        }
+      }
       const uint32_t s_addr = tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0);
       float alpha = 1.0f;
       bool rescale = false;
@@ -608,7 +716,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
     }
     if (!ok) break;
     if (ACT == kActSoftmax) {  // hand the row sum to the epilogue
-      ok = ptx::mbar_wait(&B.l_empty[ob], ((qi >> 1) & 1) ^ 1, p.timeout_ns, abort);
+      ok = ptx::mbar_wait(&B.l_empty[ob], ((qi / C::NOB) & 1) ^ 1, p.timeout_ns, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       l_buf[ob * 128 + row] = l_run;
@@ -747,8 +855,8 @@ __device__ void run_epilogue(const FwdParams& p, FwdBars<D, MODE>& B, const floa
       }
       continue;
     }
-    const int ob = qi & 1;
-    const uint32_t ph = (qi >> 1) & 1;
+    const int ob = qi % C::NOB;
+    const uint32_t ph = (qi / C::NOB) & 1;
     if constexpr (KS) {
       ok = epilogue_key_split<D, ACT>(p, B, l_buf, m_buf, x_buf, tmem, t, ob, ph, xr, quarter, lane, v8);
       ++qi;
@@ -831,6 +939,8 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
     ptx::mbar_init(&B.o_done, 1);
     ptx::mbar_init(&B.x_full, 128);
     ptx::mbar_init(&B.x_empty, 128);
+    ptx::mbar_init(&B.sf_full[0], 128);
+    ptx::mbar_init(&B.sf_full[1], 128);
     ptx::mbar_init(&B.mma_drain, 1);
     B.abort = 0;
     ptx::fence_mbar_init();

@@ -79,6 +79,10 @@ struct LaunchArgs {
   float scale;
   void* stream;
   float* lse = nullptr;   // optional: softmax row logsumexp [Tq, H]
+  // MXFP8 Q and K: q, k hold e4m3 codes [T, H, D] and these the E8M0 scale
+  // words [T, H] (4 codes each); full attention, D = 128, single-tile items
+  const void* q_sf = nullptr;
+  const void* k_sf = nullptr;
 };
 
 // Backward launch: work lists of int4 {sequence, head, first row, 0} on the

@@ -54,6 +54,21 @@ gdpa_status_t encode_rows(CUtensorMap* m, const void* base, int64_t rows, int H,
   return r == CUDA_SUCCESS ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
+// 2-D view of a [rows, H, 128] byte tensor (e4m3 codes) as [rows, H*128];
+// boxes of `box_rows` rows x 128 bytes (the swizzle width).
+gdpa_status_t encode_rows_u8(CUtensorMap* m, const void* base, int64_t rows, int H, int D, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return GDPA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
 int* status_ptr(int device) {
   static std::mutex mu;
   static int* ptrs[kMaxDevices] = {};
@@ -204,7 +219,11 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   if (!status) return GDPA_ERR_CUDA;
   FwdParams prm;
   const bool key_split = a.rows_per_item == kKeySplitRows;
-  gdpa_status_t st = encode_rows(&prm.tm_q, a.q, a.Tq, a.H, a.D, key_split ? kKeySplitRows : kBlockM);
+  const bool mx = a.q_sf != nullptr;
+  if (mx && (a.D != 128 || a.rows_per_item != kBlockM || a.kv_tile != kBlockN || a.window_blocks != 0 || !a.k_sf))
+    return GDPA_ERR_INVALID_ARG;
+  gdpa_status_t st = mx ? encode_rows_u8(&prm.tm_q, a.q, a.Tq, a.H, a.D, kBlockM)
+                        : encode_rows(&prm.tm_q, a.q, a.Tq, a.H, a.D, key_split ? kKeySplitRows : kBlockM);
   if (st != GDPA_OK) return st;
   // With no keys at all no K/V tile is ever loaded; any valid address will do.
   const void* kb = a.Tkv > 0 ? a.k : a.q;
@@ -212,8 +231,20 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   const int64_t kv_rows = a.Tkv > 0 ? a.Tkv : a.Tq;
   if (a.kv_tile != kBlockN && !(a.kv_tile == kBlockN / 2 && a.rows_per_item == 2 * kBlockM)) return GDPA_ERR_INVALID_ARG;
   const int kv_box = a.kv_tile;  // rows of a K/V tile the kernel stages
-  if ((st = encode_rows(&prm.tm_k, kb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
-  if ((st = encode_rows(&prm.tm_v, vb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
+  if (mx) {
+    if (a.Tkv > 0) {
+      if ((st = encode_rows_u8(&prm.tm_k, a.k, a.Tkv, a.H, a.D, kv_box)) != GDPA_OK) return st;
+      if ((st = encode_rows(&prm.tm_v, a.v, a.Tkv, a.H, a.D, kv_box)) != GDPA_OK) return st;
+    } else {  // nothing is loaded; maps over Q's codes keep the descriptors valid
+      if ((st = encode_rows_u8(&prm.tm_k, a.q, a.Tq, a.H, a.D, kv_box)) != GDPA_OK) return st;
+      if ((st = encode_rows_u8(&prm.tm_v, a.q, a.Tq, a.H, a.D, kv_box)) != GDPA_OK) return st;
+    }
+  } else {
+    if ((st = encode_rows(&prm.tm_k, kb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
+    if ((st = encode_rows(&prm.tm_v, vb, kv_rows, a.H, a.D, kv_box)) != GDPA_OK) return st;
+  }
+  prm.q_sf = static_cast<const uint32_t*>(a.q_sf);
+  prm.k_sf = static_cast<const uint32_t*>(a.k_sf);
   prm.items = reinterpret_cast<const int4*>(a.items);
   prm.cta_begin = a.cta_begin;
   prm.q_off = a.q_off;
@@ -261,6 +292,9 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
                                        : launch_t<64, kActSoftmax, kModeKeySplit>(prm, a.num_ctas, s, device);
   }
   if (a.rows_per_item != kBlockM) return GDPA_ERR_INVALID_ARG;
+  if (mx)
+    return a.act != GDPA_ACT_SOFTMAX ? launch_t<128, kActGelu, kModeFullMx>(prm, a.num_ctas, s, device)
+                                       : launch_t<128, kActSoftmax, kModeFullMx>(prm, a.num_ctas, s, device);
   const int mode = win ? kModeWindow : kModeFull;
   if (a.D == 128) return launch_single<128>(a.act, mode, prm, a.num_ctas, s, device);
   if (a.D == 64) return launch_single<64>(a.act, mode, prm, a.num_ctas, s, device);

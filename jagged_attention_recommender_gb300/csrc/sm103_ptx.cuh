@@ -142,6 +142,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: e4m3 A and B,
+// both K-major, fp32 accumulator, E8M0 scales (bit 23), shape M x N.  Each
+// operand's scales sit in TMEM as 32-bit words of four E8M0 codes; `sf_id`
+// (bits 4-5 for B, 29-30 for A) picks the byte an MMA uses, i.e. which
+// 32-element block of K it covers.  Layout of the words (established on
+// sm_103a with a one-MMA test of distinct codes): A row m reads lane m,
+// column m / 32 of its scale area; B row n reads column n / 32 at lane
+// n % 32 of the lane quarter of the accumulator row being computed, so B's
+// 32 x 4 words are repeated in all four quarters -- writing the repeated
+// pattern (lane quarter q, lane r, column c <- row 32 c + r) serves both.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         (sf_id << 29);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -196,6 +211,20 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled e4m3 MMA (32 elements of K per instruction, one E8M0 scale
+// per row and operand): D[tmem] (+)= (A * sA) (B * sB)^T.
+__device__ __forceinline__ void mma_mx_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred e, p;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %6, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // The elected lane is the same for every call of a converged warp, so the
 // commit tracks the MMAs that lane issued.
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
@@ -245,6 +274,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 // tcgen05.wait::ld that also "writes" r[0..63]: uses of those registers

@@ -27,7 +27,7 @@ GDPA_ERR_DEVICE_TIMEOUT = 4
 GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
-EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
            "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_fwd_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P]
     L.gdpa_fwd_lse.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
     L.gdpa_fwd_sliding.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
+    L.gdpa_fwd_mx.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, P, P]
     L.gdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_bwd_sliding.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
@@ -155,6 +156,15 @@ def gdpa_fwd_sliding(q, k, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, 
     _check(lib().gdpa_fwd_sliding(_addr(q), _addr(k), _addr(v), qo.ctypes.data, ko.ctypes.data, _addr(q_offsets),
                                   _addr(kv_offsets), int(B), int(H), int(D), int(act), int(window_tokens),
                                   float(scale), _addr(out), _addr(lse), _stream(stream)), "gdpa_fwd_sliding")
+
+
+def gdpa_fwd_mx(q8, q_sf, k8, k_sf, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, scale, out,
+                lse=None, stream=None):
+    """The forward with MXFP8 ``q8``/``k8`` (e4m3 codes) and E8M0 block scales ``q_sf``/``k_sf``."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    _check(lib().gdpa_fwd_mx(_addr(q8), _addr(q_sf), _addr(k8), _addr(k_sf), _addr(v), qo.ctypes.data,
+                             ko.ctypes.data, _addr(q_offsets), _addr(kv_offsets), int(B), int(H), int(D), int(act),
+                             float(scale), _addr(out), _addr(lse), _stream(stream)), "gdpa_fwd_mx")
 
 
 def gdpa_bwd(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, window_blocks,

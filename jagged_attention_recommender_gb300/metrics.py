@@ -41,7 +41,11 @@ def useful_flops(batch: JaggedBatch) -> float:
 
 
 def algorithmic_bytes(batch: JaggedBatch) -> float:
-    """Read Q, K, V once and write O once, bf16."""
+    """Read Q, K, V once and write O once, bf16 (MXFP8 Q and K: one byte an
+    element plus one scale byte per 32)."""
     Tq = int(batch.q_offsets[-1])
     Tkv = int(batch.kv_offsets[-1])
+    if batch.workload.mx:
+        qk = batch.H * batch.D * (1.0 + 1.0 / 32)
+        return qk * (Tq + Tkv) + 2.0 * batch.H * batch.D * (Tq + Tkv)
     return 2.0 * batch.H * batch.D * (2 * Tq + 2 * Tkv)
