@@ -58,6 +58,18 @@ def test_shape_validation_needs_no_gpu():
     gdpa.gdpa_fwd(0, 0, 0, 0, 0, 0, 1, 64, 0, 0, 1.0, 0, stream=0)
 
 
+def test_mx_argument_checks_need_no_gpu():
+    # gdpa_fwd_mx: D other than 128, a misaligned or missing scale pointer, a
+    # bad activation -- all rejected before any CUDA call
+    qo = np.array([0, 64], np.int32)
+    for D, q_sf, act, code in ((64, 256, 0, gdpa.GDPA_ERR_UNSUPPORTED), (128, 257, 0, gdpa.GDPA_ERR_INVALID_ARG),
+                               (128, 0, 0, gdpa.GDPA_ERR_INVALID_ARG), (128, 256, 9, gdpa.GDPA_ERR_INVALID_ARG)):
+        with pytest.raises(gdpa.GdpaError) as e:
+            gdpa.gdpa_fwd_mx(256, q_sf, 256, 256, 256, qo, qo, 0, 0, 1, 1, D, act, 1.0, 256, stream=0)
+        assert e.value.code == code
+    gdpa.gdpa_fwd_mx(0, 0, 0, 0, 0, np.zeros(1, np.int32), np.zeros(1, np.int32), 0, 0, 0, 1, 128, 0, 1.0, 0, stream=0)
+
+
 def test_enumerate_rejects_bad_offsets():
     for qo, ko, wb in [([0, 5, 3], [0, 1, 2], 0),   # decreasing
                        ([1, 5], [0, 5], 0),         # not starting at 0
