@@ -31,12 +31,13 @@ def _worker(rank, world, port, name, B, q):
         import oracle
 
         batch = make_batch(name, B=B, seed=31)
+        fwd = oracle.gdpa_fwd_mx_batch if batch.workload.mx else oracle.gdpa_fwd_batch
         sub, seqs = shard(batch, rank, world)
-        out = oracle.gdpa_fwd_batch(sub, nthreads=2)
+        out = fwd(sub, nthreads=2)
         gathered = [None] * world if rank == 0 else None
         dist.gather_object((seqs, out), gathered, dst=0)
         if rank == 0:
-            full = oracle.gdpa_fwd_batch(batch, nthreads=2)
+            full = fwd(batch, nthreads=2)
             got = np.full_like(full, np.nan)
             all_seqs = []
             for s, o in gathered:
@@ -48,7 +49,7 @@ def _worker(rank, world, port, name, B, q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("name,B", [("self_long", 6), ("block_window", 3), ("cross_gelu", 5)])
+@pytest.mark.parametrize("name,B", [("self_long", 6), ("block_window", 3), ("cross_gelu", 5), ("self_long_mx", 6)])
 def test_two_rank_shards_reassemble_exactly(name, B):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
