@@ -116,3 +116,29 @@ def test_to_mx_is_the_ocp_recipe():
     # e4m3 spacing at |y|: 2^(floor(log2|y|) - 3), at least 2^-9 (subnormals)
     ulp = np.ldexp(1.0, np.maximum(np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -9))) - 3, -9).astype(np.int64))
     assert np.all(np.abs(dec / np.ldexp(1.0, e)[..., None] - y) <= ulp / 2)
+
+
+def test_mx_forward_closed_form_two_blocks():
+    """A hand-built case: D = 64 (two scale blocks), one query, two keys.
+    e4m3 codes: 0x38 = 1.0, 0x3C = 1.5, 0x30 = 0.5, 0xB8 = -1.0; E8M0 codes:
+    126 = 1/2, 127 = 1, 128 = 2, 129 = 4.
+      q  = [2 x32, 0.75 x32]           (1.0 * 2, 1.5 * 1/2)
+      k0 = [1 x32, 4 x32]              (1.0 * 1, 1.0 * 4)
+      k1 = [0.5 x32, -1 x32]           (0.5 * 1, -1.0 * 1)
+    so <q, k0> = 64 + 96 = 160, <q, k1> = 32 - 24 = 8; with scale 1/32 the
+    scores are 5 and 1/4, and with v0 = 1, v1 = -2 the softmax output is
+    (e^5 - 2 e^(1/4)) / (e^5 + e^(1/4)) in every coordinate."""
+    import math
+
+    D = 64
+    q8 = np.concatenate([np.full(32, 0x38), np.full(32, 0x3C)]).astype(np.uint8).reshape(1, 1, D)
+    qs = np.array([128, 126], np.uint8).reshape(1, 1, 2)
+    k8 = np.stack([np.full(D, 0x38), np.concatenate([np.full(32, 0x30), np.full(32, 0xB8)])]).astype(np.uint8)
+    k8 = k8.reshape(2, 1, D)
+    ks = np.array([[127, 129], [127, 127]], np.uint8).reshape(2, 1, 2)
+    v = f32_to_bf16_bits(np.stack([np.full(D, 1.0), np.full(D, -2.0)]).astype(np.float32)).reshape(2, 1, D)
+    o = np.array([0, 1], np.int32)
+    ko = np.array([0, 2], np.int32)
+    got = oracle.gdpa_fwd_mx(q8, qs, k8, ks, v, o, ko, 1, D, ACT_SOFTMAX, 0, 1.0 / 32)
+    want = (math.exp(5.0) - 2.0 * math.exp(0.25)) / (math.exp(5.0) + math.exp(0.25))
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
