@@ -35,7 +35,8 @@
  *   k, v bf16 [Tkv, H, D]   row-major, contiguous, Tkv = kv_offsets[B]
  *   out  bf16 [Tq,  H, D]   every row is written (zeros for empty key sets)
  *   q_offsets, kv_offsets  int32 [B+1], offsets[0] = 0, non-decreasing
- * q, k, v and out must be 16-byte aligned.  D must be 64 or 128.  Tq and Tkv
+ * q, k, v and out must be 16-byte aligned.  D must be 64 or 128 (128 for
+ * gdpa_fwd_mx, whose q and k are e4m3 codes with E8M0 scales).  Tq and Tkv
  * must be below 2^31.  Windows (block or sliding) require q_offsets ==
  * kv_offsets and act == GDPA_ACT_SOFTMAX.
  *
