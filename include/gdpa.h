@@ -72,7 +72,7 @@ typedef enum {
 typedef enum {
   GDPA_OK = 0,
   GDPA_ERR_INVALID_ARG = 1,    /* bad pointer, size, offsets or combination */
-  GDPA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  GDPA_ERR_UNSUPPORTED = 2,    /* valid request the library does not implement */
   GDPA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
   GDPA_ERR_DEVICE_TIMEOUT = 4, /* a kernel wait ran out of time (device status word) */
   GDPA_ERR_NO_MEMORY = 5       /* host or device allocation failed, or capacity too small */
