@@ -10,8 +10,15 @@ between steps.
 
 Prints one JSON line (rank 0).  ``value`` is useful TFLOPS: 4*D*H per
 unmasked (query, key) pair, summed over all ranks, over the max-over-ranks
-time.  ``--impl reference`` times the fp64 CPU oracle instead (the slow
-baseline arm) on a bounded sample of the same workload.
+time.  With the default workload (self_long, the headline) the line also
+carries a ``workloads`` object: the other configurations of the metric
+(tiny, cross_gelu, pma, block_window), each timed the same way with its own
+roofline, end-to-end figure and clock record.  Under torchrun each rank
+takes its LPT shard (whole sequences) of one seeded global batch of N times
+the workload's sequences, so per-GPU work stays about fixed (weak scaling)
+and no data moves between ranks.  ``--impl reference`` times the fp64 CPU
+oracle instead (the slow baseline arm) on a bounded sample of the same
+workload.
 
 ``--pass backward`` times the training backward instead (``gdpa_bwd``: dq,
 dk, dv from the forward's output and row logsumexp, which are computed once
@@ -74,6 +81,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the headline workload only (skip the other configurations of the metric)")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
     return ap.parse_args()
 
@@ -274,22 +283,40 @@ def run_reference(args, rank, world):
     return 0
 
 
-def run_ours(args, rank, world, local):
+# The configurations of the target metric besides the headline one; each is
+# timed the same way and reported under "workloads" in the JSON line.
+NORTH_STAR_OTHERS = ["tiny", "cross_gelu", "pma", "block_window"]
+
+
+def bench_batch(name: str, rank: int, world: int):
+    """The rank's batch: at N = 1 the workload's seeded batch; at N > 1 the
+    rank's LPT shard (whole sequences, shard.partition_sequences) of one
+    seeded global batch of N times the workload's sequences, so per-GPU work
+    stays about fixed (weak scaling) and no data moves between ranks.  Values
+    are drawn for the rank's own sequences only.  Returns (batch, per-rank
+    useful FLOPs of every rank)."""
+    from jagged_attention_recommender_gb300.metrics import key_count
+    from jagged_attention_recommender_gb300.shard import partition_sequences
+    from jagged_attention_recommender_gb300.workloads import draw_lengths
+
+    w = WORKLOADS[name]
+    if world == 1:
+        batch = make_batch(name)
+        return batch, [useful_flops(batch)]
+    Lq, Lkv = draw_lengths(w, np.random.default_rng(w.seed), w.B * world)
+    parts = partition_sequences(Lq, Lkv, world, w.window_blocks)
+    per_rank = [4.0 * w.D * w.H * sum(key_count(int(Lq[s]), int(Lkv[s]), w.window_blocks) for s in p)
+                for p in parts]
+    mine = parts[rank]
+    return make_batch(name, seed=w.seed + 1000 * rank, lengths=(Lq[mine], Lkv[mine])), per_rank
+
+
+def measure_forward(name, args, rank, world, local, dist, gdpa, with_e2e=True):
+    """Times K steps of one workload's forward pass; returns the measurement dict."""
     import torch
 
-    from jagged_attention_recommender_gb300 import build as gbuild
-    from jagged_attention_recommender_gb300 import gdpa
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    gbuild.build()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = WORKLOADS[args.workload]
-    batch = make_batch(args.workload, seed=w.seed + 1000 * rank)
+    w = WORKLOADS[name]
+    batch, per_rank = bench_batch(name, rank, world)
     flops = useful_flops(batch)
     nbytes = algorithmic_bytes(batch)
     H, D, B = w.H, w.D, batch.B
@@ -323,7 +350,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     st = gdpa.gdpa_device_status()
     if st != gdpa.GDPA_OK:
-        raise SystemExit("device status after warm-up: " + gdpa.gdpa_status_string(st))
+        raise SystemExit("%s: device status after warm-up: %s" % (name, gdpa.gdpa_status_string(st)))
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -346,21 +373,21 @@ def run_ours(args, rank, world, local):
     clocks = sampler.stop()
     st = gdpa.gdpa_device_status()
     if st != gdpa.GDPA_OK:
-        raise SystemExit("device status after timing: " + gdpa.gdpa_status_string(st))
+        raise SystemExit("%s: device status after timing: %s" % (name, gdpa.gdpa_status_string(st)))
     elapsed_ms = e0.elapsed_time(e1)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     if dist:
         t = torch.tensor([elapsed_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    total_flops = flops * world
+    total_flops = float(sum(per_rank))
     value = total_flops * K / (elapsed_ms / 1e3) / 1e12
 
     # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step);
     # the host-buffer entry point takes bf16 inputs and block windows only, so a sliding window
     # and the MXFP8 forward have none
     e2e = None
-    if w.window_blocks >= 0 and not w.mx:
+    if with_e2e and w.window_blocks >= 0 and not w.mx:
         hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
         hk = torch.from_numpy(batch.k.view(np.int16)).pin_memory()
         hv = torch.from_numpy(batch.v.view(np.int16)).pin_memory()
@@ -383,9 +410,10 @@ def run_ours(args, rank, world, local):
         e2e_value = total_flops / e2e_s / 1e12
         e2e = {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3, "entry": "gdpa_fwd_host"}
+        del hq, hk, hv, ho
 
     peaks, peak_src = load_peaks()
-    bound = BOUND[args.workload]
+    bound = BOUND[name]
     if bound == "tensor":
         achieved = flops / (launch_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"] * (MX_PEAK_FACTOR if w.mx else 1.0)
@@ -395,7 +423,7 @@ def run_ours(args, rank, world, local):
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     kernel = kernel_for(batch, gdpa, torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
-    traffic = traffic_per_launch(args.workload, kernel)
+    traffic = traffic_per_launch(name, kernel) if world == 1 else None
     peak_note = " (burst)" if bound == "tensor" else ""
     if w.mx:
         peak_note = " (burst bf16 x 4/3: Q K^T at the nominal e4m3 rate of 2x bf16, P V at bf16)"
@@ -403,6 +431,32 @@ def run_ours(args, rank, world, local):
                 "traffic": traffic, "peak_source": peak_src + peak_note,
                 "launch_ms": launch_ms, "useful_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
                 "kernel": kernel, "kernel_hash": kernel_hash(kernel)}
+    res = {"name": name, "batch": batch, "B": B, "Tq": Tq, "Tkv": int(batch.kv_offsets[-1]), "K": K,
+           "elapsed_ms": elapsed_ms, "ms_per_step": elapsed_ms / K, "value": value, "clocks": clocks, "e2e": e2e,
+           "roofline": roofline, "flops": flops, "per_rank_flops": per_rank,
+           "input_gb": (q.numel() + k.numel() + v.numel()) * 2 / 1e9}
+    del q, k, v, out, qo, ko
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from jagged_attention_recommender_gb300 import build as gbuild
+    from jagged_attention_recommender_gb300 import gdpa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    gbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    head = measure_forward(args.workload, args, rank, world, local, dist, gdpa)
+    w = WORKLOADS[args.workload]
+    batch, B, Tq, K = head["batch"], head["B"], head["Tq"], head["K"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,26 +466,43 @@ def run_ours(args, rank, world, local):
         t = time_oracle(sample)[0]
         cpu = {"value": useful_flops(sample) / t / 1e12, "unit": "TFLOPS", "cores": oracle.num_cpus(),
                "kind": "oracle", "sample": "%d of %d sequences (seeded), all %d heads, %.3g useful GFLOP, %.1f s" % (
-                   len(seqs), B, H, useful_flops(sample) / 1e9, t)}
+                   len(seqs), B, w.H, useful_flops(sample) / 1e9, t)}
+    del head["batch"], batch
 
+    others = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        for name in NORTH_STAR_OTHERS:
+            r = measure_forward(name, args, rank, world, local, dist, gdpa)
+            others[name] = {"workload": "%s: %s" % (name, RECIPES[name]), "ms_per_step": r["ms_per_step"],
+                            "value": r["value"], "unit": "TFLOPS", "roofline": r["roofline"], "e2e": r["e2e"],
+                            "clocks": r["clocks"], "tokens_q": r["Tq"], "tokens_kv": r["Tkv"],
+                            "gpu_launches": r["K"]}
+            del r
+
+    per_rank = head["per_rank_flops"]
+    skew = max(per_rank) / (sum(per_rank) / len(per_rank)) if sum(per_rank) > 0 else 1.0
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": "TFLOPS", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 (Q, K) + bf16" if w.mx else "bf16",
             "data": "synthetic",
             "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
-                       "global_batch": B * world, "tokens_q": Tq, "tokens_kv": int(batch.kv_offsets[-1]),
-                       "l2": "inputs %.2f GB > 126 MB L2; no flush" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
-                       "parallelism": "dp%d (independent batches, no collective)" % world,
+                       "global_batch": w.B * world, "tokens_q": Tq, "tokens_kv": head["Tkv"],
+                       "l2": "inputs %.2f GB > 126 MB L2; no flush" % head["input_gb"],
+                       "parallelism": ("dp%d: LPT shard of one seeded batch of %d sequences, whole sequences per "
+                                       "rank, no collective; useful-FLOP skew max/mean %.4f"
+                                       % (world, w.B * world, skew)) if world > 1 else "dp1",
                        "entry": ("gdpa_fwd_mx" if w.mx else "gdpa_fwd_async")
                                 + " (host plan + upload + kernel per step)"},
-            "clocks": clocks,
-            "e2e": e2e,
+            "clocks": head["clocks"],
+            "e2e": head["e2e"],
             "gpu_launches": K,
-            "roofline": roofline,
+            "roofline": head["roofline"],
             "cpu_baseline": cpu,
         }
+        if others:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -459,7 +530,7 @@ def run_backward(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = WORKLOADS[args.workload]
-    batch = make_batch(args.workload, seed=w.seed + 1000 * rank)
+    batch, per_rank = bench_batch(args.workload, rank, world)
     flops = 2.5 * useful_flops(batch)
     nbytes = backward_bytes(batch)
     H, D, B = w.H, w.D, batch.B
@@ -527,7 +598,7 @@ def run_backward(args, rank, world, local):
         t = torch.tensor([elapsed_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    value = flops * world * K / (elapsed_ms / 1e3) / 1e12
+    value = 2.5 * sum(per_rank) * K / (elapsed_ms / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     bound = BOUND[args.workload]
     if bound == "tensor":
@@ -575,10 +646,11 @@ def run_backward(args, rank, world, local):
             "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "%s: %s" % (args.workload, RECIPES[args.workload]), "seed": w.seed,
-                       "pass": "backward", "global_batch": B * world, "tokens_q": Tq, "tokens_kv": Tkv,
+                       "pass": "backward", "global_batch": w.B * world, "tokens_q": Tq, "tokens_kv": Tkv,
                        "l2": "inputs %.2f GB > 126 MB L2; no flush" % (
                            (q.numel() + k.numel() + v.numel() + out.numel() + dout.numel()) * 2 / 1e9),
-                       "parallelism": "dp%d (independent batches, no collective)" % world,
+                       "parallelism": ("dp%d: LPT shard of one seeded batch of %d sequences, no collective"
+                                       % (world, w.B * world)) if world > 1 else "dp1",
                        "entry": "gdpa_bwd (host work lists + upload + 3 kernels per step)"},
             "clocks": clocks,
             "e2e": None,

@@ -218,18 +218,26 @@ gdpa_status_t gdpa_bwd_sliding(const void* q, const void* k, const void* v, cons
  * go around its own caching allocator.  This call allocates nothing -- no
  * cudaMalloc, cudaFree, cudaMallocHost or other allocating routine -- on the
  * device or the host: the work list lives in a file-scope device array of
- * 4 MiB (every GPU that loads the library holds it until the process exits)
- * and is planned in fixed host arrays.
- * Arguments, layout and results are those of gdpa_fwd (device offsets, one
- * synchronisation of `stream` to read them).  Limits: B <= 65536 sequences
- * and at most 261632 work items (query tiles x heads, about 33M query rows
- * x heads); larger requests return GDPA_ERR_NO_MEMORY before any GPU work.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call shares the array and the host arrays: calls are serialised on the
- * host, but two calls whose kernels overlap on the GPU (different streams)
- * race on the work list -- order them on one stream or synchronise between
- * them.  Each call rewrites the whole part of the array its launch reads.
+ * 4 MiB and is planned in fixed host arrays by the same planner gdpa_fwd
+ * uses.
+ * Arguments, layout and results are those of gdpa_fwd (device offsets; every
+ * call copies them to the host and synchronises `stream`).  Limits: B <= 65536
+ * sequences and at most 261632 work items (query tiles x heads, about 33M
+ * query rows x heads); larger requests return GDPA_ERR_NO_MEMORY before any
+ * GPU work.
+ * First call on a device: it looks up the array's device address (with that
+ * device current); make it before any stream capture.  With CUDA's lazy
+ * module loading (the default), the driver loads the array and the kernels
+ * onto a device the first time they are used there, and that load reserves
+ * device memory (the 4 MiB array and the kernels' code); a device holds them
+ * from then until the process exits.  A caller that carves device memory
+ * into an arena should therefore make one small call per device at start-up,
+ * before carving it (or load modules eagerly, CUDA_MODULE_LOADING=EAGER).
+ * Every call shares the array and the host arrays: calls are serialised on
+ * the host, but two calls whose kernels overlap on the GPU (different
+ * streams) race on the work list -- order them on one stream or synchronise
+ * between them.  Each call rewrites the whole part of the array its launch
+ * reads.
  */
 gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const void* v, const int32_t* q_offsets,
                                const int32_t* kv_offsets, int B, int H, int D, int act, int window_blocks,

@@ -57,6 +57,36 @@ int64_t plan_item_cost(int64_t q0, int64_t Lq, int64_t Lkv, int window_blocks, i
 // Number of work items plan_items will emit.
 int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item);
 
+// Working storage of one planning pass, all of it owned by the caller:
+// `cap_items` entries in each per-item array, `cap_buckets` counting-sort
+// cursors (the planner falls back to an in-place sort of `keys` when the
+// costs need more), and `max_leaves` >= the CTA count rounded up to a power
+// of two entries in `load` (2 * max_leaves in `tree`, num_ctas in `count`).
+struct PlanStorage {
+  gdpa_work_item_t* items;
+  int64_t* cost;
+  uint32_t* order;
+  int32_t* owner;
+  uint64_t* keys;
+  uint32_t* bucket;
+  int64_t* load;
+  int32_t* tree;
+  int32_t* count;
+  int64_t cap_items;
+  int64_t cap_buckets;
+  int max_leaves;
+};
+
+// The planner: enumerates the items, orders them by decreasing cost and
+// assigns each to the least-loaded CTA.  Writes *n_out items to items_out
+// grouped by CTA (decreasing cost within a CTA), cta_begin[num_ctas + 1] and,
+// if cost_out is not null, each item's cost.  Allocates nothing;
+// GDPA_ERR_NO_MEMORY if the storage is too small.
+gdpa_status_t plan_items_into(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
+                              int rows_per_item, int num_ctas, const PlanStorage& st, gdpa_work_item_t* items_out,
+                              int32_t* cta_begin, int64_t* cost_out, int64_t* n_out);
+
+// plan_items_into over storage it allocates (std::vector; may throw bad_alloc).
 gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
                          int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items,
                          std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost);

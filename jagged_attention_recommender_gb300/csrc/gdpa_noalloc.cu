@@ -30,16 +30,21 @@ constexpr size_t kNaScratchBytes = kNaItemBytes + (size_t)(kNaMaxCtas + 1) * siz
 static_assert(kNaScratchBytes == (size_t)4 << 20, "scratch is 4 MiB");
 
 // Work list of the most recent call (items grouped by CTA, then cta_begin).
-// Every GPU that loads the library holds these 4 MiB until the process exits.
+// A device holds these 4 MiB from the moment the driver loads this module
+// onto it (at the first call there, under lazy module loading) until the
+// process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes];
 
 // Host-side staging and planner arrays: static storage, shared by every call.
+constexpr int kNaBuckets = 1 << 16;  // counting-sort cursors; costlier batches sort in place
 struct NoAllocHost {
   int32_t offsets[2 * (kNaMaxBatch + 1)];
   gdpa_work_item_t items[kNaMaxItems];
   int64_t cost[kNaMaxItems];
-  uint64_t keys[kNaMaxItems];
+  uint32_t order[kNaMaxItems];
   int32_t owner[kNaMaxItems];
+  uint64_t keys[kNaMaxItems];
+  uint32_t bucket[kNaBuckets];
   int64_t load[2048];
   int32_t tree[4096];
   int32_t count[2048];
@@ -49,61 +54,17 @@ static NoAllocHost g_host;
 static std::mutex g_mu;
 static void* g_dev_scratch[64];
 
-// The planner of gdpa_plan.cpp restated over fixed arrays: same items, same
-// cost model, same longest-processing-time-first order and CTA choice.
+// The library's planner (plan_items_into, the same routine gdpa_fwd uses)
+// over the fixed arrays; the work list lands in the upload image: items at
+// offset 0, cta_begin at kNaItemBytes.
 gdpa_status_t na_plan(const int32_t* qo, const int32_t* ko, int B, int H, int window_blocks, int rows_per_item,
-                      int num_ctas, int64_t* n_out, size_t* bytes_out) {
-  int64_t n = 0;
-  for (int b = 0; b < B; ++b) {
-    const int64_t Lq = qo[b + 1] - qo[b], Lkv = ko[b + 1] - ko[b];
-    for (int64_t q0 = 0; q0 < Lq; q0 += rows_per_item) {
-      const int64_t kv0 = window_blocks > 0 ? window_start(q0, window_blocks) : 0;
-      const int64_t c = plan_item_cost(q0, Lq, Lkv, window_blocks, rows_per_item);
-      for (int h = 0; h < H; ++h) {
-        if (n >= kNaMaxItems) return GDPA_ERR_NO_MEMORY;
-        g_host.items[n] = gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0};
-        g_host.cost[n] = c;
-        ++n;
-      }
-    }
-  }
-  for (int64_t i = 0; i < n; ++i) {
-    const uint64_t c = (uint64_t)std::min<int64_t>(g_host.cost[i], 0x7FFFFFFF);
-    g_host.keys[i] = ((0x7FFFFFFFull - c) << 32) | (uint64_t)i;
-  }
-  std::sort(g_host.keys, g_host.keys + n);  // in place, no allocation
-  int leaves = 1;
-  while (leaves < num_ctas) leaves <<= 1;
-  for (int c = 0; c < leaves; ++c) g_host.load[c] = c < num_ctas ? 0 : INT64_MAX;
-  for (int c = 0; c < num_ctas; ++c) g_host.count[c] = 0;
-  for (int c = 0; c < leaves; ++c) g_host.tree[leaves + c] = c;
-  for (int k = leaves - 1; k >= 1; --k) {
-    const int32_t a = g_host.tree[2 * k], b = g_host.tree[2 * k + 1];
-    g_host.tree[k] = g_host.load[b] < g_host.load[a] ? b : a;
-  }
-  for (int64_t k = 0; k < n; ++k) {
-    const uint32_t idx = (uint32_t)(g_host.keys[k] & 0xFFFFFFFFu);
-    const int32_t c = g_host.tree[1];
-    g_host.owner[idx] = c;
-    g_host.count[c]++;
-    g_host.load[c] += g_host.cost[idx];
-    for (int node = (leaves + c) >> 1; node >= 1; node >>= 1) {
-      const int32_t a = g_host.tree[2 * node], b = g_host.tree[2 * node + 1];
-      g_host.tree[node] = g_host.load[b] < g_host.load[a] ? b : a;
-    }
-  }
+                      int num_ctas, int64_t* n_out) {
+  const PlanStorage st{g_host.items, g_host.cost, g_host.order, g_host.owner, g_host.keys, g_host.bucket,
+                       g_host.load,  g_host.tree, g_host.count, kNaMaxItems,  kNaBuckets,   2048};
   gdpa_work_item_t* out_items = reinterpret_cast<gdpa_work_item_t*>(g_host.upload);
   int32_t* cta_begin = reinterpret_cast<int32_t*>(g_host.upload + kNaItemBytes);
-  cta_begin[0] = 0;
-  for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + g_host.count[c];
-  for (int c = 0; c < num_ctas; ++c) g_host.count[c] = cta_begin[c];  // reuse as fill cursors
-  for (int64_t k = 0; k < n; ++k) {
-    const uint32_t idx = (uint32_t)(g_host.keys[k] & 0xFFFFFFFFu);
-    out_items[g_host.count[g_host.owner[idx]]++] = g_host.items[idx];
-  }
-  *n_out = n;
-  *bytes_out = kNaItemBytes + (size_t)(num_ctas + 1) * sizeof(int32_t);
-  return GDPA_OK;
+  return plan_items_into(qo, ko, B, H, window_blocks, rows_per_item, num_ctas, st, out_items, cta_begin, nullptr,
+                         n_out);
 }
 
 }  // namespace
@@ -151,8 +112,7 @@ extern "C" gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const vo
   if (n_est > kNaMaxItems) return GDPA_ERR_NO_MEMORY;
   const int num_ctas = (int)std::min<int64_t>(std::min<int64_t>(n_est, sms), kNaMaxCtas);
   int64_t n = 0;
-  size_t bytes = 0;
-  if ((st = na_plan(hq, hk, B, H, window_blocks, rpi, num_ctas, &n, &bytes)) != GDPA_OK) return st;
+  if ((st = na_plan(hq, hk, B, H, window_blocks, rpi, num_ctas, &n)) != GDPA_OK) return st;
   unsigned char* dev = static_cast<unsigned char*>(g_dev_scratch[device]);
   // The whole region the launch reads is rewritten here; nothing needs zeroing.
   if (cudaMemcpyAsync(dev, g_host.upload, (size_t)n * sizeof(gdpa_work_item_t), cudaMemcpyHostToDevice, s) !=
@@ -160,7 +120,6 @@ extern "C" gdpa_status_t gdpa_fwd_noalloc(const void* q, const void* k, const vo
       cudaMemcpyAsync(dev + kNaItemBytes, g_host.upload + kNaItemBytes, (size_t)(num_ctas + 1) * sizeof(int32_t),
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return GDPA_ERR_CUDA;
-  (void)bytes;
   LaunchArgs a;
   a.q = q;
   a.k = k;

@@ -111,18 +111,18 @@ int64_t count_plan_items(const int32_t* q_off, int B, int H, int rows_per_item) 
   return n;
 }
 
-gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
-                         int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items_out,
-                         std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
+gdpa_status_t plan_items_into(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
+                              int rows_per_item, int num_ctas, const PlanStorage& st, gdpa_work_item_t* items_out,
+                              int32_t* cta_begin, int64_t* cost_out, int64_t* n_out) {
+  *n_out = 0;
   if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
   const bool ok_rows = rows_per_item == kBlockM || rows_per_item == 2 * kBlockM ||
                        (rows_per_item == kKeySplitRows && window_blocks == 0);
   if (!ok_rows) return GDPA_ERR_INVALID_ARG;
-  std::vector<gdpa_work_item_t> items;
-  std::vector<int64_t> cost;
-  const int64_t n = count_plan_items(q_off, B, H, rows_per_item);
-  items.reserve((size_t)n);
-  cost.reserve((size_t)n);
+  int leaves = 1;
+  while (leaves < num_ctas) leaves <<= 1;
+  if (leaves > st.max_leaves) return GDPA_ERR_NO_MEMORY;
+  int64_t n = 0;
   for (int b = 0; b < B; ++b) {
     const int64_t Lq = q_off[b + 1] - q_off[b];
     const int64_t Lkv = kv_off[b + 1] - kv_off[b];
@@ -130,66 +130,97 @@ gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int
       const int64_t kv0 = window_blocks != 0 ? window_start(q0, window_blocks) : 0;
       const int64_t c = plan_item_cost(q0, Lq, Lkv, window_blocks, rows_per_item);
       for (int h = 0; h < H; ++h) {
-        items.push_back(gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0});
-        cost.push_back(c);
+        if (n >= st.cap_items) return GDPA_ERR_NO_MEMORY;
+        st.items[n] = gdpa_work_item_t{(int32_t)b, (int32_t)h, (int32_t)q0, (int32_t)kv0};
+        st.cost[n] = c;
+        ++n;
       }
     }
   }
   // LPT: order by decreasing cost, then give each item to the CTA with the
   // least load so far.  Costs are multiples of 16 (or the small constant of
-  // an empty item), so a stable bucket sort on cost/16 gives the order in
-  // O(n); ties keep sequence/head/tile order, so the tiles of one (sequence,
-  // head) land on different CTAs at about the same time and share its K/V
-  // through L2.  The least-loaded CTA comes from a tournament tree (min over
-  // a complete binary tree of per-CTA loads), O(log #CTAs) per item.
-  const size_t n_items = items.size();
+  // an empty item), so the order is by cost/16, ties in sequence/head/tile
+  // order: the tiles of one (sequence, head) land on different CTAs at about
+  // the same time and share its K/V through L2.  A counting sort gives that
+  // order in O(n) when the cursor array is large enough; otherwise an
+  // in-place sort of (bucket, index) keys gives the same order.  The
+  // least-loaded CTA comes from a tournament tree (min over a complete
+  // binary tree of per-CTA loads), O(log #CTAs) per item.
   int64_t max_bucket = 0;
-  for (size_t i = 0; i < n_items; ++i) max_bucket = std::max<int64_t>(max_bucket, cost[i] >> 4);
-  std::vector<uint32_t> order(n_items);
-  if (max_bucket <= (int64_t)4 * (int64_t)n_items + 1024) {
-    std::vector<uint32_t> start((size_t)max_bucket + 2, 0);
-    for (size_t i = 0; i < n_items; ++i) start[(size_t)(max_bucket - (cost[i] >> 4)) + 1]++;
-    for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
-    for (size_t i = 0; i < n_items; ++i) order[start[(size_t)(max_bucket - (cost[i] >> 4))]++] = (uint32_t)i;
+  for (int64_t i = 0; i < n; ++i) max_bucket = std::max<int64_t>(max_bucket, st.cost[i] >> 4);
+  uint32_t* order = st.order;
+  if (max_bucket + 2 <= st.cap_buckets) {
+    uint32_t* start = st.bucket;
+    std::fill(start, start + max_bucket + 2, 0u);
+    for (int64_t i = 0; i < n; ++i) start[(size_t)(max_bucket - (st.cost[i] >> 4)) + 1]++;
+    for (int64_t b = 1; b < max_bucket + 2; ++b) start[b] += start[b - 1];
+    for (int64_t i = 0; i < n; ++i) order[start[(size_t)(max_bucket - (st.cost[i] >> 4))]++] = (uint32_t)i;
   } else {
-    for (size_t i = 0; i < n_items; ++i) order[i] = (uint32_t)i;
-    std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) { return cost[a] > cost[b]; });
+    for (int64_t i = 0; i < n; ++i) {
+      const uint64_t rank = (uint64_t)std::min<int64_t>(max_bucket - (st.cost[i] >> 4), 0x7FFFFFFF);
+      st.keys[i] = (rank << 32) | (uint64_t)i;
+    }
+    std::sort(st.keys, st.keys + n);  // in place, no allocation
+    for (int64_t i = 0; i < n; ++i) order[i] = (uint32_t)(st.keys[i] & 0xFFFFFFFFu);
   }
-  int leaves = 1;
-  while (leaves < num_ctas) leaves <<= 1;
-  std::vector<int64_t> load(leaves, INT64_MAX);
-  for (int c = 0; c < num_ctas; ++c) load[c] = 0;
-  std::vector<int32_t> tree(2 * (size_t)leaves);  // tree[k] = CTA with the least load below node k
+  int64_t* load = st.load;
+  int32_t* tree = st.tree;  // tree[k] = CTA with the least load below node k
+  for (int c = 0; c < leaves; ++c) load[c] = c < num_ctas ? 0 : INT64_MAX;
   for (int c = 0; c < leaves; ++c) tree[leaves + c] = c;
   for (int k = leaves - 1; k >= 1; --k) {
     const int32_t a = tree[2 * k], b = tree[2 * k + 1];
     tree[k] = load[b] < load[a] ? b : a;
   }
-  std::vector<int32_t> owner(n_items);
-  std::vector<int64_t> count(num_ctas, 0);
-  for (size_t k = 0; k < n_items; ++k) {
+  int32_t* count = st.count;
+  for (int c = 0; c < num_ctas; ++c) count[c] = 0;
+  for (int64_t k = 0; k < n; ++k) {
     const uint32_t idx = order[k];
     const int32_t c = tree[1];
-    owner[idx] = c;
+    st.owner[idx] = c;
     count[c]++;
-    load[c] += cost[idx];
-    for (size_t node = ((size_t)leaves + c) >> 1; node >= 1; node >>= 1) {
+    load[c] += st.cost[idx];
+    for (int node = (leaves + c) >> 1; node >= 1; node >>= 1) {
       const int32_t a = tree[2 * node], b = tree[2 * node + 1];
       tree[node] = load[b] < load[a] ? b : a;
     }
   }
-  cta_begin.assign((size_t)num_ctas + 1, 0);
-  for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + (int32_t)count[c];
-  std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
-  items_out.resize(items.size());
-  if (cost_out) cost_out->resize(items.size());
-  for (size_t k = 0; k < n_items; ++k) {  // within a CTA: decreasing cost (LPT order)
+  cta_begin[0] = 0;
+  for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + count[c];
+  for (int c = 0; c < num_ctas; ++c) count[c] = cta_begin[c];  // now the fill cursors
+  for (int64_t k = 0; k < n; ++k) {  // within a CTA: decreasing cost (LPT order)
     const uint32_t idx = order[k];
-    int32_t pos = fill[owner[idx]]++;
-    items_out[pos] = items[idx];
-    if (cost_out) (*cost_out)[pos] = cost[idx];
+    const int32_t pos = count[st.owner[idx]]++;
+    items_out[pos] = st.items[idx];
+    if (cost_out) cost_out[pos] = st.cost[idx];
   }
+  *n_out = n;
   return GDPA_OK;
+}
+
+gdpa_status_t plan_items(const int32_t* q_off, const int32_t* kv_off, int B, int H, int window_blocks,
+                         int rows_per_item, int num_ctas, std::vector<gdpa_work_item_t>& items_out,
+                         std::vector<int32_t>& cta_begin, std::vector<int64_t>* cost_out) {
+  if (H <= 0 || num_ctas <= 0) return GDPA_ERR_INVALID_ARG;
+  const int64_t n = count_plan_items(q_off, B, H, rows_per_item);
+  int leaves = 1;
+  while (leaves < num_ctas) leaves <<= 1;
+  std::vector<gdpa_work_item_t> items((size_t)n);
+  std::vector<int64_t> cost((size_t)n);
+  std::vector<uint32_t> order((size_t)n), bucket((size_t)(4 * n + 1026));
+  std::vector<int32_t> owner((size_t)n), tree(2 * (size_t)leaves), count((size_t)num_ctas);
+  std::vector<uint64_t> keys((size_t)n);
+  std::vector<int64_t> load((size_t)leaves);
+  PlanStorage st{items.data(), cost.data(), order.data(), owner.data(), keys.data(), bucket.data(),
+                 load.data(), tree.data(), count.data(), n, (int64_t)bucket.size(), leaves};
+  items_out.resize((size_t)n);
+  cta_begin.assign((size_t)num_ctas + 1, 0);
+  if (cost_out) cost_out->resize((size_t)n);
+  int64_t got = 0;
+  const gdpa_status_t r = plan_items_into(q_off, kv_off, B, H, window_blocks, rows_per_item, num_ctas, st,
+                                          items_out.data(), cta_begin.data(), cost_out ? cost_out->data() : nullptr,
+                                          &got);
+  if (r != GDPA_OK) return r;
+  return got == n ? GDPA_OK : GDPA_ERR_INVALID_ARG;
 }
 
 }  // namespace gdpa

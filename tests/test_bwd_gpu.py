@@ -210,24 +210,38 @@ def test_fwd_lse_all_kernels():
         assert np.abs(got[fin] - ref[fin]).max(initial=0.0) <= LSE_ABS
 
 
-def test_bwd_full_self_long_sampled_sequences():
-    # the full workload in the launch the bench times; the oracle checks a few
-    # whole sequences (sequences are independent, so their gradients are too)
+def test_bwd_full_self_long_every_row():
+    # the full workload in the launch the bench times, every row of dq, dk,
+    # dv and the lse against the oracle, group by group of whole sequences
+    # (sequences are independent, so their gradients are too); the per-tensor
+    # bar uses the whole tensor's max |ref|, as the small cases do
+    from tests.parity import sequence_groups
     batch = make_batch("self_long")
-    w = batch.workload
     rng = np.random.default_rng(7000)
     do = rand_dout(rng, batch)
     out, lse, dq, dk, dv = run_train(batch, do)
     qo, ko = batch.q_offsets, batch.kv_offsets
-    for b in [0, int(np.argmax(np.diff(qo))), len(qo) - 2]:
-        sq, sk = slice(qo[b], qo[b + 1]), slice(ko[b], ko[b + 1])
-        rq, rk, rv, rl = oracle.gdpa_bwd(batch.q[sq], batch.k[sk], batch.v[sk], do[sq],
-                                         np.array([0, qo[b + 1] - qo[b]], np.int32),
-                                         np.array([0, ko[b + 1] - ko[b]], np.int32), w.H, w.D, w.act, 0, w.scale)
-        assert np.abs(lse[sq] - rl).max() <= LSE_ABS
-        assert_grad(dq[sq], rq, "dq seq %d" % b)
-        assert_grad(dk[sk], rk, "dk seq %d" % b)
-        assert_grad(dv[sk], rv, "dv seq %d" % b)
+    stats = {n: [0.0, 0.0, 0.0, 0.0] for n in ("dq", "dk", "dv")}  # max|d|, max|ref|, sum d^2, sum ref^2
+    rows = 0
+    for seqs in sequence_groups(qo, 1 << 15):
+        sub = batch.subset(seqs)
+        sq = slice(int(qo[seqs[0]]), int(qo[seqs[-1] + 1]))
+        sk = slice(int(ko[seqs[0]]), int(ko[seqs[-1] + 1]))
+        rq, rk, rv, rl = oracle.gdpa_bwd_batch(sub, do[sq])
+        assert np.abs(lse[sq] - rl).max(initial=0.0) <= LSE_ABS
+        for n, got, ref in (("dq", dq[sq], rq), ("dk", dk[sk], rk), ("dv", dv[sk], rv)):
+            assert np.isfinite(got).all(), "non-finite " + n
+            st = stats[n]
+            d = np.abs(got - ref)
+            st[0] = max(st[0], float(d.max(initial=0.0)))
+            st[1] = max(st[1], float(np.abs(ref).max(initial=0.0)))
+            st[2] += float(np.sum(d * d))
+            st[3] += float(np.sum(ref * ref))
+        rows += sq.stop - sq.start
+    assert rows == int(qo[-1])
+    for n, (dmax, rmax, dd, rr) in stats.items():
+        assert dmax <= MAX_REL * rmax, "%s: max |d| %.3e vs bar %.3e" % (n, dmax, MAX_REL * rmax)
+        assert np.sqrt(dd / rr) <= REL_L2, "%s: rel L2 %.3e" % (n, np.sqrt(dd / rr))
 
 
 # Windows: lengths around the 64-token blocks and the 128-row / 64-row tiles.

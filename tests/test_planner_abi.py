@@ -172,3 +172,41 @@ def test_plan_balances_the_long_jagged_workload():
     _, _, cost, loads = check_plan(Lq, Lkv, w.H, 0, 152)
     # skew (max / mean CTA load) stays close to 1
     assert loads.max() / loads.mean() < 1.05
+
+
+def lpt_reference(Lq, Lkv, H, R, num_ctas, cost_of):
+    """The planner's schedule restated in plain Python: items in (sequence,
+    query tile, head) order, a stable sort by decreasing cost // 16, each item
+    to the least-loaded CTA (the lowest index among equals), items of a CTA in
+    that order."""
+    items = [(b, h, q0) for b in range(len(Lq)) for q0 in range(0, int(Lq[b]), R) for h in range(H)]
+    cost = [cost_of[(b, q0)] for (b, h, q0) in items]
+    order = sorted(range(len(items)), key=lambda i: -(cost[i] >> 4))  # sorted() is stable
+    load = [0] * num_ctas
+    per = [[] for _ in range(num_ctas)]
+    for i in order:
+        c = min(range(num_ctas), key=lambda k: (load[k], k))
+        load[c] += cost[i]
+        per[c].append(i)
+    flat = [items[i] for c in range(num_ctas) for i in per[c]]
+    cta = np.cumsum([0] + [len(p) for p in per])
+    return flat, cta
+
+
+@pytest.mark.parametrize("huge", [False, True])
+def test_plan_matches_plain_lpt_schedule(huge):
+    # huge key counts make the cost buckets outnumber the items, which takes
+    # the in-place sort instead of the counting sort: both must give the
+    # schedule of the plain restatement, exactly
+    rng = np.random.default_rng(99 + huge)
+    B, H, ctas = 23, 3, 7
+    Lq = rng.integers(0, 600, size=B)
+    Lkv = rng.integers(0, 600, size=B) * (5000 if huge else 1)
+    qo, ko = offsets_of(Lq), offsets_of(Lkv)
+    items, cta, cost, R, _ = gdpa.gdpa_plan_enumerate(qo, ko, B, H, 128, 0, 0, ctas, with_rows=True)
+    if huge:
+        assert int(cost.max()) >> 4 > 4 * len(items) + 1026
+    cost_of = {(int(b), int(q0)): int(c) for (b, _, q0, _), c in zip(items, cost)}
+    flat, cta_ref = lpt_reference(Lq, Lkv, H, R, ctas, cost_of)
+    assert np.array_equal(cta, cta_ref)
+    assert [tuple(map(int, (b, h, q0))) for (b, h, q0, _) in items] == flat

@@ -73,3 +73,24 @@ def test_partition_is_balanced_and_complete():
     assert flat == list(range(256))
     loads = [sum(int(L[s]) ** 2 for s in p) for p in parts]
     assert max(loads) / (sum(loads) / 8) < 1.05
+
+
+def test_bench_shards_one_seeded_batch_per_rank():
+    # bench.py under torchrun: rank r times its LPT shard of one global batch
+    # of N x B sequences; the shards' lengths together are the global draw
+    import bench
+    from jagged_attention_recommender_gb300.workloads import WORKLOADS, draw_lengths
+
+    w = WORKLOADS["tiny"]
+    world = 3
+    Lq, Lkv = draw_lengths(w, np.random.default_rng(w.seed), w.B * world)
+    got_q, flops = [], None
+    for r in range(world):
+        b, per_rank = bench.bench_batch("tiny", r, world)
+        got_q += list(np.diff(b.q_offsets))
+        flops = per_rank if flops is None else flops
+        assert per_rank == flops
+        assert abs(bench.useful_flops(b) - per_rank[r]) < 1e-6
+    assert sorted(got_q) == sorted(Lq.tolist())
+    single, per1 = bench.bench_batch("tiny", 0, 1)
+    assert per1 == [bench.useful_flops(single)] and single.B == w.B
