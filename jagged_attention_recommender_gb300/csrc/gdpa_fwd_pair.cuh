@@ -396,6 +396,42 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
           livem = (1u << nch) - 1u;
           fullm = (1u << (ncols >> 5)) - 1u;
         }
+        if constexpr (ACT != kActSoftmax) {
+          // ALU activation: no row maximum, so the scores stream through
+          // registers 32 columns at a time (the next chunk's load in flight
+          // while this one is evaluated), which keeps the packed fp32x2
+          // polynomial's register pairs from spilling.  P chunk ch lands on
+          // columns [16 ch, 16 ch + 16), scores this thread has already read.
+          uint32_t sc[2][32];
+          if (livem & 1u) ptx::tmem_ld32(s_addr, sc[0]);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch >= nch) continue;
+            ptx::tmem_wait_ld_r32(sc[ch & 1]);
+            if (ch + 1 < nch && ((livem >> (ch + 1)) & 1u)) ptx::tmem_ld32(s_addr + 32 * (ch + 1), sc[(ch + 1) & 1]);
+            uint32_t pk[16];
+            if (!((livem >> ch) & 1u)) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) pk[u] = 0u;
+            } else {
+              const bool full = (fullm >> ch) & 1u;
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const int c = 32 * ch + 2 * u;
+                float e0, e1;
+                gelu_tanh_alu2(__uint_as_float(sc[ch & 1][2 * u]), __uint_as_float(sc[ch & 1][2 * u + 1]), gA2, gC2,
+                               e0, e1);
+                if (!full) {
+                  e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
+                  e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;
+                }
+                pk[u] = ptx::pack_bf16x2(e0, e1);
+              }
+            }
+            ptx::tmem_st16(s_addr + 16 * ch, pk);
+          }
+          ptx::tmem_wait_st();
+        } else {
         // The whole row of scores in registers, one TMEM round trip.
         uint32_t sr[128];
         // A whole tile of valid keys (softmax, scale > 0): the second half
@@ -429,7 +465,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             if ((livem >> ch) & 1u) ptx::tmem_ld32(s_addr + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * ch]));
           ptx::tmem_wait_ld();
         }
-        if (ACT == kActSoftmax) {
+        {
           // Scores in log2 units: x = s * scale * log2(e); masked columns
           // become -inf.  With scale > 0 the scaling is folded into the
           // exponent's FMA; otherwise it is applied first.
@@ -474,63 +510,42 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
           }
           const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
           // masked entries hold -inf and give exactly 0; with scale > 0 the
-          // entries are still unscaled and take the scale in the packed FMA
-          const uint64_t mul2 = ptx::f2_splat(fold ? sl : 1.0f);
-          const uint64_t neg2 = ptx::f2_splat(-m_use);
+          // entries are still unscaled and take the scale in the FMA.  The
+          // exponent's argument is a scalar FMA and the row sum a packed
+          // add: packing both (fma.f32x2 into add.f32x2) measured about
+          // twice as slow, the register pairs it needs pushing the row of
+          // scores out of registers.  P goes to TMEM chunk by chunk (16
+          // columns of bf16 pairs over scores already held in registers).
+          const float mul = fold ? sl : 1.0f, nm = -m_use;
           uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             if (ch >= nch) continue;
+            uint32_t pk[16];
             if (!((livem >> ch) & 1u)) {  // no valid key in the chunk: P = 0
 #pragma unroll
-              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
-              continue;
-            }
+              for (int u = 0; u < 16; ++u) pk[u] = 0u;
+            } else {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int c = 32 * ch + 2 * u;
-              const uint64_t x2 =
-                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2, neg2);
-              float e0, e1;
-              ptx::f2_unpack(x2, e0, e1);
-              e0 = ptx::ex2_approx(e0);
-              e1 = ptx::ex2_approx(e1);
-              acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(e0, e1));
-              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);  // P overwrites scores already consumed
+              for (int u = 0; u < 16; ++u) {
+                const int c = 32 * ch + 2 * u;
+                const float e0 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), mul, nm));
+                const float e1 = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + 1]), mul, nm));
+                acc[u & 3] = ptx::f2_add(acc[u & 3], ptx::f2_pack(e0, e1));
+                pk[u] = ptx::pack_bf16x2(e0, e1);
+              }
             }
+            ptx::tmem_st16(s_addr + 16 * ch, pk);
           }
           const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
           float sa, sb;
           ptx::f2_unpack(acc01, sa, sb);
           l_run += sa + sb;
-        } else {  // GELU
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (ch >= nch) continue;
-            if (!((livem >> ch) & 1u)) {
-#pragma unroll
-              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
-              continue;
-            }
-            const bool full = (fullm >> ch) & 1u;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int c = 32 * ch + 2 * u;
-              float e0, e1;
-              gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, e0, e1);
-              if (!full) {
-                e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
-                e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;
-              }
-              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);
-            }
-          }
         }
-        // P (bf16 pairs) over the first 16 * nch columns of S_x; P V reads
-        // no column beyond them.
-        ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        if (nch > 2) ptx::tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        // P (bf16 pairs) now covers the first 16 * nch columns of S_x; P V
+        // reads no column beyond them.
         ptx::tmem_wait_st();
+        }
       }
       // O_x += P_x(g-1) V(g-1) was issued before S_x(g) and has landed; the
       // wait keeps this side's view of the barrier phase exact (and spaces

@@ -224,7 +224,12 @@ struct Pair64PV {
   int first, n16;
 };
 
-template <int D>
+// SPLIT (the ALU activations): P is carried as two bf16 parts, P_hi in the
+// buffer's first 32 columns and P_lo = bf16(P - P_hi) in the next 32, and
+// O += P_hi V + P_lo V, so the weights keep ~16 significant bits: with a few
+// keys and no softmax normalisation, a single bf16 rounding of P would move
+// the output by up to 2^-8 of each term.
+template <int D, bool SPLIT>
 __device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int x,
                                               const Pair64PV& P) {
   using C = Pair64Cfg<D>;
@@ -243,11 +248,17 @@ __device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm,
     const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK, 1024);
     ptx::mma_ts_elect(tmem + C::tm_o(x), tmem + C::tm_s(x, b) + 8 * kk, bdesc, idesc, (P.first && kk == 0) ? 0u : 1u);
   }
+  if (SPLIT) {
+    for (int kk = 0; kk < P.n16; ++kk) {
+      const uint64_t bdesc = ptx::sdesc_sw128(v_base + kk * 2048, C::KV_CHUNK, 1024);
+      ptx::mma_ts_elect(tmem + C::tm_o(x), tmem + C::tm_s(x, b) + 32 + 8 * kk, bdesc, idesc, 1u);
+    }
+  }
   ptx::mma_commit_elect(&B.o_done[x]);
   return true;
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool SPLIT>
 __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend) {
   using C = Pair64Cfg<D>;
   volatile int* abort = &B.abort;
@@ -307,7 +318,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
       // tile is issued now and its V stage can be released).
       for (int x = 0; x < 2 && ok; ++x) {
         if (!pend[x]) continue;
-        ok = pair64_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
+        ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
         pend[x] = false;
       }
       if (!ok) break;
@@ -325,7 +336,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
       if (has[x]) ++qn[x];
   }
   for (int x = 0; x < 2 && ok; ++x)
-    if (pend[x]) ok = pair64_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
+    if (pend[x]) ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
   ptx::mma_commit_elect(&B.mma_drain);
@@ -549,13 +560,14 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
           float sa, sb2;
           ptx::f2_unpack(acc01, sa, sb2);
           l_run += sa + sb2;
-        } else {  // GELU
+        } else {  // GELU / SiLU: P = P_hi + P_lo, two bf16 parts (see pair64_issue_pv)
+          uint32_t plo[32];
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             if (ch >= nch) continue;
             if (!((livem >> ch) & 1u)) {
 #pragma unroll
-              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = 0u;
+              for (int u = 0; u < 16; ++u) sr[16 * ch + u] = plo[16 * ch + u] = 0u;
               continue;
             }
             const bool full = (fullm >> ch) & 1u;
@@ -568,12 +580,19 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
                 e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
                 e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;
               }
-              sr[16 * ch + u] = ptx::pack_bf16x2(e0, e1);
+              const uint32_t hi = ptx::pack_bf16x2(e0, e1);
+              const uint64_t rem = ptx::f2_sub(ptx::f2_pack(e0, e1),
+                                               ptx::f2_pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u)));
+              float r0, r1;
+              ptx::f2_unpack(rem, r0, r1);
+              sr[16 * ch + u] = hi;
+              plo[16 * ch + u] = ptx::pack_bf16x2(r0, r1);
             }
           }
+          ptx::tmem_st32(s_addr + 32, plo);  // P_lo over the buffer's last 32 columns
         }
         // P (bf16 pairs, 32 columns) over the first columns of this S
-        // buffer; P V reads no column beyond 8 * n16.
+        // buffer; P V reads no column beyond 8 * n16 (and, for P_lo, 32 + 8 * n16).
         ptx::tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         ptx::tmem_wait_st();
       }
@@ -699,7 +718,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
     } else if (warp == 2) {
       if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B, ibeg, iend);
     } else if (warp == 1) {
-      pair64_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
+      pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
     }
   } else {  // warpgroups 1 and 2: tiles A and B
     ptx::regs_inc<C::regs_act(ACT)>();
