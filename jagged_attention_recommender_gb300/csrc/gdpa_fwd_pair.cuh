@@ -62,7 +62,7 @@ struct PairBars {
   uint64_t q_full[2][PairCfg<D>::NQS], q_empty[2][PairCfg<D>::NQS];
   uint64_t k_full[PairCfg<D>::NK], k_empty[PairCfg<D>::NK];
   uint64_t v_full[PairCfg<D>::NV], v_empty[PairCfg<D>::NV];
-  uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
+  uint64_t s_full[2], p_full[2][2], o_done[2], o_empty[2];  // p_full per side and half of the keys
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort;
@@ -196,33 +196,48 @@ struct PairPV {
   uint32_t gx;  // this side's tile counter
   uint32_t g;   // K/V tile counter (selects the V stage)
   int item;     // this side's item counter
-  int first, n16;
+  int first, last, n16;
 };
 
+// O_x += P_x V for one K/V tile, in two halves of the keys: the activation
+// signals P of keys 0-63 before it computes keys 64-127, so the first four
+// MMAs run while it finishes the row.  Only an item's last P V signals
+// o_done (its epilogue waits for it): the scores' barrier already implies
+// every earlier P V of the side, since a commit tracks all the issuing
+// thread's earlier MMAs and S_x(g) is issued after O_x += P_x(g-1) V(g-1).
 template <int D>
 __device__ __forceinline__ bool pair_issue_pv(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32_t tmem, int x,
                                               const PairPV& P) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
-  if (!ptx::mbar_wait(&B.p_full[x], P.gx & 1, p.timeout_ns, abort)) return false;
+  if (!ptx::mbar_wait(&B.p_full[x][0], P.gx & 1, p.timeout_ns, abort)) return false;
   if (P.first && !ptx::mbar_wait(&B.o_empty[x], (P.item & 1) ^ 1, p.timeout_ns, abort)) return false;
   const int sv = P.g % C::NV;
   if (!ptx::mbar_wait(&B.v_full[sv], (P.g / C::NV) & 1, p.timeout_ns, abort)) return false;
   ptx::tc_fence_after();
   // One descriptor, advanced by 16 keys (2048 bytes, 128 in the address
   // field) per MMA: the V stage lies below 256 KB, so the 14-bit field
-  // never carries.  A whole tile takes the unrolled path.
+  // never carries.
   const uint64_t bd0 = ptx::sdesc_sw128(ptx::smem_u32(sm + C::OFF_V + sv * C::TILE_BYTES), C::CHUNK_BYTES, 1024);
   constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
   const uint32_t d_tm = tmem + C::tm_o(x), a_tm = tmem + C::tm_s(x);
   const uint32_t acc0 = P.first ? 0u : 1u;
+  const int n_lo = min(P.n16, 4);
+  if (n_lo == 4) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
+  } else {
+    for (int kk = 0; kk < n_lo; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
+  }
+  if (!ptx::mbar_wait(&B.p_full[x][1], P.gx & 1, p.timeout_ns, abort)) return false;
+  ptx::tc_fence_after();
   if (P.n16 == 8) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
+    for (int kk = 4; kk < 8; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, 1u);
   } else {
-    for (int kk = 0; kk < P.n16; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, kk == 0 ? acc0 : 1u);
+    for (int kk = 4; kk < P.n16; ++kk) ptx::mma_ts_elect(d_tm, a_tm + 8 * kk, bd0 + 128u * kk, idesc, 1u);
   }
-  ptx::mma_commit_elect(&B.o_done[x]);
+  if (P.last) ptx::mma_commit_elect(&B.o_done[x]);
   return true;
 }
 
@@ -235,7 +250,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   uint32_t g = 0;
   bool ok = true;
   bool pend[2] = {false, false};
-  PairPV pv[2] = {{0, 0, 0, 0, 0}, {0, 0, 0, 0, 0}};
+  PairPV pv[2] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}};
   bool pend_v = false;
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
@@ -296,7 +311,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
       }
       for (int x = 0; x < 2; ++x) {
         if (!act[x]) continue;
-        pv[x] = PairPV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
+        pv[x] = PairPV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, j == t.t1[x] - 1 ? 1 : 0, n16};
         pend[x] = true;
         ++gx[x];
       }
@@ -334,7 +349,8 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
     gC2 = ptx::f2_splat(p.act_c);
   }
   const int H = p.H;
-  uint32_t gx = 0;
+  uint32_t gx = 0;  // this side's K/V tiles (phase of s_full, p_full)
+  uint32_t ix = 0;  // this side's items (phase of o_done)
   bool ok = true;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const PairItem t = decode_pair<WIN>(p, idx);
@@ -429,8 +445,16 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
               }
             }
             ptx::tmem_st16(s_addr + 16 * ch, pk);
+            if (ch == 1) {  // keys 0-63 done: their P V may start
+              ptx::tmem_wait_st();
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(&B.p_full[x][0]);
+            }
           }
           ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          if (nch <= 1) ptx::mbar_arrive(&B.p_full[x][0]);
+          ptx::mbar_arrive(&B.p_full[x][1]);
         } else {
         // The whole row of scores in registers, one TMEM round trip.
         uint32_t sr[128];
@@ -508,6 +532,20 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
             m_run = m_new;
             rescale = true;
           }
+          // O rescale before this tile's P: the scores' barrier implies that
+          // O_x += P_x(g-1) V(g-1) has completed (see pair_issue_pv)
+          // (16 columns at a time: the row of scores is still in registers)
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t r[16];
+              ptx::tmem_ld16(o_addr + 16 * c, r);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              ptx::tmem_st16(o_addr + 16 * c, r);
+            }
+          }
           const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
           // masked entries hold -inf and give exactly 0; with scale > 0 the
           // entries are still unscaled and take the scale in the FMA.  The
@@ -536,6 +574,11 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
               }
             }
             ptx::tmem_st16(s_addr + 16 * ch, pk);
+            if (ch == 1) {  // keys 0-63 done (and O rescaled): their P V may start
+              ptx::tmem_wait_st();
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(&B.p_full[x][0]);
+            }
           }
           const uint64_t acc01 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
           float sa, sb;
@@ -545,35 +588,19 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
         // P (bf16 pairs) now covers the first 16 * nch columns of S_x; P V
         // reads no column beyond them.
         ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        if (nch <= 1) ptx::mbar_arrive(&B.p_full[x][0]);
+        ptx::mbar_arrive(&B.p_full[x][1]);
         }
+      } else {  // no valid row in this warp: nothing to compute
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&B.p_full[x][0]);
+        ptx::mbar_arrive(&B.p_full[x][1]);
       }
-      // O_x += P_x(g-1) V(g-1) was issued before S_x(g) and has landed; the
-      // wait keeps this side's view of the barrier phase exact (and spaces
-      // the two sides' activations apart, which measured faster than
-      // letting them overlap).
-      if (gx >= 1) {
-        ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(o_addr + 32 * c, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          ptx::tmem_st32(o_addr + 32 * c, r);
-        }
-        ptx::tmem_wait_st();
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&B.p_full[x]);
     }
     if (!ok) break;
-    ok = ptx::mbar_wait(&B.o_done[x], (gx - 1) & 1, p.timeout_ns, abort);  // the item's last P V
+    ok = ptx::mbar_wait(&B.o_done[x], ix & 1, p.timeout_ns, abort);  // the item's last P V
+    ++ix;
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     ptx::tc_fence_after();
@@ -603,6 +630,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
 
 template <int D, int ACT, bool WIN>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+  static_assert(!WIN, "block windows run on the 64-key pair kernel (gdpa_fwd_pair64.cuh)");
   using C = PairCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -619,7 +647,8 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_cons
         ptx::mbar_init(&B.q_empty[x][s], 1);
       }
       ptx::mbar_init(&B.s_full[x], 1);
-      ptx::mbar_init(&B.p_full[x], 128);
+      ptx::mbar_init(&B.p_full[x][0], 128);
+      ptx::mbar_init(&B.p_full[x][1], 128);
       ptx::mbar_init(&B.o_done[x], 1);
       ptx::mbar_init(&B.o_empty[x], 128);
     }
