@@ -256,7 +256,12 @@ gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_o
 /*
  * gdpa_fwd_planned -- launch the forward pass with a plan; fully asynchronous
  * on `stream`.  The device offsets must hold the values the plan was built
- * from (not checked on the device).
+ * from.  The kernels clip every work item to the rows of the tensors the plan
+ * was built for, so offsets that reach past them never make the launch read
+ * or write outside q, k, v or out; such a launch is flagged and
+ * gdpa_device_status() then returns GDPA_ERR_INVALID_ARG (its output is
+ * undefined).  Offsets that differ from the plan's but stay inside the
+ * tensors are not detected: the output is then undefined.
  */
 gdpa_status_t gdpa_fwd_planned(const gdpa_plan_t* plan, const void* q, const void* k, const void* v,
                                const int32_t* q_offsets, const int32_t* kv_offsets, float scale,
@@ -306,9 +311,11 @@ gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* 
 
 /*
  * gdpa_device_status -- synchronises `stream`, then reads and clears the
- * device status word of the current device.  Returns GDPA_OK or
+ * device status word of the current device.  Returns GDPA_OK,
  * GDPA_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait; its output is
- * undefined) or GDPA_ERR_CUDA.
+ * undefined), GDPA_ERR_INVALID_ARG (a forward launch met device offsets past
+ * its tensors, see gdpa_fwd_planned; its output is undefined) or
+ * GDPA_ERR_CUDA.
  */
 gdpa_status_t gdpa_device_status(void* stream);
 

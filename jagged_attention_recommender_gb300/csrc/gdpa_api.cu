@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -23,6 +24,12 @@ struct gdpa_plan {
 };
 
 namespace gdpa {
+
+bool fault_injected(const char* what) {
+  const char* e = std::getenv("GDPA_FAULT_INJECT");
+  return e && std::strcmp(e, what) == 0;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -51,6 +58,7 @@ struct Buf {
   size_t cap = 0;
   bool pinned = false;
   gdpa_status_t ensure(size_t bytes) {
+    if (fault_injected("alloc")) return GDPA_ERR_NO_MEMORY;  // failure-path tests
     if (bytes <= cap) return GDPA_OK;
     size_t want = bytes + bytes / 4 + 256;
     void* np = nullptr;

@@ -32,13 +32,42 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   // 32-bit word of four E8M0 scales, block b of D in byte b
   const uint32_t* q_sf;
   const uint32_t* k_sf;
+  int Tq, Tkv;               // rows of q / out and of k / v: device offsets beyond them are a bad plan
+  int test_skip_arrive;      // failure-path test only: one activation warp of CTA 0 skips one arrive
 };
 
 // kActGelu instantiates the ALU activations (tanh-GELU and SiLU, told apart
 // by the constants act_a / act_c the launcher passes).
 enum : int { kActSoftmax = 0, kActGelu = 1 };
 
-enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatusEpilogue = 8 };
+enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatusEpilogue = 8, kStatusBadPlan = 16 };
+
+// Rows a work item may touch, from the device offsets of its sequence,
+// clipped to the tensors the launch was given: a plan used with offsets it
+// was not built from (or offsets past the tensors) can then only read rows
+// that exist -- TMA fills the rest with zeros -- and never writes outside
+// `out`; the launch flags kStatusBadPlan.  Returns {first row, rows} for Q/O
+// (rows counted from qs + q0) and K/V.
+struct ItemRows {
+  int qs, ks, Lq, Lkv;
+};
+__device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
+  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
+  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
+  ItemRows r;
+  r.qs = qs;
+  r.ks = ks;
+  r.Lq = min(qe, p.Tq) - qs;
+  r.Lkv = min(ke, p.Tkv) - ks;
+  if (qs < 0 || ks < 0 || qe > p.Tq || ke > p.Tkv || r.Lq < 0 || r.Lkv < 0) {
+    atomicOr(p.status, kStatusBadPlan);
+    r.Lq = max(r.Lq, 0);
+    r.Lkv = max(r.Lkv, 0);
+    if (qs < 0 || qs > p.Tq) r.Lq = 0;
+    if (ks < 0 || ks > p.Tkv) r.Lkv = 0;
+  }
+  return r;
+}
 
 // 32 bf16 values (16 packed words) to global memory: two 32-byte stores when
 // `v8` (the address is 32-byte aligned), else four 16-byte stores.

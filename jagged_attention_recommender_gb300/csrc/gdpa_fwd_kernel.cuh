@@ -142,14 +142,13 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = it.w;
-  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
-  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
-  v.q_tok = qs + v.q0;
-  v.kv_tok = ks;
-  v.Lkv = ke - ks;
-  v.q_rows = min(128, qe - qs - v.q0);
+  const ItemRows r = item_rows(p, b);
+  v.q_tok = r.qs + v.q0;
+  v.kv_tok = r.ks;
+  v.Lkv = r.Lkv;
+  v.q_rows = max(0, min(128, r.Lq - v.q0));
   v.kv_end = WIN ? min(v.Lkv, v.q0 + 128) : v.Lkv;
-  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;
+  v.n_kv = v.kv_end > v.kv0 && v.q_rows > 0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;  // no rows: nothing to do
   return v;
 }
 

@@ -86,16 +86,15 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = WIN ? it.w : 0;
-  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
-  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
-  v.q_tok = qs + v.q0;
-  v.kv_tok = ks;
-  v.Lkv = ke - ks;
-  const int left = qe - qs - v.q0;
-  v.rows[0] = min(128, left);
+  const ItemRows r = item_rows(p, b);
+  v.q_tok = r.qs + v.q0;
+  v.kv_tok = r.ks;
+  v.Lkv = r.Lkv;
+  const int left = r.Lq - v.q0;
+  v.rows[0] = max(0, min(128, left));
   v.rows[1] = max(0, min(128, left - 128));
   v.kv_end = WIN ? min(v.Lkv, v.q0 + v.rows[0] + v.rows[1]) : v.Lkv;
-  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;
+  v.n_kv = v.kv_end > v.kv0 && v.rows[0] > 0 ? (v.kv_end - v.kv0 + 127) / 128 : 0;  // no rows: nothing to do
   v.t0[0] = 0;
   v.t1[0] = v.n_kv;
   v.t0[1] = 0;
@@ -251,7 +250,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   bool ok = true;
   bool pend[2] = {false, false};
   PairPV pv[2] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}};
-  bool pend_v = false;
+  bool pend_v = false, pend_v_read = false;  // V tile pend_v_g staged; read by some P V
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const PairItem t = decode_pair<WIN>(p, idx);
@@ -303,7 +302,13 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
         ptx::mma_commit_elect(&B.s_full[x]);
       }
       if (!ok) break;
-      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);  // both P V of the previous tile issued
+      if (pend_v) {  // both P V of the previous tile issued
+        // a stage no P V read is released only once its load has landed,
+        // so the producer never refills a stage with a copy in flight
+        if (!pend_v_read) ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
+      }
       ptx::mma_commit_elect(&B.k_empty[sk]);
       if (j == t.n_kv - 1) {
         for (int x = 0; x < 2; ++x)
@@ -316,6 +321,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
         ++gx[x];
       }
       pend_v = true;
+      pend_v_read = act[0] || act[1];
       pend_v_g = g;
     }
     for (int x = 0; x < 2; ++x)
@@ -323,6 +329,8 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
+  if (ok && pend_v && !pend_v_read)
+    ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
   ptx::mma_commit_elect(&B.mma_drain);
@@ -621,7 +629,9 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
       }
     }
     ptx::tc_fence_before();
-    ptx::mbar_arrive(&B.o_empty[x]);
+    // failure-path test: one warp of CTA 0 withholds the first item's arrival
+    const bool withhold = p.test_skip_arrive && blockIdx.x == 0 && warp == 4 && ix == 1;
+    if (!withhold) ptx::mbar_arrive(&B.o_empty[x]);
   }
   if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
 }

@@ -105,16 +105,15 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = WIN ? it.w : 0;
-  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
-  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
-  v.q_tok = qs + v.q0;
-  v.kv_tok = ks;
-  v.Lkv = ke - ks;
-  const int left = qe - qs - v.q0;
-  v.rows[0] = min(128, left);
+  const ItemRows r = item_rows(p, b);
+  v.q_tok = r.qs + v.q0;
+  v.kv_tok = r.ks;
+  v.Lkv = r.Lkv;
+  const int left = r.Lq - v.q0;
+  v.rows[0] = max(0, min(128, left));
   v.rows[1] = max(0, min(128, left - 128));
   v.kv_end = WIN ? min(v.Lkv, v.q0 + v.rows[0] + v.rows[1]) : v.Lkv;
-  v.n_kv = v.kv_end > v.kv0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;
+  v.n_kv = v.kv_end > v.kv0 && v.rows[0] > 0 ? (v.kv_end - v.kv0 + BN - 1) / BN : 0;  // no rows: nothing to do
   v.t0[0] = 0;
   v.t1[0] = v.n_kv;
   v.t0[1] = 0;
@@ -268,7 +267,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   bool ok = true;
   bool pend[2] = {false, false};
   Pair64PV pv[2] = {{0, 0, 0, 0, 0}, {0, 0, 0, 0, 0}};
-  bool pend_v = false;
+  bool pend_v = false, pend_v_read = false;  // V tile pend_v_g staged; read by some P V
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const Pair64Item t = decode_pair64<WIN>(p, idx);
@@ -322,7 +321,13 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
         pend[x] = false;
       }
       if (!ok) break;
-      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
+      if (pend_v) {
+        // a stage no P V read is released only once its load has landed,
+        // so the producer never refills a stage with a copy in flight
+        if (!pend_v_read) ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
+      }
       for (int x = 0; x < 2; ++x) {
         if (!act[x]) continue;
         pv[x] = Pair64PV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
@@ -330,6 +335,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
         ++gx[x];
       }
       pend_v = true;
+      pend_v_read = act[0] || act[1];
       pend_v_g = g;
     }
     for (int x = 0; x < 2; ++x)
@@ -337,6 +343,8 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
+  if (ok && pend_v && !pend_v_read)
+    ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
   ptx::mma_commit_elect(&B.mma_drain);

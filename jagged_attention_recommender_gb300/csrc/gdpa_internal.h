@@ -145,6 +145,15 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a);
 void plan_backward(const int32_t* q_off, const int32_t* kv_off, int B, int H, std::vector<int32_t>& dq_items,
                    std::vector<int32_t>& kv_items);
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
+
+// Failure-path tests only: true while the environment variable
+// GDPA_FAULT_INJECT names `what` ("alloc": the library's buffer growth fails
+// as if the allocator were out of memory; "skip_arrive": in the 128-key pair
+// kernel one activation warp of CTA 0 withholds its arrival on the first
+// item's O-free barrier, so the MMA warp's bounded wait runs out and the
+// launch takes its drain path).  Read on every call, so a test can set and
+// clear it between calls; unset, nothing changes.
+bool fault_injected(const char* what);
 gdpa_status_t read_and_clear_device_status(void* stream);
 gdpa_status_t launch_wait_selftest(int timeout_ms, void* stream);
 

@@ -257,6 +257,9 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.score_scale = a.act == GDPA_ACT_SOFTMAX ? a.scale * 1.4426950408889634f : a.scale;
   prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   prm.lse = a.lse;
+  prm.Tq = static_cast<int>(a.Tq);
+  prm.Tkv = static_cast<int>(a.Tkv);
+  prm.test_skip_arrive = fault_injected("skip_arrive") ? 1 : 0;
   alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks != 0;
@@ -323,7 +326,8 @@ gdpa_status_t read_and_clear_device_status(void* stream) {
   if (h != 0) {
     const int zero = 0;
     if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return GDPA_ERR_CUDA;
-    return GDPA_ERR_DEVICE_TIMEOUT;
+    // a wait that ran out outranks a bad plan (which a timeout can follow from)
+    return (h & ~kStatusBadPlan) ? GDPA_ERR_DEVICE_TIMEOUT : GDPA_ERR_INVALID_ARG;
   }
   return GDPA_OK;
 }
