@@ -100,24 +100,72 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + bias) >> 16).astype(np.uint16)
 
 
-def to_mx(x: np.ndarray):
-    """OCP MX quantisation of float32 ``[T, H, D]`` rows in blocks of 32
-    coordinates: returns (e4m3 codes uint8 ``[T, H, D]``, E8M0 scale codes
-    uint8 ``[T, H, D // 32]``).  The block scale is 2^(floor(log2 amax) - 8)
-    (8 = the largest e4m3 exponent), elements are x / scale clamped to +-448
-    and rounded to nearest even by torch's float8_e4m3fn conversion; an
-    all-zero block takes scale 1."""
+def _mx_blocks(xb: np.ndarray):
+    """OCP MX quantisation of float32 blocks ``[..., 32]``: returns (e4m3
+    codes uint8 ``[..., 32]``, E8M0 scale codes uint8 ``[...]``).  The block
+    scale is 2^(floor(log2 amax) - 8) (8 = the largest e4m3 exponent),
+    elements are x / scale clamped to +-448 and rounded to nearest even by
+    torch's float8_e4m3fn conversion; an all-zero block takes scale 1."""
     import torch
 
-    T, H, D = x.shape
-    xb = np.ascontiguousarray(x, dtype=np.float32).reshape(T, H, D // MX_BLOCK, MX_BLOCK)
+    xb = np.ascontiguousarray(xb, dtype=np.float32)
     amax = np.abs(xb).max(axis=-1)
     _, ex = np.frexp(amax)  # amax = m 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
     e = np.where(amax > 0, ex - 1 - 8, 0).clip(-127, 127).astype(np.int32)
     sf = (e + 127).astype(np.uint8)
     y = np.clip(xb * np.ldexp(np.float32(1.0), -e)[..., None].astype(np.float32), -448.0, 448.0)
-    codes = torch.from_numpy(np.ascontiguousarray(y.reshape(T, H, D))).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes.numpy(), sf
+
+
+def to_mx(x: np.ndarray):
+    """OCP MX quantisation of float32 ``[T, H, D]`` rows in blocks of 32
+    coordinates: returns (e4m3 codes uint8 ``[T, H, D]``, E8M0 scale codes
+    uint8 ``[T, H, D // 32]``), each block as :func:`_mx_blocks`."""
+    T, H, D = x.shape
+    codes, sf = _mx_blocks(np.asarray(x, dtype=np.float32).reshape(T, H, D // MX_BLOCK, MX_BLOCK))
+    return codes.reshape(T, H, D), sf
+
+
+def vt_columns(kv_offsets) -> np.ndarray:
+    """First column of each sequence in the key-major MXFP8 layout of V:
+    ``P_b = 32 * sum_{b' < b} ceil(Lkv_b' / 32)`` (int64 ``[B+1]``, last
+    entry = VT, the row length)."""
+    L = np.diff(np.asarray(kv_offsets, dtype=np.int64))
+    col = np.zeros(len(L) + 1, dtype=np.int64)
+    col[1:] = np.cumsum(MX_BLOCK * ((L + MX_BLOCK - 1) // MX_BLOCK))
+    return col
+
+
+def to_mx_vt(v: np.ndarray, kv_offsets):
+    """V ``[Tkv, H, D]`` (float32) in MXFP8 along the keys: returns (codes
+    uint8 ``[H*D, VT]``, scales uint8 ``[VT // 32, H*D]``).  Row h*D + d holds
+    coordinate d of head h; sequence b's keys sit at columns
+    ``[P_b, P_b + Lkv_b)`` (:func:`vt_columns`), the rest of its last block is
+    zero; scale ``[c, h*D + d]`` covers columns ``[32 c, 32 c + 32)`` of that
+    row; blocks as :func:`_mx_blocks`."""
+    Tkv, H, D = v.shape
+    ko = np.asarray(kv_offsets, dtype=np.int64)
+    col = vt_columns(ko)
+    VT = int(col[-1])
+    vt8 = np.zeros((H * D, VT), dtype=np.uint8)
+    vsf = np.full((VT // MX_BLOCK, H * D), 127, dtype=np.uint8)
+    for b in range(len(ko) - 1):
+        L = int(ko[b + 1] - ko[b])
+        if L == 0:
+            continue
+        n = (L + MX_BLOCK - 1) // MX_BLOCK
+        x = np.zeros((n * MX_BLOCK, H * D), dtype=np.float32)
+        x[:L] = np.asarray(v[ko[b]:ko[b + 1]], dtype=np.float32).reshape(L, H * D)
+        codes, sf = _mx_blocks(x.reshape(n, MX_BLOCK, H * D).transpose(0, 2, 1))  # [n, H*D, 32], [n, H*D]
+        c0 = int(col[b])
+        vt8[:, c0:c0 + n * MX_BLOCK] = codes.transpose(1, 0, 2).reshape(H * D, n * MX_BLOCK)
+        vsf[c0 // MX_BLOCK:c0 // MX_BLOCK + n] = sf
+    return vt8, vsf
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b).astype(np.uint32) << 16).view(np.float32)
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
@@ -199,6 +247,9 @@ class JaggedBatch:
     q_sf: np.ndarray | None = None
     k8: np.ndarray | None = None
     k_sf: np.ndarray | None = None
+    # and V in MXFP8 along the keys (to_mx_vt of the bf16 values of v)
+    vt8: np.ndarray | None = None
+    vt_sf: np.ndarray | None = None
 
     @property
     def B(self) -> int:
@@ -228,11 +279,14 @@ class JaggedBatch:
                 return None
             return np.ascontiguousarray(np.concatenate([a[off[s]:off[s + 1]] for s in seqs]) if seqs else a[:0])
 
-        return JaggedBatch(self.workload, np.ascontiguousarray(q), np.ascontiguousarray(k),
-                           np.ascontiguousarray(v),
-                           offsets_of([qo[s + 1] - qo[s] for s in seqs]),
-                           offsets_of([ko[s + 1] - ko[s] for s in seqs]),
-                           rows(self.q8, qo), rows(self.q_sf, qo), rows(self.k8, ko), rows(self.k_sf, ko))
+        sub = JaggedBatch(self.workload, np.ascontiguousarray(q), np.ascontiguousarray(k),
+                          np.ascontiguousarray(v),
+                          offsets_of([qo[s + 1] - qo[s] for s in seqs]),
+                          offsets_of([ko[s + 1] - ko[s] for s in seqs]),
+                          rows(self.q8, qo), rows(self.q_sf, qo), rows(self.k8, ko), rows(self.k_sf, ko))
+        if self.vt8 is not None:
+            sub.vt8, sub.vt_sf = to_mx_vt(bf16_bits_to_f32(sub.v), sub.kv_offsets)
+        return sub
 
 
 def make_batch(name: str, B: int | None = None, seed: int | None = None,
@@ -276,4 +330,5 @@ def make_batch(name: str, B: int | None = None, seed: int | None = None,
     b = JaggedBatch(w, q, k, v, offsets_of(Lq), offsets_of(Lkv))
     if mx is not None:
         (b.q8, b.q_sf), (b.k8, b.k_sf) = mx
+        b.vt8, b.vt_sf = to_mx_vt(bf16_bits_to_f32(v), b.kv_offsets)
     return b

@@ -53,6 +53,12 @@ def _load():
         lib.oracle_gdpa_fwd_mx.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int]
         lib.oracle_gdpa_fwd_mx.restype = ctypes.c_int
+        lib.oracle_gdpa_fwd_mxfp8.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, P,
+                                              ctypes.c_int]
+        lib.oracle_gdpa_fwd_mxfp8.restype = ctypes.c_int
+        lib.oracle_vt_columns.argtypes = [P, ctypes.c_int]
+        lib.oracle_vt_columns.restype = ctypes.c_int64
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
         lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
@@ -118,6 +124,40 @@ def gdpa_fwd_mx_batch(batch, nthreads: int = 0) -> np.ndarray:
     w = batch.workload
     return gdpa_fwd_mx(batch.q8, batch.q_sf, batch.k8, batch.k_sf, batch.v, batch.q_offsets, batch.kv_offsets,
                        w.H, w.D, w.act, w.window_blocks, w.scale, nthreads)
+
+
+def gdpa_fwd_mxfp8(q8, q_sf, k8, k_sf, vt8, vt_sf, q_offsets, kv_offsets, H: int, D: int, act: int,
+                   window_blocks: int, scale: float, nthreads: int = 0) -> np.ndarray:
+    """Oracle output, fp64 ``[Tq, H, D]``, for Q, K and V all in MXFP8.
+
+    ``q8``, ``k8``, ``q_sf``, ``k_sf`` as :func:`gdpa_fwd_mx`; ``vt8``: uint8
+    e4m3 codes ``[H*D, VT]`` of V, key-major; ``vt_sf``: uint8 E8M0 scales
+    ``[VT // 32, H*D]`` (layout in ``gdpa_oracle.c``).
+    """
+    lib = _load()
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (q8, q_sf, k8, k_sf, vt8, vt_sf)]
+    qo = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ko = np.ascontiguousarray(kv_offsets, dtype=np.int32)
+    B = len(qo) - 1
+    VT = int(arrs[4].shape[1]) if arrs[4].ndim == 2 else -1
+    out = np.zeros((int(qo[-1]), H, D), dtype=np.float64)
+    rc = lib.oracle_gdpa_fwd_mxfp8(*[_ptr(a) for a in arrs], VT, _ptr(qo), _ptr(ko), B, H, D, act,
+                                   window_blocks, float(scale), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gdpa_fwd_mxfp8 returned %d" % rc)
+    return out
+
+
+def gdpa_fwd_mxfp8_batch(batch, nthreads: int = 0) -> np.ndarray:
+    w = batch.workload
+    return gdpa_fwd_mxfp8(batch.q8, batch.q_sf, batch.k8, batch.k_sf, batch.vt8, batch.vt_sf, batch.q_offsets,
+                          batch.kv_offsets, w.H, w.D, w.act, w.window_blocks, w.scale, nthreads)
+
+
+def vt_columns(kv_offsets) -> int:
+    """VT, the row length of the key-major V layout, as the oracle counts it."""
+    ko = np.ascontiguousarray(kv_offsets, dtype=np.int32)
+    return int(_load().oracle_vt_columns(_ptr(ko), len(ko) - 1))
 
 
 def e4m3_to_double(code: int) -> float:

@@ -74,6 +74,22 @@
  * translation, section on compute efficiency ("MXFP8 attention").  Which
  * operands are quantised is not stated there; this oracle quantises the two
  * operands of the score product along their contraction (head) dimension.
+ *
+ * All three inputs in MXFP8 (oracle_gdpa_fwd_mxfp8): q and k as above, and v
+ * quantised along the contraction dimension of P V -- the keys -- so it
+ * arrives key-major: for each (head h, coordinate d) one row of VT codes,
+ * sequence b's keys at columns [P_b, P_b + Lkv_b) with
+ *
+ *   P_b = 32 * sum_{b' < b} ceil(Lkv_b' / 32),   VT = P_B,
+ *
+ * and one E8M0 scale per 32 columns of a row, stored column-block major:
+ *
+ *   v_jd = e4m3(vt8[(h D + d) VT + P_b + j]) * 2^(vt_sf[((P_b + j) / 32) H D + h D + d] - 127)
+ *
+ * (a block never spans two sequences: each sequence starts a block).  The
+ * forward is then the definition above on these values, with the weights
+ * P_ij exact; rounding them to e4m3 on the way to the P V product is a
+ * precision of the implementation that the tests' error bar accounts for.
  */
 #include <math.h>
 #include <pthread.h>
@@ -152,6 +168,11 @@ typedef struct {
   /* MXFP8 q and k (used instead of q, k when q8 is set): e4m3 codes
    * [T, H, D] and E8M0 scales [T, H, D/32] */
   const uint8_t *q8, *q_sf, *k8, *k_sf;
+  /* MXFP8 v, key-major (used instead of v when vt8 is set): codes [H D, VT],
+   * scales [VT / 32, H D], sequence b's first column vt_col[b] */
+  const uint8_t *vt8, *vt_sf;
+  const int64_t* vt_col;
+  int64_t VT;
 } job_t;
 
 /* Element d of the (token t, head h) row of q or k, as a double. */
@@ -163,6 +184,15 @@ static double qk_value(const job_t* J, int is_k, int64_t t, int h, int d) {
   return oracle_e4m3_to_double(codes[e]) * oracle_e8m0_to_double(sf[(t * J->H + h) * (J->D / 32) + d / 32]);
 }
 
+/* Element d of key j of sequence b, head h, of v, as a double. */
+static double v_value(const job_t* J, int b, int64_t j, int h, int d) {
+  const int H = J->H, D = J->D;
+  if (!J->vt8) return bf16_to_double(J->v[((J->kv_off[b] + j) * H + h) * D + d]);
+  const int64_t col = J->vt_col[b] + j, row = (int64_t)h * D + d;
+  return oracle_e4m3_to_double(J->vt8[row * J->VT + col]) *
+         oracle_e8m0_to_double(J->vt_sf[(col / 32) * ((int64_t)H * D) + row]);
+}
+
 static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, double* qrow, double* s) {
   const int H = J->H, D = J->D;
   const int64_t q0 = J->q_off[b], Lq = J->q_off[b + 1] - q0;
@@ -170,7 +200,7 @@ static void run_task(const job_t* J, int b, int h, double* kbuf, double* vbuf, d
   for (int64_t j = 0; j < Lkv; ++j)
     for (int d = 0; d < D; ++d) {
       kbuf[j * D + d] = qk_value(J, 1, k0 + j, h, d);
-      vbuf[j * D + d] = bf16_to_double(J->v[((k0 + j) * H + h) * D + d]);
+      vbuf[j * D + d] = v_value(J, b, j, h, d);
     }
   for (int64_t i = 0; i < Lq; ++i) {
     double* o = J->out + ((q0 + i) * H + h) * (int64_t)D;
@@ -260,7 +290,8 @@ static int run_fwd(job_t* J, int nthreads) {
   if (B == 0 || q_off[B] == 0) return 0;
   const int mx = J->q8 != NULL;
   if (!J->out || (mx ? !J->q_sf : !J->q)) return 1;
-  if (kv_off[B] > 0 && (!J->v || (mx ? (!J->k8 || !J->k_sf) : !J->k))) return 1;
+  if (kv_off[B] > 0 && (!(J->v || J->vt8) || (mx ? (!J->k8 || !J->k_sf) : !J->k))) return 1;
+  if (J->vt8 && kv_off[B] > 0 && !J->vt_sf) return 1;
   if (nthreads <= 0) nthreads = oracle_num_cpus();
   if (nthreads > B * H) nthreads = B * H;
   if (nthreads < 1) nthreads = 1;
@@ -293,7 +324,8 @@ static int run_fwd(job_t* J, int nthreads) {
 int oracle_gdpa_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_off,
                     const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
                     double* out, int nthreads) {
-  job_t J = {q, k, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, NULL, NULL, NULL, NULL};
+  job_t J = {q, k, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, NULL, NULL, NULL, NULL,
+             NULL, NULL, NULL, 0};
   return run_fwd(&J, nthreads);
 }
 
@@ -306,8 +338,48 @@ int oracle_gdpa_fwd_mx(const uint8_t* q8, const uint8_t* q_sf, const uint8_t* k8
                        const uint16_t* v, const int32_t* q_off, const int32_t* kv_off, int B, int H, int D, int act,
                        int window_blocks, double scale, double* out, int nthreads) {
   if (!q8 || D % 32 != 0) return 1;
-  job_t J = {NULL, NULL, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, q8, q_sf, k8, k_sf};
+  job_t J = {NULL, NULL, v, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, q8, q_sf, k8, k_sf,
+             NULL, NULL, NULL, 0};
   return run_fwd(&J, nthreads);
+}
+
+/* Columns of the key-major v layout: P_b = 32 sum_{b' < b} ceil(Lkv_b' / 32)
+ * into col[0..B] (col[B] = VT).  kv_off must be a valid prefix sum. */
+static void vt_columns(const int32_t* kv_off, int B, int64_t* col) {
+  col[0] = 0;
+  for (int b = 0; b < B; ++b) col[b + 1] = col[b] + 32 * (((int64_t)kv_off[b + 1] - kv_off[b] + 31) / 32);
+}
+
+int64_t oracle_vt_columns(const int32_t* kv_off, int B) {
+  if (B < 0 || !kv_off) return -1;
+  int64_t c = 0;
+  for (int b = 0; b < B; ++b) c += 32 * (((int64_t)kv_off[b + 1] - kv_off[b] + 31) / 32);
+  return c;
+}
+
+/*
+ * The forward with q, k and v in MXFP8: q8 / k8 e4m3 codes [T, H, D], q_sf /
+ * k_sf E8M0 scales [T, H, D/32]; vt8 e4m3 codes [H D, VT] and vt_sf E8M0
+ * scales [VT / 32, H D] in the key-major layout of the header comment (VT
+ * must equal oracle_vt_columns).  D a multiple of 32.  Full attention or a
+ * window exactly as oracle_gdpa_fwd.
+ */
+int oracle_gdpa_fwd_mxfp8(const uint8_t* q8, const uint8_t* q_sf, const uint8_t* k8, const uint8_t* k_sf,
+                          const uint8_t* vt8, const uint8_t* vt_sf, int64_t VT, const int32_t* q_off,
+                          const int32_t* kv_off, int B, int H, int D, int act, int window_blocks, double scale,
+                          double* out, int nthreads) {
+  if (!q8 || !vt8 || D % 32 != 0 || B < 0 || !kv_off) return 1;
+  for (int b = 0; b < B; ++b)
+    if (kv_off[b + 1] < kv_off[b]) return 1;
+  if (VT != oracle_vt_columns(kv_off, B)) return 1;
+  int64_t* col = (int64_t*)malloc(sizeof(int64_t) * ((size_t)B + 1));
+  if (!col) return 2;
+  vt_columns(kv_off, B, col);
+  job_t J = {NULL, NULL, NULL, q_off, kv_off, B, H, D, act, window_blocks, scale, out, 0, q8, q_sf, k8, k_sf,
+             vt8, vt_sf, col, VT};
+  const int rc = run_fwd(&J, nthreads);
+  free(col);
+  return rc;
 }
 
 /* ------------------------------------------------------------------ backward */
