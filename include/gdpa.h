@@ -22,7 +22,8 @@
  *
  * The training entry points keep the softmax row logsumexp in the forward
  * (gdpa_fwd_lse, gdpa_fwd_sliding) and return dq, dk, dv in the backward
- * (gdpa_bwd, gdpa_bwd_sliding).  gdpa_fwd_mx takes q and k in MXFP8.
+ * (gdpa_bwd, gdpa_bwd_sliding).  gdpa_fwd_mx takes q and k in MXFP8,
+ * gdpa_fwd_mxfp8 q, k and v.
  *
  * An empty key set gives o_i = 0.  The GELU is evaluated on the ALU only: the
  * tanh is rewritten as a logistic function whose exponential is a range-reduced
@@ -173,6 +174,38 @@ gdpa_status_t gdpa_fwd_mx(const void* q8, const void* q_sf, const void* k8, cons
                           const int32_t* h_q_offsets, const int32_t* h_kv_offsets, const int32_t* q_offsets,
                           const int32_t* kv_offsets, int B, int H, int D, int act, float scale, void* out, float* lse,
                           void* stream);
+
+/*
+ * gdpa_fwd_mxfp8 -- the forward (full attention, softmax) with q, k and v
+ * all in MXFP8, both products on the block-scaled e4m3 tensor-core MMA (same
+ * sources as gdpa_fwd_mx).  q8, q_sf, k8, k_sf as gdpa_fwd_mx; v is
+ * quantised along the contraction of the P V product, the keys, so it
+ * arrives key-major:
+ *
+ *   vt8    uint8 [H*D, VT]      e4m3 codes; row h*D + d holds coordinate d
+ *                               of head h for every key: sequence b's keys
+ *                               at columns [P_b, P_b + Lkv_b),
+ *                               P_b = 32 * sum_{b' < b} ceil(Lkv_b' / 32),
+ *                               VT = P_B; the columns [P_b + Lkv_b, P_{b+1})
+ *                               must hold finite codes (zero)
+ *   vt_sf  uint8 [VT/32, H*D]   E8M0 scales: byte [c, h*D + d] scales
+ *                               columns [32 c, 32 c + 32) of row h*D + d
+ *   v_jd = e4m3(vt8[h*D + d, P_b + j]) * 2^(vt_sf[(P_b + j) / 32, h*D + d] - 127)
+ *
+ * The weights P_ij (exp2 of the scaled scores less the row's running
+ * maximum) are rounded on chip to e4m3 with one E8M0 scale per 32 keys of a
+ * row -- the scale puts the block's largest weight just under 448, so no
+ * code saturates -- and the row sum takes the unrounded weights.  D must be
+ * 128 and act GDPA_ACT_SOFTMAX (GDPA_ERR_UNSUPPORTED otherwise).  q8, k8,
+ * vt8 and out 16-byte aligned; q_sf, k_sf 4-byte aligned; vt_sf any.  lse
+ * optional (may be NULL).  Offsets twice (host and device) as
+ * gdpa_fwd_async; the host copy also fixes VT.  Asynchronous on `stream`;
+ * the buffers stay the caller's.
+ */
+gdpa_status_t gdpa_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* vt8,
+                             const void* vt_sf, const int32_t* h_q_offsets, const int32_t* h_kv_offsets,
+                             const int32_t* q_offsets, const int32_t* kv_offsets, int B, int H, int D, int act,
+                             float scale, void* out, float* lse, void* stream);
 
 /*
  * gdpa_bwd -- gradients of the forward for an upstream gradient dout:

@@ -135,14 +135,17 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // buffer into c.d_work (both guarded by events against earlier calls).
 // `single_tile`: one 128-row query tile and 128-key tiles per item whatever
 // the shapes (the MXFP8 kernel's item kind).
+// `extra` (optional): an int32 array uploaded after the work list (the
+// MXFP8 V layout's sequence columns), at offset work_extra_offset().
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
                               int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
-                              int* kv_tile, int64_t* n_items, bool single_tile = false) {
+                              int* kv_tile, int64_t* n_items, bool single_tile = false, bool pair64 = false,
+                              const std::vector<int32_t>* extra = nullptr) {
   std::vector<gdpa_work_item_t> items;
   std::vector<int32_t> cta_begin;
-  const int rpi = single_tile ? kBlockM : choose_rows_per_item(h_q_off, B, D, window_blocks);
+  const int rpi = single_tile ? kBlockM : pair64 ? 2 * kBlockM : choose_rows_per_item(h_q_off, B, D, window_blocks);
   *rows_per_item = rpi;
-  *kv_tile = single_tile ? kBlockN : choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
+  *kv_tile = single_tile ? kBlockN : pair64 ? kBlockN / 2 : choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
   const int64_t n = count_plan_items(h_q_off, B, H, rpi);
   *n_items = n;
   if (n == 0) {
@@ -158,7 +161,8 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   }
   if (st != GDPA_OK) return st;
   const size_t items_bytes = items.size() * sizeof(gdpa_work_item_t);
-  const size_t total = align_up(items_bytes, 16) + cta_begin.size() * sizeof(int32_t);
+  const size_t list_bytes = align_up(items_bytes, 16) + cta_begin.size() * sizeof(int32_t);
+  const size_t total = extra ? align_up(list_bytes, 16) + extra->size() * sizeof(int32_t) : list_bytes;
   if (cudaStreamWaitEvent(stream, c.work_free, 0) != cudaSuccess) return GDPA_ERR_CUDA;
   if (c.d_work.cap < total) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;  // old buffer may be in use
@@ -169,21 +173,36 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   char* h = static_cast<char*>(c.h_stage.p);
   std::memcpy(h, items.data(), items_bytes);
   std::memcpy(h + align_up(items_bytes, 16), cta_begin.data(), cta_begin.size() * sizeof(int32_t));
+  if (extra && !extra->empty())
+    std::memcpy(h + align_up(list_bytes, 16), extra->data(), extra->size() * sizeof(int32_t));
   if (cudaMemcpyAsync(c.d_work.p, h, total, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GDPA_ERR_CUDA;
   if (cudaEventRecord(c.stage_free, stream) != cudaSuccess) return GDPA_ERR_CUDA;
   *num_ctas = ctas;
   return GDPA_OK;
 }
 
+// Device address of the `extra` array plan_and_upload placed after a work
+// list of n_items items over num_ctas CTAs.
+const int32_t* work_extra(const DeviceCtx& c, int64_t n_items, int num_ctas) {
+  const size_t list_bytes = align_up((size_t)n_items * sizeof(gdpa_work_item_t), 16) + ((size_t)num_ctas + 1) * 4;
+  return reinterpret_cast<const int32_t*>(static_cast<const char*>(c.d_work.p) + align_up(list_bytes, 16));
+}
+
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
                               const int32_t* d_q_off, const int32_t* d_kv_off, int64_t Tq, int64_t Tkv, int H, int D,
                               int act, int window_blocks, float scale, int num_ctas, int rows_per_item,
                               int kv_tile, int64_t n_items, cudaStream_t stream, float* lse = nullptr,
-                              const void* q_sf = nullptr, const void* k_sf = nullptr) {
+                              const void* q_sf = nullptr, const void* k_sf = nullptr, const void* vt_sf = nullptr,
+                              int64_t VT = -1) {
   LaunchArgs a;
   a.lse = lse;
   a.q_sf = q_sf;
   a.k_sf = k_sf;
+  if (VT >= 0) {  // all three inputs in MXFP8 (gdpa_fwd_mxfp8): the sequence columns follow the work list
+    a.vt_sf = vt_sf;
+    a.vt_col = work_extra(c, n_items, num_ctas);
+    a.VT = VT;
+  }
   a.rows_per_item = rows_per_item;
   a.kv_tile = kv_tile;
   a.q = q;
@@ -362,6 +381,56 @@ extern "C" gdpa_status_t gdpa_fwd_mx(const void* q8, const void* q_sf, const voi
   // with no keys k_sf is never read
   return fwd_async_impl(q8, k8, v, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, 0, scale, out, lse,
                         stream, q_sf, k_sf ? k_sf : q_sf);
+}
+
+extern "C" gdpa_status_t gdpa_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                        const void* vt8, const void* vt_sf, const int32_t* h_q_offsets,
+                                        const int32_t* h_kv_offsets, const int32_t* q_offsets,
+                                        const int32_t* kv_offsets, int B, int H, int D, int act, float scale,
+                                        void* out, float* lse, void* stream) {
+  gdpa_status_t st = validate_shape(B, H, D, act, 0);
+  if (st != GDPA_OK) return st;
+  if (D != 128 || act != GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+  if (B == 0) return GDPA_OK;
+  int64_t Tq = 0, Tkv = 0;
+  if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, 0, &Tq, &Tkv)) != GDPA_OK) return st;
+  if (Tq > 0 && (!q8 || !out || !aligned16(q8) || !aligned16(out))) return GDPA_ERR_INVALID_ARG;
+  if (Tq > 0 && (!q_sf || (reinterpret_cast<uintptr_t>(q_sf) & 3u) != 0)) return GDPA_ERR_INVALID_ARG;
+  if (Tkv > 0 && (!k8 || !vt8 || !vt_sf || !k_sf || !aligned16(k8) || !aligned16(vt8) ||
+                  (reinterpret_cast<uintptr_t>(k_sf) & 3u) != 0))
+    return GDPA_ERR_INVALID_ARG;
+  if (Tq >= (int64_t)1 << 31 || Tkv >= (int64_t)1 << 31) return GDPA_ERR_UNSUPPORTED;
+  if (Tq == 0) return GDPA_OK;
+  if (!q_offsets || !kv_offsets) return GDPA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GDPA_ERR_INVALID_ARG;
+  // the key-major V layout: sequence b from column 32 * sum_{b' < b} ceil(Lkv_b' / 32)
+  std::vector<int32_t> vt_col;
+  try {
+    vt_col.resize((size_t)B + 1);
+  } catch (const std::bad_alloc&) {
+    return GDPA_ERR_NO_MEMORY;
+  }
+  int64_t col = 0;
+  for (int b = 0; b < B; ++b) {
+    vt_col[b] = static_cast<int32_t>(col);
+    col += 32 * (((int64_t)h_kv_offsets[b + 1] - h_kv_offsets[b] + 31) / 32);
+    if (col >= ((int64_t)1 << 31)) return GDPA_ERR_UNSUPPORTED;
+  }
+  vt_col[B] = static_cast<int32_t>(col);
+  int device = 0, sms = 0;
+  if ((st = num_sms(&device, &sms)) != GDPA_OK) return st;
+  DeviceCtx& c = ctx(device);
+  std::lock_guard<std::mutex> lock(c.mu);
+  if ((st = c.init()) != GDPA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int num_ctas = 0, rpi = 0, kvt = 0;
+  int64_t n_items = 0;
+  if ((st = plan_and_upload(c, h_q_offsets, h_kv_offsets, B, H, D, 0, sms, s, &num_ctas, &rpi, &kvt, &n_items,
+                            false, true, &vt_col)) != GDPA_OK)
+    return st;
+  // with no keys nothing of k or v is read
+  return launch_with_ctx(c, q8, Tkv > 0 ? k8 : q8, Tkv > 0 ? vt8 : q8, out, q_offsets, kv_offsets, Tq, Tkv, H, D,
+                         act, 0, scale, num_ctas, rpi, kvt, n_items, s, lse, q_sf, k_sf ? k_sf : q_sf, vt_sf, col);
 }
 
 namespace gdpa {

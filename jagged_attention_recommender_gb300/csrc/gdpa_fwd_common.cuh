@@ -34,6 +34,11 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   const uint32_t* k_sf;
   int Tq, Tkv;               // rows of q / out and of k / v: device offsets beyond them are a bad plan
   int test_skip_arrive;      // failure-path test only: one activation warp of CTA 0 skips one arrive
+  // MXFP8 V, key-major (tm_v then views the codes [H*D, VT]): first column
+  // of each sequence [B+1], E8M0 scales [VT/32, H*D], VT/32
+  const int32_t* vt_col;
+  const uint8_t* vt_sf;
+  int vt_blocks;
 };
 
 // kActGelu instantiates the ALU activations (tanh-GELU and SiLU, told apart

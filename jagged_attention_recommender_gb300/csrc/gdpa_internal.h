@@ -113,6 +113,12 @@ struct LaunchArgs {
   // words [T, H] (4 codes each); full attention, D = 128, single-tile items
   const void* q_sf = nullptr;
   const void* k_sf = nullptr;
+  // MXFP8 V as well (q_sf, k_sf set too): v holds the key-major codes
+  // [H*D, VT], these its scales [VT/32, H*D] and each sequence's first
+  // column (device, [B+1]); 256-row items, 64-key tiles, softmax
+  const void* vt_sf = nullptr;
+  const int32_t* vt_col = nullptr;
+  int64_t VT = 0;
 };
 
 // Backward launch: work lists of int4 {sequence, head, first row, 0} on the

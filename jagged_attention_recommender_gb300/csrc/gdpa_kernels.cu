@@ -8,6 +8,7 @@
 
 #include "gdpa_fwd_kernel.cuh"
 #include "gdpa_fwd_pair.cuh"
+#include "gdpa_fwd_mxp.cuh"
 #include "gdpa_fwd_pair64.cuh"
 #include "gdpa_internal.h"
 
@@ -62,6 +63,21 @@ gdpa_status_t encode_rows_u8(CUtensorMap* m, const void* base, int64_t rows, int
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * D};
   cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+// Key-major e4m3 V: 2-D [H*D rows, VT columns] bytes; boxes of 128 rows x
+// 128 columns (the swizzle width).  Columns past VT read as zero.
+gdpa_status_t encode_vt_u8(CUtensorMap* m, const void* base, int64_t VT, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return GDPA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(VT), static_cast<cuuint64_t>(H) * D};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(VT)};
+  cuuint32_t box[2] = {128, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -159,6 +175,14 @@ gdpa_status_t launch_pair(const FwdParams& prm, int grid, cudaStream_t stream, i
                   device, attr_done, &mu);
 }
 
+// Q, K and V in MXFP8, P rounded to MXFP8 on chip (softmax, D = 128).
+gdpa_status_t launch_mxp(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
+  static std::mutex mu;
+  static bool attr_done[kMaxDevices] = {};
+  return launch_k(gdpa_fwd_mxp_kernel, MxpCfg::THREADS, MxpCfg::SMEM_BYTES, MxpCfg::MIN_LAUNCH_REGS, prm, grid, stream,
+                  device, attr_done, &mu);
+}
+
 // Evaluates the activation exactly as the kernels do: GELU two arguments at
 // a time with the packed evaluation, exp2 on the special-function unit.
 __global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
@@ -218,8 +242,47 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   int* status = status_ptr(device);
   if (!status) return GDPA_ERR_CUDA;
   FwdParams prm;
+  prm.vt_col = nullptr;
+  prm.vt_sf = nullptr;
+  prm.vt_blocks = 0;
   const bool key_split = a.rows_per_item == kKeySplitRows;
   const bool mx = a.q_sf != nullptr;
+  if (mx && a.vt_col) {  // all three inputs in MXFP8
+    if (a.D != 128 || a.rows_per_item != 2 * kBlockM || a.kv_tile != kBlockN / 2 || a.window_blocks != 0 ||
+        a.act != GDPA_ACT_SOFTMAX || !a.k_sf || (a.Tkv > 0 && !a.vt_sf) || a.VT >= ((int64_t)1 << 31))
+      return GDPA_ERR_INVALID_ARG;
+    gdpa_status_t st = encode_rows_u8(&prm.tm_q, a.q, a.Tq, a.H, a.D, kBlockM);
+    if (st != GDPA_OK) return st;
+    if (a.Tkv > 0) {
+      if ((st = encode_rows_u8(&prm.tm_k, a.k, a.Tkv, a.H, a.D, MxpCfg::KB)) != GDPA_OK) return st;
+      if ((st = encode_vt_u8(&prm.tm_v, a.v, a.VT, a.H, a.D)) != GDPA_OK) return st;
+    } else {  // nothing is loaded; maps over Q's codes keep the descriptors valid
+      if ((st = encode_rows_u8(&prm.tm_k, a.q, a.Tq, a.H, a.D, MxpCfg::KB)) != GDPA_OK) return st;
+      if ((st = encode_rows_u8(&prm.tm_v, a.q, a.Tq, a.H, a.D, kBlockM)) != GDPA_OK) return st;
+    }
+    prm.q_sf = static_cast<const uint32_t*>(a.q_sf);
+    prm.k_sf = static_cast<const uint32_t*>(a.k_sf);
+    prm.vt_col = a.vt_col;
+    prm.vt_sf = static_cast<const uint8_t*>(a.vt_sf);
+    prm.vt_blocks = static_cast<int>(a.VT / 32);
+    prm.items = reinterpret_cast<const int4*>(a.items);
+    prm.cta_begin = a.cta_begin;
+    prm.q_off = a.q_off;
+    prm.kv_off = a.kv_off;
+    prm.out = static_cast<__nv_bfloat16*>(a.out);
+    prm.status = status;
+    prm.timeout_ns = wait_timeout_ns();
+    prm.H = a.H;
+    prm.window_blocks = 0;
+    prm.score_scale = a.scale * 1.4426950408889634f;
+    prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
+    prm.lse = a.lse;
+    prm.Tq = static_cast<int>(a.Tq);
+    prm.Tkv = static_cast<int>(a.Tkv);
+    prm.test_skip_arrive = 0;
+    alu_act_consts(false, a.scale, prm.act_a, prm.act_c);
+    return launch_mxp(prm, a.num_ctas, static_cast<cudaStream_t>(a.stream), device);
+  }
   if (mx && (a.D != 128 || a.rows_per_item != kBlockM || a.kv_tile != kBlockN || a.window_blocks != 0 || !a.k_sf))
     return GDPA_ERR_INVALID_ARG;
   gdpa_status_t st = mx ? encode_rows_u8(&prm.tm_q, a.q, a.Tq, a.H, a.D, kBlockM)

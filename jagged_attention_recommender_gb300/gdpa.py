@@ -27,7 +27,7 @@ GDPA_ERR_DEVICE_TIMEOUT = 4
 GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
-EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
            "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_fwd_lse.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
     L.gdpa_fwd_sliding.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
     L.gdpa_fwd_mx.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, P, P]
+    L.gdpa_fwd_mxfp8.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, P, P]
     L.gdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_bwd_sliding.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
@@ -79,7 +80,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_status_string.restype = ctypes.c_char_p
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
-    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
+    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
                  "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
@@ -165,6 +166,16 @@ def gdpa_fwd_mx(q8, q_sf, k8, k_sf, v, h_q_offsets, h_kv_offsets, q_offsets, kv_
     _check(lib().gdpa_fwd_mx(_addr(q8), _addr(q_sf), _addr(k8), _addr(k_sf), _addr(v), qo.ctypes.data,
                              ko.ctypes.data, _addr(q_offsets), _addr(kv_offsets), int(B), int(H), int(D), int(act),
                              float(scale), _addr(out), _addr(lse), _stream(stream)), "gdpa_fwd_mx")
+
+
+def gdpa_fwd_mxfp8(q8, q_sf, k8, k_sf, vt8, vt_sf, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act,
+                   scale, out, lse=None, stream=None):
+    """The forward with ``q8``/``k8`` and the key-major ``vt8`` all MXFP8 (e4m3 codes with E8M0 scales)."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    _check(lib().gdpa_fwd_mxfp8(_addr(q8), _addr(q_sf), _addr(k8), _addr(k_sf), _addr(vt8), _addr(vt_sf),
+                                qo.ctypes.data, ko.ctypes.data, _addr(q_offsets), _addr(kv_offsets), int(B), int(H),
+                                int(D), int(act), float(scale), _addr(out), _addr(lse), _stream(stream)),
+           "gdpa_fwd_mxfp8")
 
 
 def gdpa_bwd(q, k, v, out, dout, lse, h_q_offsets, h_kv_offsets, q_offsets, kv_offsets, B, H, D, act, window_blocks,

@@ -23,8 +23,24 @@ rounded bf16 arithmetic of one-key rows comes within a few percent of 2U|o|
 (so no tighter factor is safe), and never exceeds it.  The five workloads of
 the target keep the plain bar; their full-size outputs are compared with the
 oracle over every row (``full_output_parity``).
+
+MXFP8 weights (gdpa_fwd_mxfp8).  There the kernel also rounds each weight
+P_ij to e4m3 (3 mantissa bits) under a per-32-key power-of-two scale that
+keeps every code normal or saturation-free, so each weight moves by at most
+half an e4m3 step: |dP| <= 2^-4 P (and far less for the few codes left
+subnormal).  Summed over the keys with |v_j|, the output moves by at most
+2^-4 o_abs, o_abs_i = sum_j P_ij |v_j| / sum_j P_ij (the oracle with |V|),
+so the elementwise bar adds that term; and a rounding error uniform on
++-half a step has RMS at most 2^-4 / sqrt(3) of the weight, which bounds the
+relative L2 error when V's signs are random:
+
+    |gpu - oracle| <= 1e-2 + 2U |oracle| + 2^-4 o_abs,   rel-L2 <= 2^-4 / sqrt(3)
+
+``tests/test_parity_bar.py`` pins both on the CPU with e4m3-rounded weights.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -34,8 +50,15 @@ U_BF16 = 2.0 ** -8  # unit roundoff of bf16 (round to nearest even, 8 significan
 FEW_KEY_REL = 2.0 * U_BF16  # P rounded to bf16, then the output rounded to bf16
 
 
-def bar(ref: np.ndarray, few_keys: bool = False) -> np.ndarray:
-    """Elementwise allowance for |gpu - oracle|."""
+MXP_REL = 2.0 ** -4              # half an e4m3 step, relative
+MXP_REL_L2 = MXP_REL / math.sqrt(3.0)  # RMS of a relative error uniform on +-MXP_REL
+
+
+def bar(ref: np.ndarray, few_keys: bool = False, ref_abs: np.ndarray | None = None) -> np.ndarray:
+    """Elementwise allowance for |gpu - oracle| (``ref_abs``: the oracle with
+    |V|, for outputs whose weights were rounded to e4m3)."""
+    if ref_abs is not None:
+        return MAX_ABS + FEW_KEY_REL * np.abs(ref) + MXP_REL * np.asarray(ref_abs)
     if few_keys:
         return MAX_ABS + FEW_KEY_REL * np.abs(ref)
     return np.full(ref.shape, MAX_ABS)
@@ -82,14 +105,33 @@ def sequence_groups(q_offsets, max_rows: int = 1 << 16, min_seqs: int = 8):
     return groups
 
 
+def assert_parity_mxp(got, ref, ref_abs, what: str = ""):
+    """The e4m3-weight bar (module docstring); returns (max |d|, rel-L2)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, "%s: shape %s vs %s" % (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), "non-finite output " + what
+    if not got.size:
+        return 0.0, 0.0
+    d = np.abs(got - ref)
+    b = bar(ref, ref_abs=ref_abs)
+    worst = np.unravel_index(np.argmax(d - b), d.shape)
+    assert np.all(d <= b), "%s: |d| %.3e > bar %.3e at %s (|ref| %.3g)" % (
+        what, d[worst], b[worst], worst, abs(ref[worst]))
+    rl2 = rel_l2(got, ref)
+    assert rl2 <= MXP_REL_L2, "%s: rel L2 %.3e" % (what, rl2)
+    return float(d.max()), rl2
+
+
 def full_output_parity(batch, got_fn, oracle_fn, what: str = "", few_keys: bool = False,
-                       max_rows: int = 1 << 16):
+                       max_rows: int = 1 << 16, oracle_abs_fn=None):
     """Compares every row of a launch's output with the oracle, group by group.
 
     ``got_fn(t0, t1)`` returns the GPU output rows [t0, t1) as fp64 and
     ``oracle_fn(sub_batch)`` the oracle over a subset of whole sequences; the
     elementwise bar holds in every group and rel-L2 over the whole output.
-    Returns (max |d|, rel-L2, rows compared).
+    With ``oracle_abs_fn`` (the oracle with |V| over a subset) the bar is the
+    e4m3-weight one.  Returns (max |d|, rel-L2, rows compared).
     """
     qo = np.asarray(batch.q_offsets)
     num = den = 0.0
@@ -104,7 +146,7 @@ def full_output_parity(batch, got_fn, oracle_fn, what: str = "", few_keys: bool 
         assert got.shape == ref.shape
         assert np.isfinite(got).all(), "non-finite output %s rows %d..%d" % (what, t0, t1)
         d = np.abs(got - ref)
-        b = bar(ref, few_keys)
+        b = bar(ref, few_keys, None if oracle_abs_fn is None else oracle_abs_fn(batch.subset(seqs)))
         if not np.all(d <= b):
             i = np.unravel_index(np.argmax(d - b), d.shape)
             raise AssertionError("%s: |d| %.3e > bar %.3e at row %d (|ref| %.3g)" % (
@@ -114,6 +156,7 @@ def full_output_parity(batch, got_fn, oracle_fn, what: str = "", few_keys: bool 
         den += float(np.sum(ref ** 2))
         rows += t1 - t0
     rl2 = float(np.sqrt(num / den)) if den > 0 else 0.0
-    assert rl2 <= REL_L2, "%s: rel L2 %.3e over the whole output" % (what, rl2)
+    assert rl2 <= (REL_L2 if oracle_abs_fn is None else MXP_REL_L2), "%s: rel L2 %.3e over the whole output" % (
+        what, rl2)
     assert rows == int(qo[-1]), "%s: compared %d of %d rows" % (what, rows, int(qo[-1]))
     return worst, rl2, rows

@@ -61,3 +61,45 @@ def test_few_key_allowance_is_tight():
     # and with the constant part: rows with |o| large enough that 2U|o| > 1e-2
     big = np.abs(exact) > 8.0
     assert np.any(np.abs(out - exact)[big] > 1e-2 + 1.5 * U * np.abs(exact)[big])
+
+
+# ---------------------------------------------------------------- e4m3 weights
+
+def _e4m3_weight_rows(n_rows=2000, n_keys=1024, seed=1):
+    """Softmax rows with their weights rounded to e4m3 the way the MXFP8
+    kernel does: per 32 keys a power-of-two scale 2^e with the block's
+    largest weight in (224, 448], codes by torch's float8_e4m3fn conversion,
+    the row sum over the unrounded weights.  Scores N(0, 1) (unit-variance
+    Q and K at scale 1/sqrt(D)), values N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    s = rng.standard_normal((n_rows, n_keys))
+    v = rng.standard_normal((n_rows, n_keys))
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    pb = p.reshape(n_rows, n_keys // 32, 32)
+    e = np.ceil(np.log2(pb.max(axis=2)) - np.log2(448.0))
+    y = (pb / np.ldexp(1.0, e.astype(np.int64))[..., None]).astype(np.float32)
+    q = torch.from_numpy(y).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    pq = (q * np.ldexp(1.0, e.astype(np.int64))[..., None]).reshape(n_rows, n_keys)
+    l = p.sum(axis=1)
+    exact = (p * v).sum(axis=1) / l
+    got = (pq * v).sum(axis=1) / l
+    o_abs = (p * np.abs(v)).sum(axis=1) / l
+    return exact, got, o_abs, y
+
+
+def test_e4m3_weight_bar_covers_rounded_weights():
+    exact, got, o_abs, y = _e4m3_weight_rows()
+    assert y.max() <= 448.0 and y.max() > 224.0  # the scale rule: no code saturates
+    d = np.abs(got - exact)
+    assert np.all(d <= parity.MXP_REL * o_abs)
+    assert parity.rel_l2(got, exact) <= parity.MXP_REL_L2
+
+
+def test_e4m3_weight_bar_is_tight():
+    exact, got, o_abs, _ = _e4m3_weight_rows()
+    # the RMS bound is reached to within a factor 2 (the relative step of
+    # e4m3 is 2^-3 .. 2^-4 over a binade, so the RMS sits below the bound),
+    # and the bf16 bar would reject these correctly rounded results
+    rl2 = parity.rel_l2(got, exact)
+    assert 0.5 * parity.MXP_REL_L2 <= rl2 <= parity.MXP_REL_L2
+    assert rl2 > parity.REL_L2
