@@ -288,8 +288,9 @@ def run_reference(args, rank, world):
 # The configurations of the target metric besides the headline one; each is
 # timed the same way and reported under "workloads" in the JSON line.
 NORTH_STAR_OTHERS = ["tiny", "cross_gelu", "pma", "block_window"]
-# and the headline workload with every input in MXFP8 (the precision row)
-EXTRA_WORKLOADS = ["self_long_mx"]
+# and two more rows of the path: the headline workload with every input in
+# MXFP8, and the token-granular sliding window
+EXTRA_WORKLOADS = ["self_long_mx", "sliding_window"]
 
 
 def bench_batch(name: str, rank: int, world: int):
@@ -388,9 +389,8 @@ def measure_forward(name, args, rank, world, local, dist, gdpa, with_e2e=True):
     total_flops = float(sum(per_rank))
     value = total_flops * K / (elapsed_ms / 1e3) / 1e12
 
-    # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step);
-    # the host-buffer entry point takes bf16 inputs and block windows only, so a sliding window
-    # and the MXFP8 forward have none
+    # ---- end to end through the public C ABI with host buffers (H2D + compute + D2H each step):
+    # gdpa_fwd_host where it applies (bf16, block windows), else the copies around the entry point
     e2e = None
     if with_e2e and w.window_blocks >= 0 and not w.mx:
         hq = torch.from_numpy(batch.q.view(np.int16)).pin_memory()
@@ -416,6 +416,50 @@ def measure_forward(name, args, rank, world, local, dist, gdpa, with_e2e=True):
         e2e = {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3, "entry": "gdpa_fwd_host"}
         del hq, hk, hv, ho
+    elif with_e2e:
+        # the sliding-window and MXFP8 entry points take device tensors: each
+        # step copies the inputs from pinned host memory, calls the entry
+        # point and reads the output back, all on the stream
+        if w.mx:
+            host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                       for a in (batch.q8, batch.q_sf, batch.k8, batch.k_sf, batch.vt8, batch.vt_sf)]
+            dev_in = [q8, qsf, k8, ksf, vt8, vtsf]
+            entry = "H2D copies + gdpa_fwd_mxfp8 + D2H"
+        else:
+            host_in = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in (batch.q, batch.k, batch.v)]
+            dev_in = [q.view(torch.int16), k.view(torch.int16), v.view(torch.int16)]
+            entry = "H2D copies + gdpa_fwd_sliding + D2H"
+        h_qo_t = torch.from_numpy(batch.q_offsets).pin_memory()
+        h_ko_t = torch.from_numpy(batch.kv_offsets).pin_memory()
+        ho = torch.empty((Tq, H, D), dtype=torch.int16).pin_memory()
+        h2d = int(sum(t.numel() * t.element_size() for t in host_in)) + 2 * 4 * (B + 1)
+        d2h = int(ho.numel()) * 2
+
+        def e2e_step():
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            qo.copy_(h_qo_t, non_blocking=True)
+            ko.copy_(h_ko_t, non_blocking=True)
+            step()
+            ho.copy_(out.view(torch.int16), non_blocking=True)
+            stream.synchronize()
+
+        e2e_step()
+        e2e_t = []
+        for _ in range(max(1, args.e2e_steps)):
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_t.append(time.perf_counter() - t0)
+        e2e_s = statistics.mean(e2e_t)
+        if dist:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": total_flops / e2e_s / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "entry": entry}
+        del host_in, ho
 
     peaks, peak_src = load_peaks()
     bound = BOUND[name]

@@ -51,11 +51,13 @@ enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatus
 // clipped to the tensors the launch was given: a plan used with offsets it
 // was not built from (or offsets past the tensors) can then only read rows
 // that exist -- TMA fills the rest with zeros -- and never writes outside
-// `out`; the launch flags kStatusBadPlan.  Returns {first row, rows} for Q/O
-// (rows counted from qs + q0) and K/V.
+// `out`.  Every role clips the same way; the one decode with FLAG (the Q/K
+// producer's) flags the launch with kStatusBadPlan.  Returns {first row,
+// rows} for Q/O (rows counted from qs + q0) and K/V.
 struct ItemRows {
   int qs, ks, Lq, Lkv;
 };
+template <bool FLAG = false>
 __device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
   const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
   const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
@@ -65,7 +67,7 @@ __device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
   r.Lq = min(qe, p.Tq) - qs;
   r.Lkv = min(ke, p.Tkv) - ks;
   if (qs < 0 || ks < 0 || qe > p.Tq || ke > p.Tkv || r.Lq < 0 || r.Lkv < 0) {
-    atomicOr(p.status, kStatusBadPlan);
+    if (FLAG) atomicOr(p.status, kStatusBadPlan);
     r.Lq = max(r.Lq, 0);
     r.Lkv = max(r.Lkv, 0);
     if (qs < 0 || qs > p.Tq) r.Lq = 0;

@@ -132,7 +132,7 @@ struct ItemView {
   int h, q0, kv0, kv_end, n_kv, q_rows, q_tok, kv_tok, Lkv;
 };
 
-template <int MODE>
+template <int MODE, bool FLAG = false>
 __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   constexpr bool WIN = MODE == kModeWindow;
   constexpr int BN = 128;
@@ -142,7 +142,7 @@ __device__ __forceinline__ ItemView decode_item(const FwdParams& p, int idx) {
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = it.w;
-  const ItemRows r = item_rows(p, b);
+  const ItemRows r = item_rows<FLAG>(p, b);
   v.q_tok = r.qs + v.q0;
   v.kv_tok = r.ks;
   v.Lkv = r.Lkv;
@@ -181,7 +181,7 @@ __device__ void run_producer(const FwdParams& p, uint8_t* sm, FwdBars<D, MODE>& 
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const ItemView t = decode_item<MODE>(p, idx);
+    const ItemView t = decode_item<MODE, !LOAD_V>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       const int qs = qi % C::NQ;

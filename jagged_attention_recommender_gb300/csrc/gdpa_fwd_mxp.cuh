@@ -116,7 +116,7 @@ __device__ void mxp_producer(const FwdParams& p, uint8_t* sm, MxpBars& B, int ib
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<false>(p, idx);
+    const Pair64Item t = decode_pair64<false, !LOAD_V>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {

@@ -78,7 +78,7 @@ struct PairItem {
 // window: the item's keys run from the first key tile A's rows may see to
 // the last query of tile B; tile A takes the K/V tiles up to its own last
 // query, tile B those from the first tile that holds a key its rows may see.
-template <bool WIN>
+template <bool WIN, bool FLAG = false>
 __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
   const int4 it = __ldg(p.items + idx);
   PairItem v;
@@ -86,7 +86,7 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = WIN ? it.w : 0;
-  const ItemRows r = item_rows(p, b);
+  const ItemRows r = item_rows<FLAG>(p, b);
   v.q_tok = r.qs + v.q0;
   v.kv_tok = r.ks;
   v.Lkv = r.Lkv;
@@ -132,7 +132,7 @@ __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, i
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair<WIN>(p, idx);
+    const PairItem t = decode_pair<WIN, !LOAD_V>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {
@@ -250,7 +250,10 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   bool ok = true;
   bool pend[2] = {false, false};
   PairPV pv[2] = {{0, 0, 0, 0, 0, 0}, {0, 0, 0, 0, 0, 0}};
-  bool pend_v = false, pend_v_read = false;  // V tile pend_v_g staged; read by some P V
+  // Every staged V tile is read by tile A's P V (an item without rows in
+  // tile A has no tiles), so its release always follows a read that waited
+  // for the load: the producer never refills a stage with a copy in flight.
+  bool pend_v = false;
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const PairItem t = decode_pair<WIN>(p, idx);
@@ -302,13 +305,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
         ptx::mma_commit_elect(&B.s_full[x]);
       }
       if (!ok) break;
-      if (pend_v) {  // both P V of the previous tile issued
-        // a stage no P V read is released only once its load has landed,
-        // so the producer never refills a stage with a copy in flight
-        if (!pend_v_read) ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
-        if (!ok) break;
-        ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
-      }
+      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);  // both P V of the previous tile issued
       ptx::mma_commit_elect(&B.k_empty[sk]);
       if (j == t.n_kv - 1) {
         for (int x = 0; x < 2; ++x)
@@ -321,7 +318,6 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
         ++gx[x];
       }
       pend_v = true;
-      pend_v_read = act[0] || act[1];
       pend_v_g = g;
     }
     for (int x = 0; x < 2; ++x)
@@ -329,8 +325,6 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair_issue_pv<D>(p, sm, B, tmem, x, pv[x]);
-  if (ok && pend_v && !pend_v_read)
-    ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
   ptx::mma_commit_elect(&B.mma_drain);

@@ -96,7 +96,7 @@ struct Pair64Item {
 // window: the item's keys run from the first key tile A's rows may see to
 // the last query of tile B; each tile takes the 64-key blocks of its own
 // window (blocks are K/V tiles).
-template <bool WIN>
+template <bool WIN, bool FLAG = false>
 __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx) {
   constexpr int BN = 64;
   const int4 it = __ldg(p.items + idx);
@@ -105,7 +105,7 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = WIN ? it.w : 0;
-  const ItemRows r = item_rows(p, b);
+  const ItemRows r = item_rows<FLAG>(p, b);
   v.q_tok = r.qs + v.q0;
   v.kv_tok = r.ks;
   v.Lkv = r.Lkv;
@@ -157,7 +157,7 @@ __device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
     ptx::prefetch_tensormap(&p.tm_k);
   }
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    const Pair64Item t = decode_pair64<WIN, !LOAD_V>(p, idx);
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {
@@ -267,7 +267,13 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   bool ok = true;
   bool pend[2] = {false, false};
   Pair64PV pv[2] = {{0, 0, 0, 0, 0}, {0, 0, 0, 0, 0}};
-  bool pend_v = false, pend_v_read = false;  // V tile pend_v_g staged; read by some P V
+  // V tile pend_v_g is released once both sides' P V of it are issued.  Every
+  // staged tile is read by a P V -- tile A attends to the item's first tiles
+  // and tile B to its last ones, with no gap between them (a window's start
+  // moves forward by at most tile A's rows), and an item without rows in tile
+  // A has no tiles -- so the release always follows a read that waited for
+  // the load, and the producer never refills a stage with a copy in flight.
+  bool pend_v = false;
   uint32_t pend_v_g = 0;
   for (int idx = ibeg; idx < iend && ok; ++idx) {
     const Pair64Item t = decode_pair64<WIN>(p, idx);
@@ -321,13 +327,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
         pend[x] = false;
       }
       if (!ok) break;
-      if (pend_v) {
-        // a stage no P V read is released only once its load has landed,
-        // so the producer never refills a stage with a copy in flight
-        if (!pend_v_read) ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
-        if (!ok) break;
-        ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
-      }
+      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
       for (int x = 0; x < 2; ++x) {
         if (!act[x]) continue;
         pv[x] = Pair64PV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
@@ -335,7 +335,6 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
         ++gx[x];
       }
       pend_v = true;
-      pend_v_read = act[0] || act[1];
       pend_v_g = g;
     }
     for (int x = 0; x < 2; ++x)
@@ -343,8 +342,6 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   }
   for (int x = 0; x < 2 && ok; ++x)
     if (pend[x]) ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
-  if (ok && pend_v && !pend_v_read)
-    ok = ptx::mbar_wait(&B.v_full[pend_v_g % C::NV], (pend_v_g / C::NV) & 1, p.timeout_ns, abort);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
   ptx::mma_commit_elect(&B.mma_drain);
