@@ -138,3 +138,32 @@ def test_mxfp8_rejects_bad_arguments():
         with pytest.raises(gdpa.GdpaError) as e:
             gdpa.gdpa_fwd_mxfp8(buf, qs, buf, sf, buf, sf, qo, qo, 0, 0, 1, 1, D, act, 1.0, bf)
         assert e.value.code == code
+
+
+def test_mxfp8_device_offsets_past_the_tensors_are_clipped_and_flagged():
+    """Device offsets that disagree with the host ones (reaching past the
+    tensors): every role clips the item to the rows that exist, nothing is
+    written outside `out`, the launch reports GDPA_ERR_INVALID_ARG, and the
+    next call with matching offsets is within the bar."""
+    rng = np.random.default_rng(5400)
+    L = rng.integers(1, 600, size=24, endpoint=True)
+    b = mxfp8_batch(rng, L, L, 2, 1.0 / np.sqrt(128))
+    w = b.workload
+    Tq = int(b.q_offsets[-1])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q8, qs, k8, ks, vt8, vsf = (dev(a) for a in (b.q8, b.q_sf, b.k8, b.k_sf, b.vt8, b.vt_sf))
+    guard = 5
+    full = torch.full((Tq + 2 * guard, w.H, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = full[guard:guard + Tq]
+    bad = dev(offsets_of(L * 2 + 7))
+    gdpa.gdpa_fwd_mxfp8(q8, qs, k8, ks, vt8, vsf, b.q_offsets, b.kv_offsets, bad, bad, b.B, w.H, w.D, w.act,
+                        w.scale, out)
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_ERR_INVALID_ARG
+    assert torch.isnan(torch.cat([full[:guard], full[guard + Tq:]]).float()).all(), "wrote outside out"
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_OK
+    qo, ko = dev(b.q_offsets), dev(b.kv_offsets)
+    gdpa.gdpa_fwd_mxfp8(q8, qs, k8, ks, vt8, vsf, b.q_offsets, b.kv_offsets, qo, ko, b.B, w.H, w.D, w.act, w.scale,
+                        out)
+    assert gdpa.gdpa_device_status() == gdpa.GDPA_OK
+    ref, ref_abs = oracle_pair(b)
+    assert_parity_mxp(out.float().cpu().numpy().astype(np.float64), ref, ref_abs, "after the bad offsets")
