@@ -287,7 +287,7 @@ def run_reference(args, rank, world):
 
 # The configurations of the target metric besides the headline one; each is
 # timed the same way and reported under "workloads" in the JSON line.
-NORTH_STAR_OTHERS = ["tiny", "cross_gelu", "pma", "block_window"]
+METRIC_CONFIGS = ["tiny", "cross_gelu", "pma", "block_window"]
 # and two more rows of the path: the headline workload with every input in
 # MXFP8, and the token-granular sliding window
 EXTRA_WORKLOADS = ["self_long_mx", "sliding_window"]
@@ -520,7 +520,7 @@ def run_ours(args, rank, world, local):
 
     others = {}
     if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
-        for name in NORTH_STAR_OTHERS + EXTRA_WORKLOADS:
+        for name in METRIC_CONFIGS + EXTRA_WORKLOADS:
             r = measure_forward(name, args, rank, world, local, dist, gdpa)
             others[name] = {"workload": "%s: %s" % (name, RECIPES[name]), "ms_per_step": r["ms_per_step"],
                             "dtype": "mxfp8 (Q, K, V, P) + bf16 O" if WORKLOADS[name].mx else "bf16",
