@@ -27,7 +27,8 @@
 //
 // Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
 // and K (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
-// the issue loop and one elected lane issues) and the TMA producer for V
+// the issue loop and one elected lane issues; with full attention warp 3
+// issues tile B's MMAs and warp 1 tile A's) and the TMA producer for V
 // (warp 2), and hands its registers to warpgroups 1 and 2, the
 // activation/epilogue of tiles A and B.  TMEM (512 columns): S_A buffers 0
 // and 64, S_B buffers 128 and 192, O_A 256, O_B 384.  An activation thread
@@ -81,7 +82,7 @@ struct Pair64Bars {
   uint64_t v_full[Pair64Cfg<D>::NV], v_empty[Pair64Cfg<D>::NV];
   uint64_t s_full[2][2], p_full[2][2];  // per side and S buffer
   uint64_t o_done[2], o_empty[2];
-  uint64_t mma_drain;
+  uint64_t mma_drain[2];  // one per MMA warp
   uint32_t tmem_slot;
   int abort;
 };
@@ -344,9 +345,92 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
     if (pend[x]) ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
   if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
   if (!ok) report_failure(p, abort, kStatusMma);
-  ptx::mma_commit_elect(&B.mma_drain);
+  ptx::mma_commit_elect(&B.mma_drain[0]);
   const int never = 0;
-  ptx::mbar_wait(&B.mma_drain, 0, 100000000ull, &never);
+  ptx::mbar_wait(&B.mma_drain[0], 0, 100000000ull, &never);
+}
+
+// Full attention (short key ranges): one MMA warp per side, so that a side
+// whose P is ready never waits behind the other side's (measured: cross_gelu
+// 0.631 -> 0.600 ms, cross_silu 0.646 -> 0.604 ms; windows keep the single
+// issuer above, whose fixed A-then-B order measured faster for them).
+// Side x's warp walks every item; for each K/V tile it waits for K, issues
+// S_x into its next buffer (if its rows attend to the tile), releases its
+// hold on K, then issues the pending O_x += P_x V of its previous tile and
+// releases its hold on that V.  A tile the side does not attend to is
+// released once it has landed.  K and V stages then have two-count empty
+// barriers (one arrival per side).
+template <int D, bool WIN, bool SPLIT>
+__device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int ibeg,
+                                int iend, int x) {
+  using C = Pair64Cfg<D>;
+  volatile int* abort = &B.abort;
+  int qn = 0;        // this side's items (Q stage and O use counts)
+  uint32_t gx = 0;   // this side's tiles (S buffers)
+  uint32_t g = 0;    // K/V tiles
+  bool ok = true;
+  bool pend = false;
+  Pair64PV pv = {0, 0, 0, 0, 0};
+  for (int idx = ibeg; idx < iend && ok; ++idx) {
+    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    if (t.n_kv == 0) continue;
+    const bool has = t.rows[x] > 0;
+    uint32_t q_base = 0;
+    if (has) {
+      const int s = qn % C::NQS;
+      ok = ptx::mbar_wait(&B.q_full[x][s], (qn / C::NQS) & 1, p.timeout_ns, abort);
+      q_base = ptx::smem_u32(sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::Q_TILE);
+    }
+    if (!ok) break;
+    for (int j = 0; j < t.n_kv; ++j, ++g) {
+      const int sk = g % C::NK;
+      ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const bool act = has && j >= t.t0[x] && j < t.t1[x];
+      const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
+      const int n16 = (ncols + 15) >> 4;
+      if (act) {
+        const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
+        const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + sk * C::KV_TILE);
+        const uint32_t s_col = C::tm_s(x, gx & 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+          ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base + qoff, 16, 1024),
+                            ptx::sdesc_sw128(k_base + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit_elect(&B.s_full[x][gx & 1]);
+      }
+      ptx::mma_commit_elect(&B.k_empty[sk]);
+      if (has && j == t.n_kv - 1) ptx::mma_commit_elect(&B.q_empty[x][qn % C::NQS]);
+      if (pend) {
+        ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv);
+        if (!ok) break;
+        ptx::mma_commit_elect(&B.v_empty[pv.g % C::NV]);
+        pend = false;
+      }
+      if (act) {
+        pv = Pair64PV{gx, g, qn, j == t.t0[x] ? 1 : 0, n16};
+        pend = true;
+        ++gx;
+      } else {  // V(g) is not read by this side: release it once it has landed
+        ok = ptx::mbar_wait(&B.v_full[g % C::NV], (g / C::NV) & 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::mma_commit_elect(&B.v_empty[g % C::NV]);
+      }
+    }
+    if (has) ++qn;
+  }
+  if (ok && pend) {
+    ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv);
+    if (ok) ptx::mma_commit_elect(&B.v_empty[pv.g % C::NV]);
+  }
+  if (!ok) report_failure(p, abort, kStatusMma);
+  ptx::mma_commit_elect(&B.mma_drain[x]);
+  const int never = 0;
+  ptx::mbar_wait(&B.mma_drain[x], 0, 100000000ull, &never);
 }
 
 // ------------------------------------------------------------------ activation + epilogue
@@ -696,15 +780,17 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
       ptx::mbar_init(&B.o_done[x], 1);
       ptx::mbar_init(&B.o_empty[x], 128);
     }
+    constexpr uint32_t n_mma = WIN ? 1 : 2;  // MMA warps, each releasing every K and V stage once
     for (int s = 0; s < C::NK; ++s) {
       ptx::mbar_init(&B.k_full[s], 1);
-      ptx::mbar_init(&B.k_empty[s], 1);
+      ptx::mbar_init(&B.k_empty[s], n_mma);
     }
     for (int s = 0; s < C::NV; ++s) {
       ptx::mbar_init(&B.v_full[s], 1);
-      ptx::mbar_init(&B.v_empty[s], 1);
+      ptx::mbar_init(&B.v_empty[s], n_mma);
     }
-    ptx::mbar_init(&B.mma_drain, 1);
+    ptx::mbar_init(&B.mma_drain[0], 1);
+    ptx::mbar_init(&B.mma_drain[1], 1);
     B.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -722,8 +808,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
       if (lane == 0) pair64_producer<D, WIN, false>(p, sm, B, ibeg, iend);
     } else if (warp == 2) {
       if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B, ibeg, iend);
-    } else if (warp == 1) {
-      pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
+    } else if (WIN) {
+      if (warp == 1) pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend);  // whole warp: warp-uniform issue
+    } else {  // warps 1 and 3: the MMA issuers of tiles A and B
+      pair64_mma_side<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend, warp == 1 ? 0 : 1);
     }
   } else {  // warpgroups 1 and 2: tiles A and B
     ptx::regs_inc<C::regs_act(ACT)>();
