@@ -45,7 +45,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 from jagged_attention_recommender_gb300.metrics import algorithmic_bytes, useful_flops  # noqa: E402
-from jagged_attention_recommender_gb300.workloads import WORKLOADS, make_batch  # noqa: E402
+from jagged_attention_recommender_gb300.workloads import ACT_SOFTMAX, WORKLOADS, make_batch  # noqa: E402
 
 METRIC = "jagged GDPA fwd useful TFLOPS (unpadded) & % of GB300 roofline, 1 GPU"
 METRIC_BWD = "jagged GDPA bwd useful TFLOPS (unpadded, 10*D*H per pair) & % of GB300 roofline, 1 GPU"
@@ -55,12 +55,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 RECIPES = {
     "tiny": "B=4 H=2 D=64, L~U{1..128}, softmax, scale=1/sqrt(D)",
     "self_long": "B=256 H=4 D=128, L=clip(round(lognormal(6.9,0.8)),100,4096), softmax non-causal, scale=1/sqrt(D)",
-    "cross_gelu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, GELU-tanh (ALU), scale=1, /Lkv",
+    "cross_gelu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, GELU-tanh, scale=1, /Lkv",
     "pma": "B=256 H=8 D=64, 32 shared seed queries per sample, Lkv=clip(round(lognormal(7.6,1.0)),100,16384), softmax",
     "block_window": "B=64 H=4 D=128, L=64*U{8..512}, 64-token blocks, window 4 blocks (own causal + 3 previous), softmax",
     "sliding_window": "B=64 H=4 D=128, L~U{512..32768}, causal sliding window of 256 tokens, softmax",
-    "cross_silu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, SiLU (ALU), scale=1, /Lkv",
-    "pffn": "B=256 H=4 D=128, Lq~U{256..4096}, 512 hidden units per sample as keys/values, GELU (ALU), scale=1/sqrt(D)",
+    "cross_silu": "B=512 H=4 D=128, Lq~U{256..4096}, Lkv~U{8..64}, QK-normed x4, SiLU, scale=1, /Lkv",
+    "pffn": "B=256 H=4 D=128, Lq~U{256..4096}, 512 hidden units per sample as keys/values, GELU-tanh, scale=1/sqrt(D)",
     "self_long_mx": "self_long with Q, K, V in MXFP8 (e4m3, E8M0 scale per 32 of D for Q/K, per 32 keys for V, "
                     "V key-major) and P rounded to MXFP8 on chip; both products on the block-scaled e4m3 MMA; O bf16",
 }
@@ -290,7 +290,7 @@ def run_reference(args, rank, world):
 METRIC_CONFIGS = ["tiny", "cross_gelu", "pma", "block_window"]
 # and two more rows of the path: the headline workload with every input in
 # MXFP8, and the token-granular sliding window
-EXTRA_WORKLOADS = ["self_long_mx", "sliding_window"]
+EXTRA_WORKLOADS = ["self_long_mx", "sliding_window", "pffn"]
 
 
 def bench_batch(name: str, rank: int, world: int):
@@ -528,6 +528,19 @@ def run_ours(args, rank, world, local):
                             "clocks": r["clocks"], "tokens_q": r["Tq"], "tokens_kv": r["Tkv"],
                             "gpu_launches": r["K"]}
             del r
+            if WORKLOADS[name].act != ACT_SOFTMAX:
+                # the same launch with the ALU-only sigma route (the GDPA
+                # section's polynomial) for comparison; the default route
+                # takes sigma on the special-function unit
+                gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_ALU)
+                try:
+                    r = measure_forward(name, args, rank, world, local, dist, gdpa, with_e2e=False)
+                finally:
+                    gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_SFU)
+                others[name]["alu_route"] = {"ms_per_step": r["ms_per_step"], "value": r["value"],
+                                             "roofline_frac": r["roofline"]["frac"],
+                                             "launch_ms": r["roofline"]["launch_ms"]}
+                del r
 
     per_rank = head["per_rank_flops"]
     skew = max(per_rank) / (sum(per_rank) / len(per_rank)) if sum(per_rank) > 0 else 1.0

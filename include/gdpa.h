@@ -25,11 +25,14 @@
  * (gdpa_bwd, gdpa_bwd_sliding).  gdpa_fwd_mx takes q and k in MXFP8,
  * gdpa_fwd_mxfp8 q, k and v.
  *
- * An empty key set gives o_i = 0.  The GELU is evaluated on the ALU only: the
- * tanh is rewritten as a logistic function whose exponential is a range-reduced
- * 6th-order Taylor polynomial (GDPA section: "ALU-only activation", valid
- * because QK-norm bounds the scores).  It is within 1e-3 of the exact tanh-GELU
- * for |s| <= 17 and saturates correctly beyond.
+ * An empty key set gives o_i = 0.  The GELU's tanh is rewritten as a
+ * logistic function, gelu(x) = x sigma(2u), whose sigma takes one of two
+ * routes (gdpa_act_route_t): the special-function unit's exp2 and reciprocal
+ * (the default), or the ALU-only form of the GDPA section ("ALU-only
+ * activation", valid because QK-norm bounds the scores): a range-reduced
+ * 6th-order Taylor polynomial of exp and a Newton reciprocal.  Either is
+ * within 1e-3 of the exact tanh-GELU for |s| <= 17 and saturates correctly
+ * beyond.
  *
  * Data layout (all pointers are device pointers unless named h_*):
  *   q    bf16 [Tq,  H, D]   row-major, contiguous, Tq  = q_offsets[B]
@@ -64,11 +67,27 @@ extern "C" {
 
 typedef enum {
   GDPA_ACT_SOFTMAX = 0,    /* online softmax */
-  GDPA_ACT_GELU_TANH = 1,  /* (1/Lkv) * sum gelu_tanh(s) v, ALU-only polynomial */
-  GDPA_ACT_SILU = 2        /* (1/Lkv) * sum silu(s) v, silu(x) = x sigma(x), the same ALU sigma
+  GDPA_ACT_GELU_TANH = 1,  /* (1/Lkv) * sum gelu_tanh(s) v (sigma route: gdpa_act_route_t) */
+  GDPA_ACT_SILU = 2        /* (1/Lkv) * sum silu(s) v, silu(x) = x sigma(x), the same sigma
                               (an alternative activation of GDPA: remio.ai commentary,
                               model/system co-design section); no windows */
 } gdpa_act_t;
+
+/*
+ * How the GELU and SiLU activations evaluate their sigma (process-wide, see
+ * gdpa_set_act_route).  Both compute the same function to fp32 level:
+ *   GDPA_ROUTE_SFU: sigma(z) = 1 / (1 + 2^(-z log2 e)) with the
+ *     special-function unit's ex2.approx and rcp.approx (the default: on
+ *     sm_103a it measured faster than the polynomial in every forward kernel);
+ *   GDPA_ROUTE_ALU: the ALU-only form of the GDPA section of the techfeed
+ *     summary of "GEM Training" (a 6th-order Taylor polynomial of exp after
+ *     range reduction, Newton reciprocal), FMA and integer instructions only.
+ * The backward always takes the ALU route.
+ */
+typedef enum {
+  GDPA_ROUTE_SFU = 0,
+  GDPA_ROUTE_ALU = 1
+} gdpa_act_route_t;
 
 typedef enum {
   GDPA_OK = 0,
@@ -334,13 +353,23 @@ gdpa_status_t gdpa_plan_enumerate(const int32_t* h_q_offsets, const int32_t* h_k
 
 /*
  * gdpa_act_eval -- evaluates the kernel's device activation elementwise:
- * y[i] = gelu(x[i]) with the ALU-only polynomial (act = GDPA_ACT_GELU_TANH),
- * y[i] = silu(x[i]) with the same ALU sigma (act = GDPA_ACT_SILU),
+ * y[i] = gelu(x[i]) (act = GDPA_ACT_GELU_TANH) or y[i] = silu(x[i])
+ * (act = GDPA_ACT_SILU) through the current route (gdpa_set_act_route),
  * or y[i] = 2^x[i] with the exponential the softmax path uses
  * (act = GDPA_ACT_SOFTMAX).  x, y: device fp32 [n].  For accuracy tests;
  * GDPA_ERR_INVALID_ARG for any other act.
  */
 gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
+
+/*
+ * gdpa_set_act_route -- selects the route (gdpa_act_route_t) every later
+ * forward launch and gdpa_act_eval call of this process uses for the GELU and
+ * SiLU sigma; launches already enqueued keep theirs.  Thread-safe (an atomic
+ * word).  GDPA_ERR_INVALID_ARG for any other value (the route is unchanged).
+ * gdpa_get_act_route returns the current one.
+ */
+gdpa_status_t gdpa_set_act_route(int route);
+int gdpa_get_act_route(void);
 
 /*
  * gdpa_device_status -- synchronises `stream`, then reads and clears the

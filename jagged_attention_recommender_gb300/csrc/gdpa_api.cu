@@ -824,6 +824,14 @@ extern "C" gdpa_status_t gdpa_fwd_host(const void* h_q, const void* h_k, const v
   return GDPA_OK;
 }
 
+extern "C" gdpa_status_t gdpa_set_act_route(int route) {
+  if (route != GDPA_ROUTE_SFU && route != GDPA_ROUTE_ALU) return GDPA_ERR_INVALID_ARG;
+  set_act_route(route);
+  return GDPA_OK;
+}
+
+extern "C" int gdpa_get_act_route(void) { return act_route(); }
+
 extern "C" gdpa_status_t gdpa_act_eval(int act, const float* x, float* y, int64_t n, void* stream) {
   if (act != GDPA_ACT_SOFTMAX && act != GDPA_ACT_GELU_TANH && act != GDPA_ACT_SILU) return GDPA_ERR_INVALID_ARG;
   if (n < 0 || (n > 0 && (!x || !y))) return GDPA_ERR_INVALID_ARG;

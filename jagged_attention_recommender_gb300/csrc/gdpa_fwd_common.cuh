@@ -28,6 +28,7 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   int out_align32;           // out is 32-byte aligned: 32-byte stores allowed
   float* lse;                // optional [Tq, H]: softmax row logsumexp (natural log) for the backward
   float act_a, act_c;        // ALU activations: folded constants (alu_act_consts)
+  int act_sfu;               // ALU activations: 1 = sigma on the special-function unit, 0 = the FMA polynomial
   // MXFP8 Q and K (tm_q, tm_k then view e4m3 codes): per (token, head) one
   // 32-bit word of four E8M0 scales, block b of D in byte b
   const uint32_t* q_sf;

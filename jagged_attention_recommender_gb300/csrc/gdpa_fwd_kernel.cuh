@@ -16,7 +16,7 @@
 //   warpgroup 1 (248 registers a thread): activation, one query row per
 //               thread: reads its whole row of S from TMEM at once, masks the
 //               ragged edge / window, applies the online softmax (running max
-//               with lazy rescaling of O) or the ALU-only GELU, and writes P
+//               with lazy rescaling of O) or the GELU / SiLU, and writes P
 //               (bf16) back over S; at the end of an item it hands the row
 //               sum to the epilogue through shared memory;
 //   warpgroup 2 epilogue: waits for the item's last O += P V, normalises O
@@ -405,11 +405,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float sl = p.score_scale;
-  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
-  if (ACT == kActGelu) {  // the ALU activation's folded constants
-    gA2 = ptx::f2_splat(p.act_a);
-    gC2 = ptx::f2_splat(p.act_c);
-  }
+  const ActK ak = act_k(p.act_a, p.act_c, p.act_sfu);  // GELU / SiLU: the scale folded into the cubic
   int qi = 0;
   uint32_t g = 0;
   bool ok = true;
@@ -543,7 +539,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               float a, b;
-              gelu_tanh_alu2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1]), gA2, gC2, a, b);
+              act_eval2(ak, __uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1]), a, b);
               if (!full) {
                 a = cb + 2 * u < ncols ? a : 0.0f;
                 b = cb + 2 * u + 1 < ncols ? b : 0.0f;
@@ -676,7 +672,7 @@ __device__ void run_activation(const FwdParams& p, FwdBars<D, MODE>& B, float* l
               for (int u = 0; u < 16; ++u) {
                 const int c = 32 * ch + 2 * u;
                 float a, b;
-                gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, a, b);
+                act_eval2(ak, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), a, b);
                 if (!full) {
                   a = col_ok(c, c_lo, c_hi) ? a : 0.0f;
                   b = col_ok(c + 1, c_lo, c_hi) ? b : 0.0f;

@@ -345,11 +345,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
   const uint32_t s_addr = tmem + lane_off + C::tm_s(x);
   const uint32_t o_addr = tmem + lane_off + C::tm_o(x);
   const float sl = p.score_scale;
-  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
-  if (ACT == kActGelu) {  // the ALU activation's folded constants
-    gA2 = ptx::f2_splat(p.act_a);
-    gC2 = ptx::f2_splat(p.act_c);
-  }
+  const ActK ak = act_k(p.act_a, p.act_c, p.act_sfu);  // GELU / SiLU: the scale folded into the cubic
   const int H = p.H;
   uint32_t gx = 0;  // this side's K/V tiles (phase of s_full, p_full)
   uint32_t ix = 0;  // this side's items (phase of o_done)
@@ -437,8 +433,7 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
               for (int u = 0; u < 16; ++u) {
                 const int c = 32 * ch + 2 * u;
                 float e0, e1;
-                gelu_tanh_alu2(__uint_as_float(sc[ch & 1][2 * u]), __uint_as_float(sc[ch & 1][2 * u + 1]), gA2, gC2,
-                               e0, e1);
+                act_eval2(ak, __uint_as_float(sc[ch & 1][2 * u]), __uint_as_float(sc[ch & 1][2 * u + 1]), e0, e1);
                 if (!full) {
                   e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
                   e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;

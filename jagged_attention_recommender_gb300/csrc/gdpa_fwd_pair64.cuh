@@ -445,11 +445,7 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t o_addr = tmem + lane_off + C::tm_o(x);
   const float sl = p.score_scale;
-  uint64_t gA2 = 0, gC2 = 0;  // GELU: the scale folded into the cubic
-  if (ACT == kActGelu) {  // the ALU activation's folded constants
-    gA2 = ptx::f2_splat(p.act_a);
-    gC2 = ptx::f2_splat(p.act_c);
-  }
+  const ActK ak = act_k(p.act_a, p.act_c, p.act_sfu);  // GELU / SiLU: the scale folded into the cubic
   const int H = p.H;
   uint32_t gx = 0;
   bool ok = true;
@@ -664,7 +660,7 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
             for (int u = 0; u < 16; ++u) {
               const int c = 32 * ch + 2 * u;
               float e0, e1;
-              gelu_tanh_alu2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), gA2, gC2, e0, e1);
+              act_eval2(ak, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), e0, e1);
               if (!full) {
                 e0 = (c >= c_lo && c <= c_hi) ? e0 : 0.0f;
                 e1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? e1 : 0.0f;

@@ -151,6 +151,10 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a);
 void plan_backward(const int32_t* q_off, const int32_t* kv_off, int B, int H, std::vector<int32_t>& dq_items,
                    std::vector<int32_t>& kv_items);
 gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void* stream);
+// The process-wide sigma route of the ALU activations (GDPA_ROUTE_*), read
+// by every forward launch and act_eval call.  Defined in gdpa_kernels.cu.
+int act_route();
+void set_act_route(int route);
 
 // Failure-path tests only: true while the environment variable
 // GDPA_FAULT_INJECT names `what` ("alloc": the library's buffer growth fails

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -13,6 +14,13 @@
 #include "gdpa_internal.h"
 
 namespace gdpa {
+
+namespace {
+std::atomic<int> g_act_route{GDPA_ROUTE_SFU};
+}  // namespace
+
+int act_route() { return g_act_route.load(std::memory_order_relaxed); }
+void set_act_route(int route) { g_act_route.store(route, std::memory_order_relaxed); }
 
 // Device status word: bits set by kernels whose bounded waits ran out.
 __device__ int g_device_status;
@@ -184,15 +192,15 @@ gdpa_status_t launch_mxp(const FwdParams& prm, int grid, cudaStream_t stream, in
 }
 
 // Evaluates the activation exactly as the kernels do: GELU two arguments at
-// a time with the packed evaluation, exp2 on the special-function unit.
-__global__ void act_eval_kernel(int act, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+// a time with the packed evaluation of the given sigma route, exp2 on the
+// special-function unit.
+__global__ void act_eval_kernel(int act, int sfu, const float* __restrict__ x, float* __restrict__ y, int64_t n) {
   for (int64_t i = 2 * (blockIdx.x * (int64_t)blockDim.x + threadIdx.x); i < n;
        i += 2 * (int64_t)gridDim.x * blockDim.x) {
     if (act != kActSoftmax) {
       float a, b, A, C;
       alu_act_consts(act == GDPA_ACT_SILU, 1.0f, A, C);
-      const uint64_t A2 = ptx::f2_splat(A), C2 = ptx::f2_splat(C);
-      gelu_tanh_alu2(x[i], i + 1 < n ? x[i + 1] : 0.0f, A2, C2, a, b);
+      act_eval2(act_k(A, C, sfu), x[i], i + 1 < n ? x[i + 1] : 0.0f, a, b);
       y[i] = a;
       if (i + 1 < n) y[i + 1] = b;
     } else {
@@ -324,6 +332,7 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.Tkv = static_cast<int>(a.Tkv);
   prm.test_skip_arrive = fault_injected("skip_arrive") ? 1 : 0;
   alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
+  prm.act_sfu = act_route() == GDPA_ROUTE_SFU ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks != 0;
   // sliding windows (window_blocks < 0) exist only in the 64-key pair kernel
@@ -373,7 +382,8 @@ gdpa_status_t launch_act_eval(int act, const float* x, float* y, int64_t n, void
   const int threads = 256;
   const int64_t want = (n + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 4096 ? want : 4096);
-  act_eval_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(act, x, y, n);
+  act_eval_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(act, act_route() == GDPA_ROUTE_SFU ? 1 : 0,
+                                                                             x, y, n);
   return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 

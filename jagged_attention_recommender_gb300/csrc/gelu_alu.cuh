@@ -76,6 +76,27 @@ __device__ __forceinline__ void gelu_tanh_alu2(float s0, float s1, uint64_t A2, 
   ptx::f2_unpack(ptx::f2_mul(s, ptx::f2_mul(inv, sel)), y0, y1);
 }
 
+// The same y = s * sigma(z(s)) with sigma taken on the special-function
+// unit: sigma(z) = 1 / (1 + 2^(-z log2 e)), one ex2.approx and one
+// rcp.approx per argument.  NA2 and NC2 are -log2(e) A and -log2(e) C, so
+// that the cubic gives t = -z log2 e directly.  Both instructions keep about
+// 22 bits, so the result matches gelu_tanh_alu2 to fp32 level; a large
+// positive t gives 2^t = inf and sigma = 0, a large negative one sigma = 1.
+// The forward kernels evaluate part of each row with this form and the rest
+// with gelu_tanh_alu2, so that the special-function unit and the FMA pipe
+// share the work.
+__device__ __forceinline__ void gelu_tanh_sfu2(float s0, float s1, uint64_t NA2, uint64_t NC2, float& y0,
+                                               float& y1) {
+  const uint64_t s = ptx::f2_pack(s0, s1);
+  const uint64_t t = ptx::f2_mul(s, ptx::f2_fma(NC2, ptx::f2_mul(s, s), NA2));
+  float t0, t1;
+  ptx::f2_unpack(t, t0, t1);
+  const uint64_t d = ptx::f2_add(ptx::f2_pack(ptx::ex2_approx(t0), ptx::ex2_approx(t1)), ptx::f2_splat(1.0f));
+  float d0, d1;
+  ptx::f2_unpack(d, d0, d1);
+  ptx::f2_unpack(ptx::f2_mul(s, ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1))), y0, y1);
+}
+
 // Derivative for the backward: with x = scale * s and z = s (A + C s^2),
 // gelu'(x) = sigma(z) + sigma(z) sigma(-z) s (A + 3 C s^2), where
 // sigma(z) sigma(-z) = e^-a sigma(a)^2 (a = |z|) is formed without the
@@ -117,6 +138,29 @@ __device__ __forceinline__ void gelu_tanh_grad_alu2(float s0, float s1, uint64_t
   const uint64_t sig2 = ptx::f2_mul(e, ptx::f2_mul(inv, inv));                       // sigma(z) sigma(-z)
   const uint64_t dz = ptx::f2_mul(s, ptx::f2_fma(ptx::f2_mul(C2, ptx::f2_splat(3.0f)), ss, A2));  // s (A + 3 C s^2)
   ptx::f2_unpack(ptx::f2_fma(sig2, dz, sig), g0, g1);
+}
+
+// One launch's activation constants and route: sfu selects gelu_tanh_sfu2
+// (sigma on the special-function unit), otherwise gelu_tanh_alu2 (the
+// FMA-pipe polynomial).  Both return s sigma(s (A + C s^2)).
+struct ActK {
+  uint64_t A2, C2, NA2, NC2;
+  bool sfu;
+};
+__device__ __forceinline__ ActK act_k(float A, float C, int sfu) {
+  ActK k;
+  k.A2 = ptx::f2_splat(A);
+  k.C2 = ptx::f2_splat(C);
+  k.NA2 = ptx::f2_splat(-1.4426950408889634f * A);
+  k.NC2 = ptx::f2_splat(-1.4426950408889634f * C);
+  k.sfu = sfu != 0;
+  return k;
+}
+__device__ __forceinline__ void act_eval2(const ActK& k, float s0, float s1, float& y0, float& y1) {
+  if (k.sfu)
+    gelu_tanh_sfu2(s0, s1, k.NA2, k.NC2, y0, y1);
+  else
+    gelu_tanh_alu2(s0, s1, k.A2, k.C2, y0, y1);
 }
 
 // The folded constants of the ALU activations, for which the routines above

@@ -360,6 +360,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x on the special-function unit (rcp.approx, flush-to-zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;

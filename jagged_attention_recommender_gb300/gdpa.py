@@ -19,6 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libgdpa.so")
 GDPA_ACT_SOFTMAX = 0
 GDPA_ACT_GELU_TANH = 1
 
+GDPA_ROUTE_SFU = 0
+GDPA_ROUTE_ALU = 1
+
 GDPA_OK = 0
 GDPA_ERR_INVALID_ARG = 1
 GDPA_ERR_UNSUPPORTED = 2
@@ -28,8 +31,8 @@ GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
 EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
-           "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status",
-           "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
+           "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_set_act_route",
+           "gdpa_get_act_route", "gdpa_device_status", "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
 
 class GdpaError(RuntimeError):
@@ -74,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.gdpa_plan_enumerate.argtypes = [P, P, I, I, I, I, I, I, P, I64, P, P, ctypes.POINTER(I64),
                                       ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     L.gdpa_act_eval.argtypes = [I, P, P, I64, P]
+    L.gdpa_set_act_route.argtypes = [I]
+    L.gdpa_get_act_route.argtypes = []
+    L.gdpa_get_act_route.restype = I
     L.gdpa_device_status.argtypes = [P]
     L.gdpa_wait_selftest.argtypes = [I, P]
     L.gdpa_status_string.argtypes = [I]
@@ -81,7 +87,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
     for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
-                 "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_device_status", "gdpa_wait_selftest"):
+                 "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_set_act_route", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
     return L
@@ -281,6 +287,16 @@ def gdpa_act_eval(act, x, y, *, stream=None):
     """y = act(x) elementwise on the device (``stream`` keyword-only: a stray
     positional argument must not be taken for a stream handle)."""
     _check(lib().gdpa_act_eval(int(act), _addr(x), _addr(y), int(x.numel()), _stream(stream)), "gdpa_act_eval")
+
+
+def gdpa_set_act_route(route) -> None:
+    """Selects the sigma route of the GELU / SiLU activations for later
+    launches (GDPA_ROUTE_SFU or GDPA_ROUTE_ALU)."""
+    _check(lib().gdpa_set_act_route(int(route)), "gdpa_set_act_route")
+
+
+def gdpa_get_act_route() -> int:
+    return int(lib().gdpa_get_act_route())
 
 
 def gdpa_device_status(stream=None) -> int:

@@ -40,6 +40,21 @@ def test_library_exports_every_declared_symbol():
     assert gdpa.gdpa_status_string(99) == "GDPA_ERR_UNKNOWN"
 
 
+def test_act_route_setter_needs_no_gpu():
+    assert gdpa.gdpa_get_act_route() == gdpa.GDPA_ROUTE_SFU  # the default
+    try:
+        gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_ALU)
+        assert gdpa.gdpa_get_act_route() == gdpa.GDPA_ROUTE_ALU
+        for bad in (-1, 2, 7):
+            with pytest.raises(gdpa.GdpaError) as e:
+                gdpa.gdpa_set_act_route(bad)
+            assert e.value.code == gdpa.GDPA_ERR_INVALID_ARG
+            assert gdpa.gdpa_get_act_route() == gdpa.GDPA_ROUTE_ALU  # unchanged
+    finally:
+        gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_SFU)
+    assert gdpa.gdpa_get_act_route() == gdpa.GDPA_ROUTE_SFU
+
+
 def test_shape_validation_needs_no_gpu():
     # rejected before any CUDA call
     with pytest.raises(gdpa.GdpaError) as e:
