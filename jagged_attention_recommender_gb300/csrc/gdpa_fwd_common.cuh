@@ -58,10 +58,16 @@ enum : int { kStatusProducer = 1, kStatusMma = 2, kStatusActivation = 4, kStatus
 struct ItemRows {
   int qs, ks, Lq, Lkv;
 };
+// A sequence's device offsets [qs, qe) and [ks, ke).
+struct SeqOffs {
+  int qs, qe, ks, ke;
+};
+__device__ __forceinline__ SeqOffs load_seq_offs(const FwdParams& p, int b) {
+  return SeqOffs{__ldg(p.q_off + b), __ldg(p.q_off + b + 1), __ldg(p.kv_off + b), __ldg(p.kv_off + b + 1)};
+}
 template <bool FLAG = false>
-__device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
-  const int qs = __ldg(p.q_off + b), qe = __ldg(p.q_off + b + 1);
-  const int ks = __ldg(p.kv_off + b), ke = __ldg(p.kv_off + b + 1);
+__device__ __forceinline__ ItemRows item_rows_from(const FwdParams& p, const SeqOffs& o) {
+  const int qs = o.qs, qe = o.qe, ks = o.ks, ke = o.ke;
   ItemRows r;
   r.qs = qs;
   r.ks = ks;
@@ -75,6 +81,41 @@ __device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
     if (ks < 0 || ks > p.Tkv) r.Lkv = 0;
   }
   return r;
+}
+template <bool FLAG = false>
+__device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
+  return item_rows_from<FLAG>(p, load_seq_offs(p, b));
+}
+
+// Work-item descriptors loaded ahead of their use: the raw item two ahead
+// and the sequence offsets of the item one ahead, so that neither of the two
+// dependent global loads of a decode sits on a role's critical path.
+struct ItemPrefetch {
+  int4 raw1, raw2;  // items idx + 1, idx + 2
+  SeqOffs offs1;    // offsets of item idx + 1's sequence
+};
+// Loads for the first item [ibeg] (and starts the pipeline); returns its
+// descriptor and offsets through it0 / offs0.
+__device__ __forceinline__ ItemPrefetch item_prefetch_start(const FwdParams& p, int ibeg, int iend, int4& it0,
+                                                            SeqOffs& offs0) {
+  ItemPrefetch f;
+  it0 = ibeg < iend ? __ldg(p.items + ibeg) : make_int4(0, 0, 0, 0);
+  f.raw1 = ibeg + 1 < iend ? __ldg(p.items + ibeg + 1) : make_int4(0, 0, 0, 0);
+  offs0 = load_seq_offs(p, it0.x);
+  f.raw2 = ibeg + 2 < iend ? __ldg(p.items + ibeg + 2) : make_int4(0, 0, 0, 0);
+  f.offs1 = load_seq_offs(p, f.raw1.x);
+  return f;
+}
+// Moves the pipeline on by one item (call once the current item idx has
+// been decoded): item idx + 1 becomes current, and the loads for idx + 2 and
+// idx + 3 are issued.
+__device__ __forceinline__ void item_prefetch_next(const FwdParams& p, ItemPrefetch& f, int idx, int iend, int4& it,
+                                                   SeqOffs& offs) {
+  it = f.raw1;
+  offs = f.offs1;
+  f.raw1 = f.raw2;
+  f.offs1 = load_seq_offs(p, f.raw1.x);
+  f.raw2 = idx + 3 < iend ? __ldg(p.items + idx + 3) : make_int4(0, 0, 0, 0);
 }
 
 // 32 bf16 values (16 packed words) to global memory: two 32-byte stores when

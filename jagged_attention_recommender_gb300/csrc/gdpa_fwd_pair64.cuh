@@ -98,15 +98,13 @@ struct Pair64Item {
 // the last query of tile B; each tile takes the 64-key blocks of its own
 // window (blocks are K/V tiles).
 template <bool WIN, bool FLAG = false>
-__device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx) {
+__device__ __forceinline__ Pair64Item decode_pair64_from(const FwdParams& p, const int4 it, const SeqOffs& offs) {
   constexpr int BN = 64;
-  const int4 it = __ldg(p.items + idx);
   Pair64Item v;
-  const int b = it.x;
   v.h = it.y;
   v.q0 = it.z;
   v.kv0 = WIN ? it.w : 0;
-  const ItemRows r = item_rows<FLAG>(p, b);
+  const ItemRows r = item_rows_from<FLAG>(p, offs);
   v.q_tok = r.qs + v.q0;
   v.kv_tok = r.ks;
   v.Lkv = r.Lkv;
@@ -133,6 +131,11 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
     v.t0[1] = (lo_b - v.kv0) / BN;
   }
   return v;
+}
+template <bool WIN, bool FLAG = false>
+__device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx) {
+  const int4 it = __ldg(p.items + idx);
+  return decode_pair64_from<WIN, FLAG>(p, it, load_seq_offs(p, it.x));
 }
 
 // ------------------------------------------------------------------ producer
@@ -435,6 +438,25 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
 
 // ------------------------------------------------------------------ activation + epilogue
 
+// One query row's output: O (fp32, TMEM columns [o_addr, o_addr + D)) times
+// inv, rounded to bf16 and stored to dst when `store`, 32 columns at a time.
+// (Keeping the next 16 columns' load in flight during each conversion
+// measured no faster: the stores, not the TMEM loads, set the epilogue's pace.)
+template <int D>
+__device__ __forceinline__ void store_o_row(uint32_t o_addr, float inv, __nv_bfloat16* dst, bool store, bool v8) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(o_addr + 32 * c, r);
+    ptx::tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+    if (store) store_row32(dst + 32 * c, pk, v8);
+  }
+}
+
 template <int D, int ACT, bool WIN>
 __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend, int x,
                                 int warp, int lane) {
@@ -459,25 +481,29 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
   __nv_bfloat16* pend_orow = nullptr;
   auto epilogue = [&]() {
     ptx::tc_fence_after();
-    if (pend_live) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(o_addr + 32 * c, r);
-        ptx::tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * pend_inv, __uint_as_float(r[2 * i + 1]) * pend_inv);
-        if (pend_row_ok) store_row32(pend_orow + 32 * c, pk, p.out_align32 != 0);
-      }
-    }
+    if (pend_live) store_o_row<D>(o_addr, pend_inv, pend_orow, pend_row_ok, p.out_align32 != 0);
     ptx::tc_fence_before();
     ptx::mbar_arrive(&B.o_empty[x]);
     pend = false;
   };
+  // ALU activations with full attention (short key ranges): each item's
+  // descriptor and offsets are loaded ahead, since with one-tile items the
+  // two dependent loads are a visible part of an item.  (Window items are
+  // longer; there, and in the softmax variant, the extra registers spill and
+  // measured slower.)
+  constexpr bool PF = !WIN && ACT == kActGelu;
+  int4 cur_it;
+  SeqOffs cur_offs;
+  ItemPrefetch pf;
+  if (PF) pf = item_prefetch_start(p, ibeg, iend, cur_it, cur_offs);
   for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<WIN>(p, idx);
+    Pair64Item t;
+    if (PF) {
+      t = decode_pair64_from<WIN>(p, cur_it, cur_offs);
+      item_prefetch_next(p, pf, idx, iend, cur_it, cur_offs);
+    } else {
+      t = decode_pair64<WIN>(p, idx);
+    }
     const int rows = x ? t.rows[1] : t.rows[0];
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: zero output rows
@@ -717,19 +743,7 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      if (rows_live) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(o_addr + 32 * c, r);
-          ptx::tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          if (row < rows) store_row32(orow + 32 * c, pk, p.out_align32 != 0);
-        }
-      }
+      if (rows_live) store_o_row<D>(o_addr, inv, orow, row < rows, p.out_align32 != 0);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&B.o_empty[x]);
     } else {
