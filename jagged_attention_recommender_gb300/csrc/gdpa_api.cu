@@ -79,9 +79,45 @@ struct Buf {
   }
 };
 
+// The planner's working arrays, kept from call to call (grow-only), so that
+// planning a batch allocates and first-touches nothing in the steady state.
+struct PlanScratch {
+  std::vector<gdpa_work_item_t> items;
+  std::vector<int64_t> cost, load;
+  std::vector<uint32_t> order, bucket;
+  std::vector<int32_t> owner, tree, count;
+  std::vector<uint64_t> keys;
+  gdpa_status_t ensure(int64_t n, int leaves, int ctas) {
+    try {
+      if ((int64_t)items.size() < n) {
+        items.resize((size_t)n);
+        cost.resize((size_t)n);
+        order.resize((size_t)n);
+        owner.resize((size_t)n);
+        keys.resize((size_t)n);
+        bucket.resize((size_t)(4 * n + 1026));
+      }
+      if ((int)load.size() < leaves) {
+        load.resize((size_t)leaves);
+        tree.resize(2 * (size_t)leaves);
+      }
+      if ((int)count.size() < ctas) count.resize((size_t)ctas);
+    } catch (const std::bad_alloc&) {
+      return GDPA_ERR_NO_MEMORY;
+    }
+    return GDPA_OK;
+  }
+  PlanStorage storage() {
+    return PlanStorage{items.data(), cost.data(),  order.data(), owner.data(), keys.data(), bucket.data(),
+                       load.data(),  tree.data(),  count.data(), (int64_t)items.size(), (int64_t)bucket.size(),
+                       (int)load.size()};
+  }
+};
+
 // Per-device state behind gdpa_fwd / gdpa_fwd_host.
 struct DeviceCtx {
   std::mutex mu;
+  PlanScratch plan;
   Buf h_stage{nullptr, 0, true};  // pinned: offsets in, work list out
   Buf d_work;                     // device work list + cta_begin
   Buf d_io;                       // gdpa_fwd_host: q, k, v, out, offsets, work lists
@@ -141,8 +177,6 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
                               int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
                               int* kv_tile, int64_t* n_items, bool single_tile = false, bool pair64 = false,
                               const std::vector<int32_t>* extra = nullptr) {
-  std::vector<gdpa_work_item_t> items;
-  std::vector<int32_t> cta_begin;
   const int rpi = single_tile ? kBlockM : pair64 ? 2 * kBlockM : choose_rows_per_item(h_q_off, B, D, window_blocks);
   *rows_per_item = rpi;
   *kv_tile = single_tile ? kBlockN : pair64 ? kBlockN / 2 : choose_kv_tile(h_q_off, h_kv_off, B, window_blocks, rpi);
@@ -153,15 +187,12 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
     return GDPA_OK;
   }
   const int ctas = (int)(n < sms ? n : sms);
+  int leaves = 1;
+  while (leaves < ctas) leaves <<= 1;
   gdpa_status_t st;
-  try {
-    st = plan_items(h_q_off, h_kv_off, B, H, window_blocks, rpi, ctas, items, cta_begin, nullptr);
-  } catch (const std::bad_alloc&) {
-    return GDPA_ERR_NO_MEMORY;
-  }
-  if (st != GDPA_OK) return st;
-  const size_t items_bytes = items.size() * sizeof(gdpa_work_item_t);
-  const size_t list_bytes = align_up(items_bytes, 16) + cta_begin.size() * sizeof(int32_t);
+  if ((st = c.plan.ensure(n, leaves, ctas)) != GDPA_OK) return st;
+  const size_t items_bytes = (size_t)n * sizeof(gdpa_work_item_t);
+  const size_t list_bytes = align_up(items_bytes, 16) + ((size_t)ctas + 1) * sizeof(int32_t);
   const size_t total = extra ? align_up(list_bytes, 16) + extra->size() * sizeof(int32_t) : list_bytes;
   if (cudaStreamWaitEvent(stream, c.work_free, 0) != cudaSuccess) return GDPA_ERR_CUDA;
   if (c.d_work.cap < total) {
@@ -170,9 +201,14 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   }
   if (cudaEventSynchronize(c.stage_free) != cudaSuccess) return GDPA_ERR_CUDA;
   if ((st = c.h_stage.ensure(total)) != GDPA_OK) return st;
+  // the plan lands in the pinned staging buffer directly: items, then cta_begin
   char* h = static_cast<char*>(c.h_stage.p);
-  std::memcpy(h, items.data(), items_bytes);
-  std::memcpy(h + align_up(items_bytes, 16), cta_begin.data(), cta_begin.size() * sizeof(int32_t));
+  int64_t got = 0;
+  st = plan_items_into(h_q_off, h_kv_off, B, H, window_blocks, rpi, ctas, c.plan.storage(),
+                       reinterpret_cast<gdpa_work_item_t*>(h), reinterpret_cast<int32_t*>(h + align_up(items_bytes, 16)),
+                       nullptr, &got);
+  if (st != GDPA_OK) return st;
+  if (got != n) return GDPA_ERR_INVALID_ARG;
   if (extra && !extra->empty())
     std::memcpy(h + align_up(list_bytes, 16), extra->data(), extra->size() * sizeof(int32_t));
   if (cudaMemcpyAsync(c.d_work.p, h, total, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GDPA_ERR_CUDA;

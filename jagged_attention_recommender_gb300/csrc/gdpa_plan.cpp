@@ -163,25 +163,55 @@ gdpa_status_t plan_items_into(const int32_t* q_off, const int32_t* kv_off, int B
     std::sort(st.keys, st.keys + n);  // in place, no allocation
     for (int64_t i = 0; i < n; ++i) order[i] = (uint32_t)(st.keys[i] & 0xFFFFFFFFu);
   }
-  int64_t* load = st.load;
-  int32_t* tree = st.tree;  // tree[k] = CTA with the least load below node k
-  for (int c = 0; c < leaves; ++c) load[c] = c < num_ctas ? 0 : INT64_MAX;
-  for (int c = 0; c < leaves; ++c) tree[leaves + c] = c;
-  for (int k = leaves - 1; k >= 1; --k) {
-    const int32_t a = tree[2 * k], b = tree[2 * k + 1];
-    tree[k] = load[b] < load[a] ? b : a;
-  }
   int32_t* count = st.count;
   for (int c = 0; c < num_ctas; ++c) count[c] = 0;
-  for (int64_t k = 0; k < n; ++k) {
-    const uint32_t idx = order[k];
-    const int32_t c = tree[1];
-    st.owner[idx] = c;
-    count[c]++;
-    load[c] += st.cost[idx];
-    for (int node = (leaves + c) >> 1; node >= 1; node >>= 1) {
-      const int32_t a = tree[2 * node], b = tree[2 * node + 1];
-      tree[node] = load[b] < load[a] ? b : a;
+  int64_t total = 0;
+  for (int64_t i = 0; i < n && total < (int64_t(1) << 47); ++i) total += st.cost[i];
+  if (n >= 2 * (int64_t)leaves && total < (int64_t(1) << 47)) {
+    // Every load fits in 47 bits: node k of the tree holds the key
+    // (load << 16 | cta) of the least-loaded CTA below it, so the smallest
+    // key is the least load with ties to the lowest index, as in the general
+    // form below.  An update walks up from the leaf with the new key in a
+    // register and reads only the siblings, whose addresses do not depend on
+    // the walk: one min per level on the dependent chain instead of two
+    // indirect loads.  (The keys array is free once `order` is built.)
+    uint64_t* key = st.keys;
+    for (int c = 0; c < leaves; ++c) key[leaves + c] = c < num_ctas ? (uint64_t)c : UINT64_MAX;
+    for (int k = leaves - 1; k >= 1; --k) key[k] = std::min(key[2 * k], key[2 * k + 1]);
+    uint64_t top = key[1];  // the root, carried from one item to the next
+    for (int64_t k = 0; k < n; ++k) {
+      const uint32_t idx = order[k];
+      const int32_t c = (int32_t)(top & 0xFFFFu);
+      st.owner[idx] = c;
+      count[c]++;
+      uint64_t v = top + ((uint64_t)st.cost[idx] << 16);
+      int node = leaves + c;
+      key[node] = v;
+      for (; node > 1; node >>= 1) {
+        v = std::min(v, key[node ^ 1]);
+        key[node >> 1] = v;
+      }
+      top = v;
+    }
+  } else {
+    int64_t* load = st.load;
+    int32_t* tree = st.tree;  // tree[k] = CTA with the least load below node k
+    for (int c = 0; c < leaves; ++c) load[c] = c < num_ctas ? 0 : INT64_MAX;
+    for (int c = 0; c < leaves; ++c) tree[leaves + c] = c;
+    for (int k = leaves - 1; k >= 1; --k) {
+      const int32_t a = tree[2 * k], b = tree[2 * k + 1];
+      tree[k] = load[b] < load[a] ? b : a;
+    }
+    for (int64_t k = 0; k < n; ++k) {
+      const uint32_t idx = order[k];
+      const int32_t c = tree[1];
+      st.owner[idx] = c;
+      count[c]++;
+      load[c] += st.cost[idx];
+      for (int node = (leaves + c) >> 1; node >= 1; node >>= 1) {
+        const int32_t a = tree[2 * node], b = tree[2 * node + 1];
+        tree[node] = load[b] < load[a] ? b : a;
+      }
     }
   }
   cta_begin[0] = 0;
