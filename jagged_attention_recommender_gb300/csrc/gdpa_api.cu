@@ -118,12 +118,22 @@ struct PlanScratch {
 struct DeviceCtx {
   std::mutex mu;
   PlanScratch plan;
-  Buf h_stage{nullptr, 0, true};  // pinned: offsets in, work list out
-  Buf d_work;                     // device work list + cta_begin
+  // Work lists go up through two slots used in turn, each a pinned staging
+  // buffer and a device buffer, on the upload stream s_up: the list of the
+  // next launch is copied while the current one runs, and the launch stream
+  // only waits for its own list (up_done).  stage_free[b]: slot b's staging
+  // buffer may be overwritten; work_free[b]: no launch reads d_work[b] any more.
+  Buf h_stage[2] = {{nullptr, 0, true}, {nullptr, 0, true}};
+  Buf d_work[2];
+  int slot = 0;  // the slot the next plan takes
+  int cur = 0;   // the slot of the last plan (read by the launch that follows it)
+  cudaStream_t s_up = nullptr;
+  cudaEvent_t up_done[2] = {};
+  Buf h_off{nullptr, 0, true};    // gdpa_fwd: device offsets read back
   Buf d_io;                       // gdpa_fwd_host: q, k, v, out, offsets, work lists
   Buf h_io{nullptr, 0, true};     // gdpa_fwd_host: pinned offsets + work lists
-  cudaEvent_t stage_free = nullptr;  // host staging buffer may be overwritten
-  cudaEvent_t work_free = nullptr;   // device buffers no longer read by an earlier launch
+  cudaEvent_t stage_free[2] = {};
+  cudaEvent_t work_free[2] = {};
   bool events_ok = false;
   // gdpa_bwd: device work lists + scratch, pinned staging, and their events
   Buf d_bwd;
@@ -148,12 +158,18 @@ struct DeviceCtx {
   }
   gdpa_status_t init() {
     if (events_ok) return GDPA_OK;
-    if (cudaEventCreateWithFlags(&stage_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&work_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&s_up, cudaStreamNonBlocking) != cudaSuccess) return GDPA_ERR_CUDA;
+    for (int b = 0; b < 2; ++b) {
+      if (cudaEventCreateWithFlags(&stage_free[b], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&work_free[b], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&up_done[b], cudaEventDisableTiming) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+      if (cudaEventRecord(stage_free[b], 0) != cudaSuccess || cudaEventRecord(work_free[b], 0) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+    }
     if (cudaEventCreateWithFlags(&bwd_stage_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
     if (cudaEventCreateWithFlags(&bwd_free, cudaEventDisableTiming) != cudaSuccess) return GDPA_ERR_CUDA;
-    if (cudaEventRecord(stage_free, 0) != cudaSuccess || cudaEventRecord(work_free, 0) != cudaSuccess ||
-        cudaEventRecord(bwd_stage_free, 0) != cudaSuccess || cudaEventRecord(bwd_free, 0) != cudaSuccess)
+    if (cudaEventRecord(bwd_stage_free, 0) != cudaSuccess || cudaEventRecord(bwd_free, 0) != cudaSuccess)
       return GDPA_ERR_CUDA;
     events_ok = true;
     return GDPA_OK;
@@ -167,12 +183,14 @@ DeviceCtx& ctx(int device) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Plans on the host and uploads the work list through the pinned staging
-// buffer into c.d_work (both guarded by events against earlier calls).
+// Plans on the host into the next slot's pinned staging buffer and uploads
+// the work list into that slot's device buffer on the upload stream (both
+// guarded by events against the launch that used the slot two calls ago);
+// `stream` waits for the copy.  The launch that follows reads slot c.cur.
 // `single_tile`: one 128-row query tile and 128-key tiles per item whatever
 // the shapes (the MXFP8 kernel's item kind).
 // `extra` (optional): an int32 array uploaded after the work list (the
-// MXFP8 V layout's sequence columns), at offset work_extra_offset().
+// MXFP8 V layout's sequence columns), at work_extra().
 gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_t* h_kv_off, int B, int H,
                               int D, int window_blocks, int sms, cudaStream_t stream, int* num_ctas, int* rows_per_item,
                               int* kv_tile, int64_t* n_items, bool single_tile = false, bool pair64 = false,
@@ -194,15 +212,20 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   const size_t items_bytes = (size_t)n * sizeof(gdpa_work_item_t);
   const size_t list_bytes = align_up(items_bytes, 16) + ((size_t)ctas + 1) * sizeof(int32_t);
   const size_t total = extra ? align_up(list_bytes, 16) + extra->size() * sizeof(int32_t) : list_bytes;
-  if (cudaStreamWaitEvent(stream, c.work_free, 0) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (c.d_work.cap < total) {
+  const int b = c.slot;
+  // A stream being captured into a graph keeps the copy on itself.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return GDPA_ERR_CUDA;
+  cudaStream_t us = cs == cudaStreamCaptureStatusNone ? c.s_up : stream;
+  if (cudaStreamWaitEvent(us, c.work_free[b], 0) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (c.d_work[b].cap < total) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;  // old buffer may be in use
-    if ((st = c.d_work.ensure(total)) != GDPA_OK) return st;
+    if ((st = c.d_work[b].ensure(total)) != GDPA_OK) return st;
   }
-  if (cudaEventSynchronize(c.stage_free) != cudaSuccess) return GDPA_ERR_CUDA;
-  if ((st = c.h_stage.ensure(total)) != GDPA_OK) return st;
+  if (cudaEventSynchronize(c.stage_free[b]) != cudaSuccess) return GDPA_ERR_CUDA;
+  if ((st = c.h_stage[b].ensure(total)) != GDPA_OK) return st;
   // the plan lands in the pinned staging buffer directly: items, then cta_begin
-  char* h = static_cast<char*>(c.h_stage.p);
+  char* h = static_cast<char*>(c.h_stage[b].p);
   int64_t got = 0;
   st = plan_items_into(h_q_off, h_kv_off, B, H, window_blocks, rpi, ctas, c.plan.storage(),
                        reinterpret_cast<gdpa_work_item_t*>(h), reinterpret_cast<int32_t*>(h + align_up(items_bytes, 16)),
@@ -211,8 +234,14 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
   if (got != n) return GDPA_ERR_INVALID_ARG;
   if (extra && !extra->empty())
     std::memcpy(h + align_up(list_bytes, 16), extra->data(), extra->size() * sizeof(int32_t));
-  if (cudaMemcpyAsync(c.d_work.p, h, total, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GDPA_ERR_CUDA;
-  if (cudaEventRecord(c.stage_free, stream) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (cudaMemcpyAsync(c.d_work[b].p, h, total, cudaMemcpyHostToDevice, us) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (cudaEventRecord(c.stage_free[b], us) != cudaSuccess) return GDPA_ERR_CUDA;
+  if (us != stream) {
+    if (cudaEventRecord(c.up_done[b], us) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaStreamWaitEvent(stream, c.up_done[b], 0) != cudaSuccess) return GDPA_ERR_CUDA;
+  }
+  c.cur = b;
+  c.slot = b ^ 1;
   *num_ctas = ctas;
   return GDPA_OK;
 }
@@ -221,7 +250,7 @@ gdpa_status_t plan_and_upload(DeviceCtx& c, const int32_t* h_q_off, const int32_
 // list of n_items items over num_ctas CTAs.
 const int32_t* work_extra(const DeviceCtx& c, int64_t n_items, int num_ctas) {
   const size_t list_bytes = align_up((size_t)n_items * sizeof(gdpa_work_item_t), 16) + ((size_t)num_ctas + 1) * 4;
-  return reinterpret_cast<const int32_t*>(static_cast<const char*>(c.d_work.p) + align_up(list_bytes, 16));
+  return reinterpret_cast<const int32_t*>(static_cast<const char*>(c.d_work[c.cur].p) + align_up(list_bytes, 16));
 }
 
 gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const void* v, void* out,
@@ -247,8 +276,8 @@ gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const 
   a.out = out;
   a.q_off = d_q_off;
   a.kv_off = d_kv_off;
-  a.items = static_cast<const gdpa_work_item_t*>(c.d_work.p);
-  a.cta_begin = reinterpret_cast<const int32_t*>(static_cast<const char*>(c.d_work.p) +
+  a.items = static_cast<const gdpa_work_item_t*>(c.d_work[c.cur].p);
+  a.cta_begin = reinterpret_cast<const int32_t*>(static_cast<const char*>(c.d_work[c.cur].p) +
                                                  align_up((size_t)n_items * sizeof(gdpa_work_item_t), 16));
   a.num_ctas = num_ctas;
   a.Tq = Tq;
@@ -261,7 +290,7 @@ gdpa_status_t launch_with_ctx(DeviceCtx& c, const void* q, const void* k, const 
   a.stream = stream;
   gdpa_status_t st = launch_forward(a);
   if (st != GDPA_OK) return st;
-  return cudaEventRecord(c.work_free, stream) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+  return cudaEventRecord(c.work_free[c.cur], stream) == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
 
@@ -292,9 +321,8 @@ extern "C" gdpa_status_t gdpa_fwd(const void* q, const void* k, const void* v, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::vector<int32_t> off(2 * ((size_t)B + 1));
   const size_t ob = ((size_t)B + 1) * sizeof(int32_t);
-  if (cudaEventSynchronize(c.stage_free) != cudaSuccess) return GDPA_ERR_CUDA;
-  if ((st = c.h_stage.ensure(2 * ob)) != GDPA_OK) return st;
-  int32_t* h = static_cast<int32_t*>(c.h_stage.p);
+  if ((st = c.h_off.ensure(2 * ob)) != GDPA_OK) return st;
+  int32_t* h = static_cast<int32_t*>(c.h_off.p);
   if (cudaMemcpyAsync(h, q_offsets, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (cudaMemcpyAsync(h + B + 1, kv_offsets, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDPA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDPA_ERR_CUDA;
