@@ -40,6 +40,9 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   const int32_t* vt_col;
   const uint8_t* vt_sf;
   int vt_blocks;
+  // Run-time claiming of work items (kernels that take it): [0] the next
+  // claim, [1] CTAs finished; the last CTA to finish sets both back to 0.
+  int* item_ctr;
 };
 
 // kActGelu instantiates the ALU activations (tanh-GELU and SiLU, told apart
@@ -87,37 +90,6 @@ __device__ __forceinline__ ItemRows item_rows(const FwdParams& p, int b) {
   return item_rows_from<FLAG>(p, load_seq_offs(p, b));
 }
 
-// Work-item descriptors loaded ahead of their use: the raw item two ahead
-// and the sequence offsets of the item one ahead, so that neither of the two
-// dependent global loads of a decode sits on a role's critical path.
-struct ItemPrefetch {
-  int4 raw1, raw2;  // items idx + 1, idx + 2
-  SeqOffs offs1;    // offsets of item idx + 1's sequence
-};
-// Loads for the first item [ibeg] (and starts the pipeline); returns its
-// descriptor and offsets through it0 / offs0.
-__device__ __forceinline__ ItemPrefetch item_prefetch_start(const FwdParams& p, int ibeg, int iend, int4& it0,
-                                                            SeqOffs& offs0) {
-  ItemPrefetch f;
-  it0 = ibeg < iend ? __ldg(p.items + ibeg) : make_int4(0, 0, 0, 0);
-  f.raw1 = ibeg + 1 < iend ? __ldg(p.items + ibeg + 1) : make_int4(0, 0, 0, 0);
-  offs0 = load_seq_offs(p, it0.x);
-  f.raw2 = ibeg + 2 < iend ? __ldg(p.items + ibeg + 2) : make_int4(0, 0, 0, 0);
-  f.offs1 = load_seq_offs(p, f.raw1.x);
-  return f;
-}
-// Moves the pipeline on by one item (call once the current item idx has
-// been decoded): item idx + 1 becomes current, and the loads for idx + 2 and
-// idx + 3 are issued.
-__device__ __forceinline__ void item_prefetch_next(const FwdParams& p, ItemPrefetch& f, int idx, int iend, int4& it,
-                                                   SeqOffs& offs) {
-  it = f.raw1;
-  offs = f.offs1;
-  f.raw1 = f.raw2;
-  f.offs1 = load_seq_offs(p, f.raw1.x);
-  f.raw2 = idx + 3 < iend ? __ldg(p.items + idx + 3) : make_int4(0, 0, 0, 0);
-}
-
 // 32 bf16 values (16 packed words) to global memory: two 32-byte stores when
 // `v8` (the address is 32-byte aligned), else four 16-byte stores.
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16], bool v8) {
@@ -139,6 +111,94 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 // (sum_j 2^(x_j - m) = l): ln 2 (m + log2 l); -inf for an empty row.
 __device__ __forceinline__ float row_lse(float m, float l) {
   return l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+}
+
+// ------------------------------------------------------------------ run-time work claiming
+//
+// The host plan gives each CTA a list of items (longest-processing-time
+// assignment, each list in decreasing cost).  Kernels that claim at run time
+// walk those lists interleaved -- claim k is position k / G of list k % G
+// (G = gridDim.x), so the claims run through the items in roughly decreasing
+// cost -- and each CTA takes the next claim when it is ready for another
+// item: a CTA that runs slow (or was given more) hands its remaining items
+// to the others, which is greedy list scheduling in longest-first order.
+// One thread of the CTA (the claimer) takes the claims, decodes each item and
+// publishes it in a ring of shared-memory slots that every role of the CTA
+// reads in the same order; a slot is refilled once every reader has
+// released it.
+constexpr int kRing = 4;
+
+template <typename Item>
+struct ItemRing {
+  Item slot[kRing];
+  int live[kRing];         // 0: the lists are exhausted
+  uint64_t full[kRing];    // one arrival: the claimer published the slot
+  uint64_t empty[kRing];   // one arrival per reader
+};
+
+struct ListClaim {
+  int G, lmax;
+};
+
+// The longest list (a hole in a shorter one is skipped).
+__device__ __forceinline__ ListClaim claim_init(const FwdParams& p) {
+  ListClaim L;
+  L.G = gridDim.x;
+  L.lmax = 0;
+  for (int c = 0; c < L.G; ++c) L.lmax = max(L.lmax, __ldg(p.cta_begin + c + 1) - __ldg(p.cta_begin + c));
+  return L;
+}
+
+// The next item index, or -1 once every list is exhausted.
+__device__ __forceinline__ int claim_next(const FwdParams& p, const ListClaim& L) {
+  while (true) {
+    const int k = atomicAdd(p.item_ctr, 1);
+    const int c = k % L.G, j = k / L.G;
+    if (j >= L.lmax) return -1;
+    const int b0 = __ldg(p.cta_begin + c), b1 = __ldg(p.cta_begin + c + 1);
+    if (b0 + j < b1) return b0 + j;
+  }
+}
+
+// Claimer: waits until slot k % kRing is free, then publishes t (live) or
+// the end of the lists.
+template <typename Item>
+__device__ __forceinline__ bool ring_publish(const FwdParams& p, ItemRing<Item>& R, uint32_t k, const Item& t,
+                                             bool live, volatile int* abort) {
+  const int r = k % kRing;
+  if (!ptx::mbar_wait(&R.empty[r], ((k / kRing) & 1) ^ 1, p.timeout_ns, abort)) return false;
+  R.slot[r] = t;
+  R.live[r] = live ? 1 : 0;
+  ptx::mbar_arrive(&R.full[r]);  // release: the slot's contents are visible to whoever sees the phase
+  return true;
+}
+
+// Reader: entry k of the sequence.  `mask`: the lanes of the calling warp
+// that read together (0 for a single-thread role); lane 0 of them -- or the
+// single thread -- releases the slot for the role.  Returns false at the end
+// of the lists or on a timeout (ok = false).
+template <typename Item>
+__device__ __forceinline__ bool ring_read(const FwdParams& p, ItemRing<Item>& R, uint32_t k, Item& t, unsigned mask,
+                                          volatile int* abort, bool& ok) {
+  const int r = k % kRing;
+  ok = ptx::mbar_wait(&R.full[r], (k / kRing) & 1, p.timeout_ns, abort);
+  if (mask) ok = __all_sync(mask, ok);
+  if (!ok) return false;
+  t = R.slot[r];
+  const bool live = R.live[r] != 0;
+  if (mask) __syncwarp(mask);
+  if (!mask || (threadIdx.x & 31) == (__ffs(mask) - 1)) ptx::mbar_arrive(&R.empty[r]);
+  return live;
+}
+
+// End of a claiming launch (one thread per CTA, after every role is done):
+// the last CTA sets the claim counter back for the next launch that uses it.
+__device__ __forceinline__ void claim_finish(const FwdParams& p) {
+  __threadfence();
+  if (atomicAdd(p.item_ctr + 1, 1) == (int)gridDim.x - 1) {
+    atomicExch(p.item_ctr, 0);
+    atomicExch(p.item_ctr + 1, 0);
+  }
 }
 
 __device__ __forceinline__ void report_failure(const FwdParams& p, volatile int* abort, int bit) {

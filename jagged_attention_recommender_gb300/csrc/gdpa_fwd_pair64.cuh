@@ -55,7 +55,7 @@ struct Pair64Cfg {
   static constexpr int OFF_K = OFF_QB + NQS * Q_TILE;
   static constexpr int OFF_V = OFF_K + NK * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
-  static constexpr int BAR_BYTES = 512;
+  static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   __host__ __device__ static constexpr uint32_t tm_s(int x, int b) { return 128u * x + 64u * b; }  // S_x buffer b
   __host__ __device__ static constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }           // O_A, O_B
@@ -75,6 +75,12 @@ struct Pair64Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+struct Pair64Item {
+  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
+  int rows[2];       // valid rows of tile A and tile B (B may be 0)
+  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each query tile attends to
+};
+
 template <int D>
 struct Pair64Bars {
   uint64_t q_full[2][Pair64Cfg<D>::NQS], q_empty[2][Pair64Cfg<D>::NQS];
@@ -83,14 +89,9 @@ struct Pair64Bars {
   uint64_t s_full[2][2], p_full[2][2];  // per side and S buffer
   uint64_t o_done[2], o_empty[2];
   uint64_t mma_drain[2];  // one per MMA warp
+  ItemRing<Pair64Item> ring;  // the CTA's items, in claim order
   uint32_t tmem_slot;
   int abort;
-};
-
-struct Pair64Item {
-  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
-  int rows[2];       // valid rows of tile A and tile B (B may be 0)
-  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each query tile attends to
 };
 
 // Full attention: both tiles attend to every K/V tile of the item.  Block
@@ -142,8 +143,12 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
 
 // Two producer threads: one stages Q and K, the other V, so that a K load
 // never waits behind a V slot.
+// The Q/K producer thread is also the CTA's claimer: it claims each item,
+// decodes it (flagging a bad plan) and publishes it for the other roles
+// before staging its Q tiles and K tiles; the V producer reads the items from
+// the ring.
 template <int D, bool WIN, bool LOAD_V>
-__device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, int ibeg, int iend) {
+__device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B) {
   using C = Pair64Cfg<D>;
   volatile int* abort = &B.abort;
   int qn[2] = {0, 0};
@@ -160,8 +165,18 @@ __device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
     ptx::prefetch_tensormap(&p.tm_q);
     ptx::prefetch_tensormap(&p.tm_k);
   }
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<WIN, !LOAD_V>(p, idx);
+  ListClaim L;
+  if (!LOAD_V) L = claim_init(p);
+  for (uint32_t k = 0; ok; ++k) {
+    Pair64Item t;
+    if (!LOAD_V) {
+      const int idx = claim_next(p, L);
+      if (idx >= 0) t = decode_pair64<WIN, true>(p, idx);
+      ok = ring_publish(p, B.ring, k, t, idx >= 0, abort);
+      if (!ok || idx < 0) break;
+    } else if (!ring_read(p, B.ring, k, t, 0u, abort, ok)) {
+      break;
+    }
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {
@@ -262,7 +277,7 @@ __device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm,
 }
 
 template <int D, bool WIN, bool SPLIT>
-__device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend) {
+__device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem) {
   using C = Pair64Cfg<D>;
   volatile int* abort = &B.abort;
   int qn[2] = {0, 0};       // items seen by each side (Q stage and O buffer use counts)
@@ -279,8 +294,9 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
   // the load, and the producer never refills a stage with a copy in flight.
   bool pend_v = false;
   uint32_t pend_v_g = 0;
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<WIN>(p, idx);
+  for (uint32_t k = 0; ok; ++k) {
+    Pair64Item t;
+    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     if (t.n_kv == 0) continue;
     const bool has[2] = {t.rows[0] > 0, t.rows[1] > 0};
     uint32_t q_base[2] = {0, 0};
@@ -364,8 +380,7 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
 // released once it has landed.  K and V stages then have two-count empty
 // barriers (one arrival per side).
 template <int D, bool WIN, bool SPLIT>
-__device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int ibeg,
-                                int iend, int x) {
+__device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int x) {
   using C = Pair64Cfg<D>;
   volatile int* abort = &B.abort;
   int qn = 0;        // this side's items (Q stage and O use counts)
@@ -374,8 +389,9 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
   bool ok = true;
   bool pend = false;
   Pair64PV pv = {0, 0, 0, 0, 0};
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const Pair64Item t = decode_pair64<WIN>(p, idx);
+  for (uint32_t k = 0; ok; ++k) {
+    Pair64Item t;
+    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     if (t.n_kv == 0) continue;
     const bool has = t.rows[x] > 0;
     uint32_t q_base = 0;
@@ -458,8 +474,7 @@ __device__ __forceinline__ void store_o_row(uint32_t o_addr, float inv, __nv_bfl
 }
 
 template <int D, int ACT, bool WIN>
-__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t tmem, int ibeg, int iend, int x,
-                                int warp, int lane) {
+__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t tmem, int x, int warp, int lane) {
   using C = Pair64Cfg<D>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
@@ -486,24 +501,10 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
     ptx::mbar_arrive(&B.o_empty[x]);
     pend = false;
   };
-  // ALU activations with full attention (short key ranges): each item's
-  // descriptor and offsets are loaded ahead, since with one-tile items the
-  // two dependent loads are a visible part of an item.  (Window items are
-  // longer; there, and in the softmax variant, the extra registers spill and
-  // measured slower.)
-  constexpr bool PF = !WIN && ACT == kActGelu;
-  int4 cur_it;
-  SeqOffs cur_offs;
-  ItemPrefetch pf;
-  if (PF) pf = item_prefetch_start(p, ibeg, iend, cur_it, cur_offs);
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
+  // Items come decoded through the CTA's ring (no global loads here).
+  for (uint32_t k = 0; ok; ++k) {
     Pair64Item t;
-    if (PF) {
-      t = decode_pair64_from<WIN>(p, cur_it, cur_offs);
-      item_prefetch_next(p, pf, idx, iend, cur_it, cur_offs);
-    } else {
-      t = decode_pair64<WIN>(p, idx);
-    }
+    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     const int rows = x ? t.rows[1] : t.rows[0];
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: zero output rows
@@ -775,8 +776,6 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
   Pair64Bars<D>& B = *reinterpret_cast<Pair64Bars<D>*>(sm + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ibeg = p.cta_begin[blockIdx.x];
-  const int iend = p.cta_begin[blockIdx.x + 1];
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
       for (int s = 0; s < C::NQS; ++s) {
@@ -801,6 +800,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
     }
     ptx::mbar_init(&B.mma_drain[0], 1);
     ptx::mbar_init(&B.mma_drain[1], 1);
+    for (int r = 0; r < kRing; ++r) {  // readers: the V producer, the MMA warps, the eight activation warps
+      ptx::mbar_init(&B.ring.full[r], 1);
+      ptx::mbar_init(&B.ring.empty[r], 1 + n_mma + 8);
+    }
     B.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -815,23 +818,24 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
   if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
     ptx::regs_dec<C::regs_ctrl(ACT)>();
     if (warp == 0) {
-      if (lane == 0) pair64_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+      if (lane == 0) pair64_producer<D, WIN, false>(p, sm, B);
     } else if (warp == 2) {
-      if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+      if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B);
     } else if (WIN) {
-      if (warp == 1) pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend);  // whole warp: warp-uniform issue
+      if (warp == 1) pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem);  // whole warp: warp-uniform issue
     } else {  // warps 1 and 3: the MMA issuers of tiles A and B
-      pair64_mma_side<D, WIN, ACT == kActGelu>(p, sm, B, tmem, ibeg, iend, warp == 1 ? 0 : 1);
+      pair64_mma_side<D, WIN, ACT == kActGelu>(p, sm, B, tmem, warp == 1 ? 0 : 1);
     }
   } else {  // warpgroups 1 and 2: tiles A and B
     ptx::regs_inc<C::regs_act(ACT)>();
-    pair64_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp < 8 ? 0 : 1, warp, lane);
+    pair64_activation<D, ACT, WIN>(p, B, tmem, warp < 8 ? 0 : 1, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+  if (threadIdx.x == 0) claim_finish(p);
 }
 
 }  // namespace gdpa

@@ -22,12 +22,34 @@ std::atomic<int> g_act_route{GDPA_ROUTE_SFU};
 int act_route() { return g_act_route.load(std::memory_order_relaxed); }
 void set_act_route(int route) { g_act_route.store(route, std::memory_order_relaxed); }
 
+
 // Device status word: bits set by kernels whose bounded waits ran out.
 __device__ int g_device_status;
 
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// Claim counters of the kernels that take their items at run time: one pair
+// per launch, in turn from a fixed array (zero at load; the last CTA of each
+// launch sets its pair back to zero), so that launches in flight at the same
+// time on different streams use different pairs unless more than
+// kClaimSlots of them are.
+constexpr int kClaimSlots = 1024;
+__device__ int g_claim_ctr[2 * kClaimSlots];
+
+int* claim_counter(int device) {
+  static std::mutex mu;
+  static int* base[kMaxDevices] = {};
+  static unsigned next[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[device]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_claim_ctr) != cudaSuccess) return nullptr;
+    base[device] = static_cast<int*>(a);
+  }
+  return base[device] + 2 * (next[device]++ % kClaimSlots);
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -333,11 +355,13 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   prm.test_skip_arrive = fault_injected("skip_arrive") ? 1 : 0;
   alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
   prm.act_sfu = act_route() == GDPA_ROUTE_SFU ? 1 : 0;
+  prm.item_ctr = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool win = a.window_blocks != 0;
   // sliding windows (window_blocks < 0) exist only in the 64-key pair kernel
   if (a.window_blocks < 0 && !(a.rows_per_item == 256 && a.kv_tile == kBlockN / 2)) return GDPA_ERR_INVALID_ARG;
-  if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {
+  if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {  // the 64-key pair kernel claims its items at run time
+    if (!(prm.item_ctr = claim_counter(device))) return GDPA_ERR_CUDA;
     if (win) {  // softmax only (validated on entry)
       if (a.D == 128) return launch_pair64<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
       if (a.D == 64) return launch_pair64<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
