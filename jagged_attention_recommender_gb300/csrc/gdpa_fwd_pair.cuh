@@ -40,7 +40,7 @@ struct PairCfg {
   static constexpr int OFF_K = OFF_QB + NQS * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * TILE_BYTES;
-  static constexpr int BAR_BYTES = 512;
+  static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   __host__ __device__ static constexpr uint32_t tm_s(int x) { return x ? 128u : 0u; }    // S_A, S_B
   __host__ __device__ static constexpr uint32_t tm_o(int x) { return x ? 384u : 256u; }  // O_A, O_B
@@ -57,6 +57,12 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+struct PairItem {
+  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
+  int rows[2];  // valid rows of tile A and tile B (B may be 0)
+  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each tile attends to
+};
+
 template <int D>
 struct PairBars {
   uint64_t q_full[2][PairCfg<D>::NQS], q_empty[2][PairCfg<D>::NQS];
@@ -64,15 +70,11 @@ struct PairBars {
   uint64_t v_full[PairCfg<D>::NV], v_empty[PairCfg<D>::NV];
   uint64_t s_full[2], p_full[2][2], o_done[2], o_empty[2];  // p_full per side and half of the keys
   uint64_t mma_drain;
+  ItemRing<PairItem> ring;  // the CTA's items, in claim order
   uint32_t tmem_slot;
   int abort;
 };
-
-struct PairItem {
-  int h, q0, kv0, kv_end, n_kv, q_tok, kv_tok, Lkv;
-  int rows[2];  // valid rows of tile A and tile B (B may be 0)
-  int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each tile attends to
-};
+static_assert(sizeof(PairBars<64>) <= PairCfg<64>::BAR_BYTES && sizeof(PairBars<128>) <= PairCfg<128>::BAR_BYTES, "barrier area");
 
 // Full attention: both tiles attend to every K/V tile of the item.  Block
 // window: the item's keys run from the first key tile A's rows may see to
@@ -113,8 +115,12 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int idx) {
 
 // Two producer threads: one stages Q and K, the other V, so that a K load
 // never waits behind a V slot.
+// The Q/K producer thread is also the CTA's claimer: it claims each item,
+// decodes it (flagging a bad plan) and publishes it for the other roles
+// before staging its Q and K tiles; the V producer reads the items from the
+// ring.
 template <int D, bool WIN, bool LOAD_V>
-__device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, int ibeg, int iend) {
+__device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
   int qn[2] = {0, 0};
@@ -131,8 +137,18 @@ __device__ void pair_producer(const FwdParams& p, uint8_t* sm, PairBars<D>& B, i
     ptx::prefetch_tensormap(&p.tm_q);
     ptx::prefetch_tensormap(&p.tm_k);
   }
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair<WIN, !LOAD_V>(p, idx);
+  ListClaim L;
+  if (!LOAD_V) L = claim_init(p);
+  for (uint32_t k = 0; ok; ++k) {
+    PairItem t;
+    if (!LOAD_V) {
+      const int idx = claim_next(p, L);
+      if (idx >= 0) t = decode_pair<WIN, true>(p, idx);
+      ok = ring_publish(p, B.ring, k, t, idx >= 0, abort);
+      if (!ok || idx < 0) break;
+    } else if (!ring_read(p, B.ring, k, t, 0u, abort, ok)) {
+      break;
+    }
     if (t.n_kv == 0) continue;
     if (!LOAD_V) {
       for (int x = 0; x < 2 && ok; ++x) {
@@ -241,7 +257,7 @@ __device__ __forceinline__ bool pair_issue_pv(const FwdParams& p, uint8_t* sm, P
 }
 
 template <int D, bool WIN>
-__device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32_t tmem, int ibeg, int iend) {
+__device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32_t tmem) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
   int qn[2] = {0, 0};       // items seen by each side (Q stage and O buffer use counts)
@@ -255,8 +271,9 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
   // for the load: the producer never refills a stage with a copy in flight.
   bool pend_v = false;
   uint32_t pend_v_g = 0;
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair<WIN>(p, idx);
+  for (uint32_t k = 0; ok; ++k) {
+    PairItem t;
+    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     if (t.n_kv == 0) continue;
     const bool has[2] = {t.rows[0] > 0, t.rows[1] > 0};
     uint32_t q_base[2] = {0, 0};
@@ -335,8 +352,7 @@ __device__ void pair_mma(const FwdParams& p, uint8_t* sm, PairBars<D>& B, uint32
 // ------------------------------------------------------------------ activation + epilogue
 
 template <int D, int ACT, bool WIN>
-__device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tmem, int ibeg, int iend, int x,
-                                int warp, int lane) {
+__device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tmem, int x, int warp, int lane) {
   using C = PairCfg<D>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
@@ -350,8 +366,9 @@ __device__ void pair_activation(const FwdParams& p, PairBars<D>& B, uint32_t tme
   uint32_t gx = 0;  // this side's K/V tiles (phase of s_full, p_full)
   uint32_t ix = 0;  // this side's items (phase of o_done)
   bool ok = true;
-  for (int idx = ibeg; idx < iend && ok; ++idx) {
-    const PairItem t = decode_pair<WIN>(p, idx);
+  for (uint32_t k = 0; ok; ++k) {
+    PairItem t;
+    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     const int rows = x ? t.rows[1] : t.rows[0];
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(t.q_tok + 128 * x + row) * H + t.h) * D;
     if (t.n_kv == 0) {  // no keys: zero output rows
@@ -637,8 +654,6 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_cons
   PairBars<D>& B = *reinterpret_cast<PairBars<D>*>(sm + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ibeg = p.cta_begin[blockIdx.x];
-  const int iend = p.cta_begin[blockIdx.x + 1];
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
       for (int s = 0; s < C::NQS; ++s) {
@@ -660,6 +675,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_cons
       ptx::mbar_init(&B.v_empty[s], 1);
     }
     ptx::mbar_init(&B.mma_drain, 1);
+    for (int r = 0; r < kRing; ++r) {  // readers: the V producer, the MMA warp, the eight activation warps
+      ptx::mbar_init(&B.ring.full[r], 1);
+      ptx::mbar_init(&B.ring.empty[r], 10);
+    }
     B.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -674,21 +693,22 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair_kernel(const __grid_cons
   if (warp < 4) {  // warpgroup 0: producers and MMA issuer, few registers
     ptx::regs_dec<C::REGS_CTRL>();
     if (warp == 0) {
-      if (lane == 0) pair_producer<D, WIN, false>(p, sm, B, ibeg, iend);
+      if (lane == 0) pair_producer<D, WIN, false>(p, sm, B);
     } else if (warp == 2) {
-      if (lane == 0) pair_producer<D, WIN, true>(p, sm, B, ibeg, iend);
+      if (lane == 0) pair_producer<D, WIN, true>(p, sm, B);
     } else if (warp == 1) {
-      pair_mma<D, WIN>(p, sm, B, tmem, ibeg, iend);  // the whole warp: MMAs issued warp-uniformly
+      pair_mma<D, WIN>(p, sm, B, tmem);  // the whole warp: MMAs issued warp-uniformly
     }
   } else {  // warpgroups 1 and 2: tiles A and B, a whole row of scores in registers
     ptx::regs_inc<C::REGS_ACT>();
-    pair_activation<D, ACT, WIN>(p, B, tmem, ibeg, iend, warp < 8 ? 0 : 1, warp, lane);
+    pair_activation<D, ACT, WIN>(p, B, tmem, warp < 8 ? 0 : 1, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, C::TM_COLS);
+  if (threadIdx.x == 0) claim_finish(p);
 }
 
 }  // namespace gdpa

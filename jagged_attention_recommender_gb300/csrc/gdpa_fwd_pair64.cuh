@@ -93,6 +93,7 @@ struct Pair64Bars {
   uint32_t tmem_slot;
   int abort;
 };
+static_assert(sizeof(Pair64Bars<64>) <= Pair64Cfg<64>::BAR_BYTES && sizeof(Pair64Bars<128>) <= Pair64Cfg<128>::BAR_BYTES, "barrier area");
 
 // Full attention: both tiles attend to every K/V tile of the item.  Block
 // window: the item's keys run from the first key tile A's rows may see to

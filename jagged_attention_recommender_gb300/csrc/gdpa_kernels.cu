@@ -360,8 +360,9 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   const bool win = a.window_blocks != 0;
   // sliding windows (window_blocks < 0) exist only in the 64-key pair kernel
   if (a.window_blocks < 0 && !(a.rows_per_item == 256 && a.kv_tile == kBlockN / 2)) return GDPA_ERR_INVALID_ARG;
-  if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {  // the 64-key pair kernel claims its items at run time
-    if (!(prm.item_ctr = claim_counter(device))) return GDPA_ERR_CUDA;
+  // the pair kernels (256-row items) claim their items at run time
+  if (a.rows_per_item == 256 && !mx && !(prm.item_ctr = claim_counter(device))) return GDPA_ERR_CUDA;
+  if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {
     if (win) {  // softmax only (validated on entry)
       if (a.D == 128) return launch_pair64<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
       if (a.D == 64) return launch_pair64<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
