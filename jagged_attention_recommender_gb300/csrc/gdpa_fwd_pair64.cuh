@@ -10,36 +10,43 @@
 // tiles' MMAs, which halves the K/V traffic per FLOP against one tile per
 // item.
 //
-// K/V tiles are 64 keys, and each side has two S buffers in tensor memory,
-// so the MMA thread issues S_x(t+1) = Q_x K(t+1)^T before O_x += P_x(t) V(t)
-// (the P of tile t sits in the other buffer): when a side's activation has
-// finished tile t its next scores are already there, and the activations of
-// both sides run back to back while the tensor core works off the queue:
+// K/V tiles are 64 keys, and each side has two S buffers in tensor memory.
+// Each side has its own MMA warp, which for every K/V tile g its rows attend
+// to issues S_x(g) = Q_x K(g)^T into one buffer and then O_x += P_x(g-1)
+// V(g-1) from the other (the P of the previous tile), so when a side's
+// activation has finished a tile its next scores are already there:
 //
-//   MMA thread, per K/V tile g:  S_A(g), S_B(g)            (buffers g & 1)
-//                                O_A += P_A(g-1) V(g-1),  O_B += P_B(g-1) V(g-1)
+//   MMA warp of side x, per K/V tile g:  S_x(g)                (buffer g & 1)
+//                                        O_x += P_x(g-1) V(g-1)
 //
-// This look-ahead also crosses item boundaries (the next item's Q is double
-// buffered), which is what a one-tile key range needs (the "outer loop"
+// This look-ahead also crosses item boundaries (the next item's Q is staged
+// ahead), which is what a one-tile key range needs (the "outer loop"
 // pipelining of the GDPA section of the techfeed summary of "GEM Training").
 // With 64-key tiles a block window's 64-key blocks are whole tiles, so each
-// side skips every block outside its window.
+// side skips every block outside its window; the two sides' windows start
+// two tiles apart, and with separate issuers (and five K/V stages for
+// windows at D = 128) neither side waits for the other's tiles.  Each K/V
+// stage is released by both MMA warps, a side that does not attend to a
+// tile releasing it once it has landed.
+//
+// Items are claimed at run time (see ItemRing): the Q/K producer claims and
+// decodes each item and every other role reads it from the ring.
 //
 // Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
-// and K (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
-// the issue loop and one elected lane issues; with full attention warp 3
-// issues tile B's MMAs and warp 1 tile A's) and the TMA producer for V
-// (warp 2), and hands its registers to warpgroups 1 and 2, the
-// activation/epilogue of tiles A and B.  TMEM (512 columns): S_A buffers 0
-// and 64, S_B buffers 128 and 192, O_A 256, O_B 384.  An activation thread
-// holds one query row; it reads its 64 scores of a tile from TMEM at once.
+// and K and claimer (warp 0), the MMA issuers of tiles A and B (warps 1 and
+// 3; the whole warp runs the issue loop and one elected lane issues; warp 1
+// owns the tensor memory) and the TMA producer for V (warp 2), and hands its
+// registers to warpgroups 1 and 2, the activation/epilogue of tiles A and B.
+// TMEM (512 columns): S_A buffers 0 and 64, S_B buffers 128 and 192, O_A 256,
+// O_B 384.  An activation thread holds one query row; it reads its 64 scores
+// of a tile from TMEM at once.
 #pragma once
 
 #include "gdpa_fwd_common.cuh"
 
 namespace gdpa {
 
-template <int D>
+template <int D, bool WIN>
 struct Pair64Cfg {
   static constexpr int BN = 64;                           // keys per K/V tile
   static constexpr int KCH = D / 64;
@@ -47,9 +54,12 @@ struct Pair64Cfg {
   static constexpr int Q_TILE = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;               // K/V: 64 rows x 128 bytes per chunk
   static constexpr int KV_TILE = KCH * KV_CHUNK;
-  static constexpr int NQS = 2;                           // Q stages per query tile
-  static constexpr int NK = (D == 64) ? 6 : 3;
-  static constexpr int NV = (D == 64) ? 6 : 3;
+  // Q stages per query tile, K and V stages: block windows at D = 128 trade
+  // the second Q stage for two more K/V stages, so that a side may run up to
+  // four tiles ahead of the other (their windows start two tiles apart).
+  static constexpr int NQS = (WIN && D == 128) ? 1 : 2;
+  static constexpr int NK = (D == 64) ? 6 : (WIN ? 5 : 3);
+  static constexpr int NV = (D == 64) ? 6 : (WIN ? 5 : 3);
   static constexpr int OFF_QA = 0;
   static constexpr int OFF_QB = OFF_QA + NQS * Q_TILE;
   static constexpr int OFF_K = OFF_QB + NQS * Q_TILE;
@@ -81,11 +91,11 @@ struct Pair64Item {
   int t0[2], t1[2];  // K/V tiles [t0, t1) of the item each query tile attends to
 };
 
-template <int D>
+template <int D, bool WIN>
 struct Pair64Bars {
-  uint64_t q_full[2][Pair64Cfg<D>::NQS], q_empty[2][Pair64Cfg<D>::NQS];
-  uint64_t k_full[Pair64Cfg<D>::NK], k_empty[Pair64Cfg<D>::NK];
-  uint64_t v_full[Pair64Cfg<D>::NV], v_empty[Pair64Cfg<D>::NV];
+  uint64_t q_full[2][Pair64Cfg<D, WIN>::NQS], q_empty[2][Pair64Cfg<D, WIN>::NQS];
+  uint64_t k_full[Pair64Cfg<D, WIN>::NK], k_empty[Pair64Cfg<D, WIN>::NK];
+  uint64_t v_full[Pair64Cfg<D, WIN>::NV], v_empty[Pair64Cfg<D, WIN>::NV];
   uint64_t s_full[2][2], p_full[2][2];  // per side and S buffer
   uint64_t o_done[2], o_empty[2];
   uint64_t mma_drain[2];  // one per MMA warp
@@ -93,7 +103,11 @@ struct Pair64Bars {
   uint32_t tmem_slot;
   int abort;
 };
-static_assert(sizeof(Pair64Bars<64>) <= Pair64Cfg<64>::BAR_BYTES && sizeof(Pair64Bars<128>) <= Pair64Cfg<128>::BAR_BYTES, "barrier area");
+static_assert(sizeof(Pair64Bars<64, false>) <= Pair64Cfg<64, false>::BAR_BYTES &&
+                  sizeof(Pair64Bars<128, false>) <= Pair64Cfg<128, false>::BAR_BYTES &&
+                  sizeof(Pair64Bars<64, true>) <= Pair64Cfg<64, true>::BAR_BYTES &&
+                  sizeof(Pair64Bars<128, true>) <= Pair64Cfg<128, true>::BAR_BYTES,
+              "barrier area");
 
 // Full attention: both tiles attend to every K/V tile of the item.  Block
 // window: the item's keys run from the first key tile A's rows may see to
@@ -149,8 +163,8 @@ __device__ __forceinline__ Pair64Item decode_pair64(const FwdParams& p, int idx)
 // before staging its Q tiles and K tiles; the V producer reads the items from
 // the ring.
 template <int D, bool WIN, bool LOAD_V>
-__device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B) {
-  using C = Pair64Cfg<D>;
+__device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D, WIN>& B) {
+  using C = Pair64Cfg<D, WIN>;
   volatile int* abort = &B.abort;
   int qn[2] = {0, 0};
   uint32_t g = 0;
@@ -248,10 +262,10 @@ struct Pair64PV {
 // O += P_hi V + P_lo V, so the weights keep ~16 significant bits: with a few
 // keys and no softmax normalisation, a single bf16 rounding of P would move
 // the output by up to 2^-8 of each term.
-template <int D, bool SPLIT>
-__device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int x,
+template <int D, bool WIN, bool SPLIT>
+__device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm, Pair64Bars<D, WIN>& B, uint32_t tmem, int x,
                                               const Pair64PV& P) {
-  using C = Pair64Cfg<D>;
+  using C = Pair64Cfg<D, WIN>;
   volatile int* abort = &B.abort;
   const int b = P.gx & 1;
   if (!ptx::mbar_wait(&B.p_full[x][b], (P.gx >> 1) & 1, p.timeout_ns, abort)) return false;
@@ -277,103 +291,11 @@ __device__ __forceinline__ bool pair64_issue_pv(const FwdParams& p, uint8_t* sm,
   return true;
 }
 
-template <int D, bool WIN, bool SPLIT>
-__device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem) {
-  using C = Pair64Cfg<D>;
-  volatile int* abort = &B.abort;
-  int qn[2] = {0, 0};       // items seen by each side (Q stage and O buffer use counts)
-  uint32_t gx[2] = {0, 0};  // tiles processed by each side (S buffers)
-  uint32_t g = 0;
-  bool ok = true;
-  bool pend[2] = {false, false};
-  Pair64PV pv[2] = {{0, 0, 0, 0, 0}, {0, 0, 0, 0, 0}};
-  // V tile pend_v_g is released once both sides' P V of it are issued.  Every
-  // staged tile is read by a P V -- tile A attends to the item's first tiles
-  // and tile B to its last ones, with no gap between them (a window's start
-  // moves forward by at most tile A's rows), and an item without rows in tile
-  // A has no tiles -- so the release always follows a read that waited for
-  // the load, and the producer never refills a stage with a copy in flight.
-  bool pend_v = false;
-  uint32_t pend_v_g = 0;
-  for (uint32_t k = 0; ok; ++k) {
-    Pair64Item t;
-    if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
-    if (t.n_kv == 0) continue;
-    const bool has[2] = {t.rows[0] > 0, t.rows[1] > 0};
-    uint32_t q_base[2] = {0, 0};
-    for (int x = 0; x < 2 && ok; ++x) {
-      if (!has[x]) continue;
-      const int s = qn[x] % C::NQS;
-      ok = ptx::mbar_wait(&B.q_full[x][s], (qn[x] / C::NQS) & 1, p.timeout_ns, abort);
-      q_base[x] = ptx::smem_u32(sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::Q_TILE);
-    }
-    if (!ok) break;
-    for (int j = 0; j < t.n_kv; ++j, ++g) {
-      const int sk = g % C::NK;
-      ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
-      const int n16 = (ncols + 15) >> 4;
-      const uint32_t idesc = ptx::idesc_bf16(128, n16 * 16, 0);
-      const uint32_t k_base = ptx::smem_u32(sm + C::OFF_K + sk * C::KV_TILE);
-      bool act[2];
-      // S_x(g) goes into the buffer that held P_x two tiles ago, whose P V
-      // was issued in an earlier iteration (the tensor core runs them in order).
-      for (int x = 0; x < 2; ++x) {
-        act[x] = has[x] && j >= t.t0[x] && j < t.t1[x];
-        if (!act[x]) continue;
-        const uint32_t s_col = C::tm_s(x, gx[x] & 1);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // K-major operands: 16 columns of D = 32 bytes inside a 128-byte swizzle row.
-          const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          ptx::mma_ss_elect(tmem + s_col, ptx::sdesc_sw128(q_base[x] + qoff, 16, 1024),
-                      ptx::sdesc_sw128(k_base + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit_elect(&B.s_full[x][gx[x] & 1]);
-      }
-      ptx::mma_commit_elect(&B.k_empty[sk]);
-      if (j == t.n_kv - 1) {
-        for (int x = 0; x < 2; ++x)
-          if (has[x]) ptx::mma_commit_elect(&B.q_empty[x][qn[x] % C::NQS]);
-      }
-      // Then O_x += P_x V for each side's previous tile (issued here even
-      // when this tile has no S_x, so that every P V of the previous K/V
-      // tile is issued now and its V stage can be released).
-      for (int x = 0; x < 2 && ok; ++x) {
-        if (!pend[x]) continue;
-        ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
-        pend[x] = false;
-      }
-      if (!ok) break;
-      if (pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
-      for (int x = 0; x < 2; ++x) {
-        if (!act[x]) continue;
-        pv[x] = Pair64PV{gx[x], g, qn[x], j == t.t0[x] ? 1 : 0, n16};
-        pend[x] = true;
-        ++gx[x];
-      }
-      pend_v = true;
-      pend_v_g = g;
-    }
-    for (int x = 0; x < 2; ++x)
-      if (has[x]) ++qn[x];
-  }
-  for (int x = 0; x < 2 && ok; ++x)
-    if (pend[x]) ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv[x]);
-  if (ok && pend_v) ptx::mma_commit_elect(&B.v_empty[pend_v_g % C::NV]);
-  if (!ok) report_failure(p, abort, kStatusMma);
-  ptx::mma_commit_elect(&B.mma_drain[0]);
-  const int never = 0;
-  ptx::mbar_wait(&B.mma_drain[0], 0, 100000000ull, &never);
-}
-
-// Full attention (short key ranges): one MMA warp per side, so that a side
-// whose P is ready never waits behind the other side's (measured: cross_gelu
-// 0.631 -> 0.600 ms, cross_silu 0.646 -> 0.604 ms; windows keep the single
-// issuer above, whose fixed A-then-B order measured faster for them).
+// One MMA warp per side, so that a side whose P is ready never waits behind
+// the other side's (measured: cross_gelu 0.631 -> 0.600 ms, cross_silu
+// 0.646 -> 0.604 ms against one issuer for both sides; block windows
+// 1.16 -> 1.13 ms once they had five K/V stages -- with three, one issuer
+// measured faster for them).
 // Side x's warp walks every item; for each K/V tile it waits for K, issues
 // S_x into its next buffer (if its rows attend to the tile), releases its
 // hold on K, then issues the pending O_x += P_x V of its previous tile and
@@ -381,8 +303,8 @@ __device__ void pair64_mma(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, ui
 // released once it has landed.  K and V stages then have two-count empty
 // barriers (one arrival per side).
 template <int D, bool WIN, bool SPLIT>
-__device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& B, uint32_t tmem, int x) {
-  using C = Pair64Cfg<D>;
+__device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D, WIN>& B, uint32_t tmem, int x) {
+  using C = Pair64Cfg<D, WIN>;
   volatile int* abort = &B.abort;
   int qn = 0;        // this side's items (Q stage and O use counts)
   uint32_t gx = 0;   // this side's tiles (S buffers)
@@ -426,7 +348,7 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
       ptx::mma_commit_elect(&B.k_empty[sk]);
       if (has && j == t.n_kv - 1) ptx::mma_commit_elect(&B.q_empty[x][qn % C::NQS]);
       if (pend) {
-        ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv);
+        ok = pair64_issue_pv<D, WIN, SPLIT>(p, sm, B, tmem, x, pv);
         if (!ok) break;
         ptx::mma_commit_elect(&B.v_empty[pv.g % C::NV]);
         pend = false;
@@ -444,7 +366,7 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D>& 
     if (has) ++qn;
   }
   if (ok && pend) {
-    ok = pair64_issue_pv<D, SPLIT>(p, sm, B, tmem, x, pv);
+    ok = pair64_issue_pv<D, WIN, SPLIT>(p, sm, B, tmem, x, pv);
     if (ok) ptx::mma_commit_elect(&B.v_empty[pv.g % C::NV]);
   }
   if (!ok) report_failure(p, abort, kStatusMma);
@@ -475,8 +397,8 @@ __device__ __forceinline__ void store_o_row(uint32_t o_addr, float inv, __nv_bfl
 }
 
 template <int D, int ACT, bool WIN>
-__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t tmem, int x, int warp, int lane) {
-  using C = Pair64Cfg<D>;
+__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uint32_t tmem, int x, int warp, int lane) {
+  using C = Pair64Cfg<D, WIN>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
@@ -770,11 +692,11 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D>& B, uint32_t
 
 template <int D, int ACT, bool WIN>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_constant__ FwdParams p) {
-  using C = Pair64Cfg<D>;
+  using C = Pair64Cfg<D, WIN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sm = smem_raw + pad;
-  Pair64Bars<D>& B = *reinterpret_cast<Pair64Bars<D>*>(sm + C::OFF_BAR);
+  Pair64Bars<D, WIN>& B = *reinterpret_cast<Pair64Bars<D, WIN>*>(sm + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -790,7 +712,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
       ptx::mbar_init(&B.o_done[x], 1);
       ptx::mbar_init(&B.o_empty[x], 128);
     }
-    constexpr uint32_t n_mma = WIN ? 1 : 2;  // MMA warps, each releasing every K and V stage once
+    constexpr uint32_t n_mma = 2;  // MMA warps, each releasing every K and V stage once
     for (int s = 0; s < C::NK; ++s) {
       ptx::mbar_init(&B.k_full[s], 1);
       ptx::mbar_init(&B.k_empty[s], n_mma);
@@ -822,8 +744,6 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
       if (lane == 0) pair64_producer<D, WIN, false>(p, sm, B);
     } else if (warp == 2) {
       if (lane == 0) pair64_producer<D, WIN, true>(p, sm, B);
-    } else if (WIN) {
-      if (warp == 1) pair64_mma<D, WIN, ACT == kActGelu>(p, sm, B, tmem);  // whole warp: warp-uniform issue
     } else {  // warps 1 and 3: the MMA issuers of tiles A and B
       pair64_mma_side<D, WIN, ACT == kActGelu>(p, sm, B, tmem, warp == 1 ? 0 : 1);
     }

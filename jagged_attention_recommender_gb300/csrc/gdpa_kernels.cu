@@ -163,7 +163,7 @@ gdpa_status_t launch_k(Kernel kernel, int threads, int smem, int min_regs, const
 // double-buffered (block windows, short key ranges).
 template <int D, int ACT, bool WIN>
 gdpa_status_t launch_pair64(const FwdParams& prm, int grid, cudaStream_t stream, int device) {
-  using C = Pair64Cfg<D>;
+  using C = Pair64Cfg<D, WIN>;
   static std::mutex mu;
   static bool attr_done[kMaxDevices] = {};
   return launch_k(gdpa_fwd_pair64_kernel<D, ACT, WIN>, C::THREADS, C::SMEM_BYTES, C::MIN_LAUNCH_REGS, prm, grid,
