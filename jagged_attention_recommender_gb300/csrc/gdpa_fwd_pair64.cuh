@@ -193,9 +193,14 @@ __device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D, W
       break;
     }
     if (t.n_kv == 0) continue;
-    if (!LOAD_V) {
-      for (int x = 0; x < 2 && ok; ++x) {
-        if (t.rows[x] == 0) continue;
+    for (int j = 0; j < t.n_kv && ok; ++j, ++g) {
+      const int y = t.kv_tok + t.kv0 + C::BN * j;
+      // Each tile's Q goes up just before the first K tile it attends to:
+      // with windows tile B's keys start two tiles later, and its Q stage is
+      // freed late (its window ends last), so tile A's first K tiles of the
+      // next item do not wait behind it.
+      for (int x = 0; x < 2 && ok && !LOAD_V; ++x) {
+        if (t.rows[x] == 0 || j != min(t.t0[x], t.n_kv - 1)) continue;
         const int s = qn[x] % C::NQS;
         const uint32_t ph = (qn[x] / C::NQS) & 1;
         ok = ptx::mbar_wait(&B.q_empty[x][s], ph ^ 1, p.timeout_ns, abort);
@@ -208,9 +213,7 @@ __device__ void pair64_producer(const FwdParams& p, uint8_t* sm, Pair64Bars<D, W
           ptx::tma_load_2d(sq + c * C::Q_CHUNK, &p.tm_q, &B.q_full[x][s], t.h * D + 64 * c, t.q_tok + 128 * x);
         ++qn[x];
       }
-    }
-    for (int j = 0; j < t.n_kv && ok; ++j, ++g) {
-      const int y = t.kv_tok + t.kv0 + C::BN * j;
+      if (!ok) break;
       if (!LOAD_V) {
         const int sk = g % C::NK;
         const uint32_t phk = (g / C::NK) & 1;
@@ -317,19 +320,32 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D, W
     if (!ring_read(p, B.ring, k, t, 0xffffffffu, abort, ok)) break;
     if (t.n_kv == 0) continue;
     const bool has = t.rows[x] > 0;
-    uint32_t q_base = 0;
-    if (has) {
-      const int s = qn % C::NQS;
-      ok = ptx::mbar_wait(&B.q_full[x][s], (qn / C::NQS) & 1, p.timeout_ns, abort);
-      q_base = ptx::smem_u32(sm + (x ? C::OFF_QB : C::OFF_QA) + s * C::Q_TILE);
-    }
-    if (!ok) break;
+    const int qs = qn % C::NQS;
+    const uint32_t q_base = ptx::smem_u32(sm + (x ? C::OFF_QB : C::OFF_QA) + qs * C::Q_TILE);
+    // the side's last tile reading Q (then its stage is released)
+    const int q_last = t.t1[x] > t.t0[x] ? min(t.t1[x], t.n_kv) - 1 : t.n_kv - 1;
+    bool q_ready = false;
     for (int j = 0; j < t.n_kv; ++j, ++g) {
       const int sk = g % C::NK;
       ok = ptx::mbar_wait(&B.k_full[sk], (g / C::NK) & 1, p.timeout_ns, abort);
       if (!ok) break;
       ptx::tc_fence_after();
       const bool act = has && j >= t.t0[x] && j < t.t1[x];
+      if (has && !q_ready && (act || j == q_last)) {
+        // The item's Q.  With windows (one Q stage per side), if it has not
+        // landed yet the previous tile's P V goes first rather than wait
+        // behind the load; short key ranges keep S before P V.
+        if (WIN && pend && !ptx::mbar_test_wait(&B.q_full[x][qs], (qn / C::NQS) & 1)) {
+          ok = pair64_issue_pv<D, WIN, SPLIT>(p, sm, B, tmem, x, pv);
+          if (!ok) break;
+          ptx::mma_commit_elect(&B.v_empty[pv.g % C::NV]);
+          pend = false;
+        }
+        ok = ptx::mbar_wait(&B.q_full[x][qs], (qn / C::NQS) & 1, p.timeout_ns, abort);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        q_ready = true;
+      }
       const int ncols = min(C::BN, t.kv_end - t.kv0 - C::BN * j);
       const int n16 = (ncols + 15) >> 4;
       if (act) {
@@ -346,7 +362,7 @@ __device__ void pair64_mma_side(const FwdParams& p, uint8_t* sm, Pair64Bars<D, W
         ptx::mma_commit_elect(&B.s_full[x][gx & 1]);
       }
       ptx::mma_commit_elect(&B.k_empty[sk]);
-      if (has && j == t.n_kv - 1) ptx::mma_commit_elect(&B.q_empty[x][qn % C::NQS]);
+      if (has && j == q_last) ptx::mma_commit_elect(&B.q_empty[x][qs]);
       if (pend) {
         ok = pair64_issue_pv<D, WIN, SPLIT>(p, sm, B, tmem, x, pv);
         if (!ok) break;
