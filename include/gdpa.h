@@ -82,7 +82,7 @@ typedef enum {
  *   GDPA_ROUTE_ALU: the ALU-only form of the GDPA section of the techfeed
  *     summary of "GEM Training" (a 6th-order Taylor polynomial of exp after
  *     range reduction, Newton reciprocal), FMA and integer instructions only.
- * The backward always takes the ALU route.
+ * The backward follows the same route (value and derivative).
  */
 typedef enum {
   GDPA_ROUTE_SFU = 0,

@@ -104,6 +104,7 @@ gdpa_status_t launch_backward(const BwdLaunchArgs& a) {
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const bool gelu = a.act != GDPA_ACT_SOFTMAX;  // the ALU activations
   alu_act_consts(a.act == GDPA_ACT_SILU, a.scale, prm.act_a, prm.act_c);
+  prm.act_sfu = act_route() == GDPA_ROUTE_SFU ? 1 : 0;
   if (a.D == 128)
     return gelu ? launch_bwd_d<128, kActGelu>(a, prm, s, device) : launch_bwd_d<128, kActSoftmax>(a, prm, s, device);
   if (a.D == 64)

@@ -65,6 +65,7 @@ struct BwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   float scale;
   int align32;        // dq, dk and dv all 32-byte aligned: 32-byte stores allowed
   float act_a, act_c; // ALU activations: folded constants (alu_act_consts)
+  int act_sfu;        // ALU activations: 1 = sigma on the special-function unit, 0 = the FMA polynomial
   int window;         // 0 full; > 0 block window of that many 64-token blocks;
                       // < 0 causal sliding window of -window tokens (self attention)
   int n_items;        // items in `items`; a persistent CTA takes every gridDim.x-th
@@ -367,7 +368,7 @@ __device__ void bwd_mma(const BwdParams& p, uint8_t* sm, BwdBars& B, uint32_t tm
 template <int ACT, bool PER_COL>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2c,
                                           const float* dvc, float lse2r, float dvr, int c0, int c_lo, int c_hi,
-                                          float sl, float inv_l, uint64_t gA2, uint64_t gC2,
+                                          float sl, float inv_l, uint64_t gA2, uint64_t gC2, bool sfu,
                                           uint32_t (&pk_p)[16], uint32_t (&pk_ds)[16]) {
 #pragma unroll
   for (int u = 0; u < 16; ++u) {
@@ -389,10 +390,14 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
       g1 = p1 * (d1 - v1);
     } else {
       float y0, y1;
-      gelu_tanh_alu2(s0, s1, gA2, gC2, y0, y1);  // gelu(x) / scale
+      if (sfu) {  // the sigma route of the forward (gdpa_set_act_route)
+        gelu_tanh_val_grad_sfu2(s0, s1, gA2, gC2, y0, y1, g0, g1);
+      } else {
+        gelu_tanh_alu2(s0, s1, gA2, gC2, y0, y1);  // gelu(x) / scale
+        gelu_tanh_grad_alu2(s0, s1, gA2, gC2, g0, g1);
+      }
       p0 = y0 * sl * inv_l;
       p1 = y1 * sl * inv_l;
-      gelu_tanh_grad_alu2(s0, s1, gA2, gC2, g0, g1);
       g0 *= d0 * inv_l;
       g1 *= d1 * inv_l;
     }
@@ -529,7 +534,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dq_kernel(const __grid_consta
           ptx::tmem_wait_ld();
           uint32_t pk_p[16], pk_ds[16];
           bwd_chunk<ACT, false>(sr, dr, nullptr, nullptr, lse2, dvr, 32 * ch, c_lo, c_hi, p.score_scale, inv_l,
-                                gA2, gC2, pk_p, pk_ds);
+                                gA2, gC2, p.act_sfu != 0, pk_p, pk_ds);
           ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_ds);  // dS over consumed S columns
         }
         ptx::tmem_wait_st();
@@ -621,7 +626,7 @@ __global__ void __launch_bounds__(192, 1) gdpa_bwd_dkdv_kernel(const __grid_cons
           ptx::tmem_wait_ld();
           uint32_t pk_p[16], pk_ds[16];
           bwd_chunk<ACT, true>(sr, dr, vb + 32 * ch, vb + C::BN + 32 * ch, 0.0f, 0.0f, 32 * ch, c_lo, c_hi,
-                               p.score_scale, inv_l, gA2, gC2, pk_p, pk_ds);
+                               p.score_scale, inv_l, gA2, gC2, p.act_sfu != 0, pk_p, pk_ds);
           ptx::tmem_st16(tmem + lane_off + C::tm_s(b) + 16 * ch, pk_p);   // P^T over consumed S^T columns
           ptx::tmem_st16(tmem + lane_off + C::tm_p(b) + 16 * ch, pk_ds);  // dS^T over consumed dP^T columns
         }

@@ -140,6 +140,35 @@ __device__ __forceinline__ void gelu_tanh_grad_alu2(float s0, float s1, uint64_t
   ptx::f2_unpack(ptx::f2_fma(sig2, dz, sig), g0, g1);
 }
 
+// Value and derivative for the backward with sigma on the special-function
+// unit: a = |z|, e = 2^(-a log2 e) (ex2.approx), sigma(a) = 1/(1+e)
+// (rcp.approx); sigma(z) = sigma(a) for z >= 0, e sigma(a) otherwise;
+// sigma(z) sigma(-z) = e sigma(a)^2.  Returns y = s sigma(z) (the forward's
+// value) and gelu'(x) = sigma(z) + sigma(z) sigma(-z) s (A + 3 C s^2), as
+// gelu_tanh_alu2 and gelu_tanh_grad_alu2 do.
+__device__ __forceinline__ void gelu_tanh_val_grad_sfu2(float s0, float s1, uint64_t A2, uint64_t C2, float& y0,
+                                                        float& y1, float& g0, float& g1) {
+  const uint64_t s = ptx::f2_pack(s0, s1);
+  const uint64_t ss = ptx::f2_mul(s, s);
+  const uint64_t z = ptx::f2_mul(s, ptx::f2_fma(C2, ss, A2));
+  float z0, z1;
+  ptx::f2_unpack(z, z0, z1);
+  const uint64_t t = ptx::f2_mul(ptx::f2_pack(fabsf(z0), fabsf(z1)), ptx::f2_splat(-1.4426950408889634f));
+  float t0, t1;
+  ptx::f2_unpack(t, t0, t1);
+  const uint64_t e = ptx::f2_pack(ptx::ex2_approx(t0), ptx::ex2_approx(t1));
+  float d0, d1;
+  ptx::f2_unpack(ptx::f2_add(e, ptx::f2_splat(1.0f)), d0, d1);
+  const uint64_t inv = ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
+  float e0, e1;
+  ptx::f2_unpack(e, e0, e1);
+  const uint64_t sig = ptx::f2_mul(inv, ptx::f2_pack(z0 >= 0.0f ? 1.0f : e0, z1 >= 0.0f ? 1.0f : e1));
+  ptx::f2_unpack(ptx::f2_mul(s, sig), y0, y1);
+  const uint64_t sig2 = ptx::f2_mul(e, ptx::f2_mul(inv, inv));
+  const uint64_t dz = ptx::f2_mul(s, ptx::f2_fma(ptx::f2_mul(C2, ptx::f2_splat(3.0f)), ss, A2));
+  ptx::f2_unpack(ptx::f2_fma(sig2, dz, sig), g0, g1);
+}
+
 // One launch's activation constants and route: sfu selects gelu_tanh_sfu2
 // (sigma on the special-function unit), otherwise gelu_tanh_alu2 (the
 // FMA-pipe polynomial).  Both return s sigma(s (A + C s^2)).

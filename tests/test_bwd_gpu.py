@@ -138,12 +138,18 @@ def test_bwd_softmax_cross_and_empty(D):
     check(small_batch(rng, Lq, Lkv, 2, D), 6300 + D)
 
 
+@pytest.mark.parametrize("route", ["sfu", "alu"])
 @pytest.mark.parametrize("D", [64, 128])
-def test_bwd_gelu(D):
+def test_bwd_gelu(D, route):
+    # both sigma routes (gdpa_set_act_route) through the forward and the backward
     rng = np.random.default_rng(6400 + D)
     Lq = np.array([129, 33, 300, 0, 64])
     Lkv = np.array([40, 200, 8, 9, 128])
-    check(small_batch(rng, Lq, Lkv, 2, D, act=ACT_GELU_TANH, qk_norm=True, scale=1.0), 6500 + D)
+    gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_ALU if route == "alu" else gdpa.GDPA_ROUTE_SFU)
+    try:
+        check(small_batch(rng, Lq, Lkv, 2, D, act=ACT_GELU_TANH, qk_norm=True, scale=1.0), 6500 + D)
+    finally:
+        gdpa.gdpa_set_act_route(gdpa.GDPA_ROUTE_SFU)
 
 
 @pytest.mark.parametrize("D", [64, 128])
