@@ -47,10 +47,17 @@
  * Ownership: the caller owns every buffer it passes; the library never frees
  * them and keeps no reference after the call returns (the GPU may still be
  * reading them until the stream reaches the end of the launched work).  The
- * library owns its plans and an internal per-device work-list buffer.
+ * library owns its plans and internal per-device work-list buffers (two,
+ * used in turn).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
- * stream).  All GPU work is enqueued on it.
+ * stream).  All kernels are enqueued on it; the planned entry points copy
+ * their work list up on a library-owned stream that `stream` then waits for
+ * (on a stream being captured, the copy stays on that stream).  The pair
+ * kernels take their work items at run time from a device counter; each
+ * launch uses its own counter from a fixed pool of 1024, so launches in
+ * flight at the same time on different streams are independent unless more
+ * than 1024 are.
  *
  * Errors: every entry point returns a gdpa_status_t and never throws or
  * aborts.  Kernel-side failures (a bounded wait that ran out) are recorded in
