@@ -51,9 +51,11 @@
  * used in turn).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
- * stream).  All kernels are enqueued on it; the planned entry points copy
- * their work list up on a library-owned stream that `stream` then waits for
- * (on a stream being captured, the copy stays on that stream).  The pair
+ * stream).  All kernels are enqueued on it; the entry points that plan on
+ * every call (gdpa_fwd, gdpa_fwd_async, gdpa_fwd_lse, gdpa_fwd_sliding,
+ * gdpa_fwd_mx, gdpa_fwd_mxfp8) copy their work list up on a library-owned
+ * stream that `stream` then waits for (on a stream being captured, the copy
+ * stays on that stream).  The pair
  * kernels take their work items at run time from a device counter; each
  * launch uses its own counter from a fixed pool of 1024, so launches in
  * flight at the same time on different streams are independent unless more
