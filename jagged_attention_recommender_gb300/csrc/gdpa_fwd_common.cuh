@@ -43,6 +43,11 @@ struct FwdParams {  // CUtensorMap members carry their own 64+ byte alignment
   // Run-time claiming of work items (kernels that take it): [0] the next
   // claim, [1] CTAs finished; the last CTA to finish sets both back to 0.
   int* item_ctr;
+  // The output as a 2-D view [Tq, H*D] bf16, box 64 x 128, 128-byte swizzle,
+  // for bulk tensor stores of whole 128-row tiles (64-key pair kernel);
+  // out_tma = 0: rows are stored by the threads.
+  CUtensorMap tm_o;
+  int out_tma;
 };
 
 // kActGelu instantiates the ALU activations (tanh-GELU and SiLU, told apart

@@ -54,17 +54,26 @@ struct Pair64Cfg {
   static constexpr int Q_TILE = KCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;               // K/V: 64 rows x 128 bytes per chunk
   static constexpr int KV_TILE = KCH * KV_CHUNK;
+  // Windows store whole 128-row output tiles in bulk through a staging area
+  // per side (full attention keeps per-thread stores: there the area would
+  // cost a K and a V stage, which measured slower: cross_gelu 0.456 -> 0.482 ms).
+  static constexpr bool BULK = WIN;
   // Q stages per query tile, K and V stages: block windows at D = 128 trade
-  // the second Q stage for two more K/V stages, so that a side may run up to
-  // four tiles ahead of the other (their windows start two tiles apart).
+  // the second Q stage for more K/V stages, so that a side may run ahead of
+  // the other (their windows start two tiles apart).
   static constexpr int NQS = (WIN && D == 128) ? 1 : 2;
-  static constexpr int NK = (D == 64) ? 6 : (WIN ? 5 : 3);
-  static constexpr int NV = (D == 64) ? 6 : (WIN ? 5 : 3);
+  static constexpr int NK = (D == 64) ? 6 : (WIN ? 4 : 3);
+  static constexpr int NV = (D == 64) ? 6 : (WIN ? 4 : 3);
   static constexpr int OFF_QA = 0;
   static constexpr int OFF_QB = OFF_QA + NQS * Q_TILE;
   static constexpr int OFF_K = OFF_QB + NQS * Q_TILE;
   static constexpr int OFF_V = OFF_K + NK * KV_TILE;
-  static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
+  // Output staging, one area per side: 128 rows x 64 columns of bf16 in the
+  // 128-byte-swizzled layout of the output tensor map's box, written by the
+  // side's threads and stored by one bulk tensor store per 64 columns.
+  static constexpr int STG_BYTES = 128 * 128;
+  static constexpr int OFF_STG = OFF_V + NV * KV_TILE;
+  static constexpr int OFF_BAR = OFF_STG + (BULK ? 2 * STG_BYTES : 0);
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   __host__ __device__ static constexpr uint32_t tm_s(int x, int b) { return 128u * x + 64u * b; }  // S_x buffer b
@@ -83,6 +92,7 @@ struct Pair64Cfg {
   static_assert(regs_ctrl(kActSoftmax) + 2 * regs_act(kActSoftmax) <= 3 * MIN_LAUNCH_REGS, "register split");
   static_assert(384 + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(OFF_STG % 1024 == 0, "staging areas on the swizzle's 1024-byte period");
 };
 
 struct Pair64Item {
@@ -99,6 +109,7 @@ struct Pair64Bars {
   uint64_t s_full[2][2], p_full[2][2];  // per side and S buffer
   uint64_t o_done[2], o_empty[2];
   uint64_t mma_drain[2];  // one per MMA warp
+  uint64_t epi_bar[2];    // per side: its 128 activation threads meet around a bulk output store
   ItemRing<Pair64Item> ring;  // the CTA's items, in claim order
   uint32_t tmem_slot;
   int abort;
@@ -412,8 +423,59 @@ __device__ __forceinline__ void store_o_row(uint32_t o_addr, float inv, __nv_bfl
   }
 }
 
+// The side's 128 activation threads meet on their barrier (bounded wait, so
+// a warp that has stopped on a timeout cannot hold the others forever).
+__device__ __forceinline__ bool side_sync(const FwdParams& p, uint64_t* bar, uint32_t& phase, volatile int* abort) {
+  ptx::mbar_arrive(bar);
+  bool ok = ptx::mbar_wait(bar, phase & 1, p.timeout_ns, abort);
+  ++phase;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// A whole 128-row tile's output by bulk tensor stores: per 64 columns, each
+// thread converts its row (O times inv, bf16) into the side's staging area
+// (16-byte chunk j of row r at chunk position j ^ (r mod 8): the 128-byte
+// swizzle of the output map's box), the side's 128 threads meet, and the
+// leader (row 0) issues the store.  Before it is rewritten the area must
+// have been read by the previous store: the leader waits for that, then the
+// meeting lets the others write.  False on a timeout.
+template <int D>
+__device__ __forceinline__ bool store_o_tile_bulk(const FwdParams& p, uint32_t o_addr, float inv, uint8_t* stg, int row,
+                                                  uint64_t* bar, uint32_t& phase, volatile int* abort, int x0, int y0) {
+  const bool leader = row == 0;
+  const uint32_t base = ptx::smem_u32(stg) + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+  for (int c2 = 0; c2 < D / 64; ++c2) {
+    if (leader) ptx::bulk_wait_read_all();
+    if (!side_sync(p, bar, phase, abort)) return false;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t r[32];
+      ptx::tmem_ld32(o_addr + 64 * c2 + 32 * cc, r);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 16-byte chunk j = 4 cc + q: eight bf16 = four words
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[i] = ptx::pack_bf16x2(__uint_as_float(r[8 * q + 2 * i]) * inv, __uint_as_float(r[8 * q + 2 * i + 1]) * inv);
+        const uint32_t j = static_cast<uint32_t>(4 * cc + q) ^ static_cast<uint32_t>(row & 7);
+        ptx::st_shared_v4(base + 16u * j, w[0], w[1], w[2], w[3]);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    if (!side_sync(p, bar, phase, abort)) return false;
+    if (leader) {
+      ptx::tma_store_2d(&p.tm_o, stg, x0 + 64 * c2, y0);
+      ptx::bulk_commit();
+    }
+  }
+  return true;
+}
+
 template <int D, int ACT, bool WIN>
-__device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uint32_t tmem, int x, int warp, int lane) {
+__device__ void pair64_activation(const FwdParams& p, uint8_t* sm, Pair64Bars<D, WIN>& B, uint32_t tmem, int x,
+                                  int warp, int lane) {
   using C = Pair64Cfg<D, WIN>;
   volatile int* abort = &B.abort;
   const int quarter = warp & 3;
@@ -423,6 +485,8 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uin
   const float sl = p.score_scale;
   const ActK ak = act_k(p.act_a, p.act_c, p.act_sfu);  // GELU / SiLU: the scale folded into the cubic
   const int H = p.H;
+  uint8_t* stg = sm + C::OFF_STG + x * C::STG_BYTES;  // this side's output staging area
+  uint32_t epi_phase = 0;                               // uses of this side's epi_bar
   uint32_t gx = 0;
   bool ok = true;
   // The epilogue of an item waits for its last P V.  With full attention it
@@ -430,12 +494,18 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uin
   // overlaps that activation (short key ranges: an item is one or two
   // tiles).  Window items hold several tiles per side, and there holding
   // back the next item's first P V stalls the MMA issuer: no deferral.
-  bool pend = false, pend_live = false, pend_row_ok = false;
+  bool pend = false, pend_live = false, pend_row_ok = false, pend_bulk = false;
   float pend_inv = 0.0f;
+  int pend_x0 = 0, pend_y0 = 0;
   __nv_bfloat16* pend_orow = nullptr;
   auto epilogue = [&]() {
     ptx::tc_fence_after();
-    if (pend_live) store_o_row<D>(o_addr, pend_inv, pend_orow, pend_row_ok, p.out_align32 != 0);
+    if (pend_bulk) {  // a whole tile: staged and stored in bulk
+      if (!store_o_tile_bulk<D>(p, o_addr, pend_inv, stg, row, &B.epi_bar[x], epi_phase, abort, pend_x0, pend_y0))
+        ok = false;
+    } else if (pend_live) {
+      store_o_row<D>(o_addr, pend_inv, pend_orow, pend_row_ok, p.out_align32 != 0);
+    }
     ptx::tc_fence_before();
     ptx::mbar_arrive(&B.o_empty[x]);
     pend = false;
@@ -657,6 +727,7 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uin
       }
       if constexpr (!WIN) {
         if (pend) epilogue();  // the previous item's last P V has landed
+        if (!ok) break;
       }
       if (ACT == kActSoftmax && __any_sync(0xffffffffu, rescale)) {
         ptx::tc_fence_after();
@@ -683,13 +754,22 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uin
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      if (rows_live) store_o_row<D>(o_addr, inv, orow, row < rows, p.out_align32 != 0);
+      if (C::BULK && p.out_tma && rows == 128) {
+        ok = store_o_tile_bulk<D>(p, o_addr, inv, stg, row, &B.epi_bar[x], epi_phase, abort, t.h * D,
+                                  t.q_tok + 128 * x);
+        if (!ok) break;
+      } else if (rows_live) {
+        store_o_row<D>(o_addr, inv, orow, row < rows, p.out_align32 != 0);
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&B.o_empty[x]);
     } else {
       pend = true;
       pend_live = rows_live;
       pend_row_ok = row < rows;
+      pend_bulk = C::BULK && p.out_tma && rows == 128;
+      pend_x0 = t.h * D;
+      pend_y0 = t.q_tok + 128 * x;
       pend_inv = inv;
       pend_orow = orow;
     }
@@ -701,6 +781,7 @@ __device__ void pair64_activation(const FwdParams& p, Pair64Bars<D, WIN>& B, uin
       if (ok) epilogue();
     }
   }
+  if (row == 0) ptx::bulk_wait_all();  // the side's last bulk stores
   if (!ok && lane == 0) report_failure(p, abort, kStatusActivation);
 }
 
@@ -739,6 +820,8 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
     }
     ptx::mbar_init(&B.mma_drain[0], 1);
     ptx::mbar_init(&B.mma_drain[1], 1);
+    ptx::mbar_init(&B.epi_bar[0], 128);
+    ptx::mbar_init(&B.epi_bar[1], 128);
     for (int r = 0; r < kRing; ++r) {  // readers: the V producer, the MMA warps, the eight activation warps
       ptx::mbar_init(&B.ring.full[r], 1);
       ptx::mbar_init(&B.ring.empty[r], 1 + n_mma + 8);
@@ -765,7 +848,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_pair64_kernel(const __grid_co
     }
   } else {  // warpgroups 1 and 2: tiles A and B
     ptx::regs_inc<C::regs_act(ACT)>();
-    pair64_activation<D, ACT, WIN>(p, B, tmem, warp < 8 ? 0 : 1, warp, lane);
+    pair64_activation<D, ACT, WIN>(p, sm, B, tmem, warp < 8 ? 0 : 1, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -362,7 +362,10 @@ gdpa_status_t launch_forward(const LaunchArgs& a) {
   if (a.window_blocks < 0 && !(a.rows_per_item == 256 && a.kv_tile == kBlockN / 2)) return GDPA_ERR_INVALID_ARG;
   // the pair kernels (256-row items) claim their items at run time
   if (a.rows_per_item == 256 && !mx && !(prm.item_ctr = claim_counter(device))) return GDPA_ERR_CUDA;
+  prm.out_tma = 0;
   if (a.rows_per_item == 256 && a.kv_tile == kBlockN / 2) {
+    // with windows the 64-key kernel stores whole 128-row output tiles in bulk
+    if (win) prm.out_tma = encode_rows(&prm.tm_o, a.out, a.Tq, a.H, a.D, 128) == GDPA_OK ? 1 : 0;
     if (win) {  // softmax only (validated on entry)
       if (a.D == 128) return launch_pair64<128, kActSoftmax, true>(prm, a.num_ctas, s, device);
       if (a.D == 64) return launch_pair64<64, kActSoftmax, true>(prm, a.num_ctas, s, device);
