@@ -1,6 +1,9 @@
 // gelu_alu.cuh -- tanh-GELU (and SiLU, x sigma(x), through the same sigma
-// with other constants) evaluated with FMA-pipe and integer instructions only
-// (no special-function-unit instruction).
+// with other constants) by two routes: gelu_tanh_alu2 / gelu_tanh_grad_alu2
+// with FMA-pipe and integer instructions only (no special-function-unit
+// instruction), and gelu_tanh_sfu2 / gelu_tanh_val_grad_sfu2 with the
+// special-function unit's exp2 and reciprocal; act_eval2 picks one per
+// launch (gdpa_set_act_route).
 //
 // The GDPA section of the techfeed summary of "GEM Training" replaces the tanh
 // inside GELU, a special-function-unit bottleneck, by a 6th-order Taylor
