@@ -9,13 +9,16 @@
 // traffic per FLOP against one tile per item, and the two activation
 // warpgroups (one per tile) take turns with the tensor core:
 //
-//   MMA thread, per K/V tile g:  O_A += P_A(g-1) V(g-1);  S_A = Q_A K(g)^T;
-//                                O_B += P_B(g-1) V(g-1);  S_B = Q_B K(g)^T
+//   MMA warp, per K/V tile g:  O_A += P_A(g-1) V(g-1);  S_A = Q_A K(g)^T;
+//                              O_B += P_B(g-1) V(g-1);  S_B = Q_B K(g)^T
 //   warpgroup A works on S_A(g) while the tensor core runs the B half, and
 //   the other way round.
 //
+// Items are claimed at run time (see ItemRing): the Q/K producer claims and
+// decodes each item and every other role reads it from the ring.
+//
 // Threads (384, three warpgroups): warpgroup 0 holds the TMA producer for Q
-// and K (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
+// and K and claimer (warp 0), the MMA issuer + TMEM owner (warp 1, the whole warp runs
 // the issue loop and one elected lane issues) and the TMA producer for V
 // (warp 2), and hands registers to warpgroups 1 and 2, the activation /
 // epilogue of tiles A and B (200 registers a thread, so a whole row of 128
