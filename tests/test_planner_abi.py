@@ -208,13 +208,15 @@ def lpt_reference(Lq, Lkv, H, R, num_ctas, cost_of):
     return flat, cta
 
 
-@pytest.mark.parametrize("huge", [False, True])
-def test_plan_matches_plain_lpt_schedule(huge):
+@pytest.mark.parametrize("huge,ctas", [(False, 7), (True, 7), (False, 150), (False, 131)])
+def test_plan_matches_plain_lpt_schedule(huge, ctas):
     # huge key counts make the cost buckets outnumber the items, which takes
     # the in-place sort instead of the counting sort: both must give the
-    # schedule of the plain restatement, exactly
-    rng = np.random.default_rng(99 + huge)
-    B, H, ctas = 23, 3, 7
+    # schedule of the plain restatement, exactly.  With 7 CTAs the items
+    # outnumber twice the tree's leaves (the packed-key tree); with 131 or 150
+    # CTAs they do not (the general tree): both give the same schedule.
+    rng = np.random.default_rng(99 + huge + ctas)
+    B, H = 23, 3
     Lq = rng.integers(0, 600, size=B)
     Lkv = rng.integers(0, 600, size=B) * (5000 if huge else 1)
     qo, ko = offsets_of(Lq), offsets_of(Lkv)
