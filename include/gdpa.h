@@ -315,6 +315,15 @@ gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_o
                                int D, int act, int window_blocks, gdpa_plan_t** plan);
 
 /*
+ * gdpa_plan_create_sliding -- the plan of gdpa_fwd_sliding (causal sliding
+ * window of window_tokens >= 1 tokens; self attention: h_q_offsets and
+ * h_kv_offsets equal; softmax).  Launch it with gdpa_fwd_planned.
+ * GDPA_ERR_INVALID_ARG for window_tokens < 1, unequal offsets or another act.
+ */
+gdpa_status_t gdpa_plan_create_sliding(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
+                                       int D, int act, int window_tokens, gdpa_plan_t** plan);
+
+/*
  * gdpa_fwd_planned -- launch the forward pass with a plan; fully asynchronous
  * on `stream`.  The device offsets must hold the values the plan was built
  * from.  The kernels clip every work item to the rows of the tensors the plan

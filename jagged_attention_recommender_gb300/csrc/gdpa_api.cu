@@ -603,12 +603,11 @@ extern "C" gdpa_status_t gdpa_bwd_sliding(const void* q, const void* k, const vo
                   -window_tokens, scale, dq, dk, dv, stream);
 }
 
-extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
-                                          int D, int act, int window_blocks, gdpa_plan_t** plan) {
-  if (!plan) return GDPA_ERR_INVALID_ARG;
-  *plan = nullptr;
-  gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
-  if (st != GDPA_OK) return st;
+// The plan of gdpa_plan_create (window_blocks >= 0) and gdpa_plan_create_sliding
+// (window_blocks = -window_tokens); the caller has validated the shape.
+static gdpa_status_t plan_create_impl(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H, int D,
+                                      int act, int window_blocks, gdpa_plan_t** plan) {
+  gdpa_status_t st;
   int64_t Tq = 0, Tkv = 0;
   if ((st = validate_offsets(h_q_offsets, h_kv_offsets, B, window_blocks, &Tq, &Tkv)) != GDPA_OK) return st;
   if (Tq >= (int64_t)1 << 31 || Tkv >= (int64_t)1 << 31) return GDPA_ERR_UNSUPPORTED;
@@ -666,6 +665,25 @@ extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int3
   }
   *plan = P;
   return GDPA_OK;
+}
+
+extern "C" gdpa_status_t gdpa_plan_create(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B, int H,
+                                          int D, int act, int window_blocks, gdpa_plan_t** plan) {
+  if (!plan) return GDPA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const gdpa_status_t st = validate_shape(B, H, D, act, window_blocks);
+  if (st != GDPA_OK) return st;
+  return plan_create_impl(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks, plan);
+}
+
+extern "C" gdpa_status_t gdpa_plan_create_sliding(const int32_t* h_q_offsets, const int32_t* h_kv_offsets, int B,
+                                                  int H, int D, int act, int window_tokens, gdpa_plan_t** plan) {
+  if (!plan) return GDPA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (window_tokens < 1) return GDPA_ERR_INVALID_ARG;
+  const gdpa_status_t st = validate_shape(B, H, D, act, 1);  // as a window: softmax only
+  if (st != GDPA_OK) return st;
+  return plan_create_impl(h_q_offsets, h_kv_offsets, B, H, D, act, -window_tokens, plan);
 }
 
 extern "C" gdpa_status_t gdpa_fwd_planned(const gdpa_plan_t* plan, const void* q, const void* k, const void* v,

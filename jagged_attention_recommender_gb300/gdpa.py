@@ -30,7 +30,7 @@ GDPA_ERR_DEVICE_TIMEOUT = 4
 GDPA_ERR_NO_MEMORY = 5
 
 # Every symbol include/gdpa.h declares.
-EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
+EXPORTS = ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mx", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_plan_create_sliding", "gdpa_fwd_planned", "gdpa_plan_destroy", "gdpa_plan_num_items",
            "gdpa_plan_num_ctas", "gdpa_fwd_host", "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_set_act_route",
            "gdpa_get_act_route", "gdpa_device_status", "gdpa_wait_selftest", "gdpa_status_string", "gdpa_version")
 
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_bwd_sliding.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P]
     L.gdpa_plan_create.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
+    L.gdpa_plan_create_sliding.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(P)]
     L.gdpa_fwd_planned.argtypes = [P, P, P, P, P, P, F, P, P]
     L.gdpa_plan_destroy.argtypes = [P]
     L.gdpa_plan_destroy.restype = None
@@ -86,7 +87,7 @@ def lib() -> ctypes.CDLL:
     L.gdpa_status_string.restype = ctypes.c_char_p
     L.gdpa_version.argtypes = []
     L.gdpa_version.restype = ctypes.c_char_p
-    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
+    for name in ("gdpa_fwd", "gdpa_fwd_async", "gdpa_fwd_lse", "gdpa_fwd_sliding", "gdpa_fwd_mxfp8", "gdpa_bwd", "gdpa_bwd_sliding", "gdpa_fwd_noalloc", "gdpa_plan_create", "gdpa_plan_create_sliding", "gdpa_fwd_planned", "gdpa_plan_num_ctas", "gdpa_fwd_host",
                  "gdpa_plan_enumerate", "gdpa_act_eval", "gdpa_set_act_route", "gdpa_device_status", "gdpa_wait_selftest"):
         getattr(L, name).restype = I
     _lib = L
@@ -236,6 +237,15 @@ def gdpa_plan_create(h_q_offsets, h_kv_offsets, B, H, D, act, window_blocks) -> 
     h = ctypes.c_void_p()
     _check(lib().gdpa_plan_create(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
                                   int(window_blocks), ctypes.byref(h)), "gdpa_plan_create")
+    return Plan(h.value)
+
+
+def gdpa_plan_create_sliding(h_q_offsets, h_kv_offsets, B, H, D, act, window_tokens) -> Plan:
+    """The plan of gdpa_fwd_sliding (causal window of ``window_tokens`` tokens), for gdpa_fwd_planned."""
+    qo, ko = _i32(h_q_offsets), _i32(h_kv_offsets)
+    h = ctypes.c_void_p()
+    _check(lib().gdpa_plan_create_sliding(qo.ctypes.data, ko.ctypes.data, int(B), int(H), int(D), int(act),
+                                          int(window_tokens), ctypes.byref(h)), "gdpa_plan_create_sliding")
     return Plan(h.value)
 
 

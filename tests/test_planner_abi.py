@@ -40,6 +40,16 @@ def test_library_exports_every_declared_symbol():
     assert gdpa.gdpa_status_string(99) == "GDPA_ERR_UNKNOWN"
 
 
+def test_sliding_plan_argument_checks_need_no_gpu():
+    qo = np.array([0, 64], np.int32)
+    for act, W, ko, code in ((0, 0, qo, gdpa.GDPA_ERR_INVALID_ARG),
+                             (0, -5, qo, gdpa.GDPA_ERR_INVALID_ARG),
+                             (1, 8, qo, gdpa.GDPA_ERR_UNSUPPORTED)):
+        with pytest.raises(gdpa.GdpaError) as e:
+            gdpa.gdpa_plan_create_sliding(qo, ko, 1, 1, 64, act, W)
+        assert e.value.code == code
+
+
 def test_act_route_setter_needs_no_gpu():
     assert gdpa.gdpa_get_act_route() == gdpa.GDPA_ROUTE_SFU  # the default
     try:

@@ -96,3 +96,30 @@ def test_sliding_window_rejects_bad_arguments():
         with pytest.raises(gdpa.GdpaError) as e:
             gdpa.gdpa_fwd_sliding(0, 0, 0, qo, ko, 0, 0, 1, 1, 64, act, W, 1.0, 0)
         assert e.value.code == code
+
+
+@pytest.mark.parametrize("W", [17, 256])
+def test_sliding_window_planned_matches_the_async_entry(W):
+    """gdpa_plan_create_sliding + gdpa_fwd_planned give the bits of
+    gdpa_fwd_sliding (same items, same kernel), twice in a row with one plan."""
+    rng = np.random.default_rng(8200 + W)
+    L = np.array(LENGTHS)
+    b = small_batch(rng, L, L, 2, 128, window_blocks=-W)
+    w = b.workload
+    ref = run_sliding(b, W, guard=0, as_tensor=True).clone()
+    q, k, v = dev(b.q), dev(b.k), dev(b.v)
+    qo = torch.from_numpy(b.q_offsets).cuda()
+    ko = torch.from_numpy(b.kv_offsets).cuda()
+    B = len(b.q_offsets) - 1
+    plan = gdpa.gdpa_plan_create_sliding(b.q_offsets, b.kv_offsets, B, w.H, w.D, w.act, W)
+    try:
+        for _ in range(2):
+            out = torch.full_like(ref, float("nan"))
+            gdpa.gdpa_fwd_planned(plan, q, k, v, qo, ko, w.scale, out)
+            assert gdpa.gdpa_device_status() == gdpa.GDPA_OK
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    finally:
+        torch.cuda.synchronize()
+        gdpa.gdpa_plan_destroy(plan)
+    assert_parity(ref.float().cpu().numpy().astype(np.float64), oracle.gdpa_fwd_batch(b), "planned W=%d" % W)
